@@ -1,0 +1,257 @@
+"""Seeded synthetic workloads for the paged-KV decode path.
+
+This module only *draws* inputs: sequence lengths, random page assignments, and
+N(0, 1) values rounded to bf16.  It holds none of the method's arithmetic (no
+RoPE, no softmax, no attention), so both the CUDA path and the CPU oracle can
+be fed from it without sharing any of the computation under test.
+
+bf16 data is kept as raw ``uint16`` bit patterns on the host.  Unused pool
+pages, and the slots of a live page at or beyond the appended position, hold
+the poison pattern ``0xFFFF`` (a bf16 NaN) so that any read the method should
+not make turns a result into NaN.
+
+Workload shapes follow the Tiny-vLLM model dimensions (Llama 3.2 1B: 32 query
+heads, 8 kv heads, head dim 64, 16-token pages, 2048-token context) from the
+"Hours of YouTube and 85 handtyped pages of notes on LLM Inference - Start
+here" README, sections "これまでの進捗" and "現在のスコープ".
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+POISON = 0xFFFF
+NUM_Q_HEADS = 32
+NUM_KV_HEADS = 8
+HEAD_DIM = 64
+PAGE_SIZE = 16
+MAX_BLOCKS = 128  # 2048-token context / 16-token pages
+ROPE_THETA = 500000.0
+SCALE = 0.125  # 1 / sqrt(64)
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    layers: int
+    batch: int
+    num_pages: int
+    seq_lens: np.ndarray          # int32 [B]; length after this step's append
+    block_tables: np.ndarray      # int32 [layers][B][max_blocks]; -1 beyond the live blocks
+    live_pages: np.ndarray        # int64 [n_live]; physical ids in (layer, seq, block) order
+    page_data: np.ndarray         # uint16 [n_live][2][page_size][Hkv][D]; before the append
+    q: np.ndarray                 # uint16 [layers][B][Hq][D]
+    k_new: np.ndarray             # uint16 [layers][B][Hkv][D]
+    v_new: np.ndarray             # uint16 [layers][B][Hkv][D]
+    num_q_heads: int = NUM_Q_HEADS
+    num_kv_heads: int = NUM_KV_HEADS
+    head_dim: int = HEAD_DIM
+    page_size: int = PAGE_SIZE
+    max_blocks: int = MAX_BLOCKS
+    rope_theta: float = ROPE_THETA
+    scale: float = SCALE
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def positions(self) -> np.ndarray:
+        """Decode position of the appended token: the last position of each sequence."""
+        return (self.seq_lens.astype(np.int32) - 1).astype(np.int32)
+
+    def pages_of(self, layer: int, b: int) -> np.ndarray:
+        n = _num_blocks(int(self.seq_lens[b]), self.page_size)
+        return self.block_tables[layer, b, :n]
+
+    def kv_bytes(self) -> int:
+        """Bytes of live K/V a full step streams: sum of lengths x Hkv x D x 2 (K,V) x 2 B."""
+        return int(self.layers * int(self.seq_lens.astype(np.int64).sum())
+                   * self.num_kv_heads * self.head_dim * 2 * 2)
+
+
+def _num_blocks(L: int, page_size: int) -> int:
+    return (max(L, 0) + page_size - 1) // page_size
+
+
+def _bf16_normal(gen: torch.Generator, n: int) -> np.ndarray:
+    """n draws of N(0, 1) in float32, rounded to bf16, as uint16 bits."""
+    x = torch.randn(n, generator=gen, dtype=torch.float32)
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _lengths(name: str, rng: np.random.Generator, batch: int) -> np.ndarray:
+    if name == "tiny":
+        return np.full(batch, 37, dtype=np.int32)
+    if name in ("long", "peak"):
+        return np.full(batch, 2048, dtype=np.int32)
+    if name == "small":
+        return rng.integers(1, 2048, size=batch, endpoint=True).astype(np.int32)
+    if name == "mix":
+        n_long = int(round(0.1 * batch))
+        short = rng.integers(16, 128, size=batch - n_long, endpoint=True)
+        long_ = rng.integers(1536, 2048, size=n_long, endpoint=True)
+        lens = np.concatenate([short, long_]).astype(np.int32)
+        rng.shuffle(lens)
+        return lens
+    raise ValueError(f"unknown workload {name!r}")
+
+
+# name -> (layers, batch, pool pages); see the design doc's input recipe.
+WORKLOADS = {
+    "tiny": (1, 1, 64),
+    "long": (16, 1, 4096),
+    "small": (1, 8, 4096),
+    "peak": (1, 256, 40000),
+    "mix": (16, 128, 262144),
+}
+WORKLOAD_INDEX = {"tiny": 0, "long": 1, "small": 2, "peak": 3, "mix": 4}
+
+
+def make_workload(name: str, seed: int = 0, *, seq_lens=None, batch=None, layers=None,
+                  num_pages=None, max_blocks: int = MAX_BLOCKS) -> Workload:
+    """Draw one of the named workloads (or a custom one via the keyword overrides).
+
+    The seed mixes in the workload's index so that different workloads drawn
+    with the same seed are independent.
+    """
+    if name in WORKLOADS:
+        d_layers, d_batch, d_pages = WORKLOADS[name]
+        mix = WORKLOAD_INDEX[name]
+    else:
+        d_layers, d_batch, d_pages = 1, 1, 64
+        mix = 97
+    layers = d_layers if layers is None else layers
+    num_pages = d_pages if num_pages is None else num_pages
+    full_seed = int(seed) * 1000 + mix
+    rng = np.random.default_rng(full_seed)
+    if seq_lens is None:
+        batch = d_batch if batch is None else batch
+        seq_lens = _lengths(name, rng, batch)
+    else:
+        seq_lens = np.asarray(seq_lens, dtype=np.int32)
+        batch = int(seq_lens.shape[0])
+    if np.any(seq_lens > max_blocks * PAGE_SIZE):
+        raise ValueError("sequence longer than the block table allows")
+    blocks = [_num_blocks(int(L), PAGE_SIZE) for L in seq_lens]
+    n_live = layers * sum(blocks)
+    if n_live > num_pages:
+        raise ValueError(f"{n_live} live pages do not fit a {num_pages}-page pool")
+
+    gen = torch.Generator().manual_seed(full_seed)
+    perm = torch.randperm(num_pages, generator=gen).numpy().astype(np.int64)
+    live = perm[:n_live]
+
+    bt = np.full((layers, batch, max_blocks), -1, dtype=np.int32)
+    cursor = 0
+    for layer in range(layers):
+        for b in range(batch):
+            n = blocks[b]
+            bt[layer, b, :n] = live[cursor:cursor + n]
+            cursor += n
+
+    Hq, Hkv, D, P = NUM_Q_HEADS, NUM_KV_HEADS, HEAD_DIM, PAGE_SIZE
+    page_elems = 2 * P * Hkv * D
+    page_data = np.empty((n_live, 2, P, Hkv, D), dtype=np.uint16)
+    flat = page_data.reshape(n_live, page_elems)
+    chunk = 2048
+    for s in range(0, n_live, chunk):
+        e = min(n_live, s + chunk)
+        flat[s:e] = _bf16_normal(gen, (e - s) * page_elems).reshape(e - s, page_elems)
+    # Poison every slot at or past the appended position (position L-1) of each
+    # sequence's last page; the append step writes position L-1 itself.
+    cursor = 0
+    for layer in range(layers):
+        for b in range(batch):
+            n = blocks[b]
+            if n:
+                first_dead = (int(seq_lens[b]) - 1) % P
+                page_data[cursor + n - 1, :, first_dead:, :, :] = POISON
+            cursor += n
+
+    q = _bf16_normal(gen, layers * batch * Hq * D).reshape(layers, batch, Hq, D)
+    k_new = _bf16_normal(gen, layers * batch * Hkv * D).reshape(layers, batch, Hkv, D)
+    v_new = _bf16_normal(gen, layers * batch * Hkv * D).reshape(layers, batch, Hkv, D)
+    return Workload(name=name, seed=int(seed), layers=layers, batch=batch, num_pages=num_pages,
+                    seq_lens=seq_lens, block_tables=bt, live_pages=live, page_data=page_data,
+                    q=q, k_new=k_new, v_new=v_new, max_blocks=max_blocks,
+                    meta={"full_seed": full_seed})
+
+
+# ------------------------------------------------------------ host views --
+
+def host_pool(w: Workload) -> np.ndarray:
+    """The whole physical pool on the host (small pools only): poison + live pages."""
+    pool = np.full((w.num_pages, 2, w.page_size, w.num_kv_heads, w.head_dim), POISON,
+                   dtype=np.uint16)
+    pool[w.live_pages] = w.page_data
+    return pool
+
+
+@dataclass
+class Compact:
+    """A relabelled copy of some sequences of one layer for the oracle.
+
+    ``pool`` holds only the pages those sequences use, and ``block_table`` maps
+    their blocks to indices in that compact pool (a pure relabelling of pages).
+    """
+    seqs: np.ndarray
+    pool: np.ndarray
+    block_table: np.ndarray
+    seq_lens: np.ndarray
+    positions: np.ndarray
+    q: np.ndarray
+    k_new: np.ndarray
+    v_new: np.ndarray
+
+
+def compact(w: Workload, layer: int, seqs=None) -> Compact:
+    seqs = np.arange(w.batch) if seqs is None else np.asarray(seqs, dtype=np.int64)
+    index_of = {int(p): i for i, p in enumerate(w.live_pages)}
+    bt = np.full((len(seqs), w.max_blocks), -1, dtype=np.int32)
+    pages = []
+    for r, b in enumerate(seqs):
+        for k, p in enumerate(w.pages_of(layer, int(b))):
+            bt[r, k] = len(pages)
+            pages.append(index_of[int(p)])
+    pool = w.page_data[np.asarray(pages, dtype=np.int64)] if pages else np.zeros(
+        (0, 2, w.page_size, w.num_kv_heads, w.head_dim), dtype=np.uint16)
+    pool = np.ascontiguousarray(pool)
+    return Compact(seqs=seqs, pool=pool, block_table=bt,
+                   seq_lens=w.seq_lens[seqs].copy(), positions=w.positions[seqs].copy(),
+                   q=np.ascontiguousarray(w.q[layer][seqs]),
+                   k_new=np.ascontiguousarray(w.k_new[layer][seqs]),
+                   v_new=np.ascontiguousarray(w.v_new[layer][seqs]))
+
+
+# ---------------------------------------------------------- device views --
+
+def _to_bf16_tensor(a: np.ndarray, device) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def device_inputs(w: Workload, device="cuda") -> dict:
+    """Upload a workload: the poison-filled pool with live pages scattered in,
+    per-layer tables, queries, new K/V, lengths and positions."""
+    Hkv, D, P = w.num_kv_heads, w.head_dim, w.page_size
+    pool = torch.full((w.num_pages, 2, P, Hkv, D), -1, dtype=torch.int16, device=device)
+    live = torch.from_numpy(w.live_pages).to(device)
+    chunk = 4096
+    for s in range(0, len(w.live_pages), chunk):
+        e = min(len(w.live_pages), s + chunk)
+        pool[live[s:e]] = torch.from_numpy(w.page_data[s:e].view(np.int16)).to(device)
+    return {
+        "pool": pool.view(torch.bfloat16),
+        "block_tables": torch.from_numpy(w.block_tables).to(device),
+        "q": _to_bf16_tensor(w.q, device),
+        "k_new": _to_bf16_tensor(w.k_new, device),
+        "v_new": _to_bf16_tensor(w.v_new, device),
+        "seq_lens": torch.from_numpy(w.seq_lens.astype(np.int32)).to(device),
+        "positions": torch.from_numpy(w.positions.astype(np.int32)).to(device),
+    }
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """uint16 bit patterns of a bf16 tensor (copied to the host)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
