@@ -1,0 +1,483 @@
+"""Benchmark of the paged-KV decode step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload peak] [--impl ours|reference]
+
+One step = the whole decode hot path for one batch: the KV append (RoPE on the
+new keys, K/V written into their page slots) followed by paged decode
+attention (plus the split merge when the plan splits), for every layer of the
+workload.  The default workload is 256 sequences x 2048 tokens of context,
+one layer, 32 query / 8 kv heads, head dim 64, 32768 live pages randomly
+scattered in a 40000-page pool.
+
+Prints one JSON line.  `value` is achieved algorithmic HBM GB/s of the whole
+step with all inputs resident in device memory; `e2e` repeats the measurement
+with the per-step inputs copied from pinned host memory and the output copied
+back inside the timed region.  `--impl reference` times the FP64 CPU oracle on
+the host cores instead (a deliberately slow baseline, not a target).
+Multi-GPU runs (torchrun) are independent replicas, one per rank (weak
+scaling): the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn achieved HBM GB/s (% of peak); decode steps/s at bs=256"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_attention_peak_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_decode_04_gb300", "csrc", f)
+                  for f in ("decode_attention.cu", "pkv_device.cuh", "pkv_internal.h")]
+
+WORKLOAD_TEXT = {
+    "peak": "peak: 256 seqs x 2048 ctx, 1 layer, 32q/8kv/64 bf16, 32768 live pages (1 GiB K/V) "
+            "randomly scattered in a 40000-page pool",
+    "mix": "mix: 128 seqs (115 of 16-128, 13 of 1536-2048 tokens), 16 layers with per-layer "
+           "tables, 32q/8kv/64 bf16, 8 GiB pool",
+    "long": "long: 1 seq x 2048 ctx x 16 layers, 32q/8kv/64 bf16, shuffled pages, 4096-page pool",
+    "small": "small: 8 seqs, lengths U[1,2048], 1 layer, 4096-page pool",
+    "tiny": "tiny: 1 seq x 37 ctx, 1 layer, 64-page pool",
+}
+
+
+# ------------------------------------------------------------------ bytes --
+
+def algorithmic_bytes(w, part: str = "step") -> int:
+    """Bytes the step must move at minimum, per step (all layers).
+
+    attention: K/V rows read once per kv head (sum L x Hkv x D x 2 x 2 B), q read
+               and out written (B x Hq x D x 2 B each), the live block-table
+               entries (4 B per page) and seq_lens (4 B per sequence);
+    append:    new K/V read and written once (B x Hkv x D x 2 x 2 B, twice) and
+               positions (4 B per sequence) -- the table entry it reads is
+               counted with the attention's tables.
+    """
+    B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    lens = w.seq_lens.astype(np.int64)
+    pages = (lens + w.page_size - 1) // w.page_size
+    attn = int(lens.sum()) * Hkv * D * 2 * 2 + B * Hq * D * 2 * 2 + int(pages.sum()) * 4 + B * 4
+    app = B * Hkv * D * 2 * 2 * 2 + B * 4
+    per_layer = {"attention": attn, "append": app, "step": attn + app}[part]
+    return per_layer * w.layers
+
+
+# ------------------------------------------------------------- utilities --
+
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["hbm_gbs"])
+            return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """ncu DRAM bytes per attention launch, if recorded for the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_sha") != kernel_sha() or rec.get("workload") != workload:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_selector: str):
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gpu_selector],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [r for t, r in self.rows if t0 - 0.15 <= t <= t1 + 0.15] or [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def gpu_selector(dev_index: int) -> str:
+    import torch
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev_index).uuid)
+        if uuid:
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v for v in vis.split(",") if v.strip()]
+    if dev_index < len(ids) and ids[dev_index].strip().isdigit():
+        return ids[dev_index].strip()
+    return str(dev_index)
+
+
+# ---------------------------------------------------------- distributed --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_sample_run(w, n_seqs: int, rng_seed: int = 0, threads: int = 0):
+    """Time the FP64 oracle on n_seqs sequences of every layer (append + attention).
+
+    The sample's inputs are relabelled into compact host copies first (not
+    timed).  Returns (seconds, algorithmic bytes of the sample, threads, seqs)."""
+    import oracle
+    from paged_kv_decode_04_gb300 import synth
+    rng = np.random.default_rng(rng_seed)
+    seqs = np.sort(rng.choice(w.batch, size=min(n_seqs, w.batch), replace=False))
+    threads = threads or oracle.default_threads()
+    comps = [synth.compact(w, layer, seqs) for layer in range(w.layers)]
+    t0 = time.perf_counter()
+    for c in comps:
+        oracle.kv_append(c.k_new, c.v_new, c.pool, c.block_table, c.positions,
+                         page_size=w.page_size, theta=w.rope_theta)
+        oracle.decode_attention(c.q, c.pool, c.block_table, c.seq_lens,
+                                num_kv_heads=w.num_kv_heads, page_size=w.page_size,
+                                scale=w.scale, threads=threads)
+    dt = time.perf_counter() - t0
+    sub = synth.Workload(
+        name=w.name, seed=w.seed, layers=w.layers, batch=len(seqs), num_pages=w.num_pages,
+        seq_lens=w.seq_lens[seqs], block_tables=w.block_tables[:, seqs], live_pages=w.live_pages,
+        page_data=w.page_data[:0], q=w.q[:, seqs], k_new=w.k_new[:, seqs],
+        v_new=w.v_new[:, seqs])
+    return dt, algorithmic_bytes(sub, "step"), threads, len(seqs)
+
+
+# ------------------------------------------------------------------ main --
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from paged_kv_decode_04_gb300 import synth
+    w = synth.make_workload(args.workload, args.seed)
+    n_seqs = args.ref_seqs
+    for _ in range(args.warmup):
+        oracle_sample_run(w, n_seqs, 1)
+    total_t = 0.0
+    total_b = 0
+    threads = 1
+    for k in range(args.steps):
+        dt, nb, threads, used = oracle_sample_run(w, n_seqs, 100 + k)
+        total_t += dt
+        total_b += nb
+    value = total_b / total_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "seed": args.seed,
+                   "sample": f"{used} of {w.batch} sequences x {w.layers} layer(s) per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{used} of {w.batch} sequences per step, FP64 C oracle, "
+                                   f"{threads} threads"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from paged_kv_decode_04_gb300 import binding, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    w = synth.make_workload(args.workload, args.seed)
+    d = synth.device_inputs(w, dev)
+    B, layers = w.batch, w.layers
+    stream = torch.cuda.current_stream(dev)
+    splits = binding.plan_splits(B, w.max_blocks, args.splits)
+    ws_bytes = binding.workspace_bytes(B, w.max_blocks, args.splits)
+    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    outs = torch.empty((layers, B, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kernels_per_step = layers * (2 + (1 if splits > 1 else 0))
+
+    def step(q=None, k=None, v=None, pos=None, lens=None, bts=None):
+        q = d["q"] if q is None else q
+        k = d["k_new"] if k is None else k
+        v = d["v_new"] if v is None else v
+        pos = d["positions"] if pos is None else pos
+        lens = d["seq_lens"] if lens is None else lens
+        bts = d["block_tables"] if bts is None else bts
+        for layer in range(layers):
+            binding.kv_append(k[layer], v[layer], d["pool"], bts[layer], pos,
+                              rope_theta=w.rope_theta, dev_err=err, stream=stream)
+            binding.paged_decode_attention(q[layer], d["pool"], bts[layer], lens, outs[layer],
+                                           scale=w.scale, workspace=workspace,
+                                           num_splits=args.splits, dev_err=err, stream=stream)
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
+
+    # ---- timed region: K whole steps, device-resident inputs
+    sampler = ClockSampler(gpu_selector(local)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(world)
+    if sampler:
+        sampler.stop()
+    ms_local = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms_local, world, dev)
+    step_bytes = algorithmic_bytes(w, "step")
+    total_bytes = sum_over_ranks(step_bytes * args.steps, world, dev)
+    value = total_bytes / (ms / 1e3) / 1e9
+    ms_per_step = ms / args.steps
+
+    # ---- per-kernel durations (events around each launch, same stream)
+    n_prof = min(args.steps, max(50, args.steps // 4))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_prof)]
+    for i in range(n_prof):
+        ev[i][0].record(stream)
+        for layer in range(layers):
+            binding.kv_append(d["k_new"][layer], d["v_new"][layer], d["pool"],
+                              d["block_tables"][layer], d["positions"], rope_theta=w.rope_theta,
+                              dev_err=err, stream=stream)
+        ev[i][1].record(stream)
+        for layer in range(layers):
+            binding.paged_decode_attention(d["q"][layer], d["pool"], d["block_tables"][layer],
+                                           d["seq_lens"], outs[layer], scale=w.scale,
+                                           workspace=workspace, num_splits=args.splits,
+                                           dev_err=err, stream=stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    append_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n_prof)) / layers
+    attn_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(n_prof)) / layers
+    attn_bytes = algorithmic_bytes(w, "attention") / layers
+    peak, peak_kind = measured_hbm_peak()
+    achieved = attn_bytes / (attn_ms / 1e3) / 1e9
+
+    # ---- end to end: per-step inputs from pinned host memory, output back to host
+    host = {
+        "q": d["q"].cpu().pin_memory(), "k_new": d["k_new"].cpu().pin_memory(),
+        "v_new": d["v_new"].cpu().pin_memory(), "positions": d["positions"].cpu().pin_memory(),
+        "seq_lens": d["seq_lens"].cpu().pin_memory(),
+        "block_tables": d["block_tables"].cpu().pin_memory(),
+    }
+    staged = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_host = torch.empty(outs.shape, dtype=outs.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k_, v_ in host.items():
+            staged[k_].copy_(v_, non_blocking=True)
+        step(staged["q"], staged["k_new"], staged["v_new"], staged["positions"],
+             staged["seq_lens"], staged["block_tables"])
+        out_host.copy_(outs, non_blocking=True)
+
+    for _ in range(max(3, min(args.warmup, 20))):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    n_e2e = args.steps
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
+    e2e_value = sum_over_ranks(step_bytes * n_e2e, world, dev) / (e2e_ms / 1e3) / 1e9
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} during the timed runs")
+
+    # ---- CPU baseline: the oracle on a bounded sample of the same workload
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, nb, threads, used = oracle_sample_run(w, args.cpu_seqs)
+        cpu = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"{used} of {w.batch} sequences x {w.layers} layer(s): FP64 append + "
+                         f"two-pass attention, {dt:.2f} s wall on {threads} threads"}
+
+    if rank != 0:
+        return 0
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD_TEXT[args.workload], "seed": args.seed,
+            "num_splits": splits, "layers_per_step": layers,
+            "l2": ("inputs larger than L2: %.2f GiB of K/V streamed per step vs 129 MB L2; no flush"
+                   % (w.kv_bytes() / 2 ** 30)) if w.kv_bytes() > 512 * 2 ** 20 else
+                  "working set fits in L2 (no flush): L2-resident figure",
+            "parallelism": f"replicas x{world}",
+        },
+        "steps_per_s": round(1e3 / ms_per_step * world, 1),
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_copy": round(100 * value / world / peak, 2),
+        "algorithmic_bytes_per_step": step_bytes,
+        "kernels_us": {"kv_append": round(append_ms * 1e3, 2),
+                       "paged_decode_attention": round(attn_ms * 1e3, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "paged_decode_kernel" + ("+merge_splits_kernel" if splits > 1 else ""),
+                     "peak_kind": f"{peak_kind} copy bandwidth",
+                     "bytes_per_launch": attn_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / n_e2e, 5)},
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="peak")
+    ap.add_argument("--splits", type=int, default=0, help="0 = automatic split plan")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seqs", type=int, default=256,
+                    help="sequences of the CPU-oracle baseline sample")
+    ap.add_argument("--ref-seqs", type=int, default=1,
+                    help="sequences per step of the --impl reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

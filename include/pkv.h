@@ -1,0 +1,169 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: batched paged decode attention over a shared
+ * bf16 KV page pool, with the one-token KV append (rotate-half RoPE), for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Source of the operations: the Tiny-vLLM README translation "Hours of YouTube
+ * and 85 handtyped pages of notes on LLM Inference - Start here", section
+ * "これまでの進捗" (progress so far): a shared BF16 KV page pool whose pages
+ * each hold K and V for 16 tokens, one block table per (sequence, layer);
+ * decode adds one new token per sequence at its absolute RoPE position; paged
+ * decode attention streams each sequence's cached pages with an FP32 online
+ * softmax, never gathering a contiguous prefix and never storing scores; the
+ * batched decode packs one token per active sequence and each sequence's
+ * attention reads only its own cache.  The model dimensions (32 query heads,
+ * 8 kv heads, head dim 64) are the fixed Llama 3.2 1B ones of section
+ * "現在のスコープ" (scope).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - bf16 values are passed as pkv_bf16 (the raw 16-bit pattern).
+ *  - Every tensor pointer is DEVICE memory owned by the caller, unless the
+ *    comment says otherwise.  The library never allocates, frees or
+ *    synchronizes; all work is enqueued on `stream` (NULL = the legacy
+ *    default stream) and returns before it runs.  The library keeps no state
+ *    between calls beyond a per-thread cache of TMA descriptors and of the
+ *    device's SM count; calls are thread-safe.
+ *  - Pool layout: [num_pages][2 (K, V)][page_size][num_kv_heads][head_dim]
+ *    bf16, i.e. element ((page*2 + kv)*page_size + slot)*Hkv*D + h*D + d.
+ *    The pool must be 16-byte aligned.
+ *  - Block table of one layer: int32 [batch][max_blocks]; entry k of row b is
+ *    the physical page of tokens [16k, 16k+16) of sequence b.  Entries past
+ *    the sequence's last block are never read (any value, -1 by convention).
+ *  - Query head j uses kv head j / (num_q_heads / num_kv_heads).
+ *  - Supported sizes: num_q_heads = 32, num_kv_heads = 8, head_dim = 64,
+ *    page_size = 16 (other values return PKV_EUNSUPPORTED).
+ *  - Return value: PKV_OK or a PKV_E* code (see pkv_strerror).  Argument
+ *    errors are detected on the host before anything is enqueued.  Bad DEVICE
+ *    data (a page id outside [0, num_pages), a length or position outside the
+ *    block table) never traps: the offending access is skipped and the
+ *    matching PKV_DEVERR_* bit is OR-ed into *dev_err when dev_err is not NULL.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef uint16_t pkv_bf16;
+typedef struct CUstream_st* pkv_stream_t; /* same type as cudaStream_t */
+
+/* Host-side status codes. */
+#define PKV_OK 0
+#define PKV_EINVAL 1        /* NULL pointer, non-positive size, bad scale ... */
+#define PKV_EUNSUPPORTED 2  /* head counts / dims / page size not compiled in */
+#define PKV_EWORKSPACE 3    /* workspace missing or smaller than required */
+#define PKV_ECUDA 4         /* a CUDA runtime call or launch failed */
+#define PKV_EALIGN 5        /* a pointer violates the alignment stated above */
+
+/* Device-side error bits OR-ed into *dev_err. */
+#define PKV_DEVERR_PAGE 1u      /* block-table entry outside [0, num_pages) */
+#define PKV_DEVERR_SEQLEN 2u    /* seq_lens[b] < 0 or > max_blocks*page_size */
+#define PKV_DEVERR_POSITION 4u  /* positions[b] < 0 or >= max_blocks*page_size */
+#define PKV_DEVERR_TIMEOUT 8u   /* an in-kernel wait for a page copy gave up */
+
+/* Library ABI version (bumped when a signature changes). */
+PKV_API int pkv_abi_version(void);
+
+/* Static description of a status code; never NULL. */
+PKV_API const char* pkv_strerror(int status);
+
+/*
+ * pkv_kv_append -- decode-time KV append ("これまでの進捗", KV page pool item:
+ * one new token per sequence at its absolute RoPE position).
+ *
+ * For every sequence b and kv head h, with pos = positions[b],
+ * page = block_table[b*max_blocks + pos/page_size], slot = pos % page_size:
+ *   pool[page][K][slot][h][:] = RoPE(k_new[b][h][:], pos)
+ *   pool[page][V][slot][h][:] = v_new[b][h][:]
+ * RoPE is rotate-half: for i < D/2 the pair (x_i, x_{i+D/2}) turns by the
+ * angle pos * rope_theta^(-2i/D); the rotation is evaluated in FP64 and
+ * rounded once to bf16 (round to nearest even), so results are bit-exact.
+ * If q_in and q_out are both non-NULL the same rotation is applied out of
+ * place to the queries: q_out[b][j] = RoPE(q_in[b][j], positions[b]) for
+ * j < num_q_heads (q_in/q_out: [batch][num_q_heads][head_dim]); otherwise
+ * both must be NULL.
+ *
+ *   k_new, v_new  [batch][num_kv_heads][head_dim] bf16, read only
+ *   pool          the shared page pool (layout above); written in place at
+ *                 one slot per sequence
+ *   positions     int32 [batch]
+ *   dev_err       optional int32, bits PKV_DEVERR_PAGE / _POSITION
+ * A sequence with a bad position or page is skipped (its query rotation is
+ * still written).  Two sequences must not name the same (page, slot).
+ */
+PKV_API int pkv_kv_append(const pkv_bf16* k_new, const pkv_bf16* v_new,
+                          pkv_bf16* pool, int64_t num_pages,
+                          const int32_t* block_table, int max_blocks,
+                          const int32_t* positions, int batch,
+                          int num_kv_heads, int head_dim, int page_size,
+                          double rope_theta, const pkv_bf16* q_in,
+                          pkv_bf16* q_out, int num_q_heads, int32_t* dev_err,
+                          pkv_stream_t stream);
+
+/*
+ * pkv_paged_decode_attention -- paged decode attention with an FP32 online
+ * softmax ("これまでの進捗", paged decode attention item).
+ *
+ * For every sequence b and query head j, with g = j / (Hq/Hkv) and
+ * L = seq_lens[b]:
+ *   out[b][j][:] = sum_{t<L} softmax_t(scale * q[b][j] . K_t) V_t
+ * where K_t, V_t are row (t % page_size) of kv head g in page
+ * block_table[b*max_blocks + t/page_size].  L counts the token appended in
+ * the same step.  L = 0 gives a zero row.  Scores and the softmax are FP32;
+ * the output is rounded to bf16 (nearest even).
+ *
+ *   q          [batch][num_q_heads][head_dim] bf16 (already rotated)
+ *   seq_lens   int32 [batch]
+ *   out        [batch][num_q_heads][head_dim] bf16, written
+ *   workspace  device scratch for split-K partials, at least
+ *              pkv_workspace_bytes(...) bytes, 16-byte aligned; may be NULL
+ *              when that size is 0.  Its contents need no initialisation and
+ *              are garbage afterwards.
+ *   num_splits 0 = choose automatically; S > 0 = split each sequence's pages
+ *              into at most S contiguous logical ranges, combined by a merge
+ *              kernel.  The same inputs and num_splits give bit-identical
+ *              outputs on every run.
+ *   dev_err    optional int32, bits PKV_DEVERR_PAGE / _SEQLEN / _TIMEOUT
+ * Pages of a sequence with a bad id are skipped; a length outside the block
+ * table is clamped to [0, max_blocks*page_size].
+ */
+PKV_API int pkv_paged_decode_attention(
+    const pkv_bf16* q, const pkv_bf16* pool, int64_t num_pages,
+    const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+    int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+    float scale, pkv_bf16* out, void* workspace, size_t workspace_bytes,
+    int num_splits, int32_t* dev_err, pkv_stream_t stream);
+
+/*
+ * Bytes of workspace pkv_paged_decode_attention needs for these sizes and
+ * num_splits (0 = the automatic choice on the current device).  Returns 0
+ * when no split is needed, and (size_t)-1 for invalid sizes.
+ */
+PKV_API size_t pkv_workspace_bytes(int batch, int num_q_heads,
+                                   int num_kv_heads, int head_dim,
+                                   int max_blocks, int num_splits);
+
+/*
+ * The number of logical page ranges per sequence that
+ * pkv_paged_decode_attention will use for these sizes (resolving
+ * num_splits = 0 on the current device), or -1 for invalid sizes.
+ */
+PKV_API int pkv_plan_splits(int batch, int num_kv_heads, int max_blocks,
+                            int num_splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,191 @@
+"""Thin ctypes binding of libpkv.so (include/pkv.h).
+
+Argument marshalling only: tensors are checked for dtype, shape, device and
+contiguity, then their device pointers go to the C entry points with the
+current CUDA stream.  Every step of the decode path runs in the library's
+kernels; there is no Python or CPU fallback -- importing this module without
+the built library raises ImportError, and a failing call raises PkvError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK = 0
+PKV_EINVAL = 1
+PKV_EUNSUPPORTED = 2
+PKV_EWORKSPACE = 3
+PKV_ECUDA = 4
+PKV_EALIGN = 5
+
+DEVERR_PAGE = 1
+DEVERR_SEQLEN = 2
+DEVERR_POSITION = 4
+DEVERR_TIMEOUT = 8
+
+NUM_Q_HEADS = 32
+NUM_KV_HEADS = 8
+HEAD_DIM = 64
+PAGE_SIZE = 16
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {strerror(status)} (status {status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libpkv.so not found at {LIB_PATH}; build it with "
+            "`python -m paged_kv_decode_04_gb300.build` (needs nvcc for sm_103a)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, f64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                  ctypes.c_float, ctypes.c_double, ctypes.c_size_t)
+    L.pkv_abi_version.argtypes = []
+    L.pkv_abi_version.restype = i32
+    L.pkv_strerror.argtypes = [i32]
+    L.pkv_strerror.restype = ctypes.c_char_p
+    L.pkv_plan_splits.argtypes = [i32, i32, i32, i32]
+    L.pkv_plan_splits.restype = i32
+    L.pkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.pkv_workspace_bytes.restype = sz
+    L.pkv_kv_append.argtypes = [vp, vp, vp, i64, vp, i32, vp, i32, i32, i32, i32, f64, vp, vp,
+                                i32, vp, vp]
+    L.pkv_kv_append.restype = i32
+    L.pkv_paged_decode_attention.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32, i32,
+                                             f32, vp, vp, sz, i32, vp, vp]
+    L.pkv_paged_decode_attention.restype = i32
+    return L
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def abi_version() -> int:
+    return _lib.pkv_abi_version()
+
+
+def strerror(status: int) -> str:
+    return _lib.pkv_strerror(status).decode()
+
+
+def plan_splits(batch: int, max_blocks: int, num_splits: int = 0,
+                num_kv_heads: int = NUM_KV_HEADS) -> int:
+    return _lib.pkv_plan_splits(batch, num_kv_heads, max_blocks, num_splits)
+
+
+def workspace_bytes(batch: int, max_blocks: int, num_splits: int = 0, *,
+                    num_q_heads: int = NUM_Q_HEADS, num_kv_heads: int = NUM_KV_HEADS,
+                    head_dim: int = HEAD_DIM) -> int:
+    n = _lib.pkv_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
+                                 num_splits)
+    if n == ctypes.c_size_t(-1).value:
+        raise PkvError(PKV_EINVAL, "pkv_workspace_bytes")
+    return n
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, ndim=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _pool_pages(pool):
+    _check(pool, "pool", torch.bfloat16)
+    if pool.dim() != 5 or tuple(pool.shape[1:]) != (2, PAGE_SIZE, NUM_KV_HEADS, HEAD_DIM):
+        raise ValueError("pool must be [num_pages][2][16][8][64] bf16")
+    return pool.shape[0]
+
+
+def kv_append(k_new, v_new, pool, block_table, positions, *, rope_theta: float = 500000.0,
+              q_in=None, q_out=None, dev_err=None, stream=None) -> None:
+    """Append one token per sequence: pool[bt[b][pos/16]][K|V][pos%16] = RoPE(k), v."""
+    num_pages = _pool_pages(pool)
+    dev = pool.device
+    _check(k_new, "k_new", torch.bfloat16, 3, dev)
+    _check(v_new, "v_new", torch.bfloat16, 3, dev)
+    _check(block_table, "block_table", torch.int32, 2, dev)
+    _check(positions, "positions", torch.int32, 1, dev)
+    B, Hkv, D = k_new.shape
+    if v_new.shape != k_new.shape or positions.shape[0] != B or block_table.shape[0] != B:
+        raise ValueError("k_new, v_new, positions and block_table disagree on the batch")
+    Hq = 0
+    if q_in is not None or q_out is not None:
+        _check(q_in, "q_in", torch.bfloat16, 3, dev)
+        _check(q_out, "q_out", torch.bfloat16, 3, dev)
+        if q_in.shape != q_out.shape or q_in.shape[0] != B:
+            raise ValueError("q_in / q_out shape mismatch")
+        Hq = q_in.shape[1]
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, None, dev)
+    rc = _lib.pkv_kv_append(_ptr(k_new), _ptr(v_new), _ptr(pool), num_pages, _ptr(block_table),
+                            block_table.shape[1], _ptr(positions), B, Hkv, D, PAGE_SIZE,
+                            float(rope_theta), _ptr(q_in), _ptr(q_out), Hq, _ptr(dev_err),
+                            _stream(stream))
+    if rc != PKV_OK:
+        raise PkvError(rc, "pkv_kv_append")
+
+
+def paged_decode_attention(q, pool, block_table, seq_lens, out=None, *, scale: float = None,
+                           workspace=None, num_splits: int = 0, dev_err=None,
+                           stream=None) -> torch.Tensor:
+    """out[b][j] = softmax(scale * q[b][j] . K) V over the sequence's pages."""
+    num_pages = _pool_pages(pool)
+    dev = pool.device
+    _check(q, "q", torch.bfloat16, 3, dev)
+    _check(block_table, "block_table", torch.int32, 2, dev)
+    _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    if seq_lens.shape[0] != B or block_table.shape[0] != B:
+        raise ValueError("q, seq_lens and block_table disagree on the batch")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    if scale is None:
+        scale = D ** -0.5
+    max_blocks = block_table.shape[1]
+    need = workspace_bytes(B, max_blocks, num_splits, num_q_heads=Hq, head_dim=D)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the pool's device")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, None, dev)
+    rc = _lib.pkv_paged_decode_attention(
+        _ptr(q), _ptr(pool), num_pages, _ptr(block_table), max_blocks, _ptr(seq_lens), B, Hq,
+        NUM_KV_HEADS, D, PAGE_SIZE, float(scale), _ptr(out), _ptr(workspace), ws_bytes,
+        int(num_splits), _ptr(dev_err), _stream(stream))
+    if rc != PKV_OK:
+        raise PkvError(rc, "pkv_paged_decode_attention")
+    return out

@@ -1,0 +1,124 @@
+// kv_append.cu -- decode-time KV append with rotate-half RoPE.
+//
+// Tiny-vLLM README ("Hours of YouTube and 85 handtyped pages of notes on LLM
+// Inference - Start here"), section "これまでの進捗", KV page pool item: each
+// decode step adds one new token per sequence at its absolute RoPE position
+// into the sequence's page slot of the shared BF16 pool.
+//
+// One CTA per sequence.  Warp 0 evaluates the 32 (cos, sin) pairs of the
+// token's position in FP64 once; all 256 threads then rotate the 8 kv heads'
+// keys (one thread per (head, frequency) pair), copy the values, and, when
+// asked, rotate the 32 query heads out of place.  The rotation is FP64 with
+// separately rounded products (no contraction) and one rounding to bf16, so
+// the stored keys are a deterministic function of the inputs.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kAppendThreads = 256;
+constexpr int kHalf = kHeadDim / 2;
+
+// (x1, x2) -> (x1*c - x2*s, x2*c + x1*s), each product rounded in FP64,
+// then one rounding to bf16.
+__device__ __forceinline__ void rotate_pair(uint16_t h1, uint16_t h2, double c,
+                                            double s, uint16_t* o1,
+                                            uint16_t* o2) {
+  const double x1 = static_cast<double>(bf16_to_float(h1));
+  const double x2 = static_cast<double>(bf16_to_float(h2));
+  const double y1 = __dsub_rn(__dmul_rn(x1, c), __dmul_rn(x2, s));
+  const double y2 = __dadd_rn(__dmul_rn(x2, c), __dmul_rn(x1, s));
+  *o1 = double_to_bf16_rne(y1);
+  *o2 = double_to_bf16_rne(y2);
+}
+
+__global__ void __launch_bounds__(kAppendThreads)
+    kv_append_kernel(const uint16_t* __restrict__ k_new,
+                     const uint16_t* __restrict__ v_new,
+                     uint16_t* __restrict__ pool, int64_t num_pages,
+                     const int32_t* __restrict__ block_table, int max_blocks,
+                     const int32_t* __restrict__ positions, RopeFreqs freqs,
+                     const uint16_t* __restrict__ q_in,
+                     uint16_t* __restrict__ q_out, int32_t* dev_err) {
+  __shared__ double s_cos[kHalf];
+  __shared__ double s_sin[kHalf];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int32_t pos = positions[b];
+  const bool pos_ok = pos >= 0 && pos < max_blocks * kPageSize;
+
+  if (tid < kHalf) {
+    const double angle = __dmul_rn(static_cast<double>(pos), freqs.inv_freq[tid]);
+    double sn, cs;
+    sincos(angle, &sn, &cs);
+    s_cos[tid] = cs;
+    s_sin[tid] = sn;
+  }
+  __syncthreads();
+
+  // Optional out-of-place query rotation: 32 heads x 32 pairs, 4 per thread.
+  if (q_in != nullptr) {
+    const int64_t qbase = static_cast<int64_t>(b) * kNumQHeads * kHeadDim;
+#pragma unroll
+    for (int k = 0; k < (kNumQHeads * kHalf) / kAppendThreads; ++k) {
+      const int idx = tid + k * kAppendThreads;
+      const int j = idx / kHalf, i = idx % kHalf;
+      const int64_t o = qbase + j * kHeadDim + i;
+      uint16_t y1, y2;
+      rotate_pair(q_in[o], q_in[o + kHalf], s_cos[i], s_sin[i], &y1, &y2);
+      q_out[o] = y1;
+      q_out[o + kHalf] = y2;
+    }
+  }
+
+  if (!pos_ok) {
+    if (tid == 0) record_error(dev_err, kErrPosition);
+    return;
+  }
+  const int32_t page =
+      block_table[static_cast<int64_t>(b) * max_blocks + pos / kPageSize];
+  if (page < 0 || page >= num_pages) {
+    if (tid == 0) record_error(dev_err, kErrPage);
+    return;
+  }
+  const int slot = pos % kPageSize;
+  const int64_t row = kNumKvHeads * kHeadDim;  // elements per (kv, slot)
+  uint16_t* k_dst = pool + ((static_cast<int64_t>(page) * 2 + 0) * kPageSize + slot) * row;
+  uint16_t* v_dst = pool + ((static_cast<int64_t>(page) * 2 + 1) * kPageSize + slot) * row;
+  const int64_t src = static_cast<int64_t>(b) * row;
+
+  // Keys: thread (h, i) rotates pair i of kv head h.
+  {
+    const int h = tid / kHalf, i = tid % kHalf;
+    const int64_t o = h * kHeadDim + i;
+    uint16_t y1, y2;
+    rotate_pair(k_new[src + o], k_new[src + o + kHalf], s_cos[i], s_sin[i], &y1, &y2);
+    k_dst[o] = y1;
+    k_dst[o + kHalf] = y2;
+  }
+  // Values: 512 bf16 = 256 words, one per thread.
+  reinterpret_cast<uint32_t*>(v_dst)[tid] =
+      reinterpret_cast<const uint32_t*>(v_new + src)[tid];
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new,
+                             uint16_t* pool, int64_t num_pages,
+                             const int32_t* block_table, int max_blocks,
+                             const int32_t* positions, int batch,
+                             const RopeFreqs& freqs, const uint16_t* q_in,
+                             uint16_t* q_out, int32_t* dev_err,
+                             cudaStream_t stream) {
+  kv_append_kernel<<<batch, kAppendThreads, 0, stream>>>(
+      k_new, v_new, pool, num_pages, block_table, max_blocks, positions, freqs,
+      q_in, q_out, dev_err);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,250 @@
+// pkv_api.cu -- the extern "C" boundary of libpkv (declared in include/pkv.h):
+// argument checks, the split plan, TMA descriptor encoding, and launches.
+// No entry point allocates, frees or synchronizes; everything is enqueued on
+// the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+using pkv::kHeadDim;
+using pkv::kNumKvHeads;
+using pkv::kNumQHeads;
+using pkv::kPageSize;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// SM count of the current device, cached per device (-1 when unavailable).
+int current_sm_count() {
+  static std::atomic<int> cache[64] = {};  // 0 = not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (dev < 0 || dev >= 64) return -1;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Split plan: S logical page ranges of pages_per_split pages per sequence.
+// Explicit S is honoured (capped by the table width); S = 0 aims for about
+// four CTAs per SM across (sequence, kv head, split) while keeping at least
+// four pages per range.
+bool make_plan(int batch, int max_blocks, int num_splits, pkv::SplitPlan* plan) {
+  int S;
+  if (num_splits > 0) {
+    S = num_splits;
+  } else {
+    const int sms = current_sm_count();
+    if (sms <= 0) return false;
+    const long long units = static_cast<long long>(batch) * kNumKvHeads;
+    const long long target = 4LL * sms;
+    S = static_cast<int>((target + units - 1) / units);
+    const int cap = (max_blocks + 3) / 4;
+    if (S > cap) S = cap;
+    if (S < 1) S = 1;
+  }
+  if (S > max_blocks) S = max_blocks;
+  int pps = (max_blocks + S - 1) / S;
+  if (pps > pkv::max_pages_per_split()) pps = pkv::max_pages_per_split();
+  plan->pages_per_split = pps;
+  plan->num_splits = (max_blocks + pps - 1) / pps;
+  return true;
+}
+
+bool supported_dims(int num_q_heads, int num_kv_heads, int head_dim, int page_size) {
+  return num_q_heads == kNumQHeads && num_kv_heads == kNumKvHeads &&
+         head_dim == kHeadDim && page_size == kPageSize;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    fn.store(f, std::memory_order_release);
+  }
+  return f;
+}
+
+// TMA descriptor of the pool viewed as [num_pages][32 rows (K|V x slot)][512]
+// bf16 with a 64 x 32 x 1 box (one kv head's K and V rows of one page),
+// 128-byte swizzled.  Cached per thread for the last (device, pool, pages).
+bool pool_tensor_map(const void* pool, int64_t num_pages, CUtensorMap* out) {
+  struct Entry {
+    int device = -1;
+    const void* pool = nullptr;
+    int64_t num_pages = 0;
+    CUtensorMap map;
+  };
+  thread_local Entry cached;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cached.device == dev && cached.pool == pool && cached.num_pages == num_pages) {
+    *out = cached.map;
+    return true;
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kNumKvHeads * kHeadDim),
+                              static_cast<cuuint64_t>(2 * kPageSize),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[2] = {
+      static_cast<cuuint64_t>(kNumKvHeads * kHeadDim * 2),
+      static_cast<cuuint64_t>(2 * kPageSize * kNumKvHeads * kHeadDim * 2)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim),
+                             static_cast<cuuint32_t>(2 * kPageSize), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMap m;
+  const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool),
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  cached.device = dev;
+  cached.pool = pool;
+  cached.num_pages = num_pages;
+  cached.map = m;
+  *out = m;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+PKV_API int pkv_abi_version(void) { return 1; }
+
+PKV_API const char* pkv_strerror(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_EINVAL: return "invalid argument (null pointer, bad size or bad scale/theta)";
+    case PKV_EUNSUPPORTED: return "unsupported geometry (needs 32 q heads, 8 kv heads, head dim 64, page size 16)";
+    case PKV_EWORKSPACE: return "workspace missing or smaller than pkv_workspace_bytes()";
+    case PKV_ECUDA: return "CUDA runtime error (launch failed or no usable device)";
+    case PKV_EALIGN: return "pointer alignment requirement violated";
+    default: return "unknown status";
+  }
+}
+
+PKV_API int pkv_plan_splits(int batch, int num_kv_heads, int max_blocks, int num_splits) {
+  if (batch < 1 || max_blocks < 1 || num_splits < 0 || num_kv_heads != kNumKvHeads) return -1;
+  pkv::SplitPlan plan;
+  if (!make_plan(batch, max_blocks, num_splits, &plan)) return -1;
+  return plan.num_splits;
+}
+
+PKV_API size_t pkv_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int max_blocks, int num_splits) {
+  if (batch < 0 || max_blocks < 1 || num_splits < 0 ||
+      !supported_dims(num_q_heads, num_kv_heads, head_dim, kPageSize))
+    return static_cast<size_t>(-1);
+  if (batch == 0) return 0;
+  pkv::SplitPlan plan;
+  if (!make_plan(batch, max_blocks, num_splits, &plan)) return static_cast<size_t>(-1);
+  return pkv::workspace_bytes_for(batch, num_q_heads, head_dim, plan);
+}
+
+PKV_API int pkv_kv_append(const pkv_bf16* k_new, const pkv_bf16* v_new, pkv_bf16* pool,
+                          int64_t num_pages, const int32_t* block_table, int max_blocks,
+                          const int32_t* positions, int batch, int num_kv_heads,
+                          int head_dim, int page_size, double rope_theta,
+                          const pkv_bf16* q_in, pkv_bf16* q_out, int num_q_heads,
+                          int32_t* dev_err, pkv_stream_t stream) {
+  if (!k_new || !v_new || !pool || !block_table || !positions) return PKV_EINVAL;
+  if (batch < 0 || num_pages < 1 || num_pages > INT32_MAX || max_blocks < 1) return PKV_EINVAL;
+  if ((q_in == nullptr) != (q_out == nullptr)) return PKV_EINVAL;
+  if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return PKV_EINVAL;
+  if (num_kv_heads != kNumKvHeads || head_dim != kHeadDim || page_size != kPageSize)
+    return PKV_EUNSUPPORTED;
+  if (q_in != nullptr && num_q_heads != kNumQHeads) return PKV_EUNSUPPORTED;
+  if (batch > INT32_MAX / 2) return PKV_EINVAL;
+  if (!aligned(pool, 16) || !aligned(v_new, 4) || !aligned(k_new, 2) || !aligned(q_in, 2) ||
+      !aligned(q_out, 2) || !aligned(dev_err, 4))
+    return PKV_EALIGN;
+  if (batch == 0) return PKV_OK;
+  pkv::RopeFreqs freqs;
+  for (int i = 0; i < kHeadDim / 2; ++i)
+    freqs.inv_freq[i] = pow(rope_theta, -(2.0 * i) / static_cast<double>(kHeadDim));
+  const cudaError_t err = pkv::launch_kv_append(
+      k_new, v_new, pool, num_pages, block_table, max_blocks, positions, batch, freqs, q_in,
+      q_out, dev_err, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+PKV_API int pkv_paged_decode_attention(const pkv_bf16* q, const pkv_bf16* pool,
+                                       int64_t num_pages, const int32_t* block_table,
+                                       int max_blocks, const int32_t* seq_lens, int batch,
+                                       int num_q_heads, int num_kv_heads, int head_dim,
+                                       int page_size, float scale, pkv_bf16* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       int num_splits, int32_t* dev_err,
+                                       pkv_stream_t stream) {
+  if (!q || !pool || !block_table || !seq_lens || !out) return PKV_EINVAL;
+  if (batch < 0 || batch > 65535 || num_pages < 1 || num_pages > INT32_MAX ||
+      max_blocks < 1 || max_blocks > (INT32_MAX / kPageSize) || num_splits < 0)
+    return PKV_EINVAL;
+  if (!(scale > 0.f) || !isfinite(scale)) return PKV_EINVAL;
+  if (!supported_dims(num_q_heads, num_kv_heads, head_dim, page_size)) return PKV_EUNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(out, 4) || !aligned(workspace, 16) ||
+      !aligned(dev_err, 4))
+    return PKV_EALIGN;
+  if (batch == 0) return PKV_OK;
+  pkv::SplitPlan plan;
+  if (!make_plan(batch, max_blocks, num_splits, &plan)) return PKV_ECUDA;
+  const size_t need = pkv::workspace_bytes_for(batch, num_q_heads, head_dim, plan);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
+  CUtensorMap map;
+  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
+  pkv::AttnArgs args;
+  args.q = q;
+  args.block_table = block_table;
+  args.seq_lens = seq_lens;
+  args.out = out;
+  float* ws = static_cast<float*>(workspace);
+  const size_t acc_elems = static_cast<size_t>(batch) * num_q_heads * plan.num_splits * head_dim;
+  args.part_acc = need > 0 ? ws : nullptr;
+  args.part_ml = need > 0 ? ws + acc_elems : nullptr;
+  args.dev_err = dev_err;
+  args.num_pages = num_pages;
+  args.max_blocks = max_blocks;
+  args.batch = batch;
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.plan = plan;
+  const cudaError_t err =
+      pkv::launch_paged_decode_attention(map, args, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // extern "C"

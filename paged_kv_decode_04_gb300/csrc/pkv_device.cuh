@@ -1,0 +1,202 @@
+// pkv_device.cuh -- sm_103a device helpers for libpkv: shared-memory
+// mbarriers, TMA tensor copies, packed FP32 arithmetic and bf16 bit tricks.
+// Everything here is inline PTX or plain integer/float code; no library
+// kernels are used on the decode path.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// Upper bound for one in-kernel wait on a page copy: past it the kernel
+// records kErrTimeout and stops waiting instead of spinning forever.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ void record_error(int32_t* dev_err, int bits) {
+  if (dev_err != nullptr) atomicOr(dev_err, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------ mbarrier --
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+               : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar,
+                                                      uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+          bar),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for phase `parity` of a barrier, giving up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar,
+                                                  uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ----------------------------------------------------------------- TMA --
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// 3-D tiled tensor copy global -> shared, completion signalled on `bar`
+// (transaction bytes).  Coordinates are element indices, innermost first.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map,
+                                            uint32_t bar, int x, int y, int z,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::"
+      "bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read exactly once per step (the K/V pages).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ----------------------------------------------------- shared memory I/O --
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// ------------------------------------------------------- packed FP32 ops --
+
+// d = a * b + c on two FP32 lanes at once (sm_100+ packed FMA).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  unsigned long long ra, rb, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
+// 2^x on the special-function unit (relative error ~2^-22; ex2(-inf) = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// --------------------------------------------------------------- bf16 --
+
+// Two bf16 packed in one 32-bit word -> two floats (low half first).
+// A bf16 is the upper half of a binary32, so widening is a shift / mask.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ float bf16_to_float(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// binary32 -> bf16, round to nearest even (NaN stays a quiet NaN).
+__device__ __forceinline__ uint16_t float_to_bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return static_cast<uint16_t>((u >> 16) | 0x0040u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// binary64 -> bf16 in ONE rounding step (round to nearest even), done on the
+// bit pattern: keep the sign, rebias the exponent from 1023 to 127, keep 7
+// mantissa bits and round on the 45 discarded ones; values below the bf16
+// normal range are shifted into the subnormal grid (spacing 2^-133) first.
+__device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
+  const uint64_t u = static_cast<uint64_t>(__double_as_longlong(x));
+  const uint16_t sign = static_cast<uint16_t>((u >> 48) & 0x8000u);
+  const uint64_t a = u & 0x7FFFFFFFFFFFFFFFull;
+  if (a > 0x7FF0000000000000ull) return sign | 0x7FC0u;  // NaN
+  if (a == 0x7FF0000000000000ull) return sign | 0x7F80u;  // inf
+  const int e = static_cast<int>(a >> 52) - 1023;         // unbiased exponent
+  if (e > 127) return sign | 0x7F80u;                      // overflow
+  if (e >= -126) {
+    // bits [51:0] mantissa; rebias exponent into a 60-bit field so that the
+    // bf16 pattern is (r >> 45) and a carry runs into the exponent (or inf).
+    uint64_t r = (static_cast<uint64_t>(e + 127) << 52) | (a & 0x000FFFFFFFFFFFFFull);
+    r += 0x00000FFFFFFFFFFFull + ((r >> 45) & 1ull);
+    return sign | static_cast<uint16_t>(r >> 45);
+  }
+  if ((a >> 52) == 0) return sign;  // binary64 subnormal: far below 2^-134
+  // subnormal bf16: value = sig * 2^(e-52), grid spacing 2^-133
+  const uint64_t sig = (a & 0x000FFFFFFFFFFFFFull) | (1ull << 52);
+  const int shift = -e - 81;  // = 52 - (e + 133)
+  if (shift >= 54) return sign;
+  uint64_t q = sig >> shift;
+  const uint64_t rem = sig & ((1ull << shift) - 1ull);
+  const uint64_t half = 1ull << (shift - 1);
+  if (rem > half || (rem == half && (q & 1ull))) ++q;
+  return sign | static_cast<uint16_t>(q);
+}
+
+}  // namespace pkv

@@ -1,0 +1,70 @@
+// pkv_internal.h -- launchers shared between the C-ABI layer and the kernels
+// of libpkv (not part of the public interface).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Fixed model geometry (Llama 3.2 1B as used by the Tiny-vLLM engine).
+constexpr int kHeadDim = 64;
+constexpr int kPageSize = 16;
+constexpr int kNumKvHeads = 8;
+constexpr int kNumQHeads = 32;
+constexpr int kGroup = kNumQHeads / kNumKvHeads;  // 4 query rows per kv head
+
+// Device error bits (mirror PKV_DEVERR_* in pkv.h).
+constexpr int kErrPage = 1;
+constexpr int kErrSeqLen = 2;
+constexpr int kErrPosition = 4;
+constexpr int kErrTimeout = 8;
+
+// inv_freq[i] = theta^(-2i/64) for the 32 rotation pairs, passed by value.
+struct RopeFreqs {
+  double inv_freq[32];
+};
+
+// Split plan of one attention call.
+struct SplitPlan {
+  int num_splits;       // grid extent of the split dimension (S)
+  int pages_per_split;  // logical pages per range
+};
+
+cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new,
+                             uint16_t* pool, int64_t num_pages,
+                             const int32_t* block_table, int max_blocks,
+                             const int32_t* positions, int batch,
+                             const RopeFreqs& freqs, const uint16_t* q_in,
+                             uint16_t* q_out, int32_t* dev_err,
+                             cudaStream_t stream);
+
+struct AttnArgs {
+  const uint16_t* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  uint16_t* out;
+  float* part_acc;  // [B][Hq][S][D] fp32, unnormalised
+  float* part_ml;   // [B][Hq][S][2] fp32, (max in log2 units, sum)
+  int32_t* dev_err;
+  int64_t num_pages;
+  int max_blocks;
+  int batch;
+  float scale_log2;  // softmax scale * log2(e)
+  SplitPlan plan;
+};
+
+cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
+                                          const AttnArgs& args,
+                                          cudaStream_t stream);
+
+// Largest logical page range one attention CTA handles.
+int max_pages_per_split();
+
+// Workspace bytes for a plan (0 when nothing is split).
+size_t workspace_bytes_for(int batch, int num_q_heads, int head_dim,
+                           const SplitPlan& plan);
+
+}  // namespace pkv

@@ -1,0 +1,106 @@
+"""The C-ABI library loads, exports what include/pkv.h declares, and rejects bad
+arguments on the host before anything touches a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_decode_04_gb300 import build
+    path = build.build()
+    L = ctypes.CDLL(path)
+    from paged_kv_decode_04_gb300 import binding  # sets prototypes on its own handle
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_symbols())
+    assert {"pkv_kv_append", "pkv_paged_decode_attention", "pkv_workspace_bytes",
+            "pkv_strerror", "pkv_abi_version", "pkv_plan_splits"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_strerror_and_version(lib):
+    from paged_kv_decode_04_gb300 import binding
+    assert binding.abi_version() == 1
+    for s in range(0, 7):
+        assert isinstance(binding.strerror(s), str) and binding.strerror(s)
+    assert binding.strerror(0) == "ok"
+
+
+def test_explicit_split_plans(lib):
+    from paged_kv_decode_04_gb300 import binding
+    assert binding.plan_splits(256, 128, 1) == 1
+    assert binding.plan_splits(1, 128, 32) == 32
+    assert binding.plan_splits(1, 128, 7) == 7        # ceil(128/7)=19 pages per range -> 7 ranges
+    assert binding.plan_splits(1, 128, 500) == 128    # at most one page per range
+    assert binding.plan_splits(8, 128, 10) == 10
+    assert binding.plan_splits(0, 128, 1) == -1
+    assert binding.workspace_bytes(1, 128, 1) == 0
+    assert binding.workspace_bytes(2, 128, 4) == 2 * 32 * 4 * (64 + 2) * 4
+
+
+# Fake, never-dereferenced device addresses: every call below must fail its
+# host-side checks before anything is enqueued.
+A = ctypes.c_void_p(0x10000)
+
+
+def attn(lib, **kw):
+    args = dict(q=A, pool=A, num_pages=64, bt=A, max_blocks=128, lens=A, batch=1, hq=32, hkv=8,
+                d=64, ps=16, scale=0.125, out=A, ws=None, ws_bytes=0, splits=1, err=None,
+                stream=None)
+    args.update(kw)
+    return lib.pkv_paged_decode_attention(*args.values())
+
+
+def test_attention_argument_errors(lib):
+    from paged_kv_decode_04_gb300 import binding as B
+    assert attn(lib, q=None) == B.PKV_EINVAL
+    assert attn(lib, out=None) == B.PKV_EINVAL
+    assert attn(lib, batch=-1) == B.PKV_EINVAL
+    assert attn(lib, num_pages=0) == B.PKV_EINVAL
+    assert attn(lib, scale=0.0) == B.PKV_EINVAL
+    assert attn(lib, scale=float("nan")) == B.PKV_EINVAL
+    assert attn(lib, splits=-1) == B.PKV_EINVAL
+    assert attn(lib, hq=16) == B.PKV_EUNSUPPORTED
+    assert attn(lib, d=128) == B.PKV_EUNSUPPORTED
+    assert attn(lib, ps=32) == B.PKV_EUNSUPPORTED
+    assert attn(lib, q=ctypes.c_void_p(0x10002)) == B.PKV_EALIGN
+    assert attn(lib, pool=ctypes.c_void_p(0x10008)) == B.PKV_EALIGN
+    assert attn(lib, splits=4, ws=None) == B.PKV_EWORKSPACE
+    assert attn(lib, splits=4, ws=A, ws_bytes=100) == B.PKV_EWORKSPACE
+    assert attn(lib, batch=0) == B.PKV_OK      # nothing to do, nothing enqueued
+
+
+def append(lib, **kw):
+    args = dict(k=A, v=A, pool=A, num_pages=64, bt=A, max_blocks=128, pos=A, batch=1, hkv=8,
+                d=64, ps=16, theta=500000.0, q_in=None, q_out=None, hq=0, err=None, stream=None)
+    args.update(kw)
+    return lib.pkv_kv_append(*args.values())
+
+
+def test_append_argument_errors(lib):
+    from paged_kv_decode_04_gb300 import binding as B
+    assert append(lib, k=None) == B.PKV_EINVAL
+    assert append(lib, pos=None) == B.PKV_EINVAL
+    assert append(lib, theta=-1.0) == B.PKV_EINVAL
+    assert append(lib, q_in=A) == B.PKV_EINVAL           # q_in without q_out
+    assert append(lib, hkv=4) == B.PKV_EUNSUPPORTED
+    assert append(lib, q_in=A, q_out=A, hq=8) == B.PKV_EUNSUPPORTED
+    assert append(lib, v=ctypes.c_void_p(0x10002)) == B.PKV_EALIGN
+    assert append(lib, batch=0) == B.PKV_OK
