@@ -16,13 +16,18 @@
 //    ring with 3-D TMA copies (one 4 KiB box per page: the 16 K rows and the
 //    16 V rows of head g, 128 B each, 128-byte swizzled) completing on one
 //    mbarrier per stage, kStages pages ahead of the math.
-//  * Math per page, lane = (tg = lane & 7, dg = lane >> 3): tokens tg and
-//    tg + 8, head dims [16 dg, 16 dg + 16).  QK^T partial sums use packed FP32
-//    FMAs; the 8 partial scores are reduced across the 4 d-groups with a
-//    transposing butterfly that leaves each lane two finished scores.  Each
-//    token group tg keeps its own running max / sum / accumulator (an
-//    independent online-softmax stream); the streams of all groups and warps
-//    are merged once at the end through shared memory.
+//  * Math per page on the tensor cores (mma.sync m16n8k16, bf16 in, FP32
+//    accumulate): S^T = K Q^T with the 16 page tokens as M and the 4 query
+//    rows (padded to 8) as N, then O^T += V^T P^T with the 64 head dims as M.
+//    K comes from shared memory through ldmatrix, V through ldmatrix.trans;
+//    the probabilities P enter the second product as two bf16 terms
+//    (hi + lo), which keeps about 16 significant bits of every weight.
+//  * Softmax: scores, running max, exponentials and sums stay in FP32.  The
+//    running max is a lazily updated reference: a page only forces a rescale
+//    of the accumulators when one of its scores exceeds the reference by more
+//    than kRescaleLog2 (so the weights stay <= 2^kRescaleLog2); the final
+//    normalisation by the running sum makes the result independent of the
+//    reference, exactly as in the textbook online softmax.
 //  * With more than one split per sequence the CTA writes an unnormalised
 //    (max, sum, acc) partial and a small merge kernel combines the splits of
 //    each (b, j) in fixed order, so results are run-to-run deterministic.
@@ -47,19 +52,19 @@ constexpr int kRowBytes = kHeadDim * 2;                   // 128 B: one head's r
 constexpr int kTileBytes = 2 * kPageSize * kRowBytes;     // 4 KiB: K then V
 constexpr int kStageBytes = kWarps * kStages * kTileBytes;
 constexpr int kBarBytes = kWarps * kStages * 8;
-constexpr int kStreams = kWarps * 8;  // online-softmax streams per CTA
+// A page rescales the accumulators only when a score exceeds the running
+// reference maximum by more than this many powers of two.
+constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxPagesPerSplit = 1024;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-static_assert(kStreams * (2 * kGroup + kGroup * kHeadDim) * 4 <= kStageBytes,
+static_assert(kWarps * (2 * kGroup + kGroup * kHeadDim) * 4 <= kStageBytes,
               "end-of-CTA merge scratch must fit in the stage buffers");
 
 __host__ __device__ constexpr size_t smem_bytes(int pages_per_split) {
   return 1024 /* alignment slack */ + kStageBytes + kBarBytes +
          static_cast<size_t>(pages_per_split) * 4;
 }
-
-__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
 
 __global__ void __launch_bounds__(kThreads, 3)
     paged_decode_kernel(const __grid_constant__ CUtensorMap pool_map,
@@ -107,32 +112,38 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   __syncthreads();
 
-  // ---- lane geometry and the 4 query rows (pre-scaled into log2 units)
-  const int tg = lane & 7;
-  const int dg = lane >> 3;
-  const bool hi4 = (lane & 16) != 0;  // which of the two tokens after reduction
-  const bool hi3 = (lane & 8) != 0;   // which row pair after reduction
-  float2 qf[kGroup][8];
+  // ---- lane geometry: mma fragment coordinates and ldmatrix row addresses
+  const int fg = lane >> 2;  // fragment group: token (S^T) / head dim (O^T) row
+  const int ft = lane & 3;   // thread in group: query rows 2ft, 2ft + 1
+  const int lr = lane & 7;   // ldmatrix: row within an 8x8 matrix
+  const int li = lane >> 3;  // ldmatrix: which of the four matrices
+  // Q^T as the B operand of S^T = K Q^T: columns 0..3 are the group's query
+  // rows, columns 4..7 are zero padding.
+  uint32_t qb[4][2];
   {
-    const uint16_t* qrow =
-        a.q + (static_cast<int64_t>(b) * kNumQHeads + g * kGroup) * kHeadDim + 16 * dg;
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(
+        a.q + (static_cast<int64_t>(b) * kNumQHeads + g * kGroup + (fg & 3)) * kHeadDim);
 #pragma unroll
-    for (int r = 0; r < kGroup; ++r) {
-      const uint4 w0 = *reinterpret_cast<const uint4*>(qrow + r * kHeadDim);
-      const uint4 w1 = *reinterpret_cast<const uint4*>(qrow + r * kHeadDim + 8);
-      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 x = bf16x2_to_float2(w[e]);
-        qf[r][e] = make_float2(x.x * a.scale_log2, x.y * a.scale_log2);
-      }
+    for (int kk = 0; kk < 4; ++kk) {
+      qb[kk][0] = fg < kGroup ? qw[kk * 8 + ft] : 0u;
+      qb[kk][1] = fg < kGroup ? qw[kk * 8 + 4 + ft] : 0u;
     }
   }
-  // Swizzled byte offsets of this lane's two 16-byte chunks within a row
-  // (TMA 128-byte swizzle: chunk c of row r sits at chunk c ^ (r & 7); both
-  // tokens of this lane have r & 7 == tg).
-  const uint32_t off_a = static_cast<uint32_t>(((2 * dg) ^ tg) << 4);
-  const uint32_t off_b = static_cast<uint32_t>(((2 * dg + 1) ^ tg) << 4);
+  // Swizzled row addresses (TMA 128-byte swizzle: 16-byte chunk c of row r
+  // sits at chunk c ^ (r & 7); every row used below has r & 7 == lr).
+  // K, non-transposed: matrix li covers tokens 8*(li & 1).., dims chunk 2kk + (li >> 1).
+  const uint32_t k_row = static_cast<uint32_t>((lr + 8 * (li & 1)) * kRowBytes);
+  const int k_chunk = li >> 1;
+  // V, transposed: matrix li covers tokens 8*(li >> 1).., dims chunk 2mt + (li & 1).
+  const uint32_t v_row = static_cast<uint32_t>((lr + 8 * (li >> 1)) * kRowBytes);
+  const int v_chunk = li & 1;
+  // P^T as the B operand of O^T += V^T P^T: lane (fg, ft) needs row fg's
+  // weights for tokens 2ft, 2ft+1, 2ft+8, 2ft+9, held by lanes 8ft + (fg >> 1)
+  // and 8ft + 4 + (fg >> 1) in the S^T fragment layout.
+  const int src_a = 8 * ft + (fg >> 1);
+  const int src_b = src_a + 4;
+  const bool odd_row = (fg & 1) != 0;
+  const float c = a.scale_log2;
 
   const int nw = n > warp ? (n - warp + kWarps - 1) / kWarps : 0;
   const uint64_t policy = l2_policy_evict_first();
@@ -152,13 +163,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int k = 0; k < kStages && k < nw; ++k) issue(k);
   }
 
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-  float2 o[kGroup][8];
+  float m_ref[2] = {-INFINITY, -INFINITY};  // per query row 2ft + rr, log2 units
+  float l_run[2] = {0.f, 0.f};              // this lane's share of the row sums
+  float oacc[4][4];                         // O^T fragments: dims 16mt + fg (+8), rows 2ft (+1)
 #pragma unroll
-  for (int r = 0; r < kGroup; ++r)
+  for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[r][e] = make_float2(0.f, 0.f);
+    for (int e = 0; e < 4; ++e) oacc[mt][e] = 0.f;
 
   for (int k = 0; k < nw; ++k) {
     const int st = k % kStages;
@@ -174,84 +185,86 @@ __global__ void __launch_bounds__(kThreads, 3)
       const uint32_t kt = tile0 + st * kTileBytes;
       const uint32_t vt = kt + kPageSize * kRowBytes;
 
-      // scores: s[i][r] = partial dot over this lane's 16 dims, token tg + 8i
-      float s[2][kGroup];
+      // S^T = K Q^T: s[0], s[1] = token fg, rows 2ft, 2ft+1; s[2], s[3] = token fg + 8
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint32_t row = kt + (tg + 8 * i) * kRowBytes;
-        const uint4 ka = lds128(row + off_a);
-        const uint4 kb = lds128(row + off_b);
-        const uint32_t w[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-        float2 kf[8];
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t ka[4];
+        ldsm_x4(kt + k_row + (static_cast<uint32_t>((2 * kk + k_chunk) ^ lr) << 4), ka);
+        mma_16816_bf16(s, ka, qb[kk][0], qb[kk][1]);
+      }
+      if (valid < kPageSize) {
+        // tokens at or past the sequence end: no weight, and their V rows
+        // (whatever bytes they hold) are zeroed before the second product
+        if (fg >= valid) s[0] = s[1] = -INFINITY;
+        if (fg + 8 >= valid) s[2] = s[3] = -INFINITY;
+        for (int idx = lane; idx < (kPageSize - valid) * 8; idx += 32)
+          sts128_zero(vt + (valid + (idx >> 3)) * kRowBytes + ((idx & 7) << 4));
+        __syncwarp();
+      }
+      float mx0 = fmaxf(s[0], s[2]) * c;
+      float mx1 = fmaxf(s[1], s[3]) * c;
+      const bool grow = mx0 > m_ref[0] + kRescaleLog2 || mx1 > m_ref[1] + kRescaleLog2;
+      if (__any_sync(kFull, grow)) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) kf[e] = bf16x2_to_float2(w[e]);
-#pragma unroll
-        for (int r = 0; r < kGroup; ++r) {
-          float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc = ffma2(qf[r][e], kf[e], acc);
-          s[i][r] = acc.x + acc.y;
+        for (int x = 4; x <= 16; x <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, x));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, x));
         }
-      }
-      // transposing reduction over the 4 d-groups (lanes ^16, ^8)
-      float u[kGroup];
+        const float mx[2] = {mx0, mx1};
 #pragma unroll
-      for (int r = 0; r < kGroup; ++r) {
-        const float send = hi4 ? s[0][r] : s[1][r];
-        const float keep = hi4 ? s[1][r] : s[0][r];
-        u[r] = keep + __shfl_xor_sync(kFull, send, 16);
-      }
-      float sc[2];
+        for (int rr = 0; rr < 2; ++rr) {
+          const float m_new = fmaxf(m_ref[rr], mx[rr]);
+          const float alpha = fast_exp2(m_ref[rr] - m_new);  // 0 on the first page
+          l_run[rr] *= alpha;
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const float send = hi3 ? u[rr] : u[2 + rr];
-        const float keep = hi3 ? u[2 + rr] : u[rr];
-        sc[rr] = keep + __shfl_xor_sync(kFull, send, 8);
-      }
-      // this lane now owns token tg + 8*hi4, rows 2*hi3 + {0, 1}
-      if (valid < kPageSize && tg + (hi4 ? 8 : 0) >= valid) sc[0] = sc[1] = -INFINITY;
-
-      float p[2], alpha[2];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const float pm = fmaxf(sc[rr], __shfl_xor_sync(kFull, sc[rr], 16));
-        const float m_new = fmaxf(m_run[rr], pm);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        p[rr] = fast_exp2(sc[rr] - m_use);
-        alpha[rr] = fast_exp2(m_run[rr] - m_use);
-        l_run[rr] = l_run[rr] * alpha[rr] + p[rr];
-        m_run[rr] = m_new;
-      }
-      // gather the group's rescale factors (4 rows) and weights (2 tokens x 4 rows)
-      const float ao0 = __shfl_xor_sync(kFull, alpha[0], 8);
-      const float ao1 = __shfl_xor_sync(kFull, alpha[1], 8);
-      const float a4[kGroup] = {hi3 ? ao0 : alpha[0], hi3 ? ao1 : alpha[1],
-                                hi3 ? alpha[0] : ao0, hi3 ? alpha[1] : ao1};
-      float pp[2][kGroup];
-#pragma unroll
-      for (int src = 0; src < 4; ++src) {
-        const int sl = tg + 8 * src;
-        pp[src >> 1][2 * (src & 1) + 0] = __shfl_sync(kFull, p[0], sl);
-        pp[src >> 1][2 * (src & 1) + 1] = __shfl_sync(kFull, p[1], sl);
-      }
-#pragma unroll
-      for (int r = 0; r < kGroup; ++r)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[r][e] = fmul2(o[r][e], f2(a4[r]));
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (valid == kPageSize || tg + 8 * i < valid) {
-          const uint32_t row = vt + (tg + 8 * i) * kRowBytes;
-          const uint4 va = lds128(row + off_a);
-          const uint4 vb = lds128(row + off_b);
-          const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float2 vf = bf16x2_to_float2(w[e]);
-#pragma unroll
-            for (int r = 0; r < kGroup; ++r) o[r][e] = ffma2(f2(pp[i][r]), vf, o[r][e]);
+          for (int mt = 0; mt < 4; ++mt) {
+            oacc[mt][rr] *= alpha;
+            oacc[mt][2 + rr] *= alpha;
           }
+          m_ref[rr] = m_new;
         }
+      }
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p[e] = fast_exp2(fmaf(s[e], c, -m_ref[e & 1]));
+      l_run[0] += p[0] + p[2];
+      l_run[1] += p[1] + p[3];
+
+      // P^T fragments.  P is carried as two bf16 terms, hi = bf16(P) and
+      // lo = bf16(P - hi), so the weights keep ~16 significant bits through
+      // the bf16 tensor-core product.  Words: (row 2ft | row 2ft+1) x
+      // (token fg in the low half, token fg+8 in the high half).
+      const uint32_t eh = pack_bf16x2(p[0], p[2]);
+      const uint32_t oh = pack_bf16x2(p[1], p[3]);
+      const uint32_t el = pack_bf16x2(p[0] - __uint_as_float(eh << 16),
+                                      p[2] - __uint_as_float(eh & 0xFFFF0000u));
+      const uint32_t ol = pack_bf16x2(p[1] - __uint_as_float(oh << 16),
+                                      p[3] - __uint_as_float(oh & 0xFFFF0000u));
+      uint32_t pb[2][2];
+      {
+        const uint32_t w_even[2] = {eh, el};
+        const uint32_t w_odd[2] = {oh, ol};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t ea = __shfl_sync(kFull, w_even[h], src_a);
+          const uint32_t oa = __shfl_sync(kFull, w_odd[h], src_a);
+          const uint32_t eb = __shfl_sync(kFull, w_even[h], src_b);
+          const uint32_t ob = __shfl_sync(kFull, w_odd[h], src_b);
+          const uint32_t wa = odd_row ? oa : ea;  // tokens 2ft (lo), 2ft+8 (hi)
+          const uint32_t wb = odd_row ? ob : eb;  // tokens 2ft+1 (lo), 2ft+9 (hi)
+          pb[h][0] = prmt(wa, wb, 0x5410u);
+          pb[h][1] = prmt(wa, wb, 0x7632u);
+        }
+      }
+
+      // O^T += V^T (P_hi + P_lo)^T over the four 16-dim slices
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        uint32_t va[4];
+        ldsm_x4_trans(vt + v_row + (static_cast<uint32_t>((2 * mt + v_chunk) ^ lr) << 4), va);
+        mma_16816_bf16(oacc[mt], va, pb[0][0], pb[0][1]);
+        mma_16816_bf16(oacc[mt], va, pb[1][0], pb[1][1]);
       }
     }
     __syncwarp();
@@ -261,46 +274,54 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   }
 
-  // ---- merge the 32 streams of this CTA
+  // ---- merge the warps' streams
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) l_run[rr] += __shfl_xor_sync(kFull, l_run[rr], 16);
+  for (int x = 4; x <= 16; x <<= 1) {
+    l_run[0] += __shfl_xor_sync(kFull, l_run[0], x);
+    l_run[1] += __shfl_xor_sync(kFull, l_run[1], x);
+  }
   __syncthreads();  // every warp is done with its stage ring
   float* sm_m = reinterpret_cast<float*>(smem);
-  float* sm_l = sm_m + kStreams * kGroup;
-  float* sm_o = sm_l + kStreams * kGroup;
-  const int stream = warp * 8 + tg;
-  if (!hi4) {
+  float* sm_l = sm_m + kWarps * kGroup;
+  float* sm_o = sm_l + kWarps * kGroup;
+  if (ft < 2) {
+    if (fg == 0) {
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      sm_m[stream * kGroup + 2 * hi3 + rr] = m_run[rr];
-      sm_l[stream * kGroup + 2 * hi3 + rr] = l_run[rr];
+      for (int rr = 0; rr < 2; ++rr) {
+        sm_m[warp * kGroup + 2 * ft + rr] = m_ref[rr];
+        sm_l[warp * kGroup + 2 * ft + rr] = l_run[rr];
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      float* o0 = sm_o + (warp * kGroup + 2 * ft) * kHeadDim + 16 * mt + fg;
+      o0[0] = oacc[mt][0];
+      o0[kHeadDim] = oacc[mt][1];
+      o0[8] = oacc[mt][2];
+      o0[kHeadDim + 8] = oacc[mt][3];
     }
   }
-#pragma unroll
-  for (int r = 0; r < kGroup; ++r)
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      *reinterpret_cast<float2*>(sm_o + (stream * kGroup + r) * kHeadDim + 16 * dg + 2 * e) =
-          o[r][e];
   __syncthreads();
 
   {
     const int r = warp;  // 4 warps <-> 4 query rows
     const int d = 2 * lane;
     float M = -INFINITY;
-#pragma unroll 8
-    for (int sidx = 0; sidx < kStreams; ++sidx) M = fmaxf(M, sm_m[sidx * kGroup + r]);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * kGroup + r]);
     float Ls = 0.f;
     float2 O = make_float2(0.f, 0.f);
     if (M != -INFINITY) {
-      for (int sidx = 0; sidx < kStreams; ++sidx) {
-        const float ms = sm_m[sidx * kGroup + r];
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float ms = sm_m[w * kGroup + r];
         if (ms == -INFINITY) continue;
-        const float w = fast_exp2(ms - M);
-        Ls += sm_l[sidx * kGroup + r] * w;
+        const float wt = fast_exp2(ms - M);
+        Ls += sm_l[w * kGroup + r] * wt;
         const float2 os =
-            *reinterpret_cast<const float2*>(sm_o + (sidx * kGroup + r) * kHeadDim + d);
-        O = ffma2(f2(w), os, O);
+            *reinterpret_cast<const float2*>(sm_o + (w * kGroup + r) * kHeadDim + d);
+        O.x = fmaf(wt, os.x, O.x);
+        O.y = fmaf(wt, os.y, O.y);
       }
     }
     const int j = g * kGroup + r;
@@ -347,7 +368,8 @@ __global__ void __launch_bounds__(32) merge_splits_kernel(const AttnArgs a) {
       Ls += ml.y * w;
       const float2 acc =
           *reinterpret_cast<const float2*>(a.part_acc + (base + s) * kHeadDim + 2 * lane);
-      O = ffma2(f2(w), acc, O);
+      O.x = fmaf(w, acc.x, O.x);
+      O.y = fmaf(w, acc.y, O.y);
     }
   }
   const float inv = Ls > 0.f ? 1.f / Ls : 0.f;

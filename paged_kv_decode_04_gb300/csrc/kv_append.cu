@@ -49,8 +49,19 @@ __global__ void __launch_bounds__(kAppendThreads)
   __shared__ double s_sin[kHalf];
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
+  const int h = tid / kHalf, i = tid % kHalf;
+  const int64_t row = kNumKvHeads * kHeadDim;  // elements per (kv, slot)
+  const int64_t src = static_cast<int64_t>(b) * row;
+
+  // Everything that does not depend on the position is fetched first so that
+  // its latency overlaps the position -> page lookup and the FP64 sincos.
+  const uint16_t k1 = k_new[src + h * kHeadDim + i];
+  const uint16_t k2 = k_new[src + h * kHeadDim + i + kHalf];
+  const uint32_t vw = reinterpret_cast<const uint32_t*>(v_new + src)[tid];
   const int32_t pos = positions[b];
   const bool pos_ok = pos >= 0 && pos < max_blocks * kPageSize;
+  const int32_t page =
+      pos_ok ? block_table[static_cast<int64_t>(b) * max_blocks + pos / kPageSize] : -1;
 
   if (tid < kHalf) {
     const double angle = __dmul_rn(static_cast<double>(pos), freqs.inv_freq[tid]);
@@ -64,13 +75,18 @@ __global__ void __launch_bounds__(kAppendThreads)
   // Optional out-of-place query rotation: 32 heads x 32 pairs, 4 per thread.
   if (q_in != nullptr) {
     const int64_t qbase = static_cast<int64_t>(b) * kNumQHeads * kHeadDim;
+    uint16_t x1[4], x2[4];
 #pragma unroll
-    for (int k = 0; k < (kNumQHeads * kHalf) / kAppendThreads; ++k) {
-      const int idx = tid + k * kAppendThreads;
-      const int j = idx / kHalf, i = idx % kHalf;
-      const int64_t o = qbase + j * kHeadDim + i;
+    for (int k = 0; k < 4; ++k) {
+      const int j = h + 8 * k;
+      x1[k] = q_in[qbase + j * kHeadDim + i];
+      x2[k] = q_in[qbase + j * kHeadDim + i + kHalf];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t o = qbase + (h + 8 * k) * kHeadDim + i;
       uint16_t y1, y2;
-      rotate_pair(q_in[o], q_in[o + kHalf], s_cos[i], s_sin[i], &y1, &y2);
+      rotate_pair(x1[k], x2[k], s_cos[i], s_sin[i], &y1, &y2);
       q_out[o] = y1;
       q_out[o + kHalf] = y2;
     }
@@ -80,30 +96,20 @@ __global__ void __launch_bounds__(kAppendThreads)
     if (tid == 0) record_error(dev_err, kErrPosition);
     return;
   }
-  const int32_t page =
-      block_table[static_cast<int64_t>(b) * max_blocks + pos / kPageSize];
   if (page < 0 || page >= num_pages) {
     if (tid == 0) record_error(dev_err, kErrPage);
     return;
   }
   const int slot = pos % kPageSize;
-  const int64_t row = kNumKvHeads * kHeadDim;  // elements per (kv, slot)
   uint16_t* k_dst = pool + ((static_cast<int64_t>(page) * 2 + 0) * kPageSize + slot) * row;
   uint16_t* v_dst = pool + ((static_cast<int64_t>(page) * 2 + 1) * kPageSize + slot) * row;
-  const int64_t src = static_cast<int64_t>(b) * row;
-
   // Keys: thread (h, i) rotates pair i of kv head h.
-  {
-    const int h = tid / kHalf, i = tid % kHalf;
-    const int64_t o = h * kHeadDim + i;
-    uint16_t y1, y2;
-    rotate_pair(k_new[src + o], k_new[src + o + kHalf], s_cos[i], s_sin[i], &y1, &y2);
-    k_dst[o] = y1;
-    k_dst[o + kHalf] = y2;
-  }
+  uint16_t y1, y2;
+  rotate_pair(k1, k2, s_cos[i], s_sin[i], &y1, &y2);
+  k_dst[h * kHeadDim + i] = y1;
+  k_dst[h * kHeadDim + i + kHalf] = y2;
   // Values: 512 bf16 = 256 words, one per thread.
-  reinterpret_cast<uint32_t*>(v_dst)[tid] =
-      reinterpret_cast<const uint32_t*>(v_new + src)[tid];
+  reinterpret_cast<uint32_t*>(v_dst)[tid] = vw;
 }
 
 }  // namespace
