@@ -65,6 +65,7 @@ typedef struct CUstream_st* pkv_stream_t; /* same type as cudaStream_t */
 #define PKV_EWORKSPACE 3    /* workspace missing or smaller than required */
 #define PKV_ECUDA 4         /* a CUDA runtime call or launch failed */
 #define PKV_EALIGN 5        /* a pointer violates the alignment stated above */
+#define PKV_ESCRATCH 6      /* split partials exceed PKV_STATIC_SCRATCH_BYTES */
 
 /* Device-side error bits OR-ed into *dev_err. */
 #define PKV_DEVERR_PAGE 1u      /* block-table entry outside [0, num_pages) */
@@ -161,6 +162,46 @@ PKV_API size_t pkv_workspace_bytes(int batch, int num_q_heads,
  */
 PKV_API int pkv_plan_splits(int batch, int num_kv_heads, int max_blocks,
                             int num_splits);
+
+/*
+ * pkv_paged_decode_attention_static_ws -- the same computation as
+ * pkv_paged_decode_attention, for callers that cannot allocate device memory.
+ * (The source pages have no counterpart to this entry point.)
+ *
+ * Who needs it: code that runs where cudaMalloc is not an option -- for
+ * example inside a host callback or an allocator hook, in a process whose
+ * device memory is entirely owned by another framework's caching allocator,
+ * or in a tight real-time loop that must never enter the driver's allocator.
+ * Such a caller still owns and passes every input and the output; only the
+ * split-K partials move from a caller workspace to a fixed scratch buffer
+ * that the library holds in device memory (a file-scope __device__ array of
+ * PKV_STATIC_SCRATCH_BYTES bytes, present on every GPU that loads libpkv
+ * until the process exits).  This entry point calls no cudaMalloc, cudaFree
+ * or other allocating routine.
+ *
+ * Arguments and results are those of pkv_paged_decode_attention without the
+ * workspace pair.  If the chosen split plan would need more than
+ * PKV_STATIC_SCRATCH_BYTES of partials (pkv_workspace_bytes() > that size),
+ * the call returns PKV_ESCRATCH before enqueuing anything; pass a smaller
+ * num_splits (1 needs no scratch at all) or use the workspace entry point.
+ *
+ * The first call on each device looks up the device address of the scratch
+ * buffer with that device current (cudaGetSymbolAddress) and caches it; make
+ * that first call outside any stream capture.  All calls on a device share
+ * the one buffer: two calls whose kernels overlap in time on the GPU (for
+ * example on two streams without an ordering between them) race on it and
+ * produce garbage.  Calls ordered on one stream are safe.  The buffer keeps
+ * the previous call's partials; nothing in it has to start at zero, because
+ * every partial the merge reads is written earlier in the same call.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (4u << 20)
+
+PKV_API int pkv_paged_decode_attention_static_ws(
+    const pkv_bf16* q, const pkv_bf16* pool, int64_t num_pages,
+    const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+    int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+    float scale, pkv_bf16* out, int num_splits, int32_t* dev_err,
+    pkv_stream_t stream);
 
 #ifdef __cplusplus
 }

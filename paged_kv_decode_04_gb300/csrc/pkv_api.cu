@@ -154,6 +154,7 @@ PKV_API const char* pkv_strerror(int status) {
     case PKV_EWORKSPACE: return "workspace missing or smaller than pkv_workspace_bytes()";
     case PKV_ECUDA: return "CUDA runtime error (launch failed or no usable device)";
     case PKV_EALIGN: return "pointer alignment requirement violated";
+    case PKV_ESCRATCH: return "split partials would exceed the static scratch buffer (PKV_STATIC_SCRATCH_BYTES); use fewer splits";
     default: return "unknown status";
   }
 }
@@ -248,3 +249,77 @@ PKV_API int pkv_paged_decode_attention(const pkv_bf16* q, const pkv_bf16* pool,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Attention without a caller workspace: the split-K partials live in a fixed
+// device buffer owned by the library (see pkv_paged_decode_attention_static_ws
+// in pkv.h for who needs this and the rules of sharing it).
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch, looked up once per device (with that
+// device current) and cached.  In host code the symbol itself is only a
+// stand-in for the device object, so its address must never be passed to a
+// kernel directly.
+void* static_scratch_address(int device) {
+  static std::atomic<void*> cache[64] = {};
+  if (device < 0 || device >= 64) return nullptr;
+  void* p = cache[device].load(std::memory_order_acquire);
+  if (p != nullptr) return p;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  cache[device].store(p, std::memory_order_release);
+  return p;
+}
+
+}  // namespace
+
+extern "C" PKV_API int pkv_paged_decode_attention_static_ws(
+    const pkv_bf16* q, const pkv_bf16* pool, int64_t num_pages, const int32_t* block_table,
+    int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+    int head_dim, int page_size, float scale, pkv_bf16* out, int num_splits,
+    int32_t* dev_err, pkv_stream_t stream) {
+  if (!q || !pool || !block_table || !seq_lens || !out) return PKV_EINVAL;
+  if (batch < 0 || batch > 65535 || num_pages < 1 || num_pages > INT32_MAX ||
+      max_blocks < 1 || max_blocks > (INT32_MAX / kPageSize) || num_splits < 0)
+    return PKV_EINVAL;
+  if (!(scale > 0.f) || !isfinite(scale)) return PKV_EINVAL;
+  if (!supported_dims(num_q_heads, num_kv_heads, head_dim, page_size)) return PKV_EUNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(out, 4) || !aligned(dev_err, 4))
+    return PKV_EALIGN;
+  if (batch == 0) return PKV_OK;
+  pkv::SplitPlan plan;
+  if (!make_plan(batch, max_blocks, num_splits, &plan)) return PKV_ECUDA;
+  const size_t need = pkv::workspace_bytes_for(batch, num_q_heads, head_dim, plan);
+  if (need > PKV_STATIC_SCRATCH_BYTES) return PKV_ESCRATCH;
+  float* ws = nullptr;
+  if (need > 0) {
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return PKV_ECUDA;
+    ws = static_cast<float*>(static_scratch_address(device));
+    if (ws == nullptr) return PKV_ECUDA;
+  }
+  CUtensorMap map;
+  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
+  pkv::AttnArgs args;
+  args.q = q;
+  args.block_table = block_table;
+  args.seq_lens = seq_lens;
+  args.out = out;
+  const size_t acc_elems = static_cast<size_t>(batch) * num_q_heads * plan.num_splits * head_dim;
+  args.part_acc = ws;
+  args.part_ml = ws != nullptr ? ws + acc_elems : nullptr;
+  args.dev_err = dev_err;
+  args.num_pages = num_pages;
+  args.max_blocks = max_blocks;
+  args.batch = batch;
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.plan = plan;
+  const cudaError_t err =
+      pkv::launch_paged_decode_attention(map, args, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
