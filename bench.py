@@ -41,6 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_attention_peak_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_decode_04_gb300", "csrc", f)
                   for f in ("decode_attention.cu", "pkv_device.cuh", "pkv_internal.h")]
+# The traffic file holds a list of records {workload, kernel, kernel_sha, dram_bytes_per_launch}.
 
 WORKLOAD_TEXT = {
     "peak": "peak: 256 seqs x 2048 ctx, 1 layer, 32q/8kv/64 bf16, 32768 live pages (1 GiB K/V) "
@@ -93,16 +94,18 @@ def kernel_sha() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str):
-    """ncu DRAM bytes per attention launch, if recorded for the current kernel source."""
+def recorded_traffic(workload: str, kernel: str):
+    """ncu DRAM bytes per launch of `kernel`, if recorded for the current kernel source."""
     try:
         with open(TRAFFIC_FILE) as f:
-            rec = json.load(f)
+            recs = json.load(f)
     except Exception:
         return None
-    if rec.get("kernel_sha") != kernel_sha() or rec.get("workload") != workload:
-        return None
-    return rec.get("dram_bytes_per_launch")
+    for rec in recs if isinstance(recs, list) else [recs]:
+        if (rec.get("kernel_sha") == kernel_sha() and rec.get("workload") == workload
+                and rec.get("kernel") == kernel):
+            return rec.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:
@@ -292,7 +295,7 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    dist = init_dist(world, "nccl")
+    init_dist(world, "nccl")
     w = synth.make_workload(args.workload, args.seed)
     d = synth.device_inputs(w, dev)
     B, layers = w.batch, w.layers
@@ -302,32 +305,55 @@ def run_ours(args, world, rank, local):
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     outs = torch.empty((layers, B, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    kernels_per_step = layers * (2 + (1 if splits > 1 else 0))
+    fused = args.path == "fused"
+    kernels_per_layer = (1 if fused else 2) + (1 if splits > 1 else 0)
 
-    def step(q=None, k=None, v=None, pos=None, lens=None, bts=None):
-        q = d["q"] if q is None else q
-        k = d["k_new"] if k is None else k
-        v = d["v_new"] if v is None else v
-        pos = d["positions"] if pos is None else pos
-        lens = d["seq_lens"] if lens is None else lens
-        bts = d["block_tables"] if bts is None else bts
+    def attend(layer):
+        binding.paged_decode_attention(d["q"][layer], d["pool"], d["block_tables"][layer],
+                                       d["seq_lens"], outs[layer], scale=w.scale,
+                                       workspace=workspace, num_splits=args.splits, dev_err=err)
+
+    def append(layer):
+        binding.kv_append(d["k_new"][layer], d["v_new"][layer], d["pool"],
+                          d["block_tables"][layer], d["positions"], rope_theta=w.rope_theta,
+                          dev_err=err)
+
+    def fused_layer(layer):
+        binding.decode_step(d["q"][layer], d["k_new"][layer], d["v_new"][layer], d["pool"],
+                            d["block_tables"][layer], d["seq_lens"], outs[layer],
+                            rope_theta=w.rope_theta, scale=w.scale, workspace=workspace,
+                            num_splits=args.splits, dev_err=err)
+
+    def launch_step():
+        """Enqueue one whole step (every layer) on the current stream."""
         for layer in range(layers):
-            binding.kv_append(k[layer], v[layer], d["pool"], bts[layer], pos,
-                              rope_theta=w.rope_theta, dev_err=err, stream=stream)
-            binding.paged_decode_attention(q[layer], d["pool"], bts[layer], lens, outs[layer],
-                                           scale=w.scale, workspace=workspace,
-                                           num_splits=args.splits, dev_err=err, stream=stream)
+            if fused:
+                fused_layer(layer)
+            else:
+                append(layer)
+                attend(layer)
 
-    # ---- warm-up
+    # ---- warm-up (eager), then optionally capture one step as a CUDA graph
     for _ in range(args.warmup):
-        step()
+        launch_step()
     torch.cuda.synchronize(dev)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            launch_step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        run_step = graph.replay
+    else:
+        run_step = launch_step
 
     # ---- timed region: K whole steps, device-resident inputs
     sampler = ClockSampler(gpu_selector(local)) if rank == 0 else None
-    time.sleep(0.3 if sampler else 0)
+    if sampler:
+        time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -335,77 +361,83 @@ def run_ours(args, world, rank, local):
     t_wall0 = time.time()
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        run_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     barrier(world)
     if sampler:
         sampler.stop()
-    ms_local = e0.elapsed_time(e1)
-    ms = max_over_ranks(ms_local, world, dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     step_bytes = algorithmic_bytes(w, "step")
     total_bytes = sum_over_ranks(step_bytes * args.steps, world, dev)
     value = total_bytes / (ms / 1e3) / 1e9
     ms_per_step = ms / args.steps
 
-    # ---- per-kernel durations (events around each launch, same stream)
+    # ---- per-kernel durations: CUDA events around each launch on the same stream
     n_prof = min(args.steps, max(50, args.steps // 4))
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_prof)]
-    for i in range(n_prof):
-        ev[i][0].record(stream)
-        for layer in range(layers):
-            binding.kv_append(d["k_new"][layer], d["v_new"][layer], d["pool"],
-                              d["block_tables"][layer], d["positions"], rope_theta=w.rope_theta,
-                              dev_err=err, stream=stream)
-        ev[i][1].record(stream)
-        for layer in range(layers):
-            binding.paged_decode_attention(d["q"][layer], d["pool"], d["block_tables"][layer],
-                                           d["seq_lens"], outs[layer], scale=w.scale,
-                                           workspace=workspace, num_splits=args.splits,
-                                           dev_err=err, stream=stream)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize(dev)
-    append_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n_prof)) / layers
-    attn_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(n_prof)) / layers
-    attn_bytes = algorithmic_bytes(w, "attention") / layers
+    kern = {}
+    if fused:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_prof)]
+        for i in range(n_prof):
+            ev[i][0].record(stream)
+            for layer in range(layers):
+                fused_layer(layer)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        dom_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / layers
+        dom_bytes = algorithmic_bytes(w, "step") / layers
+        kern["decode_step"] = round(dom_ms * 1e3, 2)
+        dom_name = "paged_decode_kernel<append>"
+    else:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_prof)]
+        for i in range(n_prof):
+            ev[i][0].record(stream)
+            for layer in range(layers):
+                append(layer)
+            ev[i][1].record(stream)
+            for layer in range(layers):
+                attend(layer)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        app_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / layers
+        dom_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) / layers
+        dom_bytes = algorithmic_bytes(w, "attention") / layers
+        kern["kv_append"] = round(app_ms * 1e3, 2)
+        kern["paged_decode_attention"] = round(dom_ms * 1e3, 2)
+        dom_name = "paged_decode_kernel"
+    if splits > 1:
+        dom_name += "+merge_splits_kernel"
     peak, peak_kind = measured_hbm_peak()
-    achieved = attn_bytes / (attn_ms / 1e3) / 1e9
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
 
     # ---- end to end: per-step inputs from pinned host memory, output back to host
-    host = {
-        "q": d["q"].cpu().pin_memory(), "k_new": d["k_new"].cpu().pin_memory(),
-        "v_new": d["v_new"].cpu().pin_memory(), "positions": d["positions"].cpu().pin_memory(),
-        "seq_lens": d["seq_lens"].cpu().pin_memory(),
-        "block_tables": d["block_tables"].cpu().pin_memory(),
-    }
-    staged = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    names = ["q", "k_new", "v_new", "positions", "seq_lens", "block_tables"]
+    host = {k: d[k].cpu().pin_memory() for k in names}
     out_host = torch.empty(outs.shape, dtype=outs.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        for k_, v_ in host.items():
-            staged[k_].copy_(v_, non_blocking=True)
-        step(staged["q"], staged["k_new"], staged["v_new"], staged["positions"],
-             staged["seq_lens"], staged["block_tables"])
+        for k in names:
+            d[k].copy_(host[k], non_blocking=True)
+        run_step()
         out_host.copy_(outs, non_blocking=True)
 
     for _ in range(max(3, min(args.warmup, 20))):
         e2e_step()
     torch.cuda.synchronize(dev)
     barrier(world)
-    n_e2e = args.steps
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for _ in range(n_e2e):
+    for _ in range(args.steps):
         e2e_step()
     f1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
-    e2e_value = sum_over_ranks(step_bytes * n_e2e, world, dev) / (e2e_ms / 1e3) / 1e9
+    e2e_value = sum_over_ranks(step_bytes * args.steps, world, dev) / (e2e_ms / 1e3) / 1e9
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} during the timed runs")
 
@@ -421,7 +453,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return 0
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload, dom_name)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -429,6 +461,9 @@ def run_ours(args, world, rank, local):
         "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
         "config": {
             "workload": WORKLOAD_TEXT[args.workload], "seed": args.seed,
+            "path": ("fused append+attention (pkv_decode_step)" if fused
+                     else "pkv_kv_append then pkv_paged_decode_attention"),
+            "launch": "one CUDA graph per step" if args.graph else "eager launches",
             "num_splits": splits, "layers_per_step": layers,
             "l2": ("inputs larger than L2: %.2f GiB of K/V streamed per step vs 129 MB L2; no flush"
                    % (w.kv_bytes() / 2 ** 30)) if w.kv_bytes() > 512 * 2 ** 20 else
@@ -439,17 +474,15 @@ def run_ours(args, world, rank, local):
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_copy": round(100 * value / world / peak, 2),
         "algorithmic_bytes_per_step": step_bytes,
-        "kernels_us": {"kv_append": round(append_ms * 1e3, 2),
-                       "paged_decode_attention": round(attn_ms * 1e3, 2)},
+        "kernels_us": kern,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "paged_decode_kernel" + ("+merge_splits_kernel" if splits > 1 else ""),
-                     "peak_kind": f"{peak_kind} copy bandwidth",
-                     "bytes_per_launch": attn_bytes},
+                     "kernel": dom_name, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "bytes_per_launch": dom_bytes},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / n_e2e, 5)},
-        "gpu_launches": kernels_per_step * args.steps,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 5)},
+        "gpu_launches": kernels_per_layer * layers * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -464,6 +497,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="peak")
     ap.add_argument("--splits", type=int, default=0, help="0 = automatic split plan")
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
+                    help="fused: one pkv_decode_step launch per layer; separate: pkv_kv_append "
+                         "then pkv_paged_decode_attention")
+    ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=True,
+                    help="replay each step as one captured CUDA graph")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seqs", type=int, default=256,
                     help="sequences of the CPU-oracle baseline sample")

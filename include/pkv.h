@@ -147,6 +147,33 @@ PKV_API int pkv_paged_decode_attention(
     int num_splits, int32_t* dev_err, pkv_stream_t stream);
 
 /*
+ * pkv_decode_step -- one whole decode step of one layer in a single kernel:
+ * the KV append of pkv_kv_append at position seq_lens[b] - 1 followed by the
+ * attention of pkv_paged_decode_attention over seq_lens[b] tokens ("これまで
+ * の進捗": decode adds one token per sequence at its absolute RoPE position,
+ * then every query head streams its sequence's pages).
+ *
+ * Results are the same as calling pkv_kv_append(positions = seq_lens - 1)
+ * and then pkv_paged_decode_attention with the same arguments: the pool slot
+ * receives the same bits and `out` is bit-identical.  The CTA that processes
+ * a sequence's last page computes the new K/V row itself, writes it to the
+ * pool and uses it directly, so no second launch and no global round trip
+ * separate the two stages.  Sequences with seq_lens[b] == 0 append nothing
+ * and give a zero row.  The pool is written at one slot per sequence.
+ * Workspace, num_splits and dev_err are as for pkv_paged_decode_attention
+ * (dev_err additionally reports PKV_DEVERR_PAGE for the appended block).
+ */
+PKV_API int pkv_decode_step(const pkv_bf16* q, const pkv_bf16* k_new,
+                            const pkv_bf16* v_new, pkv_bf16* pool,
+                            int64_t num_pages, const int32_t* block_table,
+                            int max_blocks, const int32_t* seq_lens, int batch,
+                            int num_q_heads, int num_kv_heads, int head_dim,
+                            int page_size, double rope_theta, float scale,
+                            pkv_bf16* out, void* workspace,
+                            size_t workspace_bytes, int num_splits,
+                            int32_t* dev_err, pkv_stream_t stream);
+
+/*
  * Bytes of workspace pkv_paged_decode_attention needs for these sizes and
  * num_splits (0 = the automatic choice on the current device).  Returns 0
  * when no split is needed, and (size_t)-1 for invalid sizes.

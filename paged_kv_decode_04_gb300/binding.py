@@ -62,6 +62,9 @@ def _load():
     L.pkv_paged_decode_attention.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32, i32,
                                              f32, vp, vp, sz, i32, vp, vp]
     L.pkv_paged_decode_attention.restype = i32
+    L.pkv_decode_step.argtypes = [vp, vp, vp, vp, i64, vp, i32, vp, i32, i32, i32, i32, i32, f64,
+                                  f32, vp, vp, sz, i32, vp, vp]
+    L.pkv_decode_step.restype = i32
     return L
 
 
@@ -188,4 +191,44 @@ def paged_decode_attention(q, pool, block_table, seq_lens, out=None, *, scale: f
         int(num_splits), _ptr(dev_err), _stream(stream))
     if rc != PKV_OK:
         raise PkvError(rc, "pkv_paged_decode_attention")
+    return out
+
+
+def decode_step(q, k_new, v_new, pool, block_table, seq_lens, out=None, *,
+                rope_theta: float = 500000.0, scale: float = None, workspace=None,
+                num_splits: int = 0, dev_err=None, stream=None) -> torch.Tensor:
+    """One fused decode step: append (k_new, v_new) at seq_lens - 1, then attend."""
+    num_pages = _pool_pages(pool)
+    dev = pool.device
+    _check(q, "q", torch.bfloat16, 3, dev)
+    _check(k_new, "k_new", torch.bfloat16, 3, dev)
+    _check(v_new, "v_new", torch.bfloat16, 3, dev)
+    _check(block_table, "block_table", torch.int32, 2, dev)
+    _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    if (seq_lens.shape[0] != B or block_table.shape[0] != B or k_new.shape[0] != B
+            or v_new.shape != k_new.shape):
+        raise ValueError("q, k_new, v_new, seq_lens and block_table disagree on the batch")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    if scale is None:
+        scale = D ** -0.5
+    max_blocks = block_table.shape[1]
+    need = workspace_bytes(B, max_blocks, num_splits, num_q_heads=Hq, head_dim=D)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the pool's device")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, None, dev)
+    rc = _lib.pkv_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(pool), num_pages, _ptr(block_table), max_blocks,
+        _ptr(seq_lens), B, Hq, k_new.shape[1], D, PAGE_SIZE, float(rope_theta), float(scale),
+        _ptr(out), _ptr(workspace), ws_bytes, int(num_splits), _ptr(dev_err), _stream(stream))
+    if rc != PKV_OK:
+        raise PkvError(rc, "pkv_decode_step")
     return out

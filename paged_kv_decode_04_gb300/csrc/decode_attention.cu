@@ -66,9 +66,10 @@ __host__ __device__ constexpr size_t smem_bytes(int pages_per_split) {
          static_cast<size_t>(pages_per_split) * 4;
 }
 
+template <bool kAppend>
 __global__ void __launch_bounds__(kThreads, 3)
     paged_decode_kernel(const __grid_constant__ CUtensorMap pool_map,
-                        const AttnArgs a) {
+                        const AttnArgs a, const AppendArgs ap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -147,6 +148,38 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   const int nw = n > warp ? (n - warp + kWarps - 1) / kWarps : 0;
   const uint64_t policy = l2_policy_evict_first();
+
+  // ---- fused append: the warp that owns the sequence's last page rotates
+  // the new token's key for head g (lane i: pair i, i + 32), copies its value
+  // (lane i: dims 2i, 2i + 1), writes both into the pool slot for later steps
+  // and keeps them to patch its copy of that page in shared memory.
+  const int last_local = npages - 1 - p_begin;  // index of the last page in this range
+  const bool owns_last = kAppend && npages > 0 && last_local >= 0 && last_local < n &&
+                         last_local % kWarps == warp;
+  uint16_t ky1 = 0, ky2 = 0;
+  uint32_t vv = 0;
+  const int a_slot = (L - 1) % kPageSize;
+  if (owns_last) {
+    const int pos = L - 1;
+    const int64_t src = (static_cast<int64_t>(b) * kNumKvHeads + g) * kHeadDim;
+    const uint16_t x1 = ap.k_new[src + lane];
+    const uint16_t x2 = ap.k_new[src + lane + 32];
+    vv = reinterpret_cast<const uint32_t*>(ap.v_new + src)[lane];
+    double sn, cs;
+    sincos(__dmul_rn(static_cast<double>(pos), ap.freqs.inv_freq[lane]), &sn, &cs);
+    rotate_pair(x1, x2, cs, sn, &ky1, &ky2);
+    const int pid = s_pages[last_local];
+    if (pid >= 0) {
+      const int64_t row = kNumKvHeads * kHeadDim;
+      uint16_t* kd = ap.pool + ((static_cast<int64_t>(pid) * 2 + 0) * kPageSize + a_slot) * row +
+                     g * kHeadDim;
+      uint16_t* vd = ap.pool + ((static_cast<int64_t>(pid) * 2 + 1) * kPageSize + a_slot) * row +
+                     g * kHeadDim;
+      kd[lane] = ky1;
+      kd[lane + 32] = ky2;
+      reinterpret_cast<uint32_t*>(vd)[lane] = vv;
+    }
+  }
   auto issue = [&](int k) {
     const int st = k % kStages;
     const int pid = s_pages[warp + k * kWarps];
@@ -184,6 +217,17 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int valid = min(kPageSize, L - (p_begin + local) * kPageSize);
       const uint32_t kt = tile0 + st * kTileBytes;
       const uint32_t vt = kt + kPageSize * kRowBytes;
+      if (owns_last && local == last_local) {
+        // put the appended token's K and V rows into the (swizzled) tile
+        const uint32_t sw = static_cast<uint32_t>(a_slot & 7);
+        const uint32_t kr = kt + a_slot * kRowBytes;
+        const uint32_t vr = vt + a_slot * kRowBytes;
+        sts16(kr + (((static_cast<uint32_t>(lane) >> 3) ^ sw) << 4) + ((lane & 7) << 1), ky1);
+        sts16(kr + (((4u + (static_cast<uint32_t>(lane) >> 3)) ^ sw) << 4) + ((lane & 7) << 1),
+              ky2);
+        sts32(vr + (((static_cast<uint32_t>(lane) >> 2) ^ sw) << 4) + ((lane & 3) << 2), vv);
+        __syncwarp();
+      }
 
       // S^T = K Q^T: s[0], s[1] = token fg, rows 2ft, 2ft+1; s[2], s[3] = token fg + 8
       float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -389,25 +433,42 @@ size_t workspace_bytes_for(int batch, int num_q_heads, int head_dim,
 
 int max_pages_per_split() { return kMaxPagesPerSplit; }
 
+namespace {
+
+// The dynamic shared-memory opt-in is per device and per kernel.
+template <bool kAppend>
+cudaError_t configure_once(int device) {
+  static std::atomic<unsigned long long> configured{0};
+  const unsigned long long bit = 1ull << (device & 63);
+  if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  const cudaError_t err = cudaFuncSetAttribute(paged_decode_kernel<kAppend>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem_bytes(kMaxPagesPerSplit)));
+  if (err == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
+  return err;
+}
+
+}  // namespace
+
 cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
                                           const AttnArgs& args,
-                                          cudaStream_t stream) {
-  // The dynamic shared-memory opt-in is per device; set it once per device.
-  static std::atomic<unsigned long long> configured{0};
+                                          cudaStream_t stream,
+                                          const AppendArgs* append) {
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
-  const unsigned long long bit = 1ull << (device & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    err = cudaFuncSetAttribute(paged_decode_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem_bytes(kMaxPagesPerSplit)));
-    if (err != cudaSuccess) return err;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
-  }
   const dim3 grid(kNumKvHeads * args.plan.num_splits, args.batch);
-  paged_decode_kernel<<<grid, kThreads, smem_bytes(args.plan.pages_per_split), stream>>>(
-      pool_map, args);
+  const size_t smem = smem_bytes(args.plan.pages_per_split);
+  if (append != nullptr) {
+    err = configure_once<true>(device);
+    if (err != cudaSuccess) return err;
+    paged_decode_kernel<true><<<grid, kThreads, smem, stream>>>(pool_map, args, *append);
+  } else {
+    err = configure_once<false>(device);
+    if (err != cudaSuccess) return err;
+    AppendArgs none{};
+    paged_decode_kernel<false><<<grid, kThreads, smem, stream>>>(pool_map, args, none);
+  }
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (args.plan.num_splits > 1) {

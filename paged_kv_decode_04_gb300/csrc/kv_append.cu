@@ -24,19 +24,6 @@ namespace {
 constexpr int kAppendThreads = 256;
 constexpr int kHalf = kHeadDim / 2;
 
-// (x1, x2) -> (x1*c - x2*s, x2*c + x1*s), each product rounded in FP64,
-// then one rounding to bf16.
-__device__ __forceinline__ void rotate_pair(uint16_t h1, uint16_t h2, double c,
-                                            double s, uint16_t* o1,
-                                            uint16_t* o2) {
-  const double x1 = static_cast<double>(bf16_to_float(h1));
-  const double x2 = static_cast<double>(bf16_to_float(h2));
-  const double y1 = __dsub_rn(__dmul_rn(x1, c), __dmul_rn(x2, s));
-  const double y2 = __dadd_rn(__dmul_rn(x2, c), __dmul_rn(x1, s));
-  *o1 = double_to_bf16_rne(y1);
-  *o2 = double_to_bf16_rne(y2);
-}
-
 __global__ void __launch_bounds__(kAppendThreads)
     kv_append_kernel(const uint16_t* __restrict__ k_new,
                      const uint16_t* __restrict__ v_new,

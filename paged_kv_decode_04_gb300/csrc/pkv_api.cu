@@ -248,6 +248,55 @@ PKV_API int pkv_paged_decode_attention(const pkv_bf16* q, const pkv_bf16* pool,
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
+PKV_API int pkv_decode_step(const pkv_bf16* q, const pkv_bf16* k_new, const pkv_bf16* v_new,
+                            pkv_bf16* pool, int64_t num_pages, const int32_t* block_table,
+                            int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads,
+                            int num_kv_heads, int head_dim, int page_size, double rope_theta,
+                            float scale, pkv_bf16* out, void* workspace, size_t workspace_bytes,
+                            int num_splits, int32_t* dev_err, pkv_stream_t stream) {
+  if (!q || !k_new || !v_new || !pool || !block_table || !seq_lens || !out) return PKV_EINVAL;
+  if (batch < 0 || batch > 65535 || num_pages < 1 || num_pages > INT32_MAX ||
+      max_blocks < 1 || max_blocks > (INT32_MAX / kPageSize) || num_splits < 0)
+    return PKV_EINVAL;
+  if (!(scale > 0.f) || !isfinite(scale)) return PKV_EINVAL;
+  if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return PKV_EINVAL;
+  if (!supported_dims(num_q_heads, num_kv_heads, head_dim, page_size)) return PKV_EUNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(out, 4) || !aligned(workspace, 16) ||
+      !aligned(dev_err, 4) || !aligned(v_new, 4) || !aligned(k_new, 2))
+    return PKV_EALIGN;
+  if (batch == 0) return PKV_OK;
+  pkv::SplitPlan plan;
+  if (!make_plan(batch, max_blocks, num_splits, &plan)) return PKV_ECUDA;
+  const size_t need = pkv::workspace_bytes_for(batch, num_q_heads, head_dim, plan);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
+  CUtensorMap map;
+  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
+  pkv::AttnArgs args;
+  args.q = q;
+  args.block_table = block_table;
+  args.seq_lens = seq_lens;
+  args.out = out;
+  float* ws = static_cast<float*>(workspace);
+  const size_t acc_elems = static_cast<size_t>(batch) * num_q_heads * plan.num_splits * head_dim;
+  args.part_acc = need > 0 ? ws : nullptr;
+  args.part_ml = need > 0 ? ws + acc_elems : nullptr;
+  args.dev_err = dev_err;
+  args.num_pages = num_pages;
+  args.max_blocks = max_blocks;
+  args.batch = batch;
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.plan = plan;
+  pkv::AppendArgs app;
+  app.k_new = k_new;
+  app.v_new = v_new;
+  app.pool = pool;
+  for (int i = 0; i < kHeadDim / 2; ++i)
+    app.freqs.inv_freq[i] = pow(rope_theta, -(2.0 * i) / static_cast<double>(kHeadDim));
+  const cudaError_t err = pkv::launch_paged_decode_attention(
+      map, args, reinterpret_cast<cudaStream_t>(stream), &app);
+  return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -200,6 +200,28 @@ __device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
 }
 
 
+// Rotate-half RoPE of one pair: (x1, x2) -> (x1*c - x2*s, x2*c + x1*s), each
+// product and the sum rounded in FP64 (no contraction), then one rounding to
+// bf16.
+__device__ __forceinline__ void rotate_pair(uint16_t h1, uint16_t h2, double c,
+                                            double s, uint16_t* o1,
+                                            uint16_t* o2) {
+  const double x1 = static_cast<double>(bf16_to_float(h1));
+  const double x2 = static_cast<double>(bf16_to_float(h2));
+  const double y1 = __dsub_rn(__dmul_rn(x1, c), __dmul_rn(x2, s));
+  const double y2 = __dadd_rn(__dmul_rn(x2, c), __dmul_rn(x1, s));
+  *o1 = double_to_bf16_rne(y1);
+  *o2 = double_to_bf16_rne(y2);
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // ------------------------------------------------ warp-level tensor ops --
 
 // Four 8x8 b16 matrices from shared memory; lane l supplies the row address

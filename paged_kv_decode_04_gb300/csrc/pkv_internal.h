@@ -56,9 +56,20 @@ struct AttnArgs {
   SplitPlan plan;
 };
 
+// Extra inputs of the fused decode step: the new token of every sequence is
+// appended at position seq_lens[b] - 1 by the attention kernel itself.
+struct AppendArgs {
+  const uint16_t* k_new;  // [B][Hkv][D]
+  const uint16_t* v_new;  // [B][Hkv][D]
+  uint16_t* pool;         // the pool, writable
+  RopeFreqs freqs;
+};
+
+// Attention only (append == nullptr) or the fused append + attention step.
 cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
                                           const AttnArgs& args,
-                                          cudaStream_t stream);
+                                          cudaStream_t stream,
+                                          const AppendArgs* append = nullptr);
 
 // Largest logical page range one attention CTA handles.
 int max_pages_per_split();

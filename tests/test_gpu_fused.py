@@ -1,0 +1,135 @@
+"""GPU parity of the fused decode step (pkv_decode_step): one kernel that
+appends the new token at seq_lens - 1 and attends over the pages.
+
+It must write the same pool bits as pkv_kv_append and give bit-identical
+outputs to pkv_kv_append + pkv_paged_decode_attention, and match the FP64
+oracle within |err| <= 1e-3 + 8e-3 * |ref|.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_04_gb300 import synth
+from _gpu_util import (appended_slots_expected, assert_close, binding, cuda_or_skip,
+                       gpu_step, oracle_step)
+
+pytestmark = pytest.mark.gpu
+
+
+@functools.lru_cache(maxsize=2)
+def workload(name, seed=0):
+    return synth.make_workload(name, seed)
+
+
+def fused(w, d, layer, **kw):
+    return binding().decode_step(d["q"][layer], d["k_new"][layer], d["v_new"][layer], d["pool"],
+                                 d["block_tables"][layer], d["seq_lens"],
+                                 rope_theta=w.rope_theta, scale=w.scale, **kw)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3, 32])
+@pytest.mark.parametrize("name", ["tiny", "small", "long"])
+def test_fused_equals_separate_bit_for_bit(name, splits):
+    dev = cuda_or_skip()
+    w = workload(name)
+    d1 = synth.device_inputs(w, dev)
+    d2 = synth.device_inputs(w, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for layer in range(w.layers):
+        a = fused(w, d1, layer, num_splits=splits, dev_err=err)
+        b = gpu_step(w, d2, layer, num_splits=splits)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (name, layer)
+    assert torch.equal(d1["pool"].view(torch.int16), d2["pool"].view(torch.int16))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "long"])
+def test_fused_matches_oracle(name):
+    dev = cuda_or_skip()
+    w = workload(name)
+    d = synth.device_inputs(w, dev)
+    for layer in range(w.layers):
+        out = fused(w, d, layer)
+        ref, _ = oracle_step(w, layer)
+        assert_close(synth.bits(out), ref, f"fused {name} layer {layer}")
+        kexp, vexp = appended_slots_expected(w, layer, range(w.batch))
+        for b in range(w.batch):
+            pos = int(w.positions[b])
+            page = int(w.block_tables[layer, b, pos // 16])
+            assert np.array_equal(synth.bits(d["pool"][page, 0, pos % 16]), kexp[b])
+            assert np.array_equal(synth.bits(d["pool"][page, 1, pos % 16]), vexp[b])
+
+
+def test_fused_peak_full_size_sampled():
+    dev = cuda_or_skip()
+    w = workload("peak")
+    d = synth.device_inputs(w, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = synth.bits(fused(w, d, 0, dev_err=err))
+    seqs = np.sort(np.random.default_rng(1).choice(w.batch, size=16, replace=False))
+    ref, _ = oracle_step(w, 0, seqs)
+    assert_close(out[seqs], ref, "fused peak sampled")
+    kexp, vexp = appended_slots_expected(w, 0, range(w.batch))
+    pos = torch.from_numpy(w.positions.astype(np.int64)).to(dev)
+    pages = d["block_tables"][0].long().gather(1, (pos // 16)[:, None])[:, 0]
+    sb = synth.bits(d["pool"][pages, :, pos % 16])
+    assert np.array_equal(sb[:, 0], kexp) and np.array_equal(sb[:, 1], vexp)
+    assert np.all(np.isfinite(oracle.bf16_to_f64(out)))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+
+def test_fused_mix_full_size_sampled():
+    dev = cuda_or_skip()
+    w = workload("mix")
+    d = synth.device_inputs(w, dev)
+    outs = [synth.bits(fused(w, d, layer)) for layer in range(w.layers)]
+    seqs = np.sort(np.concatenate([np.nonzero(w.seq_lens >= 1536)[0][:6],
+                                   np.nonzero(w.seq_lens <= 128)[0][:6]]))
+    for layer in (0, 15):
+        ref, _ = oracle_step(w, layer, seqs)
+        assert_close(outs[layer][seqs], ref, f"fused mix layer {layer}")
+
+
+@pytest.mark.parametrize("splits", [0, 2])
+def test_fused_ragged_lengths_with_empty_sequences(splits):
+    dev = cuda_or_skip()
+    lens = [0, 1, 2, 15, 16, 17, 33, 2048, 0, 500]
+    w = synth.make_workload("edge", 9, seq_lens=lens, num_pages=512)
+    d = synth.device_inputs(w, dev)
+    before = synth.bits(d["pool"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = synth.bits(fused(w, d, 0, num_splits=splits, dev_err=err))
+    live = np.nonzero(w.seq_lens > 0)[0]
+    ref, _ = oracle_step(w, 0, live)
+    assert_close(out[live], ref, "fused ragged")
+    for b in np.nonzero(w.seq_lens == 0)[0]:
+        assert np.all(out[b] == 0)
+    # only the appended slots changed
+    after = synth.bits(d["pool"])
+    changed = np.argwhere(np.any(after != before, axis=(3, 4)))
+    want = {(int(w.block_tables[0, b, (L - 1) // 16]), kv, (L - 1) % 16)
+            for b, L in enumerate(lens) if L > 0 for kv in (0, 1)}
+    assert {tuple(map(int, c)) for c in changed} <= want
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+
+def test_fused_bad_last_block_is_reported():
+    dev = cuda_or_skip()
+    w = synth.make_workload("edge", 10, seq_lens=[40, 20], num_pages=64)
+    d = synth.device_inputs(w, dev)
+    bt = d["block_tables"][0].clone()
+    bt[0, 2] = 1000          # the block holding position 39
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    b = binding()
+    out = b.decode_step(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"], bt, d["seq_lens"],
+                        dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & b.DEVERR_PAGE
+    ref, _ = oracle_step(w, 0, [1])
+    assert_close(synth.bits(out)[1:], ref, "untouched sequence")
