@@ -489,6 +489,65 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_prefill(args, world, rank, local):
+    """Throughput of the paged prefill write: 256 prompts x 2047 tokens per call."""
+    import torch
+    from paged_kv_decode_04_gb300 import binding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    B, L, num_pages = 256, 2047, 40000
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    perm = torch.randperm(num_pages, generator=g, device=dev)[:B * 128].view(B, 128).int()
+    k = torch.randn((B * L, 8, 64), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((B * L, 8, 64), generator=g, device=dev).to(torch.bfloat16)
+    off = torch.arange(0, B * L + 1, L, dtype=torch.int32, device=dev)
+    st = torch.zeros(B, dtype=torch.int32, device=dev)
+    pool = torch.full((num_pages, 2, 16, 8, 64), -1, dtype=torch.int16, device=dev).view(
+        torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        binding.kv_write_prefill(k, v, off, st, pool, perm, dev_err=err)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    T = B * L
+    step_bytes = T * 8 * 64 * 2 * 2 * 2 + (B + 1) * 4 + B * 4 + B * 128 * 4
+    value = sum_over_ranks(step_bytes * args.steps, world, dev) / (ms / 1e3) / 1e9
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())}")
+    if rank == 0:
+        peak, kind = measured_hbm_peak()
+        print(json.dumps({
+            "metric": "paged prefill write achieved HBM GB/s", "value": round(value, 2),
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "storage_dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"prefill write: {B} prompts x {L} tokens, 32q/8kv/64 bf16, "
+                                   f"{num_pages}-page pool", "seed": args.seed},
+            "algorithmic_bytes_per_step": step_bytes,
+            "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(value / world / peak, 4),
+                         "traffic": None, "kernel": "kv_write_prefill_kernel",
+                         "peak_kind": f"{kind} copy bandwidth"},
+            "gpu_launches": args.steps}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -508,12 +567,16 @@ def main(argv=None):
     ap.add_argument("--ref-seqs", type=int, default=1,
                     help="sequences per step of the --impl reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["decode", "prefill"], default="decode",
+                    help="decode: the decode step (headline); prefill: the paged prefill write")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.op == "prefill":
+        return run_prefill(args, world, rank, local)
     return run_ours(args, world, rank, local)
 
 

@@ -72,6 +72,7 @@ typedef struct CUstream_st* pkv_stream_t; /* same type as cudaStream_t */
 #define PKV_DEVERR_SEQLEN 2u    /* seq_lens[b] < 0 or > max_blocks*page_size */
 #define PKV_DEVERR_POSITION 4u  /* positions[b] < 0 or >= max_blocks*page_size */
 #define PKV_DEVERR_TIMEOUT 8u   /* an in-kernel wait for a page copy gave up */
+#define PKV_DEVERR_OFFSETS 16u  /* a token outside the ranges of token_offsets */
 
 /* Library ABI version (bumped when a signature changes). */
 PKV_API int pkv_abi_version(void);
@@ -111,6 +112,35 @@ PKV_API int pkv_kv_append(const pkv_bf16* k_new, const pkv_bf16* v_new,
                           double rope_theta, const pkv_bf16* q_in,
                           pkv_bf16* q_out, int num_q_heads, int32_t* dev_err,
                           pkv_stream_t stream);
+
+/*
+ * pkv_kv_write_prefill -- paged prefill write ("これまでの進捗", KV page pool
+ * item: prefill fills the prompt pages).  Writes a ragged batch of new tokens
+ * into the pool through the block tables, each exactly as pkv_kv_append
+ * would write it at its position.
+ *
+ * Sequence b owns tokens [token_offsets[b], token_offsets[b+1]) of k and v
+ * ([num_tokens][num_kv_heads][head_dim] bf16); its i-th token goes to
+ * position start_positions[b] + i, i.e. slot (pos % page_size) of page
+ * block_table[b*max_blocks + pos/page_size], K rotated by RoPE at pos (FP64,
+ * one rounding to bf16) and V unchanged.
+ *
+ *   token_offsets    int32 [batch + 1], non-decreasing, token_offsets[0] = 0,
+ *                    token_offsets[batch] = num_tokens
+ *   start_positions  int32 [batch]
+ *   dev_err          optional int32, bits PKV_DEVERR_PAGE / _POSITION /
+ *                    _OFFSETS (a token whose offsets do not bracket it)
+ * A token with a bad position, page or offset is skipped.  No two tokens may
+ * name the same (page, slot).
+ */
+PKV_API int pkv_kv_write_prefill(const pkv_bf16* k, const pkv_bf16* v,
+                                 int num_tokens, const int32_t* token_offsets,
+                                 const int32_t* start_positions,
+                                 pkv_bf16* pool, int64_t num_pages,
+                                 const int32_t* block_table, int max_blocks,
+                                 int batch, int num_kv_heads, int head_dim,
+                                 int page_size, double rope_theta,
+                                 int32_t* dev_err, pkv_stream_t stream);
 
 /*
  * pkv_paged_decode_attention -- paged decode attention with an FP32 online

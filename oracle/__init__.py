@@ -57,6 +57,10 @@ def lib():
                                     _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_double]
         L.orc_kv_append.restype = ctypes.c_int
+        L.orc_kv_write_prefill.argtypes = [_u16p, _u16p, _i32p, _i32p, _u16p, ctypes.c_int64,
+                                           _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_double]
+        L.orc_kv_write_prefill.restype = ctypes.c_int
         L.orc_rope_queries.argtypes = [_u16p, _u16p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_double]
         L.orc_rope_queries.restype = None
@@ -171,6 +175,23 @@ def kv_append(k_new, v_new, pool, block_table, positions, *, page_size: int = 16
                                _ptr(pool, ctypes.c_uint16), num_pages,
                                _ptr(bt, ctypes.c_int32), bt.shape[1], _ptr(pos, ctypes.c_int32),
                                B, Hkv, D, page_size, theta)
+
+
+def kv_write_prefill(k, v, token_offsets, start_positions, pool, block_table, *,
+                     page_size: int = 16, theta: float = 500000.0) -> int:
+    """Write every sequence's new tokens (ragged, [num_tokens][Hkv][D]) into ``pool``."""
+    ka = _u16(k)
+    va = _u16(v)
+    assert pool.dtype == np.uint16 and pool.flags["C_CONTIGUOUS"]
+    off = _i32(token_offsets)
+    st = _i32(start_positions)
+    bt = _i32(block_table)
+    B = st.shape[0]
+    return lib().orc_kv_write_prefill(_ptr(ka, ctypes.c_uint16), _ptr(va, ctypes.c_uint16),
+                                      _ptr(off, ctypes.c_int32), _ptr(st, ctypes.c_int32),
+                                      _ptr(pool, ctypes.c_uint16), pool.shape[0],
+                                      _ptr(bt, ctypes.c_int32), bt.shape[1], B, ka.shape[1],
+                                      ka.shape[2], page_size, theta)
 
 
 # ------------------------------------------------------------- attention --

@@ -178,6 +178,36 @@ int orc_kv_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* pool,
   return status;
 }
 
+/*
+ * [README] "これまでの進捗", KV page pool item: prefill fills the prompt's
+ * pages.  Sequence b contributes the tokens [token_offsets[b],
+ * token_offsets[b+1]) of k/v ([num_tokens][Hkv][D]); token i of sequence b
+ * sits at absolute position start_positions[b] + i and is stored exactly as a
+ * one-token append at that position would store it (K rotated by RoPE at its
+ * position, V as given).  Tokens with a bad position or page are skipped and
+ * reported in the returned bit set.
+ */
+int orc_kv_write_prefill(const uint16_t* k, const uint16_t* v,
+                         const int32_t* token_offsets,
+                         const int32_t* start_positions, uint16_t* pool,
+                         int64_t num_pages, const int32_t* block_table,
+                         int max_blocks, int batch, int num_kv_heads,
+                         int head_dim, int page_size, double theta) {
+  int status = ORC_OK;
+  for (int b = 0; b < batch; ++b) {
+    for (int32_t t = token_offsets[b]; t < token_offsets[b + 1]; ++t) {
+      int32_t pos = start_positions[b] + (t - token_offsets[b]);
+      /* one token of sequence b, appended at pos through b's block table */
+      status |= orc_kv_append(k + (int64_t)t * num_kv_heads * head_dim,
+                              v + (int64_t)t * num_kv_heads * head_dim, pool,
+                              num_pages, block_table + (int64_t)b * max_blocks,
+                              max_blocks, &pos, 1, num_kv_heads, head_dim,
+                              page_size, theta);
+    }
+  }
+  return status;
+}
+
 /* Optional query rotation: q_out[b][j] = RoPE(q_in[b][j], positions[b]). */
 void orc_rope_queries(const uint16_t* q_in, uint16_t* q_out,
                       const int32_t* positions, int batch, int num_q_heads,

@@ -8,7 +8,7 @@ into it.  The binding is loaded lazily so that the seeded workload generator
 __version__ = "0.1.0"
 
 _BINDING_NAMES = {
-    "kv_append", "paged_decode_attention", "decode_step", "workspace_bytes", "plan_splits", "strerror",
+    "kv_append", "paged_decode_attention", "decode_step", "kv_write_prefill", "workspace_bytes", "plan_splits", "strerror",
     "abi_version", "PkvError",
 }
 

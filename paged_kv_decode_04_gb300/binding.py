@@ -27,6 +27,7 @@ DEVERR_PAGE = 1
 DEVERR_SEQLEN = 2
 DEVERR_POSITION = 4
 DEVERR_TIMEOUT = 8
+DEVERR_OFFSETS = 16
 
 NUM_Q_HEADS = 32
 NUM_KV_HEADS = 8
@@ -65,6 +66,9 @@ def _load():
     L.pkv_decode_step.argtypes = [vp, vp, vp, vp, i64, vp, i32, vp, i32, i32, i32, i32, i32, f64,
                                   f32, vp, vp, sz, i32, vp, vp]
     L.pkv_decode_step.restype = i32
+    L.pkv_kv_write_prefill.argtypes = [vp, vp, i32, vp, vp, vp, i64, vp, i32, i32, i32, i32, i32,
+                                       f64, vp, vp]
+    L.pkv_kv_write_prefill.restype = i32
     return L
 
 
@@ -232,3 +236,27 @@ def decode_step(q, k_new, v_new, pool, block_table, seq_lens, out=None, *,
     if rc != PKV_OK:
         raise PkvError(rc, "pkv_decode_step")
     return out
+
+
+def kv_write_prefill(k, v, token_offsets, start_positions, pool, block_table, *,
+                     rope_theta: float = 500000.0, dev_err=None, stream=None) -> None:
+    """Write a ragged batch of tokens (k, v: [num_tokens][Hkv][D]) into their pages."""
+    num_pages = _pool_pages(pool)
+    dev = pool.device
+    _check(k, "k", torch.bfloat16, 3, dev)
+    _check(v, "v", torch.bfloat16, 3, dev)
+    _check(token_offsets, "token_offsets", torch.int32, 1, dev)
+    _check(start_positions, "start_positions", torch.int32, 1, dev)
+    _check(block_table, "block_table", torch.int32, 2, dev)
+    B = start_positions.shape[0]
+    if token_offsets.shape[0] != B + 1 or block_table.shape[0] != B or v.shape != k.shape:
+        raise ValueError("token_offsets must have batch + 1 entries; k/v shapes must match")
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, None, dev)
+    rc = _lib.pkv_kv_write_prefill(_ptr(k), _ptr(v), k.shape[0], _ptr(token_offsets),
+                                   _ptr(start_positions), _ptr(pool), num_pages,
+                                   _ptr(block_table), block_table.shape[1], B, k.shape[1],
+                                   k.shape[2], PAGE_SIZE, float(rope_theta), _ptr(dev_err),
+                                   _stream(stream))
+    if rc != PKV_OK:
+        raise PkvError(rc, "pkv_kv_write_prefill")

@@ -99,7 +99,79 @@ __global__ void __launch_bounds__(kAppendThreads)
   reinterpret_cast<uint32_t*>(v_dst)[tid] = vw;
 }
 
+// Prefill write: one warp per token.  The token's sequence is found by a
+// binary search over token_offsets; lane i evaluates the (cos, sin) pair i of
+// the token's position in FP64 and rotates pair i of all 8 kv heads; the 512
+// value elements are copied as 8 words per lane.
+constexpr int kPrefillTokensPerCta = 8;
+
+__global__ void __launch_bounds__(kPrefillTokensPerCta * 32)
+    kv_write_prefill_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                            int num_tokens, const int32_t* __restrict__ token_offsets,
+                            const int32_t* __restrict__ start_positions,
+                            uint16_t* __restrict__ pool, int64_t num_pages,
+                            const int32_t* __restrict__ block_table, int max_blocks, int batch,
+                            RopeFreqs freqs, int32_t* dev_err) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kPrefillTokensPerCta + (threadIdx.x >> 5);
+  if (t >= num_tokens) return;
+  // largest b with token_offsets[b] <= t
+  int lo = 0, hi = batch;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (token_offsets[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int32_t first = token_offsets[b];
+  if (t < first || t >= token_offsets[b + 1]) {
+    if (lane == 0) record_error(dev_err, kErrOffsets);
+    return;
+  }
+  const int32_t pos = start_positions[b] + (t - first);
+  if (pos < 0 || pos >= max_blocks * kPageSize) {
+    if (lane == 0) record_error(dev_err, kErrPosition);
+    return;
+  }
+  const int32_t page = block_table[static_cast<int64_t>(b) * max_blocks + pos / kPageSize];
+  if (page < 0 || page >= num_pages) {
+    if (lane == 0) record_error(dev_err, kErrPage);
+    return;
+  }
+  const int slot = pos % kPageSize;
+  const int64_t row = kNumKvHeads * kHeadDim;
+  const int64_t src = static_cast<int64_t>(t) * row;
+  uint16_t* k_dst = pool + ((static_cast<int64_t>(page) * 2 + 0) * kPageSize + slot) * row;
+  uint16_t* v_dst = pool + ((static_cast<int64_t>(page) * 2 + 1) * kPageSize + slot) * row;
+  double sn, cs;
+  sincos(__dmul_rn(static_cast<double>(pos), freqs.inv_freq[lane]), &sn, &cs);
+#pragma unroll
+  for (int h = 0; h < kNumKvHeads; ++h) {
+    uint16_t y1, y2;
+    rotate_pair(k[src + h * kHeadDim + lane], k[src + h * kHeadDim + lane + kHalf], cs, sn,
+                &y1, &y2);
+    k_dst[h * kHeadDim + lane] = y1;
+    k_dst[h * kHeadDim + lane + kHalf] = y2;
+  }
+  const uint32_t* vs = reinterpret_cast<const uint32_t*>(v + src);
+  uint32_t* vd = reinterpret_cast<uint32_t*>(v_dst);
+#pragma unroll
+  for (int j = 0; j < static_cast<int>(row / 2) / 32; ++j) vd[lane + 32 * j] = vs[lane + 32 * j];
+}
+
 }  // namespace
+
+cudaError_t launch_kv_write_prefill(const uint16_t* k, const uint16_t* v, int num_tokens,
+                                    const int32_t* token_offsets,
+                                    const int32_t* start_positions, uint16_t* pool,
+                                    int64_t num_pages, const int32_t* block_table,
+                                    int max_blocks, int batch, const RopeFreqs& freqs,
+                                    int32_t* dev_err, cudaStream_t stream) {
+  const int ctas = (num_tokens + kPrefillTokensPerCta - 1) / kPrefillTokensPerCta;
+  kv_write_prefill_kernel<<<ctas, kPrefillTokensPerCta * 32, 0, stream>>>(
+      k, v, num_tokens, token_offsets, start_positions, pool, num_pages, block_table,
+      max_blocks, batch, freqs, dev_err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new,
                              uint16_t* pool, int64_t num_pages,

@@ -204,6 +204,31 @@ PKV_API int pkv_kv_append(const pkv_bf16* k_new, const pkv_bf16* v_new, pkv_bf16
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
+PKV_API int pkv_kv_write_prefill(const pkv_bf16* k, const pkv_bf16* v, int num_tokens,
+                                 const int32_t* token_offsets, const int32_t* start_positions,
+                                 pkv_bf16* pool, int64_t num_pages, const int32_t* block_table,
+                                 int max_blocks, int batch, int num_kv_heads, int head_dim,
+                                 int page_size, double rope_theta, int32_t* dev_err,
+                                 pkv_stream_t stream) {
+  if (!k || !v || !token_offsets || !start_positions || !pool || !block_table) return PKV_EINVAL;
+  if (num_tokens < 0 || batch < 1 || num_pages < 1 || num_pages > INT32_MAX || max_blocks < 1 ||
+      max_blocks > (INT32_MAX / kPageSize))
+    return PKV_EINVAL;
+  if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return PKV_EINVAL;
+  if (num_kv_heads != kNumKvHeads || head_dim != kHeadDim || page_size != kPageSize)
+    return PKV_EUNSUPPORTED;
+  if (!aligned(pool, 16) || !aligned(v, 4) || !aligned(k, 2) || !aligned(dev_err, 4))
+    return PKV_EALIGN;
+  if (num_tokens == 0) return PKV_OK;
+  pkv::RopeFreqs freqs;
+  for (int i = 0; i < kHeadDim / 2; ++i)
+    freqs.inv_freq[i] = pow(rope_theta, -(2.0 * i) / static_cast<double>(kHeadDim));
+  const cudaError_t err = pkv::launch_kv_write_prefill(
+      k, v, num_tokens, token_offsets, start_positions, pool, num_pages, block_table, max_blocks,
+      batch, freqs, dev_err, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 PKV_API int pkv_paged_decode_attention(const pkv_bf16* q, const pkv_bf16* pool,
                                        int64_t num_pages, const int32_t* block_table,
                                        int max_blocks, const int32_t* seq_lens, int batch,

@@ -21,6 +21,7 @@ constexpr int kErrPage = 1;
 constexpr int kErrSeqLen = 2;
 constexpr int kErrPosition = 4;
 constexpr int kErrTimeout = 8;
+constexpr int kErrOffsets = 16;
 
 // inv_freq[i] = theta^(-2i/64) for the 32 rotation pairs, passed by value.
 struct RopeFreqs {
@@ -40,6 +41,13 @@ cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new,
                              const RopeFreqs& freqs, const uint16_t* q_in,
                              uint16_t* q_out, int32_t* dev_err,
                              cudaStream_t stream);
+
+cudaError_t launch_kv_write_prefill(const uint16_t* k, const uint16_t* v, int num_tokens,
+                                    const int32_t* token_offsets,
+                                    const int32_t* start_positions, uint16_t* pool,
+                                    int64_t num_pages, const int32_t* block_table,
+                                    int max_blocks, int batch, const RopeFreqs& freqs,
+                                    int32_t* dev_err, cudaStream_t stream);
 
 struct AttnArgs {
   const uint16_t* q;

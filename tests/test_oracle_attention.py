@@ -246,3 +246,74 @@ def test_query_rotation_matches_single_vector_rotation():
     for b in range(2):
         for j in (0, 17, 31):
             assert np.array_equal(out[b, j], oracle.rope_rotate(q[b, j], int(pos[b]), THETA))
+
+
+# ----------------------------------------------------------------- prefill --
+
+def _complex_rope_bits(x_bits, pos, theta=THETA):
+    """RoPE through complex multiplication (independent of the oracle's loop),
+    rounded once to bf16 with the separately pinned converter."""
+    xv = oracle.bf16_to_f64(x_bits)
+    z = (xv[:32] + 1j * xv[32:]) * np.exp(1j * pos * np.power(theta, -np.arange(32) / 32.0))
+    return oracle.f64_to_bf16(np.concatenate([z.real, z.imag]))
+
+
+def test_prefill_writes_rotated_tokens_at_consecutive_positions():
+    rng = np.random.default_rng(30)
+    starts = np.array([0, 5, 30, 0], np.int32)
+    counts = np.array([20, 11, 3, 0], np.int32)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    T = int(off[-1])
+    k = bf16(rng.standard_normal((T, HKV, D)))
+    v = bf16(rng.standard_normal((T, HKV, D)))
+    pool = np.full((16, 2, P, HKV, D), POISON, dtype=np.uint16)
+    bt = np.full((4, 8), -1, np.int32)
+    bt[0, :2] = [3, 7]
+    bt[1, :1] = [9]
+    bt[2, :3] = [1, 2, 11]
+    before = pool.copy()
+    assert oracle.kv_write_prefill(k, v, off, starts, pool, bt) == 0
+    expect = before.copy()
+    for b in range(4):
+        for i in range(counts[b]):
+            t = off[b] + i
+            pos = starts[b] + i
+            page, slot = bt[b, pos // P], pos % P
+            for h in range(HKV):
+                expect[page, 0, slot, h] = _complex_rope_bits(k[t, h], pos)
+            expect[page, 1, slot] = v[t]
+    assert np.array_equal(pool, expect)
+
+
+def test_prefill_then_attention_equals_brute_force_on_rotated_keys():
+    rng = np.random.default_rng(31)
+    L = 37
+    k = bf16(rng.standard_normal((L, HKV, D)))
+    v = bf16(rng.standard_normal((L, HKV, D)))
+    q = bf16(rng.standard_normal((1, HQ, D)))
+    pool = np.full((8, 2, P, HKV, D), POISON, dtype=np.uint16)
+    bt = np.array([[4, 0, 6, -1]], np.int32)
+    assert oracle.kv_write_prefill(k, v, np.array([0, L], np.int32), np.array([0], np.int32),
+                                   pool, bt) == 0
+    got = oracle.decode_attention(q, pool, bt, np.array([L], np.int32))
+    for j in (0, 9, 31):
+        g = j // 4
+        K = np.stack([oracle.bf16_to_f64(_complex_rope_bits(k[t, g], t)) for t in range(L)])
+        V = oracle.bf16_to_f64(v[:, g])
+        w = scipy.special.softmax(SCALE * (K @ oracle.bf16_to_f64(q[0, j])))
+        assert np.allclose(got[0, j], w @ V, rtol=1e-12, atol=1e-14)
+
+
+def test_prefill_bad_positions_are_skipped():
+    rng = np.random.default_rng(32)
+    k = bf16(rng.standard_normal((3, HKV, D)))
+    pool = np.full((4, 2, P, HKV, D), POISON, dtype=np.uint16)
+    bt = np.array([[1, -1]], np.int32)          # block 1 is unmapped
+    before = pool.copy()
+    rc = oracle.kv_write_prefill(k, k, np.array([0, 3], np.int32), np.array([15], np.int32),
+                                 pool, bt)
+    assert rc & oracle.ORC_EBADPAGE
+    # position 15 was written, 16 and 17 (block 1) were not
+    assert not np.array_equal(pool[1, :, 15], before[1, :, 15])
+    changed = np.argwhere(np.any(pool != before, axis=(3, 4)))
+    assert {tuple(c) for c in changed.tolist()} == {(1, 0, 15), (1, 1, 15)}
