@@ -51,6 +51,9 @@ WORKLOAD_TEXT = {
     "long": "long: 1 seq x 2048 ctx x 16 layers, 32q/8kv/64 bf16, shuffled pages, 4096-page pool",
     "small": "small: 8 seqs, lengths U[1,2048], 1 layer, 4096-page pool",
     "tiny": "tiny: 1 seq x 37 ctx, 1 layer, 64-page pool",
+    "prefix": "prefix: 256 seqs x 2048 ctx, groups of 16 share a 1536-token prefix (96 aliased "
+              "pages) + 32 private pages each, 9728 live pages in a 40000-page pool; K/V bytes "
+              "are counted per sequence (effective bandwidth: shared pages may hit in L2)",
 }
 
 

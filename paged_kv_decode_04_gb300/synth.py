@@ -83,7 +83,7 @@ def _bf16_normal(gen: torch.Generator, n: int) -> np.ndarray:
 def _lengths(name: str, rng: np.random.Generator, batch: int) -> np.ndarray:
     if name == "tiny":
         return np.full(batch, 37, dtype=np.int32)
-    if name in ("long", "peak"):
+    if name in ("long", "peak", "prefix"):
         return np.full(batch, 2048, dtype=np.int32)
     if name == "small":
         return rng.integers(1, 2048, size=batch, endpoint=True).astype(np.int32)
@@ -104,17 +104,28 @@ WORKLOADS = {
     "small": (1, 8, 4096),
     "peak": (1, 256, 40000),
     "mix": (16, 128, 262144),
+    "prefix": (1, 256, 40000),
 }
-WORKLOAD_INDEX = {"tiny": 0, "long": 1, "small": 2, "peak": 3, "mix": 4}
+WORKLOAD_INDEX = {"tiny": 0, "long": 1, "small": 2, "peak": 3, "mix": 4, "prefix": 5}
+# "prefix": consecutive groups of PREFIX_GROUP sequences share their first
+# PREFIX_BLOCKS pages (a common 1536-token prompt prefix).
+PREFIX_GROUP = 16
+PREFIX_BLOCKS = 96
 
 
 def make_workload(name: str, seed: int = 0, *, seq_lens=None, batch=None, layers=None,
-                  num_pages=None, max_blocks: int = MAX_BLOCKS) -> Workload:
+                  num_pages=None, max_blocks: int = MAX_BLOCKS, share_group: int = None,
+                  share_blocks: int = None) -> Workload:
     """Draw one of the named workloads (or a custom one via the keyword overrides).
 
     The seed mixes in the workload's index so that different workloads drawn
-    with the same seed are independent.
+    with the same seed are independent.  With share_group = G and
+    share_blocks = S, consecutive groups of G sequences alias the same S
+    physical pages as their first S blocks (a shared prompt prefix); every
+    sequence must then be longer than S pages' worth of tokens.
     """
+    if name == "prefix" and share_group is None:
+        share_group, share_blocks = PREFIX_GROUP, PREFIX_BLOCKS
     if name in WORKLOADS:
         d_layers, d_batch, d_pages = WORKLOADS[name]
         mix = WORKLOAD_INDEX[name]
@@ -134,7 +145,12 @@ def make_workload(name: str, seed: int = 0, *, seq_lens=None, batch=None, layers
     if np.any(seq_lens > max_blocks * PAGE_SIZE):
         raise ValueError("sequence longer than the block table allows")
     blocks = [_num_blocks(int(L), PAGE_SIZE) for L in seq_lens]
-    n_live = layers * sum(blocks)
+    share_group = share_group or 1
+    share_blocks = share_blocks or 0
+    if share_blocks and any(int(L) <= share_blocks * PAGE_SIZE for L in seq_lens):
+        raise ValueError("shared prefixes need every sequence longer than the shared pages")
+    followers = batch - (-(-batch // share_group)) if share_blocks else 0
+    n_live = layers * (sum(blocks) - followers * share_blocks)
     if n_live > num_pages:
         raise ValueError(f"{n_live} live pages do not fit a {num_pages}-page pool")
 
@@ -144,11 +160,18 @@ def make_workload(name: str, seed: int = 0, *, seq_lens=None, batch=None, layers
 
     bt = np.full((layers, batch, max_blocks), -1, dtype=np.int32)
     cursor = 0
+    owned = []  # (b, first owned block, blocks) for each run of live pages, in order
     for layer in range(layers):
         for b in range(batch):
             n = blocks[b]
-            bt[layer, b, :n] = live[cursor:cursor + n]
-            cursor += n
+            first = 0
+            if share_blocks and b % share_group != 0:
+                lead = b - b % share_group  # alias the group leader's prefix pages
+                bt[layer, b, :share_blocks] = bt[layer, lead, :share_blocks]
+                first = share_blocks
+            bt[layer, b, first:n] = live[cursor:cursor + n - first]
+            owned.append((b, first, n))
+            cursor += n - first
 
     Hq, Hkv, D, P = NUM_Q_HEADS, NUM_KV_HEADS, HEAD_DIM, PAGE_SIZE
     page_elems = 2 * P * Hkv * D
@@ -161,13 +184,11 @@ def make_workload(name: str, seed: int = 0, *, seq_lens=None, batch=None, layers
     # Poison every slot at or past the appended position (position L-1) of each
     # sequence's last page; the append step writes position L-1 itself.
     cursor = 0
-    for layer in range(layers):
-        for b in range(batch):
-            n = blocks[b]
-            if n:
-                first_dead = (int(seq_lens[b]) - 1) % P
-                page_data[cursor + n - 1, :, first_dead:, :, :] = POISON
-            cursor += n
+    for b, first, n in owned:
+        if n > first:
+            first_dead = (int(seq_lens[b]) - 1) % P
+            page_data[cursor + n - first - 1, :, first_dead:, :, :] = POISON
+        cursor += n - first
 
     q = _bf16_normal(gen, layers * batch * Hq * D).reshape(layers, batch, Hq, D)
     k_new = _bf16_normal(gen, layers * batch * Hkv * D).reshape(layers, batch, Hkv, D)

@@ -62,3 +62,20 @@ def test_compact_is_a_relabelling():
     for r, b in enumerate([1, 5]):
         n = -(-int(w.seq_lens[b]) // 16)
         assert np.array_equal(c.pool[c.block_table[r, :n]], pool[w.block_tables[0, b, :n]])
+
+
+def test_prefix_workload_aliases_group_prefixes():
+    w = synth.make_workload("prefix", 0, batch=32, num_pages=4096)
+    bt = w.block_tables[0]
+    G, S = synth.PREFIX_GROUP, synth.PREFIX_BLOCKS
+    for b in range(32):
+        lead = b - b % G
+        assert np.array_equal(bt[b, :S], bt[lead, :S])
+    assert not np.any(np.isin(bt[0, :S], bt[G, :S]))          # groups do not share
+    private = bt[:, S:][bt[:, S:] >= 0]
+    assert len(np.unique(private)) == len(private)              # tails are private
+    assert len(np.unique(bt[bt >= 0])) == len(w.live_pages)
+    # shared pages hold no poison; each private last page holds poison from slot 15 on
+    pool = synth.host_pool(w)
+    assert not np.any(pool[bt[0, :S]] == synth.POISON)
+    assert np.all(pool[bt[:, 127], :, 15:] == synth.POISON)
