@@ -551,6 +551,46 @@ def run_prefill(args, world, rank, local):
     return 0
 
 
+def run_serve(args, world, rank, local):
+    """Continuous-batching serving simulation driven by the host scheduler."""
+    import torch
+    from paged_kv_decode_04_gb300.engine import Engine
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    rng = np.random.default_rng(args.seed)
+    layers, num_pages = 16, 65536
+    reqs = [(int(rng.integers(16, 1025)), int(rng.integers(16, 513)))
+            for _ in range(args.serve_requests)]
+    warm = Engine(num_pages, layers, dev, static_batching=args.static, seed=args.seed + 1)
+    warm.run(reqs[:8])
+    eng = Engine(num_pages, layers, dev, static_batching=args.static, seed=args.seed)
+    barrier(world)
+    res = eng.run(reqs)
+    barrier(world)
+    secs = max_over_ranks(res["seconds"], world, dev)
+    toks = sum_over_ranks(res["decode_tokens"], world, dev)
+    if rank == 0:
+        st = res["stats"]
+        print(json.dumps({
+            "metric": "serving simulation decode tokens/s (scheduler-driven, 16 layers)",
+            "value": round(toks / secs, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": res["iterations"], "warmup": 1, "ms_per_step": round(secs / res["iterations"] * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "storage_dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{len(reqs)} requests, prompt U[16,1024], max_new U[16,512], "
+                                   f"{layers} layers, {num_pages}-page pool (2 GiB), "
+                                   f"{'static' if args.static else 'continuous'} batching",
+                       "seed": args.seed},
+            "stats": {k: st[k] for k in ("pool_pages", "peak_active", "largest_decode_batch",
+                                         "peak_allocated_pages", "admission_wait_total",
+                                         "admission_wait_max", "free_pages", "rejected",
+                                         "finished")},
+            "wall_s": round(secs, 3)}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -570,8 +610,11 @@ def main(argv=None):
     ap.add_argument("--ref-seqs", type=int, default=1,
                     help="sequences per step of the --impl reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["decode", "prefill"], default="decode",
-                    help="decode: the decode step (headline); prefill: the paged prefill write")
+    ap.add_argument("--op", choices=["decode", "prefill", "serve"], default="decode",
+                    help="decode: the decode step (headline); prefill: the paged prefill write; "
+                         "serve: scheduler-driven serving simulation")
+    ap.add_argument("--serve-requests", type=int, default=512)
+    ap.add_argument("--static", action="store_true", help="serve: static instead of continuous")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -580,6 +623,8 @@ def main(argv=None):
         return run_reference(args, world, rank)
     if args.op == "prefill":
         return run_prefill(args, world, rank, local)
+    if args.op == "serve":
+        return run_serve(args, world, rank, local)
     return run_ours(args, world, rank, local)
 
 

@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "pkv")
 LIB = os.path.join(PKG, "libpkv.so")
-SOURCES = ["kv_append.cu", "decode_attention.cu", "pkv_api.cu"]
+SOURCES = ["kv_append.cu", "decode_attention.cu", "pkv_api.cu", "scheduler.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,7 +34,7 @@ def nvcc() -> str:
 
 def _deps():
     paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    paths.append(os.path.join(INCLUDE, "pkv.h"))
+    paths += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     return paths
 
 
@@ -56,7 +56,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         cmd = common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -154,6 +154,8 @@ PKV_API const char* pkv_strerror(int status) {
     case PKV_EWORKSPACE: return "workspace missing or smaller than pkv_workspace_bytes()";
     case PKV_ECUDA: return "CUDA runtime error (launch failed or no usable device)";
     case PKV_EALIGN: return "pointer alignment requirement violated";
+    case 7: return "request rejected: its page budget exceeds the whole pool";
+    case 8: return "unknown or already finished request id";
     case PKV_ESCRATCH: return "split partials would exceed the static scratch buffer (PKV_STATIC_SCRATCH_BYTES); use fewer splits";
     default: return "unknown status";
   }

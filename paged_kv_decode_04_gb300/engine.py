@@ -1,0 +1,102 @@
+"""A synthetic serving loop: the host scheduler (include/pkv_sched.h) drives the
+prefill write and the fused decode step on the GPU.
+
+Each iteration is one scheduling point: admit waiting requests, prefill at
+most one admitted prompt (its K/V written into freshly allocated pages of
+every layer), then run one decode step for every prefilled sequence (one new
+token appended at its next position and attended over its pages, per
+layer).  Request K/V/q values are synthetic (seeded N(0, 1) rounded to bf16);
+there are no weights, so "tokens" are the decode steps the scheduler issues.
+This mirrors the engine loop of the Tiny-vLLM README ("これまでの進捗":
+static and continuous batching; "現在のスコープ": one prompt prefilled
+between decode iterations).
+"""
+from __future__ import annotations
+
+import time
+
+import numpy as np
+import torch
+
+from . import binding
+from .scheduler import Scheduler
+
+HQ, HKV, D, P = 32, 8, 64, 16
+
+
+class Engine:
+    def __init__(self, num_pages: int, layers: int, device, *, max_context: int = 2048,
+                 static_batching: bool = False, max_batch: int = 256, seed: int = 0,
+                 host_inputs: bool = False):
+        self.dev = torch.device(device)
+        self.layers = layers
+        self.max_batch = max_batch
+        self.max_blocks = max_context // P
+        self.sched = Scheduler(num_pages, layers, max_context, P, static_batching)
+        self.pool = torch.full((num_pages, 2, P, HKV, D), -1, dtype=torch.int16,
+                               device=self.dev).view(torch.bfloat16)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.dev)
+        # the automatic split plan depends on the batch size: size the
+        # workspace for the largest need over every batch the loop may build
+        need = max(binding.workspace_bytes(n, self.max_blocks) for n in range(1, max_batch + 1))
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.dev)
+        self.host_inputs = host_inputs
+        self.rng = np.random.default_rng(seed)
+        self.gen = torch.Generator(device=self.dev).manual_seed(seed)
+
+    def _normal(self, shape):
+        if self.host_inputs:
+            x = torch.from_numpy(self.rng.standard_normal(shape).astype(np.float32))
+            return x.to(torch.bfloat16).to(self.dev)
+        return torch.randn(shape, generator=self.gen, device=self.dev).to(torch.bfloat16)
+
+    def step(self, on_prefill=None, on_decode=None) -> int:
+        """One scheduling point; returns the decode batch size."""
+        self.sched.admit()
+        got = self.sched.next_prefill()
+        if got is not None:
+            rid, plen, bt = got
+            off = torch.tensor([0, plen], dtype=torch.int32, device=self.dev)
+            st = torch.zeros(1, dtype=torch.int32, device=self.dev)
+            for layer in range(self.layers):
+                k = self._normal((plen, HKV, D))
+                v = self._normal((plen, HKV, D))
+                btl = torch.from_numpy(bt[layer:layer + 1].copy()).to(self.dev)
+                binding.kv_write_prefill(k, v, off, st, self.pool, btl, dev_err=self.err)
+                if on_prefill is not None:
+                    on_prefill(layer, rid, k, v, bt[layer])
+        ids, lens, bts = self.sched.decode_batch(self.max_batch)
+        n = len(ids)
+        if n:
+            dlens = torch.from_numpy(lens).to(self.dev)
+            for layer in range(self.layers):
+                q = self._normal((n, HQ, D))
+                kn = self._normal((n, HKV, D))
+                vn = self._normal((n, HKV, D))
+                btl = torch.from_numpy(bts[layer]).to(self.dev)
+                out = binding.decode_step(q, kn, vn, self.pool, btl, dlens, workspace=self.ws,
+                                          dev_err=self.err)
+                if on_decode is not None:
+                    on_decode(layer, ids, lens, bts[layer], q, kn, vn, out)
+        return n
+
+    def run(self, requests, max_iters: int = 1_000_000, on_prefill=None, on_decode=None):
+        """Serve `requests` [(prompt_tokens, max_new_tokens)] to completion."""
+        ids = [self.sched.submit(p, n) for p, n in requests]
+        tokens = 0
+        iters = 0
+        torch.cuda.synchronize(self.dev)
+        t0 = time.perf_counter()
+        while iters < max_iters:
+            st = self.sched.stats()
+            if st["waiting"] == 0 and st["active"] == 0:
+                break
+            tokens += self.step(on_prefill, on_decode)
+            iters += 1
+        torch.cuda.synchronize(self.dev)
+        dt = time.perf_counter() - t0
+        self.sched.admit()   # release what the last step finished
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(self.err.item())}")
+        return {"request_ids": ids, "decode_tokens": tokens, "iterations": iters,
+                "seconds": dt, "stats": self.sched.stats()}
