@@ -7,7 +7,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pkv.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -20,14 +21,18 @@ def lib():
 
 
 def declared_symbols():
-    text = open(HEADER).read()
-    return re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)
+    names = []
+    for h in HEADERS:
+        names += re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", open(h).read())
+    return names
 
 
 def test_header_declares_the_boundary():
     names = set(declared_symbols())
     assert {"pkv_kv_append", "pkv_paged_decode_attention", "pkv_workspace_bytes",
-            "pkv_strerror", "pkv_abi_version", "pkv_plan_splits"} <= names
+            "pkv_strerror", "pkv_abi_version", "pkv_plan_splits", "pkv_decode_step",
+            "pkv_kv_write_prefill", "pkv_sched_create", "pkv_sched_admit",
+            "pkv_sched_decode_batch"} <= names
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -104,3 +109,35 @@ def test_append_argument_errors(lib):
     assert append(lib, q_in=A, q_out=A, hq=8) == B.PKV_EUNSUPPORTED
     assert append(lib, v=ctypes.c_void_p(0x10002)) == B.PKV_EALIGN
     assert append(lib, batch=0) == B.PKV_OK
+
+
+def test_decode_step_and_prefill_argument_errors(lib):
+    from paged_kv_decode_04_gb300 import binding as B
+    f = lib.pkv_decode_step
+
+    def step(**kw):
+        args = dict(q=A, k=A, v=A, pool=A, num_pages=64, bt=A, max_blocks=128, lens=A, batch=1,
+                    hq=32, hkv=8, d=64, ps=16, theta=500000.0, scale=0.125, out=A, ws=None,
+                    ws_bytes=0, splits=1, err=None, stream=None)
+        args.update(kw)
+        return f(*args.values())
+    assert step(k=None) == B.PKV_EINVAL
+    assert step(theta=0.0) == B.PKV_EINVAL
+    assert step(hkv=4) == B.PKV_EUNSUPPORTED
+    assert step(v=ctypes.c_void_p(0x10002)) == B.PKV_EALIGN
+    assert step(splits=8) == B.PKV_EWORKSPACE
+    assert step(batch=0) == B.PKV_OK
+
+    g = lib.pkv_kv_write_prefill
+
+    def pre(**kw):
+        args = dict(k=A, v=A, n=10, off=A, st=A, pool=A, num_pages=64, bt=A, max_blocks=128,
+                    batch=1, hkv=8, d=64, ps=16, theta=500000.0, err=None, stream=None)
+        args.update(kw)
+        return g(*args.values())
+    assert pre(off=None) == B.PKV_EINVAL
+    assert pre(n=-1) == B.PKV_EINVAL
+    assert pre(batch=0) == B.PKV_EINVAL
+    assert pre(d=128) == B.PKV_EUNSUPPORTED
+    assert pre(pool=ctypes.c_void_p(0x10004)) == B.PKV_EALIGN
+    assert pre(n=0) == B.PKV_OK
