@@ -299,7 +299,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
-    w = synth.make_workload(args.workload, args.seed)
+    w = synth.make_workload(args.workload, args.seed, num_pages=args.pool_pages)
     d = synth.device_inputs(w, dev)
     B, layers = w.batch, w.layers
     stream = torch.cuda.current_stream(dev)
@@ -467,7 +467,7 @@ def run_ours(args, world, rank, local):
             "path": ("fused append+attention (pkv_decode_step)" if fused
                      else "pkv_kv_append then pkv_paged_decode_attention"),
             "launch": "one CUDA graph per step" if args.graph else "eager launches",
-            "num_splits": splits, "layers_per_step": layers,
+            "num_splits": splits, "layers_per_step": layers, "pool_pages": w.num_pages,
             "l2": ("inputs larger than L2: %.2f GiB of K/V streamed per step vs 129 MB L2; no flush"
                    % (w.kv_bytes() / 2 ** 30)) if w.kv_bytes() > 512 * 2 ** 20 else
                   "working set fits in L2 (no flush): L2-resident figure",
@@ -614,6 +614,8 @@ def main(argv=None):
                     help="decode: the decode step (headline); prefill: the paged prefill write; "
                          "serve: scheduler-driven serving simulation")
     ap.add_argument("--serve-requests", type=int, default=512)
+    ap.add_argument("--pool-pages", type=int, default=None,
+                    help="override the workload's pool size in pages (same live pages, denser pool)")
     ap.add_argument("--static", action="store_true", help="serve: static instead of continuous")
     args = ap.parse_args(argv)
     if args.warmup < 3:

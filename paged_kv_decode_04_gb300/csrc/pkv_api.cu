@@ -43,10 +43,10 @@ int current_sm_count() {
   return v;
 }
 
-// Split plan: S logical page ranges of pages_per_split pages per sequence.
-// Explicit S is honoured (capped by the table width); S = 0 aims for about
-// four CTAs per SM across (sequence, kv head, split) while keeping at least
-// four pages per range.
+// Split plan: S logical page ranges of pages_per_split pages per sequence,
+// one CTA each.  Explicit S is honoured (capped by the table width); S = 0
+// aims for about four CTAs per SM across (sequence, kv head, range) while
+// keeping at least four pages per range.
 bool make_plan(int batch, int max_blocks, int num_splits, pkv::SplitPlan* plan) {
   int S;
   if (num_splits > 0) {
@@ -67,6 +67,35 @@ bool make_plan(int batch, int max_blocks, int num_splits, pkv::SplitPlan* plan) 
   plan->pages_per_split = pps;
   plan->num_splits = (max_blocks + pps - 1) / pps;
   return true;
+}
+
+size_t plan_workspace(int batch, const pkv::SplitPlan& plan) {
+  return pkv::workspace_bytes_for(batch, kNumQHeads, kHeadDim, plan);
+}
+
+// Launch attention (append == nullptr) or the fused step under `plan`.
+cudaError_t launch_attention(const pkv::SplitPlan& plan, const CUtensorMap& map,
+                             const pkv_bf16* q, const int32_t* block_table, int max_blocks,
+                             const int32_t* seq_lens, int batch, float scale, pkv_bf16* out,
+                             void* workspace, int32_t* dev_err, int64_t num_pages,
+                             cudaStream_t stream, const pkv::AppendArgs* append) {
+  pkv::AttnArgs args;
+  args.q = q;
+  args.block_table = block_table;
+  args.seq_lens = seq_lens;
+  args.out = out;
+  const size_t need = pkv::workspace_bytes_for(batch, kNumQHeads, kHeadDim, plan);
+  float* ws = static_cast<float*>(workspace);
+  const size_t acc_elems = static_cast<size_t>(batch) * kNumQHeads * plan.num_splits * kHeadDim;
+  args.part_acc = need > 0 ? ws : nullptr;
+  args.part_ml = need > 0 ? ws + acc_elems : nullptr;
+  args.dev_err = dev_err;
+  args.num_pages = num_pages;
+  args.max_blocks = max_blocks;
+  args.batch = batch;
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.plan = plan;
+  return pkv::launch_paged_decode_attention(map, args, stream, append);
 }
 
 bool supported_dims(int num_q_heads, int num_kv_heads, int head_dim, int page_size) {
@@ -176,7 +205,7 @@ PKV_API size_t pkv_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
   if (batch == 0) return 0;
   pkv::SplitPlan plan;
   if (!make_plan(batch, max_blocks, num_splits, &plan)) return static_cast<size_t>(-1);
-  return pkv::workspace_bytes_for(batch, num_q_heads, head_dim, plan);
+  return plan_workspace(batch, plan);
 }
 
 PKV_API int pkv_kv_append(const pkv_bf16* k_new, const pkv_bf16* v_new, pkv_bf16* pool,
@@ -251,27 +280,14 @@ PKV_API int pkv_paged_decode_attention(const pkv_bf16* q, const pkv_bf16* pool,
   if (batch == 0) return PKV_OK;
   pkv::SplitPlan plan;
   if (!make_plan(batch, max_blocks, num_splits, &plan)) return PKV_ECUDA;
-  const size_t need = pkv::workspace_bytes_for(batch, num_q_heads, head_dim, plan);
+  const size_t need = plan_workspace(batch, plan);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
   CUtensorMap map;
   if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
-  pkv::AttnArgs args;
-  args.q = q;
-  args.block_table = block_table;
-  args.seq_lens = seq_lens;
-  args.out = out;
-  float* ws = static_cast<float*>(workspace);
-  const size_t acc_elems = static_cast<size_t>(batch) * num_q_heads * plan.num_splits * head_dim;
-  args.part_acc = need > 0 ? ws : nullptr;
-  args.part_ml = need > 0 ? ws + acc_elems : nullptr;
-  args.dev_err = dev_err;
-  args.num_pages = num_pages;
-  args.max_blocks = max_blocks;
-  args.batch = batch;
-  args.scale_log2 = scale * 1.4426950408889634f;
-  args.plan = plan;
   const cudaError_t err =
-      pkv::launch_paged_decode_attention(map, args, reinterpret_cast<cudaStream_t>(stream));
+      launch_attention(plan, map, q, block_table, max_blocks, seq_lens, batch, scale, out,
+                       workspace, dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream),
+                       nullptr);
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -294,33 +310,20 @@ PKV_API int pkv_decode_step(const pkv_bf16* q, const pkv_bf16* k_new, const pkv_
   if (batch == 0) return PKV_OK;
   pkv::SplitPlan plan;
   if (!make_plan(batch, max_blocks, num_splits, &plan)) return PKV_ECUDA;
-  const size_t need = pkv::workspace_bytes_for(batch, num_q_heads, head_dim, plan);
+  const size_t need = plan_workspace(batch, plan);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
   CUtensorMap map;
   if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
-  pkv::AttnArgs args;
-  args.q = q;
-  args.block_table = block_table;
-  args.seq_lens = seq_lens;
-  args.out = out;
-  float* ws = static_cast<float*>(workspace);
-  const size_t acc_elems = static_cast<size_t>(batch) * num_q_heads * plan.num_splits * head_dim;
-  args.part_acc = need > 0 ? ws : nullptr;
-  args.part_ml = need > 0 ? ws + acc_elems : nullptr;
-  args.dev_err = dev_err;
-  args.num_pages = num_pages;
-  args.max_blocks = max_blocks;
-  args.batch = batch;
-  args.scale_log2 = scale * 1.4426950408889634f;
-  args.plan = plan;
   pkv::AppendArgs app;
   app.k_new = k_new;
   app.v_new = v_new;
   app.pool = pool;
   for (int i = 0; i < kHeadDim / 2; ++i)
     app.freqs.inv_freq[i] = pow(rope_theta, -(2.0 * i) / static_cast<double>(kHeadDim));
-  const cudaError_t err = pkv::launch_paged_decode_attention(
-      map, args, reinterpret_cast<cudaStream_t>(stream), &app);
+  const cudaError_t err =
+      launch_attention(plan, map, q, block_table, max_blocks, seq_lens, batch, scale, out,
+                       workspace, dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream),
+                       &app);
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -370,7 +373,7 @@ extern "C" PKV_API int pkv_paged_decode_attention_static_ws(
   if (batch == 0) return PKV_OK;
   pkv::SplitPlan plan;
   if (!make_plan(batch, max_blocks, num_splits, &plan)) return PKV_ECUDA;
-  const size_t need = pkv::workspace_bytes_for(batch, num_q_heads, head_dim, plan);
+  const size_t need = plan_workspace(batch, plan);
   if (need > PKV_STATIC_SCRATCH_BYTES) return PKV_ESCRATCH;
   float* ws = nullptr;
   if (need > 0) {
@@ -381,21 +384,8 @@ extern "C" PKV_API int pkv_paged_decode_attention_static_ws(
   }
   CUtensorMap map;
   if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
-  pkv::AttnArgs args;
-  args.q = q;
-  args.block_table = block_table;
-  args.seq_lens = seq_lens;
-  args.out = out;
-  const size_t acc_elems = static_cast<size_t>(batch) * num_q_heads * plan.num_splits * head_dim;
-  args.part_acc = ws;
-  args.part_ml = ws != nullptr ? ws + acc_elems : nullptr;
-  args.dev_err = dev_err;
-  args.num_pages = num_pages;
-  args.max_blocks = max_blocks;
-  args.batch = batch;
-  args.scale_log2 = scale * 1.4426950408889634f;
-  args.plan = plan;
   const cudaError_t err =
-      pkv::launch_paged_decode_attention(map, args, reinterpret_cast<cudaStream_t>(stream));
+      launch_attention(plan, map, q, block_table, max_blocks, seq_lens, batch, scale, out, ws,
+                       dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream), nullptr);
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
