@@ -21,9 +21,15 @@
  *  - Every tensor pointer is DEVICE memory owned by the caller, unless the
  *    comment says otherwise.  The library never allocates, frees or
  *    synchronizes; all work is enqueued on `stream` (NULL = the legacy
- *    default stream) and returns before it runs.  The library keeps no state
- *    between calls beyond a per-thread cache of TMA descriptors and of the
- *    device's SM count; calls are thread-safe.
+ *    default stream) and returns before it runs.  Calls are thread-safe.
+ *    State kept between calls: a per-thread cache of TMA descriptors, the
+ *    device's SM count, and one RoPE cos/sin table per device for positions
+ *    below 2048 (1.5 MiB of static device memory).  The table is rebuilt on
+ *    the calling stream whenever a call brings a rope_theta different from
+ *    the last one seen on that device; kernels use it only while it holds
+ *    their theta and otherwise evaluate sincos themselves, with identical
+ *    results.  Calls with different rope_theta values must not run
+ *    concurrently on one device (a rebuild would race with the readers).
  *  - Pool layout: [num_pages][2 (K, V)][page_size][num_kv_heads][head_dim]
  *    bf16, i.e. element ((page*2 + kv)*page_size + slot)*Hkv*D + h*D + d.
  *    The pool must be 16-byte aligned.

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   AppendRow arow{};
   if (owns_last) {
     const int64_t src = (static_cast<int64_t>(b) * kNumKvHeads + g) * kHeadDim;
-    arow = make_append_row(ap.k_new + src, ap.v_new + src, L - 1, ap.freqs.inv_freq, lane);
+    arow = make_append_row(ap.k_new + src, ap.v_new + src, L - 1, ap.freqs, lane);
     const int pid = s_pages[last_local];
     if (pid >= 0) store_append_row(ap.pool, pid, a_slot, g, arow, lane);
   }

@@ -188,14 +188,14 @@ struct AppendRow {
 
 __device__ __forceinline__ AppendRow make_append_row(const uint16_t* k_src,
                                                      const uint16_t* v_src, int pos,
-                                                     const double* inv_freq, int lane) {
+                                                     const RopeFreqs& f, int lane) {
   AppendRow r;
   const uint16_t x1 = k_src[lane];
   const uint16_t x2 = k_src[lane + 32];
   r.v = reinterpret_cast<const uint32_t*>(v_src)[lane];
-  double sn, cs;
-  sincos(__dmul_rn(static_cast<double>(pos), inv_freq[lane]), &sn, &cs);
-  rotate_pair(x1, x2, cs, sn, &r.k1, &r.k2);
+  const bool table_ok = rope_table_ready(f);
+  RopeCS cs = rope_cs(f, table_ok, pos, lane);
+  rotate_pair_rope(f, table_ok, pos, lane, cs, x1, x2, &r.k1, &r.k2);
   return r;
 }
 

@@ -1,18 +1,24 @@
-// kv_append.cu -- decode-time KV append with rotate-half RoPE.
+// kv_append.cu -- KV writes with rotate-half RoPE: the one-token decode append
+// and the multi-token prefill write, plus the per-device cos/sin table they
+// (and the fused decode step) read.
 //
 // Tiny-vLLM README ("Hours of YouTube and 85 handtyped pages of notes on LLM
 // Inference - Start here"), section "これまでの進捗", KV page pool item: each
 // decode step adds one new token per sequence at its absolute RoPE position
-// into the sequence's page slot of the shared BF16 pool.
+// into the sequence's page slot of the shared BF16 pool; prefill fills the
+// prompt's pages.
 //
-// One CTA per sequence.  Warp 0 evaluates the 32 (cos, sin) pairs of the
-// token's position in FP64 once; all 256 threads then rotate the 8 kv heads'
-// keys (one thread per (head, frequency) pair), copy the values, and, when
-// asked, rotate the 32 query heads out of place.  The rotation is FP64 with
-// separately rounded products (no contraction) and one rounding to bf16, so
-// the stored keys are a deterministic function of the inputs.
+// The stored key is rotate_pair's value: the rotation evaluated in FP64 with
+// separately rounded products and one rounding to bf16.  rotate_pair_rope
+// reaches the same bits with FP32 arithmetic plus an FP64 redo of the rare
+// elements that land next to a bf16 rounding midpoint, and the (cos, sin)
+// pairs come from a table built once per rope_theta instead of an FP64
+// sincos per element, since FP64 is slow on this part.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -23,7 +29,28 @@ namespace {
 
 constexpr int kAppendThreads = 256;
 constexpr int kHalf = kHeadDim / 2;
+constexpr int kRopeEntries = kRopeTablePositions * kHalf;
 
+// This device's cos/sin table and the theta it holds (NaN = none).
+__device__ float2 g_rope32[kRopeEntries];
+__device__ double2 g_rope64[kRopeEntries];
+__device__ double g_rope_theta;
+
+__global__ void rope_tag_kernel(double value) { g_rope_theta = value; }
+
+__global__ void __launch_bounds__(256) rope_table_kernel(RopeFreqs f) {
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  if (e >= kRopeEntries) return;
+  const int pos = e / kHalf, i = e % kHalf;
+  double sn, cs;
+  sincos(__dmul_rn(static_cast<double>(pos), f.inv_freq[i]), &sn, &cs);
+  g_rope64[e] = make_double2(cs, sn);
+  g_rope32[e] = make_float2(static_cast<float>(cs), static_cast<float>(sn));
+}
+
+// One CTA per sequence, thread (h, i) rotates pair i of kv head h (and of
+// query heads h, h + 8, h + 16, h + 24 when asked); V is copied one word per
+// thread.  Every load that does not depend on the position is issued first.
 __global__ void __launch_bounds__(kAppendThreads)
     kv_append_kernel(const uint16_t* __restrict__ k_new,
                      const uint16_t* __restrict__ v_new,
@@ -32,32 +59,21 @@ __global__ void __launch_bounds__(kAppendThreads)
                      const int32_t* __restrict__ positions, RopeFreqs freqs,
                      const uint16_t* __restrict__ q_in,
                      uint16_t* __restrict__ q_out, int32_t* dev_err) {
-  __shared__ double s_cos[kHalf];
-  __shared__ double s_sin[kHalf];
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int h = tid / kHalf, i = tid % kHalf;
   const int64_t row = kNumKvHeads * kHeadDim;  // elements per (kv, slot)
   const int64_t src = static_cast<int64_t>(b) * row;
 
-  // Everything that does not depend on the position is fetched first so that
-  // its latency overlaps the position -> page lookup and the FP64 sincos.
   const uint16_t k1 = k_new[src + h * kHeadDim + i];
   const uint16_t k2 = k_new[src + h * kHeadDim + i + kHalf];
   const uint32_t vw = reinterpret_cast<const uint32_t*>(v_new + src)[tid];
+  const bool table_ok = rope_table_ready(freqs);
   const int32_t pos = positions[b];
   const bool pos_ok = pos >= 0 && pos < max_blocks * kPageSize;
   const int32_t page =
       pos_ok ? block_table[static_cast<int64_t>(b) * max_blocks + pos / kPageSize] : -1;
-
-  if (tid < kHalf) {
-    const double angle = __dmul_rn(static_cast<double>(pos), freqs.inv_freq[tid]);
-    double sn, cs;
-    sincos(angle, &sn, &cs);
-    s_cos[tid] = cs;
-    s_sin[tid] = sn;
-  }
-  __syncthreads();
+  RopeCS cs = rope_cs(freqs, table_ok, pos, i);
 
   // Optional out-of-place query rotation: 32 heads x 32 pairs, 4 per thread.
   if (q_in != nullptr) {
@@ -73,7 +89,7 @@ __global__ void __launch_bounds__(kAppendThreads)
     for (int k = 0; k < 4; ++k) {
       const int64_t o = qbase + (h + 8 * k) * kHeadDim + i;
       uint16_t y1, y2;
-      rotate_pair(x1[k], x2[k], s_cos[i], s_sin[i], &y1, &y2);
+      rotate_pair_rope(freqs, table_ok, pos, i, cs, x1[k], x2[k], &y1, &y2);
       q_out[o] = y1;
       q_out[o + kHalf] = y2;
     }
@@ -90,19 +106,17 @@ __global__ void __launch_bounds__(kAppendThreads)
   const int slot = pos % kPageSize;
   uint16_t* k_dst = pool + ((static_cast<int64_t>(page) * 2 + 0) * kPageSize + slot) * row;
   uint16_t* v_dst = pool + ((static_cast<int64_t>(page) * 2 + 1) * kPageSize + slot) * row;
-  // Keys: thread (h, i) rotates pair i of kv head h.
   uint16_t y1, y2;
-  rotate_pair(k1, k2, s_cos[i], s_sin[i], &y1, &y2);
+  rotate_pair_rope(freqs, table_ok, pos, i, cs, k1, k2, &y1, &y2);
   k_dst[h * kHeadDim + i] = y1;
   k_dst[h * kHeadDim + i + kHalf] = y2;
-  // Values: 512 bf16 = 256 words, one per thread.
   reinterpret_cast<uint32_t*>(v_dst)[tid] = vw;
 }
 
 // Prefill write: one warp per token.  The token's sequence is found by a
-// binary search over token_offsets; lane i evaluates the (cos, sin) pair i of
-// the token's position in FP64 and rotates pair i of all 8 kv heads; the 512
-// value elements are copied as 8 words per lane.
+// binary search over token_offsets; lane i takes the (cos, sin) pair i of the
+// token's position and rotates pair i of all 8 kv heads; the 512 value
+// elements are copied as 8 words per lane.
 constexpr int kPrefillTokensPerCta = 8;
 
 __global__ void __launch_bounds__(kPrefillTokensPerCta * 32)
@@ -142,23 +156,70 @@ __global__ void __launch_bounds__(kPrefillTokensPerCta * 32)
   const int64_t src = static_cast<int64_t>(t) * row;
   uint16_t* k_dst = pool + ((static_cast<int64_t>(page) * 2 + 0) * kPageSize + slot) * row;
   uint16_t* v_dst = pool + ((static_cast<int64_t>(page) * 2 + 1) * kPageSize + slot) * row;
-  double sn, cs;
-  sincos(__dmul_rn(static_cast<double>(pos), freqs.inv_freq[lane]), &sn, &cs);
-#pragma unroll
-  for (int h = 0; h < kNumKvHeads; ++h) {
-    uint16_t y1, y2;
-    rotate_pair(k[src + h * kHeadDim + lane], k[src + h * kHeadDim + lane + kHalf], cs, sn,
-                &y1, &y2);
-    k_dst[h * kHeadDim + lane] = y1;
-    k_dst[h * kHeadDim + lane + kHalf] = y2;
-  }
   const uint32_t* vs = reinterpret_cast<const uint32_t*>(v + src);
   uint32_t* vd = reinterpret_cast<uint32_t*>(v_dst);
 #pragma unroll
   for (int j = 0; j < static_cast<int>(row / 2) / 32; ++j) vd[lane + 32 * j] = vs[lane + 32 * j];
+  const bool table_ok = rope_table_ready(freqs);
+  RopeCS cs = rope_cs(freqs, table_ok, pos, lane);
+#pragma unroll
+  for (int h = 0; h < kNumKvHeads; ++h) {
+    uint16_t y1, y2;
+    rotate_pair_rope(freqs, table_ok, pos, lane, cs, k[src + h * kHeadDim + lane],
+                     k[src + h * kHeadDim + lane + kHalf], &y1, &y2);
+    k_dst[h * kHeadDim + lane] = y1;
+    k_dst[h * kHeadDim + lane + kHalf] = y2;
+  }
 }
 
+// Device addresses of this device's table, looked up once per device.
+struct RopeTableAddrs {
+  float2* t32 = nullptr;
+  double2* t64 = nullptr;
+  double* theta = nullptr;
+  double built_for = NAN;  // theta of the last rebuild enqueued on this device
+};
+
+std::mutex g_rope_mutex;
+RopeTableAddrs g_rope_addrs[64];
+
 }  // namespace
+
+cudaError_t prepare_rope(double theta, RopeFreqs* f, cudaStream_t stream) {
+  for (int i = 0; i < kHalf; ++i)
+    f->inv_freq[i] = pow(theta, -(2.0 * i) / static_cast<double>(kHeadDim));
+  f->theta = theta;
+  f->table32 = nullptr;
+  f->table64 = nullptr;
+  f->table_theta = nullptr;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaSuccess;  // no table: kernels evaluate sincos
+  std::lock_guard<std::mutex> lock(g_rope_mutex);
+  RopeTableAddrs& a = g_rope_addrs[dev];
+  if (a.t32 == nullptr) {
+    void *p32 = nullptr, *p64 = nullptr, *pt = nullptr;
+    if ((err = cudaGetSymbolAddress(&p32, g_rope32)) != cudaSuccess) return err;
+    if ((err = cudaGetSymbolAddress(&p64, g_rope64)) != cudaSuccess) return err;
+    if ((err = cudaGetSymbolAddress(&pt, g_rope_theta)) != cudaSuccess) return err;
+    a.t32 = static_cast<float2*>(p32);
+    a.t64 = static_cast<double2*>(p64);
+    a.theta = static_cast<double*>(pt);
+  }
+  if (!(a.built_for == theta)) {
+    // invalidate, rebuild, then publish the theta -- in stream order
+    rope_tag_kernel<<<1, 1, 0, stream>>>(NAN);
+    rope_table_kernel<<<(kRopeEntries + 255) / 256, 256, 0, stream>>>(*f);
+    rope_tag_kernel<<<1, 1, 0, stream>>>(theta);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    a.built_for = theta;
+  }
+  f->table32 = a.t32;
+  f->table64 = a.t64;
+  f->table_theta = a.theta;
+  return cudaSuccess;
+}
 
 cudaError_t launch_kv_write_prefill(const uint16_t* k, const uint16_t* v, int num_tokens,
                                     const int32_t* token_offsets,

@@ -227,8 +227,9 @@ PKV_API int pkv_kv_append(const pkv_bf16* k_new, const pkv_bf16* v_new, pkv_bf16
     return PKV_EALIGN;
   if (batch == 0) return PKV_OK;
   pkv::RopeFreqs freqs;
-  for (int i = 0; i < kHeadDim / 2; ++i)
-    freqs.inv_freq[i] = pow(rope_theta, -(2.0 * i) / static_cast<double>(kHeadDim));
+  if (pkv::prepare_rope(rope_theta, &freqs, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return PKV_ECUDA;
   const cudaError_t err = pkv::launch_kv_append(
       k_new, v_new, pool, num_pages, block_table, max_blocks, positions, batch, freqs, q_in,
       q_out, dev_err, reinterpret_cast<cudaStream_t>(stream));
@@ -252,8 +253,9 @@ PKV_API int pkv_kv_write_prefill(const pkv_bf16* k, const pkv_bf16* v, int num_t
     return PKV_EALIGN;
   if (num_tokens == 0) return PKV_OK;
   pkv::RopeFreqs freqs;
-  for (int i = 0; i < kHeadDim / 2; ++i)
-    freqs.inv_freq[i] = pow(rope_theta, -(2.0 * i) / static_cast<double>(kHeadDim));
+  if (pkv::prepare_rope(rope_theta, &freqs, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return PKV_ECUDA;
   const cudaError_t err = pkv::launch_kv_write_prefill(
       k, v, num_tokens, token_offsets, start_positions, pool, num_pages, block_table, max_blocks,
       batch, freqs, dev_err, reinterpret_cast<cudaStream_t>(stream));
@@ -318,8 +320,9 @@ PKV_API int pkv_decode_step(const pkv_bf16* q, const pkv_bf16* k_new, const pkv_
   app.k_new = k_new;
   app.v_new = v_new;
   app.pool = pool;
-  for (int i = 0; i < kHeadDim / 2; ++i)
-    app.freqs.inv_freq[i] = pow(rope_theta, -(2.0 * i) / static_cast<double>(kHeadDim));
+  if (pkv::prepare_rope(rope_theta, &app.freqs, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return PKV_ECUDA;
   const cudaError_t err =
       launch_attention(plan, map, q, block_table, max_blocks, seq_lens, batch, scale, out,
                        workspace, dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream),

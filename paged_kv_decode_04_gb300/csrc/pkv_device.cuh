@@ -202,7 +202,8 @@ __device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
 
 // Rotate-half RoPE of one pair: (x1, x2) -> (x1*c - x2*s, x2*c + x1*s), each
 // product and the sum rounded in FP64 (no contraction), then one rounding to
-// bf16.
+// bf16.  This is the defining evaluation; rotate_pair_rope reaches the same
+// bits faster.
 __device__ __forceinline__ void rotate_pair(uint16_t h1, uint16_t h2, double c,
                                             double s, uint16_t* o1,
                                             uint16_t* o2) {
@@ -212,6 +213,85 @@ __device__ __forceinline__ void rotate_pair(uint16_t h1, uint16_t h2, double c,
   const double y2 = __dadd_rn(__dmul_rn(x2, c), __dmul_rn(x1, s));
   *o1 = double_to_bf16_rne(y1);
   *o2 = double_to_bf16_rne(y2);
+}
+
+// True when every value within `err` of y rounds to the same bf16 as y: y is
+// farther than err from both bf16 rounding midpoints around it.
+__device__ __forceinline__ bool bf16_rounding_stable(float y, float err) {
+  const float ay = fabsf(y);
+  if (!(ay >= 0x1p-100f) || !(ay < 0x1p+126f)) return false;  // tiny, huge, NaN
+  const uint32_t hi = __float_as_uint(ay) & 0xFFFF0000u;
+  const float m_hi = __uint_as_float(hi | 0x8000u);               // above (or at) ay's bf16
+  const float m_lo = __uint_as_float((hi - 0x10000u) | 0x8000u);  // below it
+  return fabsf(ay - m_hi) > err && fabsf(ay - m_lo) > err;
+}
+
+// cos/sin of pair i at position pos: from the device table when it holds
+// this theta, else evaluated here (identical values either way).
+struct RopeCS {
+  float c32, s32;    // the double values rounded to float
+  double c64, s64;   // valid when have64
+  bool have64;
+};
+
+__device__ __forceinline__ RopeCS rope_cs(const RopeFreqs& f, bool table_ok, int pos, int i) {
+  RopeCS r;
+  if (table_ok && pos >= 0 && pos < kRopeTablePositions) {
+    const float2 t = f.table32[pos * 32 + i];
+    r.c32 = t.x;
+    r.s32 = t.y;
+    r.c64 = r.s64 = 0.0;
+    r.have64 = false;
+  } else {
+    sincos(__dmul_rn(static_cast<double>(pos), f.inv_freq[i]), &r.s64, &r.c64);
+    r.c32 = static_cast<float>(r.c64);
+    r.s32 = static_cast<float>(r.s64);
+    r.have64 = true;
+  }
+  return r;
+}
+
+// The result of rotate_pair with c, s = cos/sin of pair i at pos, computed
+// in FP32 whenever that is provably the same bf16.  With c32 = float(c),
+// s32 = float(s), y = fma(x1, c32, -float(x2*s32)) differs from the FP64
+// value by at most 2^-24 * (2|x1| + 2|x2| + |y|) plus about 2^-52 * (|x1| +
+// |x2|); if y is farther than 2^-20 * (|x1| + |x2| + |y|) from every bf16
+// rounding midpoint, both round to the same bf16.  Otherwise (about one
+// element in a few thousand) the element is redone by rotate_pair's FP64
+// arithmetic.
+__device__ __forceinline__ void rotate_pair_rope(const RopeFreqs& f, bool table_ok, int pos,
+                                                 int i, RopeCS& cs, uint16_t h1, uint16_t h2,
+                                                 uint16_t* o1, uint16_t* o2) {
+  const float x1 = bf16_to_float(h1);
+  const float x2 = bf16_to_float(h2);
+  const float y1 = fmaf(x1, cs.c32, -(x2 * cs.s32));
+  const float y2 = fmaf(x2, cs.c32, x1 * cs.s32);
+  const float base = fabsf(x1) + fabsf(x2);
+  const bool ok1 = bf16_rounding_stable(y1, 0x1p-20f * (base + fabsf(y1)));
+  const bool ok2 = bf16_rounding_stable(y2, 0x1p-20f * (base + fabsf(y2)));
+  if (ok1 && ok2) {
+    *o1 = float_to_bf16_rne(y1);
+    *o2 = float_to_bf16_rne(y2);
+    return;
+  }
+  if (!cs.have64) {
+    if (table_ok && pos >= 0 && pos < kRopeTablePositions) {
+      const double2 t = f.table64[pos * 32 + i];
+      cs.c64 = t.x;
+      cs.s64 = t.y;
+    } else {
+      sincos(__dmul_rn(static_cast<double>(pos), f.inv_freq[i]), &cs.s64, &cs.c64);
+    }
+    cs.have64 = true;
+  }
+  uint16_t e1, e2;
+  rotate_pair(h1, h2, cs.c64, cs.s64, &e1, &e2);
+  *o1 = ok1 ? float_to_bf16_rne(y1) : e1;
+  *o2 = ok2 ? float_to_bf16_rne(y2) : e2;
+}
+
+__device__ __forceinline__ bool rope_table_ready(const RopeFreqs& f) {
+  return f.table_theta != nullptr && *f.table_theta == f.theta;
 }
 
 __device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {

@@ -23,10 +23,25 @@ constexpr int kErrPosition = 4;
 constexpr int kErrTimeout = 8;
 constexpr int kErrOffsets = 16;
 
-// inv_freq[i] = theta^(-2i/64) for the 32 rotation pairs, passed by value.
+// Positions covered by the per-device cos/sin table (the 2048-token context).
+constexpr int kRopeTablePositions = 2048;
+
+// RoPE parameters passed by value to the kernels: inv_freq[i] =
+// theta^(-2i/64) for the 32 rotation pairs, and this device's cos/sin table
+// of angle pos * inv_freq[i] for pos < kRopeTablePositions.  A kernel uses the
+// table only while *table_theta == theta; otherwise it evaluates sincos
+// itself (same arithmetic, same values).
 struct RopeFreqs {
   double inv_freq[32];
+  double theta;
+  const float2* table32;     // [pos][i] (cos, sin) rounded to float
+  const double2* table64;    // [pos][i] (cos, sin)
+  const double* table_theta; // theta the table holds
 };
+
+// Fill `f` for theta and, when this device's table holds another theta,
+// enqueue its rebuild on `stream`.
+cudaError_t prepare_rope(double theta, RopeFreqs* f, cudaStream_t stream);
 
 // Split plan of one attention call.
 struct SplitPlan {

@@ -287,3 +287,27 @@ def test_rope_over_every_position_bit_exact():
                      for i in range(B)])
     mism = np.argwhere(got != want)
     assert mism.size == 0, f"{len(mism)} mismatches, first {mism[:4].tolist()}"
+
+
+def test_rope_beyond_the_table_and_theta_switch_bit_exact():
+    # positions 2048..4095 (past the per-device cos/sin table) take the
+    # in-kernel sincos path; switching theta rebuilds the table in between.
+    dev = cuda_or_skip()
+    B = 512
+    rng = np.random.default_rng(23)
+    k = torch.from_numpy(rng.standard_normal((B, 8, 64)).astype(np.float32)).to(torch.bfloat16)
+    kb = k.view(torch.int16).numpy().view(np.uint16)
+    b = binding()
+    for theta, base in ((500000.0, 2048), (10000.0, 0), (500000.0, 1536), (10000.0, 3000)):
+        pos = (base + np.arange(B) * 2).astype(np.int32)
+        bt = np.full((B, 256), -1, np.int32)
+        bt[np.arange(B), pos // 16] = np.arange(B)
+        pool = torch.full((B, 2, 16, 8, 64), -1, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        kd = k.to(dev)
+        b.kv_append(kd, kd, pool, torch.from_numpy(bt).to(dev), torch.from_numpy(pos).to(dev),
+                    rope_theta=theta)
+        got = synth.bits(pool[torch.arange(B, device=dev), 0,
+                              torch.from_numpy(pos % 16).long().to(dev)])
+        want = np.stack([np.stack([oracle.rope_rotate(kb[i, h], int(pos[i]), theta)
+                                   for h in range(8)]) for i in range(B)])
+        assert np.array_equal(got, want), (theta, base)
