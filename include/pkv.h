@@ -131,6 +131,7 @@ PKV_API int pkv_kv_append(const pkv_bf16* k_new, const pkv_bf16* v_new,
  * block_table[b*max_blocks + pos/page_size], K rotated by RoPE at pos (FP64,
  * one rounding to bf16) and V unchanged.
  *
+ *   k, v             16-byte aligned
  *   token_offsets    int32 [batch + 1], non-decreasing, token_offsets[0] = 0,
  *                    token_offsets[batch] = num_tokens
  *   start_positions  int32 [batch]

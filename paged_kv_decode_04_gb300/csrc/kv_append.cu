@@ -32,8 +32,8 @@ constexpr int kHalf = kHeadDim / 2;
 constexpr int kRopeEntries = kRopeTablePositions * kHalf;
 
 // This device's cos/sin table and the theta it holds (NaN = none).
-__device__ float2 g_rope32[kRopeEntries];
-__device__ double2 g_rope64[kRopeEntries];
+__device__ __align__(16) float2 g_rope32[kRopeEntries];
+__device__ __align__(16) double2 g_rope64[kRopeEntries];
 __device__ double g_rope_theta;
 
 __global__ void rope_tag_kernel(double value) { g_rope_theta = value; }
@@ -114,30 +114,50 @@ __global__ void __launch_bounds__(kAppendThreads)
 }
 
 // Prefill write: one warp per token.  The token's sequence is found by a
-// binary search over token_offsets; lane i takes the (cos, sin) pair i of the
-// token's position and rotates pair i of all 8 kv heads; the 512 value
-// elements are copied as 8 words per lane.
+// binary search over token_offsets.  Lane l holds bf16 elements
+// [16l, 16l + 16) of the token's 512-element K row (kv head l / 4, dims
+// 16 (l % 4) ..) and of its V row, loaded and stored 16 bytes at a time; the
+// rotation partner of dims 0..31 is dims 32..63, i.e. lane l ^ 2, reached
+// with shuffles.  Lanes holding dims < 32 produce x1*c - x2*s, the others
+// x2*c + x1*s, for 16 pairs each.
 constexpr int kPrefillTokensPerCta = 8;
 
-__global__ void __launch_bounds__(kPrefillTokensPerCta * 32)
+// Batches up to this size search token_offsets in shared memory.
+constexpr int kPrefillSmemBatch = 2048;
+
+__global__ void __launch_bounds__(kPrefillTokensPerCta * 32, 4)
     kv_write_prefill_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                             int num_tokens, const int32_t* __restrict__ token_offsets,
                             const int32_t* __restrict__ start_positions,
                             uint16_t* __restrict__ pool, int64_t num_pages,
                             const int32_t* __restrict__ block_table, int max_blocks, int batch,
                             RopeFreqs freqs, int32_t* dev_err) {
+  __shared__ int32_t s_off[kPrefillSmemBatch + 1];
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kPrefillTokensPerCta + (threadIdx.x >> 5);
+  const bool smem_offsets = batch <= kPrefillSmemBatch;
+  if (smem_offsets) {
+    for (int i = threadIdx.x; i <= batch; i += blockDim.x) s_off[i] = token_offsets[i];
+    __syncthreads();
+  }
   if (t >= num_tokens) return;
+  const int32_t* off = smem_offsets ? s_off : token_offsets;
+  const int64_t row = kNumKvHeads * kHeadDim;
+  const int64_t src = static_cast<int64_t>(t) * row;
+  // position-independent loads first: this lane's 16 K and 16 V elements
+  const uint4* ks = reinterpret_cast<const uint4*>(k + src) + 2 * lane;
+  const uint4* vs = reinterpret_cast<const uint4*>(v + src) + 2 * lane;
+  const uint4 k0 = ks[0], k1 = ks[1];
+  const uint4 v0 = vs[0], v1 = vs[1];
   // largest b with token_offsets[b] <= t
   int lo = 0, hi = batch;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (token_offsets[mid] <= t) lo = mid; else hi = mid;
+    if (off[mid] <= t) lo = mid; else hi = mid;
   }
   const int b = lo;
-  const int32_t first = token_offsets[b];
-  if (t < first || t >= token_offsets[b + 1]) {
+  const int32_t first = off[b];
+  if (t < first || t >= off[b + 1]) {
     if (lane == 0) record_error(dev_err, kErrOffsets);
     return;
   }
@@ -152,23 +172,57 @@ __global__ void __launch_bounds__(kPrefillTokensPerCta * 32)
     return;
   }
   const int slot = pos % kPageSize;
-  const int64_t row = kNumKvHeads * kHeadDim;
-  const int64_t src = static_cast<int64_t>(t) * row;
   uint16_t* k_dst = pool + ((static_cast<int64_t>(page) * 2 + 0) * kPageSize + slot) * row;
   uint16_t* v_dst = pool + ((static_cast<int64_t>(page) * 2 + 1) * kPageSize + slot) * row;
-  const uint32_t* vs = reinterpret_cast<const uint32_t*>(v + src);
-  uint32_t* vd = reinterpret_cast<uint32_t*>(v_dst);
+  reinterpret_cast<uint4*>(v_dst)[2 * lane] = v0;
+  reinterpret_cast<uint4*>(v_dst)[2 * lane + 1] = v1;
+
+  const bool first_half = (lane & 2) == 0;  // my dims are the x1 side of their pairs
+  const bool table_ok = rope_table_ready(freqs) && pos < kRopeTablePositions;
+  uint4* kd = reinterpret_cast<uint4*>(k_dst) + 2 * lane;
 #pragma unroll
-  for (int j = 0; j < static_cast<int>(row / 2) / 32; ++j) vd[lane + 32 * j] = vs[lane + 32 * j];
-  const bool table_ok = rope_table_ready(freqs);
-  RopeCS cs = rope_cs(freqs, table_ok, pos, lane);
+  for (int part = 0; part < 2; ++part) {  // 8 pairs at a time
+    const uint4 mine4 = part ? k1 : k0;
+    const uint32_t mine[4] = {mine4.x, mine4.y, mine4.z, mine4.w};
+    uint32_t other[4];
 #pragma unroll
-  for (int h = 0; h < kNumKvHeads; ++h) {
-    uint16_t y1, y2;
-    rotate_pair_rope(freqs, table_ok, pos, lane, cs, k[src + h * kHeadDim + lane],
-                     k[src + h * kHeadDim + lane + kHalf], &y1, &y2);
-    k_dst[h * kHeadDim + lane] = y1;
-    k_dst[h * kHeadDim + lane + kHalf] = y2;
+    for (int e = 0; e < 4; ++e) other[e] = __shfl_xor_sync(0xFFFFFFFFu, mine[e], 2);
+    const int i0 = 16 * (lane & 1) + 8 * part;  // pair index of element 0 of this part
+    float c32[8], s32[8];
+    if (table_ok) {
+      const float4* tc = reinterpret_cast<const float4*>(freqs.table32 + pos * kHalf + i0);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 q = tc[e];
+        c32[2 * e] = q.x;
+        s32[2 * e] = q.y;
+        c32[2 * e + 1] = q.z;
+        s32[2 * e + 1] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        double sn, cs;
+        sincos(__dmul_rn(static_cast<double>(pos), freqs.inv_freq[i0 + e]), &sn, &cs);
+        c32[e] = static_cast<float>(cs);
+        s32[e] = static_cast<float>(sn);
+      }
+    }
+    uint32_t out[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint16_t r[2];
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int el = 2 * e + hlf;
+        const uint16_t a = static_cast<uint16_t>(hlf ? mine[e] >> 16 : mine[e] & 0xFFFFu);
+        const uint16_t o = static_cast<uint16_t>(hlf ? other[e] >> 16 : other[e] & 0xFFFFu);
+        r[hlf] = rope_one(freqs, table_ok, pos, i0 + el, first_half, c32[el], s32[el],
+                          first_half ? a : o, first_half ? o : a);
+      }
+      out[e] = static_cast<uint32_t>(r[0]) | (static_cast<uint32_t>(r[1]) << 16);
+    }
+    kd[part] = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 

@@ -249,7 +249,7 @@ PKV_API int pkv_kv_write_prefill(const pkv_bf16* k, const pkv_bf16* v, int num_t
   if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return PKV_EINVAL;
   if (num_kv_heads != kNumKvHeads || head_dim != kHeadDim || page_size != kPageSize)
     return PKV_EUNSUPPORTED;
-  if (!aligned(pool, 16) || !aligned(v, 4) || !aligned(k, 2) || !aligned(dev_err, 4))
+  if (!aligned(pool, 16) || !aligned(v, 16) || !aligned(k, 16) || !aligned(dev_err, 4))
     return PKV_EALIGN;
   if (num_tokens == 0) return PKV_OK;
   pkv::RopeFreqs freqs;

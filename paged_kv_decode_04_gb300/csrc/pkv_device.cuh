@@ -251,13 +251,19 @@ __device__ __forceinline__ RopeCS rope_cs(const RopeFreqs& f, bool table_ok, int
   return r;
 }
 
+// Error allowance of the FP32 rotation (see rotate_pair_rope).
+__device__ __forceinline__ float rope_fp32_allowance(float x1, float x2, float y) {
+  return 0x1p-22f * (fabsf(x1) + fabsf(x2) + fabsf(y));
+}
+
 // The result of rotate_pair with c, s = cos/sin of pair i at pos, computed
 // in FP32 whenever that is provably the same bf16.  With c32 = float(c),
 // s32 = float(s), y = fma(x1, c32, -float(x2*s32)) differs from the FP64
-// value by at most 2^-24 * (2|x1| + 2|x2| + |y|) plus about 2^-52 * (|x1| +
-// |x2|); if y is farther than 2^-20 * (|x1| + |x2| + |y|) from every bf16
-// rounding midpoint, both round to the same bf16.  Otherwise (about one
-// element in a few thousand) the element is redone by rotate_pair's FP64
+// value by at most 2^-24 * (2|x1| + 2|x2| + |y|) plus about 2^-51 * (|x1| +
+// |x2|), which is at most half of rope_fp32_allowance; if y is farther than
+// the allowance from both bf16 rounding midpoints around it, both values
+// round to the same bf16.  Otherwise (about one element in a thousand,
+// mostly under cancellation) the element is redone by rotate_pair's FP64
 // arithmetic.
 __device__ __forceinline__ void rotate_pair_rope(const RopeFreqs& f, bool table_ok, int pos,
                                                  int i, RopeCS& cs, uint16_t h1, uint16_t h2,
@@ -266,9 +272,8 @@ __device__ __forceinline__ void rotate_pair_rope(const RopeFreqs& f, bool table_
   const float x2 = bf16_to_float(h2);
   const float y1 = fmaf(x1, cs.c32, -(x2 * cs.s32));
   const float y2 = fmaf(x2, cs.c32, x1 * cs.s32);
-  const float base = fabsf(x1) + fabsf(x2);
-  const bool ok1 = bf16_rounding_stable(y1, 0x1p-20f * (base + fabsf(y1)));
-  const bool ok2 = bf16_rounding_stable(y2, 0x1p-20f * (base + fabsf(y2)));
+  const bool ok1 = bf16_rounding_stable(y1, rope_fp32_allowance(x1, x2, y1));
+  const bool ok2 = bf16_rounding_stable(y2, rope_fp32_allowance(x1, x2, y2));
   if (ok1 && ok2) {
     *o1 = float_to_bf16_rne(y1);
     *o2 = float_to_bf16_rne(y2);
@@ -288,6 +293,29 @@ __device__ __forceinline__ void rotate_pair_rope(const RopeFreqs& f, bool table_
   rotate_pair(h1, h2, cs.c64, cs.s64, &e1, &e2);
   *o1 = ok1 ? float_to_bf16_rne(y1) : e1;
   *o2 = ok2 ? float_to_bf16_rne(y2) : e2;
+}
+
+// One output element of rotate_pair for pair i at pos: first ? x1*c - x2*s
+// : x2*c + x1*s, with the same FP32 fast path and FP64 redo as
+// rotate_pair_rope (c32, s32: the float cos/sin of the pair).
+__device__ __forceinline__ uint16_t rope_one(const RopeFreqs& f, bool table_ok, int pos, int i,
+                                             bool first, float c32, float s32, uint16_t h1,
+                                             uint16_t h2) {
+  const float x1 = bf16_to_float(h1);
+  const float x2 = bf16_to_float(h2);
+  const float y = first ? fmaf(x1, c32, -(x2 * s32)) : fmaf(x2, c32, x1 * s32);
+  if (bf16_rounding_stable(y, rope_fp32_allowance(x1, x2, y))) return float_to_bf16_rne(y);
+  double c64, s64;
+  if (table_ok && pos >= 0 && pos < kRopeTablePositions) {
+    const double2 t = f.table64[pos * 32 + i];
+    c64 = t.x;
+    s64 = t.y;
+  } else {
+    sincos(__dmul_rn(static_cast<double>(pos), f.inv_freq[i]), &s64, &c64);
+  }
+  uint16_t e1, e2;
+  rotate_pair(h1, h2, c64, s64, &e1, &e2);
+  return first ? e1 : e2;
 }
 
 __device__ __forceinline__ bool rope_table_ready(const RopeFreqs& f) {
