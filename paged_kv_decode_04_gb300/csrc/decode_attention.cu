@@ -73,6 +73,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int split = blockIdx.x / kNumKvHeads;
   const int b = blockIdx.y;
   const int pps = a.plan.pages_per_split;
+  if (tid == 0) tma_prefetch_desc(&pool_map);
+  wait_for_prior_grids();
+  allow_dependent_grids();
 
   // ---- sequence extent and this CTA's page range
   int L = a.seq_lens[b];
@@ -121,10 +124,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       mbar_arrive(bar);  // keep the stage's phase sequence in step
     }
   };
-  if (lane == 0) {
-    tma_prefetch_desc(&pool_map);
+  if (lane == 0)
     for (int k = 0; k < kStages && k < nw; ++k) issue(k);
-  }
 
   // ---- fused append: computed while the first copies are in flight
   const int last_local = npages - 1 - p_begin;  // the sequence's last page, in this range
@@ -229,6 +230,8 @@ __global__ void __launch_bounds__(32) merge_splits_kernel(const AttnArgs a) {
   const int b = blockIdx.y;
   const int lane = threadIdx.x;
   const int pps = a.plan.pages_per_split;
+  wait_for_prior_grids();
+  allow_dependent_grids();
   int L = a.seq_lens[b];
   const int Lmax = a.max_blocks * kPageSize;
   L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
@@ -302,18 +305,22 @@ cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
   if (append != nullptr) {
     err = configure_once<true>(device);
     if (err != cudaSuccess) return err;
-    paged_decode_kernel<true><<<grid, kThreads, smem, stream>>>(pool_map, args, *append);
+    err = launch_pdl(paged_decode_kernel<true>, grid, dim3(kThreads), smem, stream, pool_map,
+                     args, *append);
+    if (err != cudaSuccess) return err;
   } else {
     err = configure_once<false>(device);
     if (err != cudaSuccess) return err;
     AppendArgs none{};
-    paged_decode_kernel<false><<<grid, kThreads, smem, stream>>>(pool_map, args, none);
+    err = launch_pdl(paged_decode_kernel<false>, grid, dim3(kThreads), smem, stream, pool_map,
+                     args, none);
+    if (err != cudaSuccess) return err;
   }
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (args.plan.num_splits > 1) {
-    merge_splits_kernel<<<dim3(kNumQHeads, args.batch), 32, 0, stream>>>(args);
-    err = cudaGetLastError();
+    err = launch_pdl(merge_splits_kernel, dim3(kNumQHeads, args.batch), dim3(32), 0, stream,
+                     args);
   }
   return err;
 }

@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(kAppendThreads)
   const int h = tid / kHalf, i = tid % kHalf;
   const int64_t row = kNumKvHeads * kHeadDim;  // elements per (kv, slot)
   const int64_t src = static_cast<int64_t>(b) * row;
+  wait_for_prior_grids();
+  allow_dependent_grids();
 
   const uint16_t k1 = k_new[src + h * kHeadDim + i];
   const uint16_t k2 = k_new[src + h * kHeadDim + i + kHalf];
@@ -133,6 +135,8 @@ __global__ void __launch_bounds__(kPrefillTokensPerCta * 32, 4)
                             const int32_t* __restrict__ block_table, int max_blocks, int batch,
                             RopeFreqs freqs, int32_t* dev_err) {
   __shared__ int32_t s_off[kPrefillSmemBatch + 1];
+  wait_for_prior_grids();
+  allow_dependent_grids();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kPrefillTokensPerCta + (threadIdx.x >> 5);
   const bool smem_offsets = batch <= kPrefillSmemBatch;
@@ -282,10 +286,9 @@ cudaError_t launch_kv_write_prefill(const uint16_t* k, const uint16_t* v, int nu
                                     int max_blocks, int batch, const RopeFreqs& freqs,
                                     int32_t* dev_err, cudaStream_t stream) {
   const int ctas = (num_tokens + kPrefillTokensPerCta - 1) / kPrefillTokensPerCta;
-  kv_write_prefill_kernel<<<ctas, kPrefillTokensPerCta * 32, 0, stream>>>(
-      k, v, num_tokens, token_offsets, start_positions, pool, num_pages, block_table,
-      max_blocks, batch, freqs, dev_err);
-  return cudaGetLastError();
+  return launch_pdl(kv_write_prefill_kernel, dim3(ctas), dim3(kPrefillTokensPerCta * 32), 0,
+                    stream, k, v, num_tokens, token_offsets, start_positions, pool, num_pages,
+                    block_table, max_blocks, batch, freqs, dev_err);
 }
 
 cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new,
@@ -295,10 +298,9 @@ cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new,
                              const RopeFreqs& freqs, const uint16_t* q_in,
                              uint16_t* q_out, int32_t* dev_err,
                              cudaStream_t stream) {
-  kv_append_kernel<<<batch, kAppendThreads, 0, stream>>>(
-      k_new, v_new, pool, num_pages, block_table, max_blocks, positions, freqs,
-      q_in, q_out, dev_err);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3(batch), dim3(kAppendThreads), 0, stream, k_new,
+                    v_new, pool, num_pages, block_table, max_blocks, positions, freqs, q_in,
+                    q_out, dev_err);
 }
 
 }  // namespace pkv

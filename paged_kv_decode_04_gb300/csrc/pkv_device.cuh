@@ -15,6 +15,19 @@ namespace pkv {
 // records kErrTimeout and stops waiting instead of spinning forever.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// Programmatic dependent launch.  Every library kernel is launched allowed to
+// start before the previous kernel on its stream has finished; it calls
+// wait_for_prior_grids() before its first read of global memory (which
+// returns once the prior grids have completed and their writes are visible,
+// and at once when there is no such dependency), then
+// allow_dependent_grids() so that the next kernel may be scheduled in turn.
+__device__ __forceinline__ void wait_for_prior_grids() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_grids() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void record_error(int32_t* dev_err, int bits) {
   if (dev_err != nullptr) atomicOr(dev_err, bits);
 }

@@ -43,6 +43,24 @@ struct RopeFreqs {
 // enqueue its rebuild on `stream`.
 cudaError_t prepare_rope(double theta, RopeFreqs* f, cudaStream_t stream);
 
+// Launch `kernel` with programmatic stream serialization allowed (see
+// wait_for_prior_grids in pkv_device.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Split plan of one attention call.
 struct SplitPlan {
   int num_splits;       // grid extent of the split dimension (S)
