@@ -138,3 +138,55 @@ def test_prefill_reports_bad_offsets_and_pages():
                        to_dev(st, dev), dpool, to_dev(bt2, dev), dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) & b.DEVERR_PAGE
+
+
+def special_bf16(rng, shape):
+    """bf16 bit patterns mixing normal values with zeros, subnormals, tiny and
+    huge normals, infinities, NaNs and exact x1 == x2 pairs (cancellation)."""
+    x = bf16_normal(rng, shape)
+    kind = rng.integers(0, 10, size=shape)
+    sign = (rng.integers(0, 2, size=shape) << 15).astype(np.uint16)
+    mant = rng.integers(0, 128, size=shape).astype(np.uint16)
+    x = np.where(kind == 1, sign, x)                                            # +-0
+    x = np.where(kind == 2, sign | np.maximum(mant, 1), x)                      # subnormal
+    tiny = (rng.integers(1, 31, size=shape).astype(np.uint16) << 7) | mant
+    x = np.where(kind == 3, sign | tiny, x)                                     # tiny normal
+    huge = (rng.integers(220, 255, size=shape).astype(np.uint16) << 7) | mant
+    x = np.where(kind == 4, sign | huge, x)                                     # huge normal
+    x = np.where((kind == 5) & (mant < 16), sign | 0x7F80, x)                   # +-inf
+    x = np.where((kind == 5) & (mant >= 120), 0x7FC1 | sign, x)                 # NaN
+    x = x.astype(np.uint16)
+    pair = kind[..., :32] == 6                                                  # x2 := x1
+    x[..., 32:] = np.where(pair, x[..., :32], x[..., 32:])
+    return x
+
+
+def is_nan_bf16(x):
+    return ((x & 0x7F80) == 0x7F80) & ((x & 0x7F) != 0)
+
+
+@pytest.mark.parametrize("theta", [500000.0, 10000.0])
+def test_prefill_special_values_bit_exact(theta):
+    # positions 0..2739 (the last sequence runs past the 2048-entry cos/sin
+    # table), values that send pairs down the FP64 redo path; NaN payload and
+    # sign are not compared, every other bit is
+    dev = cuda_or_skip()
+    counts, starts = [700, 300, 700], [0, 1021, 2040]
+    rng = np.random.default_rng(29)
+    k0, v0, off, st, bt = ragged_case(31, counts, starts, num_pages=512, max_blocks=256)
+    k = special_bf16(rng, k0.shape)
+    v = special_bf16(rng, v0.shape)
+    pool = np.full((512, 2, 16, 8, 64), 0x1234, dtype=np.uint16)   # a finite poison
+    want = pool.copy()
+    assert oracle.kv_write_prefill(k, v, off, st, want, bt, theta=theta) == 0
+    dpool = to_dev(pool, dev, bf=True)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    binding().kv_write_prefill(to_dev(k, dev, True), to_dev(v, dev, True), to_dev(off, dev),
+                               to_dev(st, dev), dpool, to_dev(bt, dev), rope_theta=theta,
+                               dev_err=err)
+    got = synth.bits(dpool)
+    both_nan = is_nan_bf16(got) & is_nan_bf16(want)
+    mism = np.argwhere((got != want) & ~both_nan)
+    assert mism.size == 0, f"{len(mism)} mismatching elements, first {mism[:3].tolist()}"
+    assert int(err.item()) == 0
+    assert is_nan_bf16(want).any() and (want == 0).any()
