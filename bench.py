@@ -20,6 +20,7 @@ scaling): the path has no exchange step.
 from __future__ import annotations
 
 import argparse
+import copy
 import hashlib
 import json
 import os
@@ -303,29 +304,70 @@ def run_ours(args, world, rank, local):
     d = synth.device_inputs(w, dev)
     B, layers = w.batch, w.layers
     stream = torch.cuda.current_stream(dev)
-    splits = binding.plan_splits(B, w.max_blocks, args.splits)
-    ws_bytes = binding.workspace_bytes(B, w.max_blocks, args.splits)
+    planned = args.plan == "host"   # None (the default) is the fixed automatic plan
+    plan = binding.Plan(w.seq_lens, w.max_blocks, device=dev) if planned else None
+    if planned:
+        d["plan"] = plan.dev
+        splits = max(1, max((int(m[2]) for m in plan.merges()), default=1))
+        ws_bytes = plan.workspace_bytes
+        split_text = (f"host work plan: {plan.num_items} items of at most {plan.range_pages} "
+                      f"pages or 4 packed sequences, {plan.num_merges} merged sequences")
+    else:
+        splits = binding.plan_splits(B, w.max_blocks, args.splits)
+        ws_bytes = binding.workspace_bytes(B, w.max_blocks, args.splits)
+        split_text = f"fixed: {splits} ranges per sequence"
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     outs = torch.empty((layers, B, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     fused = args.path == "fused"
-    kernels_per_layer = (1 if fused else 2) + (1 if splits > 1 else 0)
+    merges = (plan.num_merges > 0) if planned else (splits > 1)
+    kernels_per_layer = (1 if fused else 2) + (1 if merges else 0)
 
-    def attend(layer):
-        binding.paged_decode_attention(d["q"][layer], d["pool"], d["block_tables"][layer],
-                                       d["seq_lens"], outs[layer], scale=w.scale,
-                                       workspace=workspace, num_splits=args.splits, dev_err=err)
+    def plan_for(dset):
+        """The plan whose device copy is dset["plan"] (one per input set)."""
+        if not planned:
+            return None
+        if dset["plan"] is plan.dev:
+            return plan
+        p2 = copy.copy(plan)
+        p2.dev = dset["plan"]
+        return p2
 
-    def append(layer):
-        binding.kv_append(d["k_new"][layer], d["v_new"][layer], d["pool"],
-                          d["block_tables"][layer], d["positions"], rope_theta=w.rope_theta,
+    def attend_on(dset, layer, out):
+        if planned:
+            binding.paged_decode_attention_planned(
+                dset["q"][layer], d["pool"], dset["block_tables"][layer], dset["seq_lens"],
+                plan_for(dset), out, scale=w.scale, workspace=workspace, dev_err=err)
+        else:
+            binding.paged_decode_attention(
+                dset["q"][layer], d["pool"], dset["block_tables"][layer], dset["seq_lens"], out,
+                scale=w.scale, workspace=workspace, num_splits=args.splits, dev_err=err)
+
+    def fused_on(dset, layer, out):
+        if planned:
+            binding.decode_step_planned(
+                dset["q"][layer], dset["k_new"][layer], dset["v_new"][layer], d["pool"],
+                dset["block_tables"][layer], dset["seq_lens"], plan_for(dset), out,
+                rope_theta=w.rope_theta, scale=w.scale, workspace=workspace, dev_err=err)
+        else:
+            binding.decode_step(
+                dset["q"][layer], dset["k_new"][layer], dset["v_new"][layer], d["pool"],
+                dset["block_tables"][layer], dset["seq_lens"], out, rope_theta=w.rope_theta,
+                scale=w.scale, workspace=workspace, num_splits=args.splits, dev_err=err)
+
+    def append_on(dset, layer):
+        binding.kv_append(dset["k_new"][layer], dset["v_new"][layer], d["pool"],
+                          dset["block_tables"][layer], dset["positions"], rope_theta=w.rope_theta,
                           dev_err=err)
 
+    def attend(layer):
+        attend_on(d, layer, outs[layer])
+
+    def append(layer):
+        append_on(d, layer)
+
     def fused_layer(layer):
-        binding.decode_step(d["q"][layer], d["k_new"][layer], d["v_new"][layer], d["pool"],
-                            d["block_tables"][layer], d["seq_lens"], outs[layer],
-                            rope_theta=w.rope_theta, scale=w.scale, workspace=workspace,
-                            num_splits=args.splits, dev_err=err)
+        fused_on(d, layer, outs[layer])
 
     def launch_step():
         """Enqueue one whole step (every layer) on the current stream."""
@@ -391,7 +433,7 @@ def run_ours(args, world, rank, local):
         dom_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / layers
         dom_bytes = algorithmic_bytes(w, "step") / layers
         kern["decode_step"] = round(dom_ms * 1e3, 2)
-        dom_name = "paged_decode_kernel<append>"
+        dom_name = "paged_decode_kernel<append,planned>" if planned else "paged_decode_kernel<append>"
     else:
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_prof)]
         for i in range(n_prof):
@@ -408,9 +450,9 @@ def run_ours(args, world, rank, local):
         dom_bytes = algorithmic_bytes(w, "attention") / layers
         kern["kv_append"] = round(app_ms * 1e3, 2)
         kern["paged_decode_attention"] = round(dom_ms * 1e3, 2)
-        dom_name = "paged_decode_kernel"
-    if splits > 1:
-        dom_name += "+merge_splits_kernel"
+        dom_name = "paged_decode_kernel<planned>" if planned else "paged_decode_kernel"
+    if merges:
+        dom_name += "+merge_plan_kernel" if planned else "+merge_splits_kernel"
     peak, peak_kind = measured_hbm_peak()
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
 
@@ -420,6 +462,8 @@ def run_ours(args, world, rank, local):
     # while step k computes; every step still moves its own inputs in and its
     # output out inside the timed region.
     names = ["q", "k_new", "v_new", "positions", "seq_lens", "block_tables"]
+    if planned:
+        names.append("plan")                  # the step's work plan travels with its inputs
     host = {k: d[k].cpu().pin_memory() for k in names}
     out_host = [torch.empty(outs.shape, dtype=outs.dtype).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -431,19 +475,10 @@ def run_ours(args, world, rank, local):
         def launch():
             for layer in range(layers):
                 if fused:
-                    binding.decode_step(dset["q"][layer], dset["k_new"][layer],
-                                        dset["v_new"][layer], d["pool"],
-                                        dset["block_tables"][layer], dset["seq_lens"], out[layer],
-                                        rope_theta=w.rope_theta, scale=w.scale,
-                                        workspace=workspace, num_splits=args.splits, dev_err=err)
+                    fused_on(dset, layer, out[layer])
                 else:
-                    binding.kv_append(dset["k_new"][layer], dset["v_new"][layer], d["pool"],
-                                      dset["block_tables"][layer], dset["positions"],
-                                      rope_theta=w.rope_theta, dev_err=err)
-                    binding.paged_decode_attention(dset["q"][layer], d["pool"],
-                                                   dset["block_tables"][layer], dset["seq_lens"],
-                                                   out[layer], scale=w.scale, workspace=workspace,
-                                                   num_splits=args.splits, dev_err=err)
+                    append_on(dset, layer)
+                    attend_on(dset, layer, out[layer])
         if not args.graph:
             return launch
         g = torch.cuda.CUDAGraph()
@@ -519,7 +554,8 @@ def run_ours(args, world, rank, local):
             "path": ("fused append+attention (pkv_decode_step)" if fused
                      else "pkv_kv_append then pkv_paged_decode_attention"),
             "launch": "one CUDA graph per step" if args.graph else "eager launches",
-            "num_splits": splits, "layers_per_step": layers, "pool_pages": w.num_pages,
+            "num_splits": splits, "split_plan": split_text,
+            "layers_per_step": layers, "pool_pages": w.num_pages,
             "l2": ("inputs larger than L2: %.2f GiB of K/V streamed per step vs 129 MB L2; no flush"
                    % (w.kv_bytes() / 2 ** 30)) if w.kv_bytes() > 512 * 2 ** 20 else
                   "working set fits in L2 (no flush): L2-resident figure",
@@ -616,9 +652,12 @@ def run_serve(args, world, rank, local):
     layers, num_pages = 16, 65536
     reqs = [(int(rng.integers(16, 1025)), int(rng.integers(16, 513)))
             for _ in range(args.serve_requests)]
-    warm = Engine(num_pages, layers, dev, static_batching=args.static, seed=args.seed + 1)
+    use_plan = args.plan != "auto"
+    warm = Engine(num_pages, layers, dev, static_batching=args.static, seed=args.seed + 1,
+                  use_plan=use_plan)
     warm.run(reqs[:8])
-    eng = Engine(num_pages, layers, dev, static_batching=args.static, seed=args.seed)
+    eng = Engine(num_pages, layers, dev, static_batching=args.static, seed=args.seed,
+                 use_plan=use_plan)
     barrier(world)
     res = eng.run(reqs)
     barrier(world)
@@ -635,6 +674,7 @@ def run_serve(args, world, rank, local):
             "config": {"workload": f"{len(reqs)} requests, prompt U[16,1024], max_new U[16,512], "
                                    f"{layers} layers, {num_pages}-page pool (2 GiB), "
                                    f"{'static' if args.static else 'continuous'} batching",
+                       "split_plan": "host work plan per step" if use_plan else "fixed (automatic)",
                        "seed": args.seed},
             "stats": {k: st[k] for k in ("pool_pages", "peak_active", "largest_decode_batch",
                                          "peak_allocated_pages", "admission_wait_total",
@@ -652,6 +692,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="peak")
     ap.add_argument("--splits", type=int, default=0, help="0 = automatic split plan")
+    ap.add_argument("--plan", choices=["auto", "host"], default=None,
+                    help="host: a work plan built on the host from the lengths (pkv_plan_build) "
+                         "and passed to the planned entry points; auto: the fixed split plan "
+                         "(default: auto for --op decode, host for --op serve)")
     ap.add_argument("--path", choices=["fused", "separate"], default="fused",
                     help="fused: one pkv_decode_step launch per layer; separate: pkv_kv_append "
                          "then pkv_paged_decode_attention")

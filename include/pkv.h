@@ -79,6 +79,7 @@ typedef struct CUstream_st* pkv_stream_t; /* same type as cudaStream_t */
 #define PKV_DEVERR_POSITION 4u  /* positions[b] < 0 or >= max_blocks*page_size */
 #define PKV_DEVERR_TIMEOUT 8u   /* an in-kernel wait for a page copy gave up */
 #define PKV_DEVERR_OFFSETS 16u  /* a token outside the ranges of token_offsets */
+#define PKV_DEVERR_PLAN 32u     /* seq_lens[b] differs from the length a work plan holds */
 
 /* Library ABI version (bumped when a signature changes). */
 PKV_API int pkv_abi_version(void);
@@ -226,6 +227,81 @@ PKV_API size_t pkv_workspace_bytes(int batch, int num_q_heads,
  */
 PKV_API int pkv_plan_splits(int batch, int num_kv_heads, int max_blocks,
                             int num_splits);
+
+/*
+ * Work plans: split a ragged batch on the host, run it on the device.
+ *
+ * The automatic split plan of the calls above cannot see the lengths (they
+ * live on the device), so a batch that mixes a few long sequences with many
+ * short ones waits on its long sequences.  A caller that holds the lengths
+ * on the host -- a scheduler always does -- can build a work plan instead
+ * and pass it to the _planned entry points.  A plan is sized by a work unit
+ * of U pages per warp: ranges of R = clamp(4 U, 8, min(max_blocks, 1024))
+ * pages, and
+ *   - sequences of more than R pages are cut into ceil(p / R) ranges of
+ *     near-equal size, one CTA per (range, kv head), combined afterwards by
+ *     a merge kernel; sequences of up to R pages get one such CTA;
+ *   - sequences of at most min(R / 4, 16) pages (and empty ones) are packed
+ *     four to a CTA, one warp each, so a warp again streams about U pages;
+ *   - CTAs run in order of the pages their busiest warp streams, most first.
+ * U is the smallest unit, from ceil(P / (2 SMs)) up (P: the batch's pages),
+ * whose plan fits in one wave of four CTAs per SM; when none does, the
+ * ranges take the whole table width (a batch of long sequences then gets
+ * one range each, as with num_splits = 1).
+ * The plan is plain data: 8 header words
+ *   {PKV_PLAN_MAGIC, batch, max_blocks, num_items, num_merges, num_slots,
+ *    range_pages, bytes_used},
+ * then num_items items of 16 int32 words
+ *   {kind (0 range, 1 packed), slot (-1: not split), p_begin, n,
+ *    seq[4], len[4], 0, 0, 0, 0}
+ * (a range item repeats its sequence in all four seq/len words; a packed
+ * item holds one sequence per warp, -1 for none), then num_merges entries
+ * {b, first slot, ranges, 0}.  The results follow the same numerics as the
+ * calls above (same tolerance, bit-identical on repeated runs of a plan).
+ */
+#define PKV_PLAN_MAGIC 0x31564b50 /* "PKV1" */
+
+/* Bytes a plan for this batch and table width can take (host buffer). */
+PKV_API size_t pkv_plan_bytes(int batch, int max_blocks);
+
+/*
+ * Build a plan from the host copy of the lengths (after this step's append,
+ * as seq_lens), for a device with num_sms SMs (0 = the current device).
+ * plan: host memory, 16-byte aligned, at least pkv_plan_bytes() bytes.
+ * Returns PKV_OK, PKV_EINVAL (a length outside [0, max_blocks * page_size],
+ * bad sizes or buffer), PKV_EALIGN, PKV_EUNSUPPORTED (more than 65535 work
+ * items) or PKV_ECUDA (no device to size it for).  Pure host code.
+ */
+PKV_API int pkv_plan_build(const int32_t* seq_lens_host, int batch, int max_blocks,
+                           int num_sms, void* plan, size_t plan_bytes);
+
+/* Device workspace bytes a built plan needs (0 when nothing is split). */
+PKV_API size_t pkv_plan_workspace_bytes(const void* plan);
+
+/*
+ * pkv_paged_decode_attention / pkv_decode_step under a work plan.
+ * plan_host: the built plan (read on the host for the grid sizes);
+ * plan_dev: a device copy of its first bytes_used bytes, 16-byte aligned,
+ * which must stay unchanged until the call's kernels have run.  The kernels
+ * take every length from the plan; seq_lens is only compared with it, and a
+ * difference sets PKV_DEVERR_PLAN (the outputs then follow the plan's
+ * lengths).  workspace: at least pkv_plan_workspace_bytes(plan_host).
+ * Other arguments as for the calls above.
+ */
+PKV_API int pkv_paged_decode_attention_planned(
+    const pkv_bf16* q, const pkv_bf16* pool, int64_t num_pages,
+    const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+    int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+    float scale, pkv_bf16* out, const void* plan_host, const void* plan_dev,
+    void* workspace, size_t workspace_bytes, int32_t* dev_err, pkv_stream_t stream);
+
+PKV_API int pkv_decode_step_planned(
+    const pkv_bf16* q, const pkv_bf16* k_new, const pkv_bf16* v_new, pkv_bf16* pool,
+    int64_t num_pages, const int32_t* block_table, int max_blocks,
+    const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+    int head_dim, int page_size, double rope_theta, float scale, pkv_bf16* out,
+    const void* plan_host, const void* plan_dev, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, pkv_stream_t stream);
 
 /*
  * pkv_paged_decode_attention_static_ws -- the same computation as

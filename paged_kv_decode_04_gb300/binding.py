@@ -11,6 +11,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -28,6 +29,8 @@ DEVERR_SEQLEN = 2
 DEVERR_POSITION = 4
 DEVERR_TIMEOUT = 8
 DEVERR_OFFSETS = 16
+DEVERR_PLAN = 32
+PLAN_MAGIC = 0x31564B50
 
 NUM_Q_HEADS = 32
 NUM_KV_HEADS = 8
@@ -69,6 +72,18 @@ def _load():
     L.pkv_kv_write_prefill.argtypes = [vp, vp, i32, vp, vp, vp, i64, vp, i32, i32, i32, i32, i32,
                                        f64, vp, vp]
     L.pkv_kv_write_prefill.restype = i32
+    L.pkv_plan_bytes.argtypes = [i32, i32]
+    L.pkv_plan_bytes.restype = sz
+    L.pkv_plan_build.argtypes = [vp, i32, i32, i32, vp, sz]
+    L.pkv_plan_build.restype = i32
+    L.pkv_plan_workspace_bytes.argtypes = [vp]
+    L.pkv_plan_workspace_bytes.restype = sz
+    L.pkv_paged_decode_attention_planned.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32,
+                                                     i32, i32, f32, vp, vp, vp, vp, sz, vp, vp]
+    L.pkv_paged_decode_attention_planned.restype = i32
+    L.pkv_decode_step_planned.argtypes = [vp, vp, vp, vp, i64, vp, i32, vp, i32, i32, i32, i32,
+                                          i32, f64, f32, vp, vp, vp, vp, sz, vp, vp]
+    L.pkv_decode_step_planned.restype = i32
     return L
 
 
@@ -260,3 +275,129 @@ def kv_write_prefill(k, v, token_offsets, start_positions, pool, block_table, *,
                                    _stream(stream))
     if rc != PKV_OK:
         raise PkvError(rc, "pkv_kv_write_prefill")
+
+
+# ------------------------------------------------------------- work plans --
+
+class Plan:
+    """A work plan for one batch, built on the host from host lengths
+    (pkv_plan_build in include/pkv.h): ranges of the long sequences first,
+    short sequences packed one per warp.  ``to(device)`` uploads it; the
+    planned calls take the plan object itself."""
+
+    HEADER = ("magic", "batch", "max_blocks", "num_items", "num_merges", "num_slots",
+              "range_pages", "bytes_used")
+
+    def __init__(self, seq_lens_host, max_blocks: int, *, num_sms: int = 0, device=None):
+        lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+        if lens.ndim != 1:
+            raise ValueError("seq_lens_host must be one-dimensional")
+        nbytes = _lib.pkv_plan_bytes(lens.shape[0], max_blocks)
+        if nbytes == 0:
+            raise PkvError(PKV_EINVAL, "pkv_plan_bytes")
+        raw = np.zeros(nbytes // 4 + 4, dtype=np.int32)
+        off = (-raw.ctypes.data % 16) // 4      # 16-byte aligned view
+        buf = raw[off:off + nbytes // 4]
+        rc = _lib.pkv_plan_build(lens.ctypes.data_as(ctypes.c_void_p), lens.shape[0], max_blocks,
+                                 num_sms, buf.ctypes.data_as(ctypes.c_void_p), nbytes)
+        if rc != PKV_OK:
+            raise PkvError(rc, "pkv_plan_build")
+        self._raw = raw
+        self.host = buf[: int(buf[7]) // 4]
+        for i, name in enumerate(self.HEADER):
+            setattr(self, name, int(buf[i]))
+        self.workspace_bytes = int(_lib.pkv_plan_workspace_bytes(buf.ctypes.data_as(ctypes.c_void_p)))
+        self.dev = None
+        if device is not None:
+            self.to(device)
+
+    def items(self) -> np.ndarray:
+        """[num_items][16] int32: kind, slot, p_begin, n, seq[4], len[4], 0 x 4."""
+        return self.host[8:8 + 16 * self.num_items].reshape(self.num_items, 16)
+
+    def merges(self) -> np.ndarray:
+        """[num_merges][4] int32: sequence, first slot, ranges, 0."""
+        o = 8 + 16 * self.num_items
+        return self.host[o:o + 4 * self.num_merges].reshape(self.num_merges, 4)
+
+    def to(self, device):
+        """Copy the plan to `device`, asynchronously on the current stream (through
+        pinned memory, so the host does not wait for the work queued before it)."""
+        staged = torch.empty(self.host.shape[0], dtype=torch.int32, pin_memory=True)
+        staged.numpy()[:] = self.host
+        self.dev = staged.to(device, non_blocking=True)
+        return self
+
+    def _host_ptr(self):
+        return self.host.ctypes.data_as(ctypes.c_void_p)
+
+
+def _plan_workspace(plan, workspace, dev):
+    if plan.dev is None or plan.dev.device != dev:
+        raise ValueError("upload the plan to the pool's device first (Plan.to)")
+    need = plan.workspace_bytes
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the pool's device")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    return workspace, ws_bytes
+
+
+def paged_decode_attention_planned(q, pool, block_table, seq_lens, plan, out=None, *,
+                                   scale: float = None, workspace=None, dev_err=None,
+                                   stream=None) -> torch.Tensor:
+    """paged_decode_attention under a work plan built for these lengths."""
+    num_pages = _pool_pages(pool)
+    dev = pool.device
+    _check(q, "q", torch.bfloat16, 3, dev)
+    _check(block_table, "block_table", torch.int32, 2, dev)
+    _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    if scale is None:
+        scale = D ** -0.5
+    workspace, ws_bytes = _plan_workspace(plan, workspace, dev)
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, None, dev)
+    rc = _lib.pkv_paged_decode_attention_planned(
+        _ptr(q), _ptr(pool), num_pages, _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+        Hq, NUM_KV_HEADS, D, PAGE_SIZE, float(scale), _ptr(out), plan._host_ptr(), _ptr(plan.dev),
+        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    if rc != PKV_OK:
+        raise PkvError(rc, "pkv_paged_decode_attention_planned")
+    return out
+
+
+def decode_step_planned(q, k_new, v_new, pool, block_table, seq_lens, plan, out=None, *,
+                        rope_theta: float = 500000.0, scale: float = None, workspace=None,
+                        dev_err=None, stream=None) -> torch.Tensor:
+    """decode_step under a work plan built for these lengths."""
+    num_pages = _pool_pages(pool)
+    dev = pool.device
+    _check(q, "q", torch.bfloat16, 3, dev)
+    _check(k_new, "k_new", torch.bfloat16, 3, dev)
+    _check(v_new, "v_new", torch.bfloat16, 3, dev)
+    _check(block_table, "block_table", torch.int32, 2, dev)
+    _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    if scale is None:
+        scale = D ** -0.5
+    workspace, ws_bytes = _plan_workspace(plan, workspace, dev)
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, None, dev)
+    rc = _lib.pkv_decode_step_planned(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(pool), num_pages, _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, Hq, k_new.shape[1], D, PAGE_SIZE,
+        float(rope_theta), float(scale), _ptr(out), plan._host_ptr(), _ptr(plan.dev),
+        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    if rc != PKV_OK:
+        raise PkvError(rc, "pkv_decode_step_planned")
+    return out

@@ -44,6 +44,7 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPagesPerSplit = 1024;
+static_assert(kWarps == kPlanWarps, "work plans pack one sequence per warp");
 
 // Stage ring depth per warp.  With at most kDeepStages pages per warp the
 // ring holds all of them at once (3 CTAs per SM fit); longer ranges use
@@ -65,7 +66,12 @@ __host__ __device__ constexpr size_t smem_bytes(int stages, int pages_per_split)
          static_cast<size_t>(pages_per_split) * 4;
 }
 
-template <bool kAppend, int kStages>
+// pick(v, i): component i of an int4.
+__device__ __forceinline__ int pick(int4 v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+template <bool kAppend, int kStages, bool kPlanned>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
     paged_decode_kernel(const __grid_constant__ CUtensorMap pool_map,
                         const AttnArgs a, const AppendArgs ap) {
@@ -79,33 +85,92 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int g = blockIdx.x % kNumKvHeads;
-  const int split = blockIdx.x / kNumKvHeads;
-  const int b = blockIdx.y;
-  const int pps = a.plan.pages_per_split;
   if (tid == 0) tma_prefetch_desc(&pool_map);
   wait_for_prior_grids();
   allow_dependent_grids();
 
-  // ---- sequence extent and this CTA's page range
-  int L = a.seq_lens[b];
+  // ---- this CTA's work.  Range: the 4 warps share the logical pages
+  // [p_begin, p_begin + n) of sequence b (warp w takes every 4th page from
+  // p_begin + w).  Packed (work plans only): warp w attends the whole of its
+  // own sequence wb (-1: none), pages [0, pages(wL)).
+  bool packed = false;
+  int wb, wL;         // this warp's sequence and its length
+  int p_begin = 0, n = 0;
+  int64_t part_row0 = -1;  // partial slot of query row 4g, -1: write the output itself
+  int dev_len = -2;        // planned: device length of wb, read for the plan check
+  int plan_len = 0;        // planned: the length the plan was built for
+  int part_step = 0;       // slot distance between consecutive query rows
   const int Lmax = a.max_blocks * kPageSize;
-  if (L < 0 || L > Lmax) {
-    if (tid == 0 && blockIdx.x == 0) record_error(a.dev_err, kErrSeqLen);
-    L = L < 0 ? 0 : Lmax;
-  }
-  const int npages = (L + kPageSize - 1) / kPageSize;
-  const int nsplit = npages > 0 ? (npages + pps - 1) / pps : 1;
-  if (split >= nsplit) return;
-  const int p_begin = split * pps;
-  const int n = min(pps, npages - p_begin);  // 0 only when L == 0
-
-  for (int i = tid; i < n; i += kThreads) {
-    int32_t pid = a.block_table[static_cast<int64_t>(b) * a.max_blocks + p_begin + i];
-    if (pid < 0 || pid >= a.num_pages) {
-      record_error(a.dev_err, kErrPage);
-      pid = -1;
+  if constexpr (kPlanned) {
+    const int4* it = a.plan_items + static_cast<int64_t>(blockIdx.y) * (kPlanItemWords / 4);
+    const int4 head = it[0];  // (kind, slot, p_begin, n)
+    const int4 bs = it[1];    // sequence of each warp
+    const int4 ls = it[2];    // its length, as the plan was built for
+    packed = head.x == kPlanKindPacked;
+    p_begin = head.z;
+    n = head.w;
+    wb = pick(bs, packed ? warp : 0);
+    wL = pick(ls, packed ? warp : 0);
+    plan_len = wL;
+    if (head.y >= 0) {
+      part_row0 = static_cast<int64_t>(head.y) * kNumQHeads + g * kGroup;
+      part_step = 1;
     }
-    s_pages[i] = pid;
+    // the lengths come from the plan; seq_lens is only checked against it
+    // (the load is consumed at the end of the kernel, off the critical path)
+    if (wb >= 0 && lane == 0 && (packed || warp == 0) && g == 0) dev_len = a.seq_lens[wb];
+    wL = wL < 0 ? 0 : (wL > Lmax ? Lmax : wL);
+  } else {
+    const int split = blockIdx.x / kNumKvHeads;
+    const int pps = a.plan.pages_per_split;
+    wb = blockIdx.y;
+    wL = a.seq_lens[wb];
+    if (wL < 0 || wL > Lmax) {
+      if (tid == 0 && blockIdx.x == 0) record_error(a.dev_err, kErrSeqLen);
+      wL = wL < 0 ? 0 : Lmax;
+    }
+    const int np = (wL + kPageSize - 1) / kPageSize;
+    const int nsplit = np > 0 ? (np + pps - 1) / pps : 1;
+    if (split >= nsplit) return;
+    p_begin = split * pps;
+    n = min(pps, np - p_begin);  // 0 only when L == 0
+    if (nsplit > 1) {
+      part_row0 = (static_cast<int64_t>(wb) * kNumQHeads + g * kGroup) * a.plan.num_splits + split;
+      part_step = a.plan.num_splits;
+    }
+  }
+  const int npages = (wL + kPageSize - 1) / kPageSize;  // pages of this warp's sequence
+
+  // ---- page ids of the CTA's pages (range) or of each warp's (packed)
+  int s_base, s_step, nw, l_base, l_step;
+  if (packed) {
+    nw = wb >= 0 ? min(npages, kPackPages) : 0;
+    s_base = warp * kPackPages;
+    s_step = 1;
+    l_base = 0;
+    l_step = 1;
+    for (int i = lane; i < nw; i += 32) {
+      int32_t pid = a.block_table[static_cast<int64_t>(wb) * a.max_blocks + i];
+      if (pid < 0 || pid >= a.num_pages) {
+        record_error(a.dev_err, kErrPage);
+        pid = -1;
+      }
+      s_pages[s_base + i] = pid;
+    }
+  } else {
+    nw = n > warp ? (n - warp + kWarps - 1) / kWarps : 0;
+    s_base = warp;
+    s_step = kWarps;
+    l_base = p_begin + warp;
+    l_step = kWarps;
+    for (int i = tid; i < n; i += kThreads) {
+      int32_t pid = a.block_table[static_cast<int64_t>(wb) * a.max_blocks + p_begin + i];
+      if (pid < 0 || pid >= a.num_pages) {
+        record_error(a.dev_err, kErrPage);
+        pid = -1;
+      }
+      s_pages[i] = pid;
+    }
   }
   const uint32_t bar0 = smem_addr(bars) + warp * kStages * 8;
   const uint32_t tile0 = smem_addr(smem) + warp * kStages * kTileBytes;
@@ -116,15 +181,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
   __syncthreads();
 
   const LaneGeom G(lane);
-  uint32_t qb[4][2];
-  load_q_frags(a.q + (static_cast<int64_t>(b) * kNumQHeads + g * kGroup) * kHeadDim, G, qb);
+  uint32_t qb[4][2] = {};
+  if (wb >= 0)
+    load_q_frags(a.q + (static_cast<int64_t>(wb) * kNumQHeads + g * kGroup) * kHeadDim, G, qb);
   const float c = a.scale_log2;
 
-  const int nw = n > warp ? (n - warp + kWarps - 1) / kWarps : 0;
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int k) {
     const int st = k % kStages;
-    const int pid = s_pages[warp + k * kWarps];
+    const int pid = s_pages[s_base + k * s_step];
     const uint32_t bar = bar0 + 8 * st;
     if (pid >= 0) {
       mbar_arrive_expect_tx(bar, kTileBytes);
@@ -136,16 +201,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
   if (lane == 0)
     for (int k = 0; k < kStages && k < nw; ++k) issue(k);
 
-  // ---- fused append: computed while the first copies are in flight
-  const int last_local = npages - 1 - p_begin;  // the sequence's last page, in this range
-  const bool owns_last = kAppend && npages > 0 && last_local >= 0 && last_local < n &&
-                         last_local % kWarps == warp;
-  const int a_slot = (L - 1) % kPageSize;
+  // ---- fused append: computed while the first copies are in flight.  The
+  // owner is the warp whose page list holds the sequence's last page; k_last
+  // is that page's position in the list.
+  int k_last = -1;
+  if (kAppend && npages > 0) {
+    const int d = npages - 1 - l_base;
+    if (d >= 0 && d % l_step == 0 && d / l_step < nw) k_last = d / l_step;
+  }
+  const int a_slot = (wL - 1) % kPageSize;
   AppendRow arow{};
-  if (owns_last) {
-    const int64_t src = (static_cast<int64_t>(b) * kNumKvHeads + g) * kHeadDim;
-    arow = make_append_row(ap.k_new + src, ap.v_new + src, L - 1, ap.freqs, lane);
-    const int pid = s_pages[last_local];
+  if (k_last >= 0) {
+    const int64_t src = (static_cast<int64_t>(wb) * kNumKvHeads + g) * kHeadDim;
+    arow = make_append_row(ap.k_new + src, ap.v_new + src, wL - 1, ap.freqs, lane);
+    const int pid = s_pages[s_base + k_last * s_step];
     if (pid >= 0) store_append_row(ap.pool, pid, a_slot, g, arow, lane);
   }
 
@@ -158,11 +227,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
       if (lane == 0) record_error(a.dev_err, kErrTimeout);
       break;
     }
-    const int local = warp + k * kWarps;
-    if (s_pages[local] >= 0) {
+    if (s_pages[s_base + k * s_step] >= 0) {
       const uint32_t kt = tile0 + st * kTileBytes;
-      if (owns_last && local == last_local) patch_append_row(kt, a_slot, arow, lane);
-      const int valid = min(kPageSize, L - (p_begin + local) * kPageSize);
+      if (k == k_last) patch_append_row(kt, a_slot, arow, lane);
+      const int valid = min(kPageSize, wL - (l_base + k * l_step) * kPageSize);
       attend_page(kt, valid, qb, c, G, lane, S);
     }
     __syncwarp();
@@ -172,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
     }
   }
 
-  // ---- merge the warps' states through shared memory
+  // ---- the warps' states through shared memory
   reduce_row_sums(S);
   __syncthreads();  // every warp is done with its stage ring
   float* sm_m = reinterpret_cast<float*>(smem);
@@ -197,9 +265,35 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
   }
   __syncthreads();
 
-  {
+  const int d = 2 * lane;
+  auto write_row = [&](int seq, int r, float M, float Ls, float2 O, int64_t part) {
+    if (part < 0) {
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      const uint32_t v = static_cast<uint32_t>(float_to_bf16_rne(O.x * inv)) |
+                         (static_cast<uint32_t>(float_to_bf16_rne(O.y * inv)) << 16);
+      const int64_t row = static_cast<int64_t>(seq) * kNumQHeads + g * kGroup + r;
+      *reinterpret_cast<uint32_t*>(a.out + row * kHeadDim + d) = v;
+    } else {
+      *reinterpret_cast<float2*>(a.part_acc + part * kHeadDim + d) = O;
+      if (lane == 0) *reinterpret_cast<float2*>(a.part_ml + part * 2) = make_float2(M, Ls);
+    }
+  };
+  if (kPlanned && dev_len != -2 && dev_len != plan_len) record_error(a.dev_err, kErrPlan);
+  if (packed) {
+    // each warp normalises its own 4 rows
+    if (wb >= 0) {
+#pragma unroll
+      for (int r = 0; r < kGroup; ++r) {
+        const float M = sm_m[warp * kGroup + r];
+        const float Ls = M == -INFINITY ? 0.f : sm_l[warp * kGroup + r];
+        const float2 O = M == -INFINITY ? make_float2(0.f, 0.f)
+                                        : *reinterpret_cast<const float2*>(
+                                              sm_o + (warp * kGroup + r) * kHeadDim + d);
+        write_row(wb, r, M, Ls, O, -1);
+      }
+    }
+  } else {
     const int r = warp;  // 4 warps <-> 4 query rows
-    const int d = 2 * lane;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * kGroup + r]);
@@ -218,18 +312,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
         O.y = fmaf(wt, os.y, O.y);
       }
     }
-    const int j = g * kGroup + r;
-    const int64_t row = static_cast<int64_t>(b) * kNumQHeads + j;
-    if (nsplit == 1) {
-      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-      const uint32_t packed = static_cast<uint32_t>(float_to_bf16_rne(O.x * inv)) |
-                              (static_cast<uint32_t>(float_to_bf16_rne(O.y * inv)) << 16);
-      *reinterpret_cast<uint32_t*>(a.out + row * kHeadDim + d) = packed;
-    } else {
-      const int64_t idx = row * a.plan.num_splits + split;
-      *reinterpret_cast<float2*>(a.part_acc + idx * kHeadDim + d) = O;
-      if (lane == 0) *reinterpret_cast<float2*>(a.part_ml + idx * 2) = make_float2(M, Ls);
-    }
+    write_row(wb, r, M, Ls, O, part_row0 < 0 ? -1 : part_row0 + static_cast<int64_t>(r) * part_step);
   }
 }
 
@@ -312,6 +395,18 @@ __global__ void __launch_bounds__(32) merge_splits_kernel(const AttnArgs a) {
   merge_row(a, row * a.plan.num_splits, 1, nsplit, a.out + row * kHeadDim, threadIdx.x);
 }
 
+// Work plan: combine the ranges of the split sequences listed in the plan;
+// grid (Hq, merges), one warp per (sequence, query row).
+__global__ void __launch_bounds__(32) merge_plan_kernel(const AttnArgs a) {
+  wait_for_prior_grids();
+  allow_dependent_grids();
+  const int4 e = a.plan_merges[blockIdx.y];  // (b, first slot, ranges, 0)
+  const int j = blockIdx.x;
+  const int64_t row = static_cast<int64_t>(e.x) * kNumQHeads + j;
+  merge_row(a, static_cast<int64_t>(e.y) * kNumQHeads + j, kNumQHeads, e.z,
+            a.out + row * kHeadDim, threadIdx.x);
+}
+
 }  // namespace
 
 size_t workspace_bytes_for(int batch, int num_q_heads, int head_dim,
@@ -326,27 +421,44 @@ int max_pages_per_split() { return kMaxPagesPerSplit; }
 namespace {
 
 // The dynamic shared-memory opt-in is per device and per kernel.
-template <bool kAppend, int kStages>
+template <bool kAppend, int kStages, bool kPlanned>
 cudaError_t configure_once(int device) {
   static std::atomic<unsigned long long> configured{0};
   const unsigned long long bit = 1ull << (device & 63);
   if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
   const cudaError_t err = cudaFuncSetAttribute(
-      paged_decode_kernel<kAppend, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      paged_decode_kernel<kAppend, kStages, kPlanned>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       static_cast<int>(smem_bytes(kStages, kMaxPagesPerSplit)));
   if (err == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
 
-template <bool kAppend, int kStages>
+template <bool kAppend, int kStages, bool kPlanned>
 cudaError_t launch_variant(const CUtensorMap& pool_map, const AttnArgs& args,
-                           const AppendArgs& append, int device, cudaStream_t stream) {
-  const cudaError_t err = configure_once<kAppend, kStages>(device);
+                           const AppendArgs& append, dim3 grid, int page_list, int device,
+                           cudaStream_t stream) {
+  const cudaError_t err = configure_once<kAppend, kStages, kPlanned>(device);
   if (err != cudaSuccess) return err;
-  const dim3 grid(kNumKvHeads * args.plan.num_splits, args.batch);
-  return launch_pdl(paged_decode_kernel<kAppend, kStages>, grid, dim3(kThreads),
-                    smem_bytes(kStages, args.plan.pages_per_split), stream, pool_map, args,
-                    append);
+  return launch_pdl(paged_decode_kernel<kAppend, kStages, kPlanned>, grid, dim3(kThreads),
+                    smem_bytes(kStages, page_list), stream, pool_map, args, append);
+}
+
+// Ring depth by the pages a warp gets: deep when the ring holds them all.
+template <bool kPlanned>
+cudaError_t launch_attention_kernel(const CUtensorMap& pool_map, const AttnArgs& args,
+                                    const AppendArgs* append, dim3 grid, int range_pages,
+                                    int page_list, int device, cudaStream_t stream) {
+  const bool deep = range_pages <= kWarps * kDeepStages;
+  const AppendArgs none{};
+  if (append != nullptr)
+    return deep ? launch_variant<true, kDeepStages, kPlanned>(pool_map, args, *append, grid,
+                                                              page_list, device, stream)
+                : launch_variant<true, kShallowStages, kPlanned>(pool_map, args, *append, grid,
+                                                                 page_list, device, stream);
+  return deep ? launch_variant<false, kDeepStages, kPlanned>(pool_map, args, none, grid,
+                                                             page_list, device, stream)
+              : launch_variant<false, kShallowStages, kPlanned>(pool_map, args, none, grid,
+                                                                page_list, device, stream);
 }
 
 }  // namespace
@@ -358,14 +470,10 @@ cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
-  const bool deep = args.plan.pages_per_split <= kWarps * kDeepStages;
-  const AppendArgs none{};
-  if (append != nullptr)
-    err = deep ? launch_variant<true, kDeepStages>(pool_map, args, *append, device, stream)
-               : launch_variant<true, kShallowStages>(pool_map, args, *append, device, stream);
-  else
-    err = deep ? launch_variant<false, kDeepStages>(pool_map, args, none, device, stream)
-               : launch_variant<false, kShallowStages>(pool_map, args, none, device, stream);
+  const int pps = args.plan.pages_per_split;
+  err = launch_attention_kernel<false>(pool_map, args, append,
+                                       dim3(kNumKvHeads * args.plan.num_splits, args.batch), pps,
+                                       pps, device, stream);
   if (err != cudaSuccess) return err;
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -373,6 +481,23 @@ cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
     err = launch_pdl(merge_splits_kernel, dim3(kNumQHeads, args.batch), dim3(32), 0, stream,
                      args);
   }
+  return err;
+}
+
+cudaError_t launch_planned_decode_attention(const CUtensorMap& pool_map,
+                                            const AttnArgs& args, int num_items,
+                                            int num_merges, int range_pages,
+                                            cudaStream_t stream, const AppendArgs* append) {
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
+  if (err != cudaSuccess) return err;
+  const int page_list = range_pages > kWarps * kPackPages ? range_pages : kWarps * kPackPages;
+  err = launch_attention_kernel<true>(pool_map, args, append, dim3(kNumKvHeads, num_items),
+                                      range_pages, page_list, device, stream);
+  if (err != cudaSuccess) return err;
+  if (num_merges > 0)
+    err = launch_pdl(merge_plan_kernel, dim3(kNumQHeads, num_merges), dim3(32), 0, stream,
+                     args);
   return err;
 }
 

@@ -393,3 +393,153 @@ extern "C" PKV_API int pkv_paged_decode_attention_static_ws(
                        dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream), nullptr);
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
+
+// ---------------------------------------------------------------------------
+// Work plans (include/pkv.h): built on the host by planner.cpp, run by the
+// attention kernel's planned instances.
+
+namespace {
+
+struct PlanHeader {
+  int32_t magic, batch, max_blocks, num_items, num_merges, num_slots, range_pages, bytes_used;
+};
+
+// The plan's header when it is well formed for this batch and table, else nullptr.
+const PlanHeader* plan_header(const void* plan, int batch, int max_blocks) {
+  if (plan == nullptr || !aligned(plan, 16)) return nullptr;
+  const PlanHeader* h = static_cast<const PlanHeader*>(plan);
+  if (h->magic != static_cast<int32_t>(PKV_PLAN_MAGIC) || h->batch != batch ||
+      h->max_blocks != max_blocks || h->num_items < 1 || h->num_items > 65535 ||
+      h->num_merges < 0 || h->num_slots < 0 || h->range_pages < 1 || h->range_pages > 1024)
+    return nullptr;
+  return h;
+}
+
+size_t plan_slots_bytes(const PlanHeader& h) {
+  return static_cast<size_t>(h.num_slots) * kNumQHeads * (kHeadDim + 2) * sizeof(float);
+}
+
+cudaError_t launch_planned(const PlanHeader& h, const CUtensorMap& map, const pkv_bf16* q,
+                           const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                           int batch, float scale, pkv_bf16* out, const void* plan_dev,
+                           void* workspace, int32_t* dev_err, int64_t num_pages,
+                           cudaStream_t stream, const pkv::AppendArgs* append) {
+  pkv::AttnArgs args = {};
+  args.q = q;
+  args.block_table = block_table;
+  args.seq_lens = seq_lens;
+  args.out = out;
+  float* ws = static_cast<float*>(workspace);
+  const size_t slots = static_cast<size_t>(h.num_slots) * kNumQHeads;
+  args.part_acc = h.num_slots > 0 ? ws : nullptr;
+  args.part_ml = h.num_slots > 0 ? ws + slots * kHeadDim : nullptr;
+  const int32_t* words = static_cast<const int32_t*>(plan_dev);
+  args.plan_items = reinterpret_cast<const int4*>(words + pkv::kPlanHeaderWords);
+  args.plan_merges = reinterpret_cast<const int4*>(
+      words + pkv::kPlanHeaderWords + static_cast<size_t>(h.num_items) * pkv::kPlanItemWords);
+  args.dev_err = dev_err;
+  args.num_pages = num_pages;
+  args.max_blocks = max_blocks;
+  args.batch = batch;
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.plan.num_splits = 1;
+  args.plan.pages_per_split = h.range_pages;
+  return pkv::launch_planned_decode_attention(map, args, h.num_items, h.num_merges,
+                                              h.range_pages, stream, append);
+}
+
+}  // namespace
+
+extern "C" {
+
+PKV_API size_t pkv_plan_bytes(int batch, int max_blocks) {
+  return pkv::plan_bytes(batch, max_blocks);
+}
+
+PKV_API int pkv_plan_build(const int32_t* seq_lens_host, int batch, int max_blocks, int num_sms,
+                           void* plan, size_t plan_bytes) {
+  if (num_sms < 0) return PKV_EINVAL;
+  if (num_sms == 0) {
+    num_sms = current_sm_count();
+    if (num_sms <= 0) return PKV_ECUDA;
+  }
+  return pkv::build_plan(seq_lens_host, batch, max_blocks, num_sms, static_cast<int32_t*>(plan),
+                         plan_bytes);
+}
+
+PKV_API size_t pkv_plan_workspace_bytes(const void* plan) {
+  if (plan == nullptr || !aligned(plan, 16)) return static_cast<size_t>(-1);
+  const PlanHeader* h = static_cast<const PlanHeader*>(plan);
+  if (h->magic != static_cast<int32_t>(PKV_PLAN_MAGIC) || h->num_slots < 0)
+    return static_cast<size_t>(-1);
+  return plan_slots_bytes(*h);
+}
+
+PKV_API int pkv_paged_decode_attention_planned(
+    const pkv_bf16* q, const pkv_bf16* pool, int64_t num_pages, const int32_t* block_table,
+    int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+    int head_dim, int page_size, float scale, pkv_bf16* out, const void* plan_host,
+    const void* plan_dev, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+    pkv_stream_t stream) {
+  if (!q || !pool || !block_table || !seq_lens || !out || !plan_host || !plan_dev)
+    return PKV_EINVAL;
+  if (batch < 1 || batch > 65535 || num_pages < 1 || num_pages > INT32_MAX || max_blocks < 1 ||
+      max_blocks > (INT32_MAX / kPageSize))
+    return PKV_EINVAL;
+  if (!(scale > 0.f) || !isfinite(scale)) return PKV_EINVAL;
+  if (!supported_dims(num_q_heads, num_kv_heads, head_dim, page_size)) return PKV_EUNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(out, 4) || !aligned(workspace, 16) ||
+      !aligned(dev_err, 4) || !aligned(plan_dev, 16) || !aligned(plan_host, 16))
+    return PKV_EALIGN;
+  const PlanHeader* h = plan_header(plan_host, batch, max_blocks);
+  if (h == nullptr) return PKV_EINVAL;
+  const size_t need = plan_slots_bytes(*h);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
+  CUtensorMap map;
+  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
+  const cudaError_t err =
+      launch_planned(*h, map, q, block_table, max_blocks, seq_lens, batch, scale, out, plan_dev,
+                     workspace, dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream),
+                     nullptr);
+  return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+PKV_API int pkv_decode_step_planned(
+    const pkv_bf16* q, const pkv_bf16* k_new, const pkv_bf16* v_new, pkv_bf16* pool,
+    int64_t num_pages, const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+    int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+    double rope_theta, float scale, pkv_bf16* out, const void* plan_host, const void* plan_dev,
+    void* workspace, size_t workspace_bytes, int32_t* dev_err, pkv_stream_t stream) {
+  if (!q || !k_new || !v_new || !pool || !block_table || !seq_lens || !out || !plan_host ||
+      !plan_dev)
+    return PKV_EINVAL;
+  if (batch < 1 || batch > 65535 || num_pages < 1 || num_pages > INT32_MAX || max_blocks < 1 ||
+      max_blocks > (INT32_MAX / kPageSize))
+    return PKV_EINVAL;
+  if (!(scale > 0.f) || !isfinite(scale)) return PKV_EINVAL;
+  if (!(rope_theta > 0.0) || !isfinite(rope_theta)) return PKV_EINVAL;
+  if (!supported_dims(num_q_heads, num_kv_heads, head_dim, page_size)) return PKV_EUNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(out, 4) || !aligned(workspace, 16) ||
+      !aligned(dev_err, 4) || !aligned(v_new, 4) || !aligned(k_new, 2) ||
+      !aligned(plan_dev, 16) || !aligned(plan_host, 16))
+    return PKV_EALIGN;
+  const PlanHeader* h = plan_header(plan_host, batch, max_blocks);
+  if (h == nullptr) return PKV_EINVAL;
+  const size_t need = plan_slots_bytes(*h);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
+  CUtensorMap map;
+  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
+  pkv::AppendArgs app;
+  app.k_new = k_new;
+  app.v_new = v_new;
+  app.pool = pool;
+  if (pkv::prepare_rope(rope_theta, &app.freqs, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return PKV_ECUDA;
+  const cudaError_t err =
+      launch_planned(*h, map, q, block_table, max_blocks, seq_lens, batch, scale, out, plan_dev,
+                     workspace, dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream), &app);
+  return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // extern "C"

@@ -22,6 +22,22 @@ constexpr int kErrSeqLen = 2;
 constexpr int kErrPosition = 4;
 constexpr int kErrTimeout = 8;
 constexpr int kErrOffsets = 16;
+constexpr int kErrPlan = 32;
+
+// Work plans (include/pkv.h): header words, item and merge entry sizes.
+constexpr int kPlanHeaderWords = 8;
+constexpr int kPlanItemWords = 16;
+constexpr int kPlanMergeWords = 4;
+constexpr int kPlanKindRange = 0;   // 4 warps share pages [p_begin, p_begin + n) of one sequence
+constexpr int kPlanKindPacked = 1;  // one whole sequence per warp
+constexpr int kPackPages = 16;      // most pages a packed sequence may have
+constexpr int kPlanWarps = 4;       // warps per attention CTA: one packed sequence each
+
+// Host side of the work plans (planner.cpp): an upper bound on a plan's
+// bytes, and the plan itself from host lengths (PKV_* status).
+size_t plan_bytes(int batch, int max_blocks);
+int build_plan(const int32_t* lens, int batch, int max_blocks, int num_sms, int32_t* out,
+               size_t out_bytes);
 
 // Positions covered by the per-device cos/sin table (the 2048-token context).
 constexpr int kRopeTablePositions = 2048;
@@ -89,6 +105,8 @@ struct AttnArgs {
   uint16_t* out;
   float* part_acc;  // [B][Hq][S][D] fp32, unnormalised
   float* part_ml;   // [B][Hq][S][2] fp32, (max in log2 units, sum)
+  const int4* plan_items;   // work plan items (kPlanItemWords words each), or nullptr
+  const int4* plan_merges;  // work plan merge entries (b, first slot, ranges, 0)
   int32_t* dev_err;
   int64_t num_pages;
   int max_blocks;
@@ -111,6 +129,14 @@ cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
                                           const AttnArgs& args,
                                           cudaStream_t stream,
                                           const AppendArgs* append = nullptr);
+
+// The same under a work plan: grid (Hkv, num_items), then the merge of the
+// num_merges split sequences.  range_pages sizes the shared page list.
+cudaError_t launch_planned_decode_attention(const CUtensorMap& pool_map,
+                                            const AttnArgs& args, int num_items,
+                                            int num_merges, int range_pages,
+                                            cudaStream_t stream,
+                                            const AppendArgs* append = nullptr);
 
 // Largest logical page range one attention CTA handles.
 int max_pages_per_split();

@@ -1,0 +1,187 @@
+// planner.cpp -- host-side work plans for ragged decode batches (the
+// pkv_plan_* entry points of include/pkv.h).  Plain C++17, no CUDA.
+//
+// The attention kernel handles one (work item, kv head) per CTA.  A work
+// item is either a range of logical pages of one sequence, shared by the
+// CTA's 4 warps, or up to 4 short sequences, one per warp.  The plan below
+// is made from the lengths the caller already holds on the host (its
+// scheduler allocated every page), so the grid holds exactly the needed
+// CTAs and the longest work starts first.
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kMinRangePages = 8;     // shortest range worth a CTA of its own
+constexpr int kResidentPerSm = 4;     // attention CTAs resident per SM (shallow ring)
+constexpr int kMaxRangePages = 1024;  // the kernel's shared page list
+
+struct Range {
+  int b, L, p_begin, n, slot;
+};
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+}  // namespace
+
+size_t plan_bytes(int batch, int max_blocks) {
+  if (batch < 1 || max_blocks < 1) return 0;
+  const int rmin = max_blocks < kMinRangePages ? max_blocks : kMinRangePages;
+  const size_t items = static_cast<size_t>(batch) * ceil_div(max_blocks, rmin) + 1;
+  return 4 * (kPlanHeaderWords + items * kPlanItemWords +
+              static_cast<size_t>(batch) * kPlanMergeWords);
+}
+
+// Sizes for work unit u (the pages one warp streams): ranges of R = 4 u
+// pages (at least kMinRangePages, at most the table width and
+// kMaxRangePages), sequences of at most R / 4 pages (and kPackPages) packed
+// one per warp.
+struct Sizes {
+  int range, pack_max;
+};
+
+Sizes sizes_for(long long u, int max_blocks) {
+  const int rmin = max_blocks < kMinRangePages ? max_blocks : kMinRangePages;
+  const int rmax = max_blocks < kMaxRangePages ? max_blocks : kMaxRangePages;
+  long long R = u * kPlanWarps;
+  R = std::max<long long>(R, rmin);
+  R = std::min<long long>(R, rmax);
+  const int range = static_cast<int>(R);
+  return {range, std::min(kPackPages, std::max(1, range / kPlanWarps))};
+}
+
+// Work items (CTAs per kv head) of the plan for sizes z.
+long long count_items(const std::vector<int>& pages, Sizes z) {
+  long long items = 0, packed = 0;
+  for (int p : pages) {
+    if (p <= z.pack_max) ++packed;
+    else items += (p + z.range - 1) / z.range;
+  }
+  return items + (packed + kPlanWarps - 1) / kPlanWarps;
+}
+
+// The work unit U: the smallest whose plan fits in one wave of resident
+// CTAs (kResidentPerSm per SM, 8 kv heads each item), starting from
+// ceil(P / (2 SMs)), the unit at which the ranges alone would fill that
+// wave; when none fits (a batch too large for one wave), the ranges take
+// the whole table width.  Sequences of up to R pages get one range; longer
+// ones are cut into ceil(p / R) ranges of near-equal size, which the merge
+// kernel combines.  Items run in order of the pages their busiest warp
+// streams, most first (ranges before packed items on ties).
+int build_plan(const int32_t* lens, int batch, int max_blocks, int num_sms, int32_t* out,
+               size_t out_bytes) {
+  if (lens == nullptr || out == nullptr || batch < 1 || max_blocks < 1 || num_sms < 1)
+    return PKV_EINVAL;
+  if (reinterpret_cast<uintptr_t>(out) % 16 != 0) return PKV_EALIGN;
+  if (out_bytes < plan_bytes(batch, max_blocks)) return PKV_EINVAL;
+  const long long Lmax = static_cast<long long>(max_blocks) * kPageSize;
+  std::vector<int> pages(batch);
+  long long total = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (lens[b] < 0 || lens[b] > Lmax) return PKV_EINVAL;
+    pages[b] = ceil_div(lens[b], kPageSize);
+    total += pages[b];
+  }
+  const long long wave = static_cast<long long>(kResidentPerSm) * num_sms;  // CTAs
+  const long long u0 = std::max<long long>(1, (total + 2LL * num_sms - 1) / (2LL * num_sms));
+  const long long umax = std::max<long long>(u0, (max_blocks + kPlanWarps - 1) / kPlanWarps);
+  long long lo = u0, hi = umax;  // smallest u in [u0, umax] that fits, else umax
+  while (lo < hi) {
+    const long long mid = (lo + hi) / 2;
+    if (count_items(pages, sizes_for(mid, max_blocks)) * kNumKvHeads <= wave) hi = mid;
+    else lo = mid + 1;
+  }
+  const Sizes z = sizes_for(lo, max_blocks);
+  const int range = z.range;
+  const int pack_max = z.pack_max;
+
+  std::vector<Range> ranges;
+  std::vector<int> packed;
+  std::vector<int32_t> merges;  // (b, first slot, ranges, 0) per split sequence
+  int slots = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int p = pages[b];
+    if (p <= pack_max) {
+      packed.push_back(b);
+    } else if (p <= range) {
+      ranges.push_back({b, lens[b], 0, p, -1});
+    } else {
+      const int nr = ceil_div(p, range);
+      const int base = p / nr, extra = p % nr;
+      int begin = 0;
+      for (int r = 0; r < nr; ++r) {
+        const int n = base + (r < extra ? 1 : 0);
+        ranges.push_back({b, lens[b], begin, n, slots + r});
+        begin += n;
+      }
+      merges.insert(merges.end(), {b, slots, nr, 0});
+      slots += nr;
+    }
+  }
+  std::stable_sort(packed.begin(), packed.end(),
+                   [&](int x, int y) { return pages[x] > pages[y]; });
+  // work items with the pages of their busiest warp, then a stable sort
+  struct Item {
+    int work, kind, index;  // index into ranges or into packed (first of 4)
+  };
+  std::vector<Item> order;
+  for (size_t i = 0; i < ranges.size(); ++i)
+    order.push_back({(ranges[i].n + kPlanWarps - 1) / kPlanWarps, kPlanKindRange,
+                     static_cast<int>(i)});
+  for (size_t i = 0; i < packed.size(); i += kPlanWarps)
+    order.push_back({pages[packed[i]], kPlanKindPacked, static_cast<int>(i)});
+  std::stable_sort(order.begin(), order.end(), [](const Item& x, const Item& y) {
+    return x.work != y.work ? x.work > y.work : x.kind < y.kind;
+  });
+  const size_t num_items = order.size();
+  const size_t num_merges = merges.size() / kPlanMergeWords;
+  if (num_items > 65535) return PKV_EUNSUPPORTED;  // grid y limit
+
+  const size_t words = kPlanHeaderWords + num_items * kPlanItemWords + merges.size();
+  memset(out, 0, words * 4);
+  out[0] = static_cast<int32_t>(PKV_PLAN_MAGIC);
+  out[1] = batch;
+  out[2] = max_blocks;
+  out[3] = static_cast<int32_t>(num_items);
+  out[4] = static_cast<int32_t>(num_merges);
+  out[5] = slots;
+  out[6] = range;
+  out[7] = static_cast<int32_t>(words * 4);
+  int32_t* item = out + kPlanHeaderWords;
+  for (const Item& o : order) {
+    if (o.kind == kPlanKindRange) {
+      const Range& r = ranges[o.index];
+      item[0] = kPlanKindRange;
+      item[1] = r.slot;
+      item[2] = r.p_begin;
+      item[3] = r.n;
+      for (int w = 0; w < kPlanWarps; ++w) {
+        item[4 + w] = r.b;
+        item[8 + w] = r.L;
+      }
+    } else {
+      item[0] = kPlanKindPacked;
+      item[1] = -1;
+      for (int w = 0; w < kPlanWarps; ++w) {
+        const size_t k = static_cast<size_t>(o.index) + w;
+        const bool has = k < packed.size();
+        item[4 + w] = has ? packed[k] : -1;
+        item[8 + w] = has ? lens[packed[k]] : 0;
+      }
+    }
+    item += kPlanItemWords;
+  }
+  if (!merges.empty()) memcpy(item, merges.data(), merges.size() * 4);
+  return PKV_OK;
+}
+
+}  // namespace pkv

@@ -27,7 +27,7 @@ HQ, HKV, D, P = 32, 8, 64, 16
 class Engine:
     def __init__(self, num_pages: int, layers: int, device, *, max_context: int = 2048,
                  static_batching: bool = False, max_batch: int = 256, seed: int = 0,
-                 host_inputs: bool = False):
+                 host_inputs: bool = False, use_plan: bool = True):
         self.dev = torch.device(device)
         self.layers = layers
         self.max_batch = max_batch
@@ -41,6 +41,9 @@ class Engine:
         need = max(binding.workspace_bytes(n, self.max_blocks) for n in range(1, max_batch + 1))
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.dev)
         self.host_inputs = host_inputs
+        # the scheduler knows every length, so each decode step runs under a
+        # work plan built from them (pkv_plan_build), shared by all layers
+        self.use_plan = use_plan
         self.rng = np.random.default_rng(seed)
         self.gen = torch.Generator(device=self.dev).manual_seed(seed)
 
@@ -69,13 +72,23 @@ class Engine:
         n = len(ids)
         if n:
             dlens = torch.from_numpy(lens).to(self.dev)
+            plan = None
+            if self.use_plan:
+                plan = binding.Plan(lens, self.max_blocks, device=self.dev)
+                if plan.workspace_bytes > self.ws.numel():
+                    self.ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8,
+                                          device=self.dev)
             for layer in range(self.layers):
                 q = self._normal((n, HQ, D))
                 kn = self._normal((n, HKV, D))
                 vn = self._normal((n, HKV, D))
                 btl = torch.from_numpy(bts[layer]).to(self.dev)
-                out = binding.decode_step(q, kn, vn, self.pool, btl, dlens, workspace=self.ws,
-                                          dev_err=self.err)
+                if plan is not None:
+                    out = binding.decode_step_planned(q, kn, vn, self.pool, btl, dlens, plan,
+                                                      workspace=self.ws, dev_err=self.err)
+                else:
+                    out = binding.decode_step(q, kn, vn, self.pool, btl, dlens,
+                                              workspace=self.ws, dev_err=self.err)
                 if on_decode is not None:
                     on_decode(layer, ids, lens, bts[layer], q, kn, vn, out)
         return n

@@ -15,13 +15,13 @@ pytestmark = pytest.mark.gpu
 POISON = 0xFFFF
 
 
-@pytest.mark.parametrize("static", [False, True])
-def test_engine_run_matches_oracle_mirror(static):
+@pytest.mark.parametrize("static,use_plan", [(False, True), (True, True), (False, False)])
+def test_engine_run_matches_oracle_mirror(static, use_plan):
     dev = cuda_or_skip()
     from paged_kv_decode_04_gb300.engine import Engine
     num_pages, layers = 96, 2
     eng = Engine(num_pages, layers, dev, static_batching=static, max_batch=8, seed=3,
-                 host_inputs=True)
+                 host_inputs=True, use_plan=use_plan)
     mirror = np.full((num_pages, 2, 16, 8, 64), POISON, dtype=np.uint16)
     checked = {"prefill": 0, "decode": 0}
 

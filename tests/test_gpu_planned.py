@@ -1,0 +1,193 @@
+"""GPU parity of the planned calls (pkv_*_planned): attention and the fused
+step under a work plan built on the host from the lengths.
+
+Outputs are checked against the FP64 oracle with the attention tolerance of
+_gpu_util.  A plan that reproduces the fixed one-range-per-sequence split must
+give the same bits as the unplanned call; the fused step must equal append +
+attention bit for bit under the same plan; repeated calls give identical bits.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_04_gb300 import synth
+from _gpu_util import assert_close, binding, cuda_or_skip
+
+pytestmark = pytest.mark.gpu
+
+
+def case(lens, seed=13, max_blocks=128):
+    lens = np.asarray(lens, np.int32)
+    pages = int(sum((int(L) + 15) // 16 for L in lens))
+    w = synth.make_workload("edge", seed, seq_lens=lens, num_pages=max(64, pages + 16),
+                            max_blocks=max_blocks)
+    pool = synth.host_pool(w)
+    live = np.nonzero(w.seq_lens > 0)[0]
+    if len(live):
+        assert oracle.kv_append(w.k_new[0][live], w.v_new[0][live], pool,
+                                w.block_tables[0][live], w.positions[live]) == 0
+    return w, pool
+
+
+def dev_bf16(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def planned_attention(w, pool_dev, dev, plan, lens=None, err=None):
+    lens = w.seq_lens if lens is None else lens
+    return binding().paged_decode_attention_planned(
+        dev_bf16(w.q[0], dev), pool_dev, torch.from_numpy(w.block_tables[0]).to(dev),
+        torch.from_numpy(np.asarray(lens, np.int32)).to(dev), plan, dev_err=err)
+
+
+def mixed_lengths(rng, n_short, n_long):
+    lens = np.concatenate([rng.integers(16, 129, n_short), rng.integers(1536, 2049, n_long)])
+    return rng.permutation(lens).astype(np.int32)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_mixed_batch_every_output(seed):
+    dev = cuda_or_skip()
+    lens = mixed_lengths(np.random.default_rng(seed), 115, 13)
+    w, pool = case(lens, seed=seed)
+    plan = binding().Plan(w.seq_lens, w.max_blocks, device=dev)
+    assert plan.num_merges > 0 and any(plan.items()[:, 0] == 1)   # both item kinds
+    ref = oracle.decode_attention(w.q[0], pool, w.block_tables[0], w.seq_lens)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pool_dev = dev_bf16(pool, dev)
+    got = synth.bits(planned_attention(w, pool_dev, dev, plan, err=err))
+    assert_close(got, ref, f"planned mixed batch seed {seed}")
+    again = synth.bits(planned_attention(w, pool_dev, dev, plan, err=err))
+    assert np.array_equal(got, again)
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("lens", [
+    [0, 0, 0, 0, 0],
+    [1],
+    [37],
+    [2048],
+    [2048] + [0] * 30,
+    [128 * 16, 8 * 16, 8 * 16 + 1, 16 * 16 - 1, 16 * 16, 16 * 16 + 1, 3],
+    [0, 2048, 0, 1, 2047, 0],
+    list(range(1, 200, 7)),
+])
+def test_edge_batches(lens):
+    dev = cuda_or_skip()
+    w, pool = case(lens)
+    plan = binding().Plan(w.seq_lens, w.max_blocks, device=dev)
+    ref = oracle.decode_attention(w.q[0], pool, w.block_tables[0], w.seq_lens)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    got = synth.bits(planned_attention(w, dev_bf16(pool, dev), dev, plan, err=err))
+    assert_close(got, ref, f"lens={lens}")
+    for i, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[i] == 0)
+    assert int(err.item()) == 0
+
+
+def test_fused_step_equals_append_then_attention():
+    dev = cuda_or_skip()
+    lens = mixed_lengths(np.random.default_rng(5), 40, 6)
+    w = synth.make_workload("edge", 5, seq_lens=lens, num_pages=2048)
+    b = binding()
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev)
+    outs, pools = [], []
+    for fused in (False, True):
+        d = synth.device_inputs(w, dev)
+        bt = d["block_tables"][0]
+        if fused:
+            out = b.decode_step_planned(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"], bt,
+                                        d["seq_lens"], plan, rope_theta=w.rope_theta,
+                                        scale=w.scale)
+        else:
+            b.kv_append(d["k_new"][0], d["v_new"][0], d["pool"], bt, d["positions"],
+                        rope_theta=w.rope_theta)
+            out = b.paged_decode_attention_planned(d["q"][0], d["pool"], bt, d["seq_lens"], plan,
+                                                   scale=w.scale)
+        outs.append(synth.bits(out))
+        pools.append(synth.bits(d["pool"]))
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(pools[0], pools[1])
+    # and the appended slots are the oracle's
+    c_pool = synth.host_pool(w)
+    assert oracle.kv_append(w.k_new[0], w.v_new[0], c_pool, w.block_tables[0], w.positions) == 0
+    live = w.block_tables[0][np.arange(w.batch), w.positions // 16]
+    slots = w.positions % 16
+    assert np.array_equal(pools[1][live, :, slots], c_pool[live, :, slots])
+
+
+def test_uniform_plan_matches_the_unplanned_call_bit_for_bit():
+    # 64 x 2048, planned as for a 16-SM part: one range per sequence, which is
+    # the fixed S = 1 split (a plan made for another SM count is still valid)
+    dev = cuda_or_skip()
+    w = synth.make_workload("edge", 21, seq_lens=np.full(64, 2048, np.int32), num_pages=8192)
+    d = synth.device_inputs(w, dev)
+    b = binding()
+    plan = b.Plan(w.seq_lens, w.max_blocks, num_sms=16, device=dev)
+    assert plan.num_merges == 0 and set(plan.items()[:, 3].tolist()) == {128}
+    bt = d["block_tables"][0]
+    want = b.paged_decode_attention(d["q"][0], d["pool"], bt, d["seq_lens"], num_splits=1)
+    got = b.paged_decode_attention_planned(d["q"][0], d["pool"], bt, d["seq_lens"], plan)
+    assert np.array_equal(synth.bits(got), synth.bits(want))
+
+
+def test_plan_mismatch_and_bad_pages_are_reported():
+    dev = cuda_or_skip()
+    w, pool = case([600, 40, 2048, 7])
+    b = binding()
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev)
+    pool_dev = dev_bf16(pool, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lens = w.seq_lens.copy()
+    lens[1] += 1                                   # the device disagrees with the plan
+    got = synth.bits(planned_attention(w, pool_dev, dev, plan, lens=lens, err=err))
+    assert int(err.item()) & b.DEVERR_PLAN
+    ref = oracle.decode_attention(w.q[0], pool, w.block_tables[0], w.seq_lens)
+    assert_close(got, ref, "outputs follow the plan's lengths")
+    err.zero_()
+    bt = w.block_tables[0].copy()
+    bt[2, 5] = w.num_pages + 3
+    bt[3, 0] = -7
+    out = b.paged_decode_attention_planned(
+        dev_bf16(w.q[0], dev), pool_dev, torch.from_numpy(bt).to(dev),
+        torch.from_numpy(w.seq_lens).to(dev), plan, dev_err=err)
+    assert int(err.item()) & b.DEVERR_PAGE
+    got = synth.bits(out)
+    assert_close(got[:2], ref[:2], "untouched sequences")
+    assert np.all(np.isfinite(oracle.bf16_to_f64(got)))
+
+
+def test_plan_must_match_the_batch():
+    dev = cuda_or_skip()
+    w, pool = case([100, 200])
+    b = binding()
+    plan = b.Plan([100, 200, 300], w.max_blocks, device=dev)   # built for another batch
+    with pytest.raises(b.PkvError):
+        planned_attention(w, dev_bf16(pool, dev), dev, plan)
+
+
+def test_mix_workload_planned_sampled():
+    # the 16-layer mix workload in its benchmark form: one plan for all layers
+    dev = cuda_or_skip()
+    w = synth.make_workload("mix", 0)
+    d = synth.device_inputs(w, dev)
+    b = binding()
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = []
+    for layer in range(w.layers):
+        outs.append(synth.bits(b.decode_step_planned(
+            d["q"][layer], d["k_new"][layer], d["v_new"][layer], d["pool"],
+            d["block_tables"][layer], d["seq_lens"], plan, rope_theta=w.rope_theta,
+            scale=w.scale, dev_err=err)))
+    from _gpu_util import oracle_step
+    long_seqs = np.nonzero(w.seq_lens >= 1536)[0]
+    short_seqs = np.nonzero(w.seq_lens <= 128)[0][:8]
+    seqs = np.sort(np.concatenate([long_seqs, short_seqs]))
+    for layer in (0, 15):
+        ref, _ = oracle_step(w, layer, seqs)
+        assert_close(outs[layer][seqs], ref, f"mix layer {layer}")
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0

@@ -1,0 +1,182 @@
+"""Host-side work plans (pkv_plan_build, include/pkv.h) -- CPU only.
+
+The plan is checked against what it must guarantee whatever its heuristics:
+every page of every sequence is attended exactly once, in a range or by one
+packed warp; split sequences list their ranges' slots for the merge; CTAs
+run in order of the pages their busiest warp streams; the sizes follow the
+stated formula.
+"""
+import numpy as np
+import pytest
+
+from paged_kv_decode_04_gb300 import binding as B
+
+SMS = 152
+
+
+def build(lens, max_blocks=128, sms=SMS):
+    return B.Plan(np.asarray(lens, np.int32), max_blocks, num_sms=sms)
+
+
+def coverage(plan, lens):
+    """Per sequence: the list of (first page, count) pieces the plan attends."""
+    pieces = {b: [] for b in range(len(lens))}
+    slots = {}
+    for it in plan.items():
+        kind, slot, p0, n = (int(x) for x in it[:4])
+        seqs, ls = it[4:8], it[8:12]
+        if kind == 0:
+            assert len(set(seqs.tolist())) == 1 and len(set(ls.tolist())) == 1
+            b = int(seqs[0])
+            assert int(ls[0]) == lens[b]
+            pieces[b].append((p0, n))
+            if slot >= 0:
+                assert slot not in slots
+                slots[slot] = (b, p0)
+        else:
+            assert kind == 1 and slot == -1
+            for s, L in zip(seqs.tolist(), ls.tolist()):
+                if s >= 0:
+                    assert L == lens[s]
+                    pieces[s].append((0, -(-L // 16)))
+    return pieces, slots
+
+
+@pytest.mark.parametrize("lens", [
+    [2048] * 256,
+    [2048],
+    [37],
+    [0, 0, 0],
+    [0, 1, 15, 16, 17, 2047, 2048, 300, 128, 129],
+    list(np.random.default_rng(1).integers(0, 2049, 300)),
+    list(np.random.default_rng(2).permutation(
+        np.concatenate([np.random.default_rng(3).integers(16, 129, 115),
+                        np.random.default_rng(4).integers(1536, 2049, 13)]))),
+])
+def test_every_page_once_and_merges_consistent(lens):
+    lens = [int(x) for x in lens]
+    plan = build(lens)
+    assert plan.magic == B.PLAN_MAGIC and plan.batch == len(lens) and plan.max_blocks == 128
+    pieces, slots = coverage(plan, lens)
+    for b, L in enumerate(lens):
+        p = -(-L // 16)
+        got = sorted(pieces[b])
+        assert len(got) >= 1, b                    # even an empty sequence gets its zero row
+        covered = []
+        for p0, n in got:
+            covered += list(range(p0, p0 + n))
+        assert covered == list(range(p)), (b, got)
+    merged = set()
+    for b, first, nr, zero in plan.merges().tolist():
+        assert zero == 0 and nr >= 2 and b not in merged
+        merged.add(b)
+        assert [slots[first + r][0] for r in range(nr)] == [b] * nr
+        assert [slots[first + r][1] for r in range(nr)] == sorted(p0 for p0, _ in pieces[b])
+    split = {b for b in range(len(lens)) if len(pieces[b]) > 1}
+    assert split == merged
+    assert plan.num_slots == len(slots)
+    assert plan.workspace_bytes == plan.num_slots * 32 * 66 * 4
+
+
+def expected_sizes(lens, sms, max_blocks=128):
+    """The stated rule, written out: the smallest work unit u >= ceil(P / (2 SMs))
+    whose plan has at most 4 * SMs CTAs (8 per item), else the widest ranges."""
+    pages = [-(-int(L) // 16) for L in lens]
+    P = sum(pages)
+
+    def sizes(u):
+        R = min(max_blocks, 1024, max(min(8, max_blocks), 4 * u))
+        return R, min(16, max(1, R // 4))
+
+    def items(u):
+        R, pack = sizes(u)
+        n_packed = sum(1 for p in pages if p <= pack)
+        return sum(-(-p // R) for p in pages if p > pack) + -(-n_packed // 4)
+
+    u = max(1, -(-P // (2 * sms)))
+    umax = max(u, -(-max_blocks // 4))
+    while u < umax and items(u) * 8 > 4 * sms:
+        u += 1
+    return sizes(u)
+
+
+def test_sizes_follow_the_formula():
+    rng = np.random.default_rng(9)
+    for _ in range(50):
+        n = int(rng.integers(1, 400))
+        lens = rng.integers(0, 2049, n)
+        sms = int(rng.choice([1, 16, 132, 152]))
+        plan = build(lens, sms=sms)
+        R, pack = expected_sizes(lens, sms)
+        assert plan.range_pages == R
+        for it in plan.items():
+            if it[0] == 0:
+                assert 1 <= it[3] <= R
+                assert -(-int(it[8]) // 16) > pack    # longer sequences only
+            else:
+                for L in it[8:12]:
+                    assert -(-int(L) // 16) <= pack
+
+
+def busiest_warp_pages(item):
+    if item[0] == 0:
+        return -(-int(item[3]) // 4)
+    return max(-(-int(L) // 16) for L in item[8:12])
+
+
+@pytest.mark.parametrize("seed", [5, 6, 7])
+def test_order_busiest_warp_first(seed):
+    rng = np.random.default_rng(seed)
+    lens = np.concatenate([rng.integers(0, 200, 150), rng.integers(1000, 2049, 10)])
+    it = build(rng.permutation(lens)).items()
+    work = [busiest_warp_pages(x) for x in it]
+    assert work == sorted(work, reverse=True)
+    for a, b in zip(it[:-1], it[1:]):              # ranges before packed items on ties
+        if busiest_warp_pages(a) == busiest_warp_pages(b):
+            assert a[0] <= b[0]
+
+
+def test_uniform_batch_is_one_range_per_sequence():
+    plan = build([2048] * 256)
+    assert plan.num_items == 256 and plan.num_merges == 0 and plan.num_slots == 0
+    it = plan.items()
+    assert it[:, 4].tolist() == list(range(256))   # sequence order kept
+    assert set(it[:, 3].tolist()) == {128} and set(it[:, 1].tolist()) == {-1}
+
+
+def test_single_long_sequence_is_split_in_equal_ranges():
+    plan = build([2048])
+    assert plan.range_pages == 8 and plan.num_items == 16
+    assert plan.merges().tolist() == [[0, 0, 16, 0]]
+    assert plan.items()[:, 2].tolist() == list(range(0, 128, 8))
+
+
+def test_same_lengths_same_bytes():
+    lens = np.random.default_rng(6).integers(0, 2049, 77)
+    assert np.array_equal(build(lens).host, build(lens).host)
+
+
+def test_invalid_inputs():
+    with pytest.raises(B.PkvError):
+        build([-1])
+    with pytest.raises(B.PkvError):
+        build([2049])                               # past the table
+    with pytest.raises(B.PkvError):
+        build([16], max_blocks=0)
+    lib = B.lib()
+    assert lib.pkv_plan_bytes(0, 128) == 0
+    import ctypes
+    lens = np.array([16], np.int32)
+    buf = np.zeros(64, np.int32)
+    rc = lib.pkv_plan_build(lens.ctypes.data_as(ctypes.c_void_p), 1, 128, SMS,
+                            buf.ctypes.data_as(ctypes.c_void_p), 16)   # too small
+    assert rc == B.PKV_EINVAL
+    assert lib.pkv_plan_workspace_bytes(buf.ctypes.data_as(ctypes.c_void_p)) == \
+        ctypes.c_size_t(-1).value                   # no magic
+
+
+def test_wide_tables_cap_the_range():
+    # max_blocks past the kernel's 1024-entry page list: ranges stay <= 1024
+    plan = build([65536] * 2, max_blocks=4096, sms=1)
+    assert plan.range_pages == 1024
+    assert max(int(n) for n in plan.items()[:, 3]) <= 1024
