@@ -66,6 +66,60 @@ __host__ __device__ constexpr size_t smem_bytes(int stages, int pages_per_split)
          static_cast<size_t>(pages_per_split) * 4;
 }
 
+// Merge of one query row over the partial slots base + s * stride, s < nr,
+// into a bf16 output row: one warp, lane l holding dims 2l and 2l + 1.  The
+// splits are taken 16 at a time: lane s loads split s's (max, sum) pair and
+// every lane loads its two dims of all 16 accumulators at once (they do not
+// depend on the max), so one round of loads serves up to 16 splits; the
+// pairs are combined with shuffles and the accumulators added in split
+// order (deterministic).  Splits that saw no valid key (sum 0) get weight 0.
+// The partials are read through L2 (ld.global.cg).
+constexpr int kMergeBatch = 16;
+
+__device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t base, int64_t stride,
+                                          int nr, uint16_t* out_row, int lane) {
+  float M = -INFINITY, Ls = 0.f;
+  float2 O = make_float2(0.f, 0.f);
+  for (int s0 = 0; s0 < nr; s0 += kMergeBatch) {
+    const int cnt = min(kMergeBatch, nr - s0);
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < cnt)
+      ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (base + (s0 + lane) * stride) * 2));
+    float2 acc[kMergeBatch];
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u)
+      acc[u] = u < cnt ? __ldcg(reinterpret_cast<const float2*>(
+                             a.part_acc + (base + (s0 + u) * stride) * kHeadDim + 2 * lane))
+                       : make_float2(0.f, 0.f);
+    float m = ml.y > 0.f ? ml.x : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
+    if (m == -INFINITY) continue;  // no valid key in these splits
+    // rescale what earlier batches gathered to the new maximum
+    const float Mn = fmaxf(M, m);
+    const float r = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
+    Ls *= r;
+    O.x *= r;
+    O.y *= r;
+    M = Mn;
+    const float wgt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
+    float lw = ml.y * wgt;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(kFullMask, lw, o);
+    Ls += lw;
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const float wu = __shfl_sync(kFullMask, wgt, u);
+      O.x = fmaf(wu, acc[u].x, O.x);
+      O.y = fmaf(wu, acc[u].y, O.y);
+    }
+  }
+  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  *reinterpret_cast<uint32_t*>(out_row + 2 * lane) =
+      static_cast<uint32_t>(float_to_bf16_rne(O.x * inv)) |
+      (static_cast<uint32_t>(float_to_bf16_rne(O.y * inv)) << 16);
+}
+
 // pick(v, i): component i of an int4.
 __device__ __forceinline__ int pick(int4 v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
@@ -316,68 +370,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
   }
 }
 
-// Merge of one query row over the partial slots base + s * stride, s < nr,
-// into a bf16 output row: one warp, lane l holding dims 2l and 2l + 1.  The
-// (max, sum) pairs are loaded one per lane, 32 splits at a time, and combined
-// with shuffles; the accumulators are then read 8 splits at a time so that
-// their loads overlap, and added in split order (deterministic).  Splits
-// that saw no valid key (sum 0) are skipped.
-__device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t base, int64_t stride,
-                                          int nr, uint16_t* out_row, int lane) {
-  float M = -INFINITY;
-  for (int s0 = 0; s0 < nr; s0 += 32) {
-    float m = -INFINITY;
-    if (s0 + lane < nr) {
-      const float2 ml =
-          *reinterpret_cast<const float2*>(a.part_ml + (base + (s0 + lane) * stride) * 2);
-      if (ml.y > 0.f) m = ml.x;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
-    M = fmaxf(M, m);
-  }
-  float Ls = 0.f;
-  float2 O = make_float2(0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < nr; s0 += 32) {
-      float wgt = 0.f, lw = 0.f;
-      if (s0 + lane < nr) {
-        const float2 ml =
-            *reinterpret_cast<const float2*>(a.part_ml + (base + (s0 + lane) * stride) * 2);
-        if (ml.y > 0.f) {
-          wgt = fast_exp2(ml.x - M);
-          lw = ml.y * wgt;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(kFullMask, lw, o);
-      Ls += lw;
-      const int cnt = min(32, nr - s0);
-      for (int k = 0; k < cnt; k += 8) {
-        float wk[8];
-        float2 acc[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          wk[u] = __shfl_sync(kFullMask, wgt, (k + u) & 31);
-          acc[u] = make_float2(0.f, 0.f);
-          if (k + u < cnt && wk[u] != 0.f)
-            acc[u] = *reinterpret_cast<const float2*>(
-                a.part_acc + (base + (s0 + k + u) * stride) * kHeadDim + 2 * lane);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          O.x = fmaf(wk[u], acc[u].x, O.x);
-          O.y = fmaf(wk[u], acc[u].y, O.y);
-        }
-      }
-    }
-  }
-  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-  *reinterpret_cast<uint32_t*>(out_row + 2 * lane) =
-      static_cast<uint32_t>(float_to_bf16_rne(O.x * inv)) |
-      (static_cast<uint32_t>(float_to_bf16_rne(O.y * inv)) << 16);
-}
-
 // Combine the split partials of one (b, j): grid (Hq, B), one warp.
 __global__ void __launch_bounds__(32) merge_splits_kernel(const AttnArgs a) {
   const int j = blockIdx.x;
@@ -395,7 +387,7 @@ __global__ void __launch_bounds__(32) merge_splits_kernel(const AttnArgs a) {
   merge_row(a, row * a.plan.num_splits, 1, nsplit, a.out + row * kHeadDim, threadIdx.x);
 }
 
-// Work plan: combine the ranges of the split sequences listed in the plan;
+// Work plan: combine the ranges of the split sequences the plan lists;
 // grid (Hq, merges), one warp per (sequence, query row).
 __global__ void __launch_bounds__(32) merge_plan_kernel(const AttnArgs a) {
   wait_for_prior_grids();

@@ -191,3 +191,31 @@ def test_mix_workload_planned_sampled():
         assert_close(outs[layer][seqs], ref, f"mix layer {layer}")
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+
+
+def test_graph_replays_reuse_the_plan():
+    # a captured planned call (attention + merge) replays to the eager result
+    dev = cuda_or_skip()
+    lens = mixed_lengths(np.random.default_rng(8), 60, 8)
+    w = synth.make_workload("edge", 8, seq_lens=lens, num_pages=4096)
+    d = synth.device_inputs(w, dev)
+    b = binding()
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev)
+    assert plan.num_merges > 0
+    bt = d["block_tables"][0]
+    ws = torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device=dev)
+    want = b.paged_decode_attention_planned(d["q"][0], d["pool"], bt, d["seq_lens"], plan,
+                                            workspace=ws)
+    want_bits = synth.bits(want)
+    out = torch.zeros_like(want)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        b.paged_decode_attention_planned(d["q"][0], d["pool"], bt, d["seq_lens"], plan, out,
+                                         workspace=ws)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(synth.bits(out), want_bits)

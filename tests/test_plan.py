@@ -76,6 +76,9 @@ def test_every_page_once_and_merges_consistent(lens):
     assert split == merged
     assert plan.num_slots == len(slots)
     assert plan.workspace_bytes == plan.num_slots * 32 * 66 * 4
+    for it in plan.items():                        # words 12..15 are reserved zeros
+        assert not it[12:].any()
+    assert plan.bytes_used == 4 * (8 + 16 * plan.num_items + 4 * plan.num_merges)
 
 
 def expected_sizes(lens, sms, max_blocks=128):
