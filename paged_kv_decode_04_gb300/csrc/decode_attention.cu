@@ -278,7 +278,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
     const int st = k % kStages;
     const bool ready = mbar_wait_bounded(bar0 + 8 * st, (k / kStages) & 1);
     if (!__all_sync(kFullMask, ready)) {
-      if (lane == 0) record_error(a.dev_err, kErrTimeout);
+      // give up on this warp's pages, but not before the copies it issued
+      // (pages k .. k + kStages - 1) have landed -- each wait bounded again --
+      // since the epilogue reuses the stage buffers
+      if (lane == 0) {
+        record_error(a.dev_err, kErrTimeout);
+        for (int j = k; j < k + kStages && j < nw; ++j)
+          mbar_wait_bounded(bar0 + 8 * (j % kStages), (j / kStages) & 1);
+      }
+      __syncwarp();
       break;
     }
     if (s_pages[s_base + k * s_step] >= 0) {
