@@ -234,27 +234,29 @@ def oracle_sample_run(w, n_seqs: int, rng_seed: int = 0, threads: int = 0):
     """Time the FP64 oracle on n_seqs sequences of every layer (append + attention).
 
     The sample's inputs are relabelled into compact host copies first (not
-    timed).  Returns (seconds, algorithmic bytes of the sample, threads, seqs)."""
+    timed).  Returns (seconds, algorithmic bytes of the sample, threads, number
+    of sequences, the sampled sequence ids, the oracle's outputs per layer)."""
     import oracle
     from paged_kv_decode_04_gb300 import synth
     rng = np.random.default_rng(rng_seed)
     seqs = np.sort(rng.choice(w.batch, size=min(n_seqs, w.batch), replace=False))
     threads = threads or oracle.default_threads()
     comps = [synth.compact(w, layer, seqs) for layer in range(w.layers)]
+    refs = []
     t0 = time.perf_counter()
     for c in comps:
         oracle.kv_append(c.k_new, c.v_new, c.pool, c.block_table, c.positions,
                          page_size=w.page_size, theta=w.rope_theta)
-        oracle.decode_attention(c.q, c.pool, c.block_table, c.seq_lens,
-                                num_kv_heads=w.num_kv_heads, page_size=w.page_size,
-                                scale=w.scale, threads=threads)
+        refs.append(oracle.decode_attention(c.q, c.pool, c.block_table, c.seq_lens,
+                                            num_kv_heads=w.num_kv_heads, page_size=w.page_size,
+                                            scale=w.scale, threads=threads))
     dt = time.perf_counter() - t0
     sub = synth.Workload(
         name=w.name, seed=w.seed, layers=w.layers, batch=len(seqs), num_pages=w.num_pages,
         seq_lens=w.seq_lens[seqs], block_tables=w.block_tables[:, seqs], live_pages=w.live_pages,
         page_data=w.page_data[:0], q=w.q[:, seqs], k_new=w.k_new[:, seqs],
         v_new=w.v_new[:, seqs])
-    return dt, algorithmic_bytes(sub, "step"), threads, len(seqs)
+    return dt, algorithmic_bytes(sub, "step"), threads, len(seqs), seqs, refs
 
 
 # ------------------------------------------------------------------ main --
@@ -271,7 +273,7 @@ def run_reference(args, world, rank):
     total_b = 0
     threads = 1
     for k in range(args.steps):
-        dt, nb, threads, used = oracle_sample_run(w, n_seqs, 100 + k)
+        dt, nb, threads, used, _, _ = oracle_sample_run(w, n_seqs, 100 + k)
         total_t += dt
         total_b += nb
     value = total_b / total_t / 1e9
@@ -554,11 +556,21 @@ def run_ours(args, world, rank, local):
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        dt, nb, threads, used = oracle_sample_run(w, args.cpu_seqs)
+        dt, nb, threads, used, seqs, refs = oracle_sample_run(w, args.cpu_seqs)
         cpu = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
                "kind": "oracle",
                "sample": f"{used} of {w.batch} sequences x {w.layers} layer(s): FP64 append + "
                          f"two-pass attention, {dt:.2f} s wall on {threads} threads"}
+        # the same sample, set against the GPU's outputs of the timed steps
+        # (every step recomputes the same outputs from the same inputs)
+        got = outs.view(torch.int16).cpu().numpy().view(np.uint16)[:, seqs]
+        got = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ref = np.stack(refs)
+        err = np.abs(got - ref)
+        cpu["parity_vs_gpu"] = {
+            "max_abs_err": float(err.max()),
+            "worst_err_over_tolerance": float((err / (1e-3 + 8e-3 * np.abs(ref))).max()),
+            "tolerance": "|err| <= 1e-3 + 8e-3 |ref|"}
 
     if rank != 0:
         return 0

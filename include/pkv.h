@@ -229,6 +229,21 @@ PKV_API int pkv_plan_splits(int batch, int num_kv_heads, int max_blocks,
                             int num_splits);
 
 /*
+ * Host-side check of a batch's block tables and lengths, for callers that
+ * want bad entries found before a launch (the kernels themselves skip them
+ * and report PKV_DEVERR_* bits): every seq_lens[b] in [0, max_blocks *
+ * page_size], and every live table entry (block < ceil(seq_lens[b] /
+ * page_size)) in [0, num_pages).  block_table [batch][max_blocks] and
+ * seq_lens [batch] are host memory.  Returns PKV_OK, or PKV_EINVAL with
+ * *bad_seq and *bad_block (either may be NULL) set to the first offending
+ * sequence and block (*bad_block = -1 for a bad length, and both -1 for bad
+ * sizes or pointers).  Pure host code.
+ */
+PKV_API int pkv_check_tables(const int32_t* block_table, int max_blocks,
+                             const int32_t* seq_lens, int batch, int64_t num_pages,
+                             int page_size, int* bad_seq, int* bad_block);
+
+/*
  * Work plans: split a ragged batch on the host, run it on the device.
  *
  * The automatic split plan of the calls above cannot see the lengths (they

@@ -72,6 +72,8 @@ def _load():
     L.pkv_kv_write_prefill.argtypes = [vp, vp, i32, vp, vp, vp, i64, vp, i32, i32, i32, i32, i32,
                                        f64, vp, vp]
     L.pkv_kv_write_prefill.restype = i32
+    L.pkv_check_tables.argtypes = [vp, i32, vp, i32, i64, i32, vp, vp]
+    L.pkv_check_tables.restype = i32
     L.pkv_plan_bytes.argtypes = [i32, i32]
     L.pkv_plan_bytes.restype = sz
     L.pkv_plan_build.argtypes = [vp, i32, i32, i32, vp, sz]
@@ -275,6 +277,26 @@ def kv_write_prefill(k, v, token_offsets, start_positions, pool, block_table, *,
                                    _stream(stream))
     if rc != PKV_OK:
         raise PkvError(rc, "pkv_kv_write_prefill")
+
+
+# ----------------------------------------------------------- host checks --
+
+def check_tables(block_table, seq_lens, num_pages: int, page_size: int = PAGE_SIZE) -> None:
+    """Raise PkvError naming the first bad length or live block-table entry
+    (pkv_check_tables: host arrays, checked before any launch)."""
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    if bt.ndim != 2 or lens.ndim != 1 or bt.shape[0] != lens.shape[0]:
+        raise ValueError("block_table must be [batch][max_blocks] and seq_lens [batch]")
+    seq, blk = ctypes.c_int(0), ctypes.c_int(0)
+    rc = _lib.pkv_check_tables(bt.ctypes.data_as(ctypes.c_void_p), bt.shape[1],
+                               lens.ctypes.data_as(ctypes.c_void_p), lens.shape[0], num_pages,
+                               page_size, ctypes.byref(seq), ctypes.byref(blk))
+    if rc != PKV_OK:
+        where = (f"sequence {seq.value}: length {int(lens[seq.value])}" if blk.value < 0 and
+                 seq.value >= 0 else f"sequence {seq.value}, block {blk.value}: page "
+                 f"{int(bt[seq.value, blk.value])}" if seq.value >= 0 else "bad sizes")
+        raise PkvError(rc, f"pkv_check_tables ({where})")
 
 
 # ------------------------------------------------------------- work plans --

@@ -185,3 +185,29 @@ int build_plan(const int32_t* lens, int batch, int max_blocks, int num_sms, int3
 }
 
 }  // namespace pkv
+
+extern "C" PKV_API int pkv_check_tables(const int32_t* block_table, int max_blocks,
+                                        const int32_t* seq_lens, int batch, int64_t num_pages,
+                                        int page_size, int* bad_seq, int* bad_block) {
+  auto fail = [&](int b, int blk) {
+    if (bad_seq != nullptr) *bad_seq = b;
+    if (bad_block != nullptr) *bad_block = blk;
+    return PKV_EINVAL;
+  };
+  if (block_table == nullptr || seq_lens == nullptr || batch < 0 || max_blocks < 1 ||
+      num_pages < 1 || page_size < 1)
+    return fail(-1, -1);
+  const long long Lmax = static_cast<long long>(max_blocks) * page_size;
+  for (int b = 0; b < batch; ++b) {
+    const int32_t L = seq_lens[b];
+    if (L < 0 || L > Lmax) return fail(b, -1);
+    const int live = static_cast<int>((static_cast<long long>(L) + page_size - 1) / page_size);
+    const int32_t* row = block_table + static_cast<int64_t>(b) * max_blocks;
+    for (int k = 0; k < live; ++k)
+      if (row[k] < 0 || row[k] >= num_pages) return fail(b, k);
+  }
+  if (bad_seq != nullptr) *bad_seq = -1;
+  if (bad_block != nullptr) *bad_block = -1;
+  return PKV_OK;
+}
+

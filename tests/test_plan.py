@@ -183,3 +183,36 @@ def test_wide_tables_cap_the_range():
     plan = build([65536] * 2, max_blocks=4096, sms=1)
     assert plan.range_pages == 1024
     assert max(int(n) for n in plan.items()[:, 3]) <= 1024
+
+
+# ------------------------------------------------ host table check (pkv_check_tables) --
+
+def test_check_tables_accepts_a_valid_batch():
+    from paged_kv_decode_04_gb300 import synth
+    w = synth.make_workload("small", 0)
+    B.check_tables(w.block_tables[0], w.seq_lens, w.num_pages)
+
+
+@pytest.mark.parametrize("case", ["negative_len", "long_len", "negative_page", "page_past_pool"])
+def test_check_tables_names_the_first_bad_entry(case):
+    lens = np.array([40, 17, 0, 33], np.int32)
+    bt = np.full((4, 8), -1, np.int32)
+    bt[0, :3] = [5, 6, 7]
+    bt[1, :2] = [1, 2]
+    bt[3, :3] = [9, 10, 11]
+    B.check_tables(bt, lens, 64)                       # entries past a length are never read
+    if case == "negative_len":
+        lens[2] = -1
+        want = "sequence 2: length -1"
+    elif case == "long_len":
+        lens[1] = 8 * 16 + 1
+        want = "sequence 1: length 129"
+    elif case == "negative_page":
+        bt[3, 2] = -4
+        want = "sequence 3, block 2: page -4"
+    else:
+        bt[1, 1] = 64
+        want = "sequence 1, block 1: page 64"
+    with pytest.raises(B.PkvError) as e:
+        B.check_tables(bt, lens, 64)
+    assert want in str(e.value) and e.value.status == B.PKV_EINVAL

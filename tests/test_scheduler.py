@@ -139,9 +139,13 @@ def run_trace(seed, static, num_pages=600, layers=2, steps=300):
         assert ids.tolist() == [x[0] for x in w] and lens.tolist() == [x[1] for x in w]
         for i, x in enumerate(w):
             assert np.array_equal(bt[:, i], np.array(x[2]))
-        # live block tables never share a page
+        # live block tables never share a page, and every live entry is a pool page
         used = bt[bt >= 0]
         assert len(np.unique(used)) == len(used)
+        if ids.size:
+            from paged_kv_decode_04_gb300 import binding
+            for layer in range(bt.shape[0]):
+                binding.check_tables(bt[layer], lens, num_pages)
         if live and rng.random() < 0.2:
             victim = int(rng.choice(live))
             assert cxx.finish(victim) == ref.finish(victim)
