@@ -68,3 +68,40 @@ def appended_slots_expected(w, layer, seqs):
                             for h in range(w.num_kv_heads)]))
         vs.append(w.v_new[layer, b])
     return np.stack(ks), np.stack(vs)
+
+
+def bf16_normal(rng, shape):
+    """N(0, 1) drawn in FP32 and rounded to bf16 bit patterns."""
+    x = torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16)
+    return x.view(torch.int16).numpy().view(np.uint16)
+
+
+def special_bf16(rng, shape):
+    """bf16 bit patterns mixing normal values with zeros, subnormals, tiny and
+    huge normals, infinities, NaNs and exact x1 == x2 pairs (cancellation) along
+    the last axis of 64 dims."""
+    x = bf16_normal(rng, shape)
+    kind = rng.integers(0, 10, size=shape)
+    sign = (rng.integers(0, 2, size=shape) << 15).astype(np.uint16)
+    mant = rng.integers(0, 128, size=shape).astype(np.uint16)
+    x = np.where(kind == 1, sign, x)                                            # +-0
+    x = np.where(kind == 2, sign | np.maximum(mant, 1), x)                      # subnormal
+    tiny = (rng.integers(1, 31, size=shape).astype(np.uint16) << 7) | mant
+    x = np.where(kind == 3, sign | tiny, x)                                     # tiny normal
+    huge = (rng.integers(220, 255, size=shape).astype(np.uint16) << 7) | mant
+    x = np.where(kind == 4, sign | huge, x)                                     # huge normal
+    x = np.where((kind == 5) & (mant < 16), sign | 0x7F80, x)                   # +-inf
+    x = np.where((kind == 5) & (mant >= 120), 0x7FC1 | sign, x)                 # NaN
+    x = x.astype(np.uint16)
+    pair = kind[..., :32] == 6                                                  # x2 := x1
+    x[..., 32:] = np.where(pair, x[..., :32], x[..., 32:])
+    return x
+
+
+def is_nan_bf16(x):
+    return ((x & 0x7F80) == 0x7F80) & ((x & 0x7F) != 0)
+
+
+def equal_but_nan_payload(got, want):
+    """Bit equality, except that any two NaNs are equal (payload and sign free)."""
+    return (got == want) | (is_nan_bf16(got) & is_nan_bf16(want))

@@ -16,7 +16,7 @@ import torch
 import oracle
 from paged_kv_decode_04_gb300 import synth
 from _gpu_util import (appended_slots_expected, assert_close, binding, cuda_or_skip,
-                       gpu_step, oracle_step)
+                       equal_but_nan_payload, gpu_step, oracle_step, special_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -311,3 +311,44 @@ def test_rope_beyond_the_table_and_theta_switch_bit_exact():
         want = np.stack([np.stack([oracle.rope_rotate(kb[i, h], int(pos[i]), theta)
                                    for h in range(8)]) for i in range(B)])
         assert np.array_equal(got, want), (theta, base)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_append_special_values_bit_exact(fused):
+    # zeros, subnormals, tiny/huge normals, inf, NaN and cancelling pairs in the
+    # new keys, at positions inside and past the cos/sin table; the fused step
+    # appends through its own copy of the rotation.  NaN payloads are not compared.
+    dev = cuda_or_skip()
+    rng = np.random.default_rng(31)
+    B = 640
+    pos = np.concatenate([rng.integers(0, 2048, B - 64), rng.integers(2048, 4096, 64)])
+    pos = pos.astype(np.int32)
+    k = special_bf16(rng, (B, 8, 64))
+    v = special_bf16(rng, (B, 8, 64))
+    # sequence i appends into page i; the fused step also attends over the
+    # earlier blocks, which all point at one extra zero page (index B)
+    bt = np.full((B, 256), -1, np.int32)
+    for i in range(B):
+        bt[i, :pos[i] // 16] = B
+    bt[np.arange(B), pos // 16] = np.arange(B)
+    pool = torch.full((B + 1, 2, 16, 8, 64), 0x1234, dtype=torch.int16,
+                      device=dev).view(torch.bfloat16)
+    pool[B] = 0
+    b = binding()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kd = torch.from_numpy(k.view(np.int16)).to(dev).view(torch.bfloat16)
+    vd = torch.from_numpy(v.view(np.int16)).to(dev).view(torch.bfloat16)
+    btd = torch.from_numpy(bt).to(dev)
+    if fused:
+        q = torch.zeros((B, 32, 64), dtype=torch.bfloat16, device=dev)
+        b.decode_step(q, kd, vd, pool, btd, torch.from_numpy(pos + 1).to(dev), dev_err=err)
+    else:
+        b.kv_append(kd, vd, pool, btd, torch.from_numpy(pos).to(dev), dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = synth.bits(pool[torch.arange(B, device=dev), :,
+                          torch.from_numpy(pos % 16).long().to(dev)])
+    for i in range(B):
+        want_k = np.stack([oracle.rope_rotate(k[i, h], int(pos[i]), 500000.0) for h in range(8)])
+        assert equal_but_nan_payload(got[i, 0], want_k).all(), (i, int(pos[i]))
+        assert np.array_equal(got[i, 1], v[i]), i

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from paged_kv_decode_04_gb300 import synth
-from _gpu_util import assert_close, binding, cuda_or_skip
+from _gpu_util import assert_close, binding, cuda_or_skip, is_nan_bf16, special_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -138,31 +138,6 @@ def test_prefill_reports_bad_offsets_and_pages():
                        to_dev(st, dev), dpool, to_dev(bt2, dev), dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) & b.DEVERR_PAGE
-
-
-def special_bf16(rng, shape):
-    """bf16 bit patterns mixing normal values with zeros, subnormals, tiny and
-    huge normals, infinities, NaNs and exact x1 == x2 pairs (cancellation)."""
-    x = bf16_normal(rng, shape)
-    kind = rng.integers(0, 10, size=shape)
-    sign = (rng.integers(0, 2, size=shape) << 15).astype(np.uint16)
-    mant = rng.integers(0, 128, size=shape).astype(np.uint16)
-    x = np.where(kind == 1, sign, x)                                            # +-0
-    x = np.where(kind == 2, sign | np.maximum(mant, 1), x)                      # subnormal
-    tiny = (rng.integers(1, 31, size=shape).astype(np.uint16) << 7) | mant
-    x = np.where(kind == 3, sign | tiny, x)                                     # tiny normal
-    huge = (rng.integers(220, 255, size=shape).astype(np.uint16) << 7) | mant
-    x = np.where(kind == 4, sign | huge, x)                                     # huge normal
-    x = np.where((kind == 5) & (mant < 16), sign | 0x7F80, x)                   # +-inf
-    x = np.where((kind == 5) & (mant >= 120), 0x7FC1 | sign, x)                 # NaN
-    x = x.astype(np.uint16)
-    pair = kind[..., :32] == 6                                                  # x2 := x1
-    x[..., 32:] = np.where(pair, x[..., :32], x[..., 32:])
-    return x
-
-
-def is_nan_bf16(x):
-    return ((x & 0x7F80) == 0x7F80) & ((x & 0x7F) != 0)
 
 
 @pytest.mark.parametrize("theta", [500000.0, 10000.0])
