@@ -41,7 +41,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_attention_peak_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_decode_04_gb300", "csrc", f)
-                  for f in ("decode_attention.cu", "pkv_device.cuh", "pkv_internal.h")]
+                  for f in ("decode_attention.cu", "decode_pagebox.cu", "decode_page.cuh",
+                            "pkv_device.cuh", "pkv_internal.h")]
 # The traffic file holds a list of records {workload, kernel, kernel_sha, dram_bytes_per_launch}.
 
 WORKLOAD_TEXT = {
@@ -330,6 +331,7 @@ def run_ours(args, world, rank, local):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     fused = args.path == "fused"
     merges = (plan.num_merges > 0) if planned else (splits > 1)
+    launched = binding.attention_kernels(B, w.max_blocks, args.splits, plan)
     kernels_per_layer = (1 if fused else 2) + (1 if merges else 0)
 
     def plan_for(dset):
@@ -454,7 +456,7 @@ def run_ours(args, world, rank, local):
         kern["decode_step_median"] = round(statistics.median(per) * 1e3, 2)
         dom_bytes = algorithmic_bytes(w, "step") / layers
         kern["decode_step"] = round(dom_ms * 1e3, 2)
-        dom_name = "paged_decode_kernel<append,planned>" if planned else "paged_decode_kernel<append>"
+        dom_name = launched + " (fused step)"
     else:
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_prof)]
         for i in range(n_prof):
@@ -472,9 +474,7 @@ def run_ours(args, world, rank, local):
         dom_bytes = algorithmic_bytes(w, "attention") / layers
         kern["kv_append"] = round(app_ms * 1e3, 2)
         kern["paged_decode_attention"] = round(dom_ms * 1e3, 2)
-        dom_name = "paged_decode_kernel<planned>" if planned else "paged_decode_kernel"
-    if merges:
-        dom_name += "+merge_plan_kernel" if planned else "+merge_splits_kernel"
+        dom_name = launched + " (attention)"
     peak, peak_kind = measured_hbm_peak()
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
 

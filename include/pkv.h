@@ -319,6 +319,18 @@ PKV_API int pkv_decode_step_planned(
     size_t workspace_bytes, int32_t* dev_err, pkv_stream_t stream);
 
 /*
+ * The kernels pkv_paged_decode_attention (plan == NULL, with num_splits as
+ * given) or the _planned calls (plan = a built plan; num_splits ignored) launch
+ * for this batch on the current device, joined by '+': the attention kernel
+ * ("paged_decode_pagebox_kernel", one CTA per sequence range covering all kv
+ * heads, for batches that fill the SMs; else "paged_decode_kernel", one CTA
+ * per (sequence range, kv head)), then the split merge when one runs.  The
+ * fused steps launch the same kernels.  Static strings; NULL for invalid sizes.
+ */
+PKV_API const char* pkv_attention_kernels(int batch, int max_blocks, int num_splits,
+                                          const void* plan);
+
+/*
  * pkv_paged_decode_attention_static_ws -- the same computation as
  * pkv_paged_decode_attention, for callers that cannot allocate device memory.
  * (The source pages have no counterpart to this entry point.)

@@ -72,6 +72,8 @@ def _load():
     L.pkv_kv_write_prefill.argtypes = [vp, vp, i32, vp, vp, vp, i64, vp, i32, i32, i32, i32, i32,
                                        f64, vp, vp]
     L.pkv_kv_write_prefill.restype = i32
+    L.pkv_attention_kernels.argtypes = [i32, i32, i32, vp]
+    L.pkv_attention_kernels.restype = ctypes.c_char_p
     L.pkv_check_tables.argtypes = [vp, i32, vp, i32, i64, i32, vp, vp]
     L.pkv_check_tables.restype = i32
     L.pkv_plan_bytes.argtypes = [i32, i32]
@@ -277,6 +279,15 @@ def kv_write_prefill(k, v, token_offsets, start_positions, pool, block_table, *,
                                    _stream(stream))
     if rc != PKV_OK:
         raise PkvError(rc, "pkv_kv_write_prefill")
+
+
+def attention_kernels(batch: int, max_blocks: int, num_splits: int = 0, plan=None) -> str:
+    """The kernels an attention call launches for these sizes ('+'-joined)."""
+    r = _lib.pkv_attention_kernels(batch, max_blocks, num_splits,
+                                   None if plan is None else plan._host_ptr())
+    if r is None:
+        raise PkvError(PKV_EINVAL, "pkv_attention_kernels")
+    return r.decode()
 
 
 # ----------------------------------------------------------- host checks --

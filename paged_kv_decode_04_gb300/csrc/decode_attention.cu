@@ -484,6 +484,17 @@ cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
   return err;
 }
 
+cudaError_t launch_split_merge(const AttnArgs& args, int num_merges, cudaStream_t stream) {
+  if (args.plan_items != nullptr)
+    return num_merges > 0 ? launch_pdl(merge_plan_kernel, dim3(kNumQHeads, num_merges), dim3(32),
+                                       0, stream, args)
+                          : cudaSuccess;
+  return args.plan.num_splits > 1 ? launch_pdl(merge_splits_kernel,
+                                               dim3(kNumQHeads, args.batch), dim3(32), 0, stream,
+                                               args)
+                                  : cudaSuccess;
+}
+
 cudaError_t launch_planned_decode_attention(const CUtensorMap& pool_map,
                                             const AttnArgs& args, int num_items,
                                             int num_merges, int range_pages,

@@ -74,31 +74,6 @@ size_t plan_workspace(int batch, const pkv::SplitPlan& plan) {
   return pkv::workspace_bytes_for(batch, kNumQHeads, kHeadDim, plan);
 }
 
-// Launch attention (append == nullptr) or the fused step under `plan`.
-cudaError_t launch_attention(const pkv::SplitPlan& plan, const CUtensorMap& map,
-                             const pkv_bf16* q, const int32_t* block_table, int max_blocks,
-                             const int32_t* seq_lens, int batch, float scale, pkv_bf16* out,
-                             void* workspace, int32_t* dev_err, int64_t num_pages,
-                             cudaStream_t stream, const pkv::AppendArgs* append) {
-  pkv::AttnArgs args;
-  args.q = q;
-  args.block_table = block_table;
-  args.seq_lens = seq_lens;
-  args.out = out;
-  const size_t need = pkv::workspace_bytes_for(batch, kNumQHeads, kHeadDim, plan);
-  float* ws = static_cast<float*>(workspace);
-  const size_t acc_elems = static_cast<size_t>(batch) * kNumQHeads * plan.num_splits * kHeadDim;
-  args.part_acc = need > 0 ? ws : nullptr;
-  args.part_ml = need > 0 ? ws + acc_elems : nullptr;
-  args.dev_err = dev_err;
-  args.num_pages = num_pages;
-  args.max_blocks = max_blocks;
-  args.batch = batch;
-  args.scale_log2 = scale * 1.4426950408889634f;
-  args.plan = plan;
-  return pkv::launch_paged_decode_attention(map, args, stream, append);
-}
-
 bool supported_dims(int num_q_heads, int num_kv_heads, int head_dim, int page_size) {
   return num_q_heads == kNumQHeads && num_kv_heads == kNumKvHeads &&
          head_dim == kHeadDim && page_size == kPageSize;
@@ -168,6 +143,95 @@ bool pool_tensor_map(const void* pool, int64_t num_pages, CUtensorMap* out) {
   cached.map = m;
   *out = m;
   return true;
+}
+
+// TMA descriptor of the pool as the 4-D tensor (dim 64, row 32, kv head 8,
+// page) with strides (2 B, 1 KiB, 128 B, 32 KiB) and a box of one whole page:
+// the box lands in shared memory as [head][32 rows][64], 128-byte swizzled,
+// i.e. each head's 4 KiB tile laid out as in pool_tensor_map's box.
+bool pool_page_map(const void* pool, int64_t num_pages, CUtensorMap* out) {
+  struct Entry {
+    int device = -1;
+    const void* pool = nullptr;
+    int64_t num_pages = 0;
+    CUtensorMap map;
+  };
+  thread_local Entry cached;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cached.device == dev && cached.pool == pool && cached.num_pages == num_pages) {
+    *out = cached.map;
+    return true;
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim),
+                              static_cast<cuuint64_t>(2 * kPageSize),
+                              static_cast<cuuint64_t>(kNumKvHeads),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[3] = {
+      static_cast<cuuint64_t>(kNumKvHeads * kHeadDim * 2),  // next row (slot, K|V)
+      static_cast<cuuint64_t>(kHeadDim * 2),                 // next kv head
+      static_cast<cuuint64_t>(2 * kPageSize * kNumKvHeads * kHeadDim * 2)};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(kHeadDim),
+                             static_cast<cuuint32_t>(2 * kPageSize),
+                             static_cast<cuuint32_t>(kNumKvHeads), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMap m;
+  const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool),
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  cached.device = dev;
+  cached.pool = pool;
+  cached.num_pages = num_pages;
+  cached.map = m;
+  *out = m;
+  return true;
+}
+
+// Whole-page boxes pay off once the CTAs (one per sequence range, all heads)
+// fill every SM at least once.
+bool use_pagebox(long long ctas, int range_pages) {
+  const int sms = current_sm_count();
+  return sms > 0 && ctas >= sms && range_pages <= pkv::pagebox_max_range_pages();
+}
+
+// Launch attention (append == nullptr) or the fused step under `plan`: the
+// whole-page kernel when the batch fills the SMs, else the per-(sequence,
+// kv head) kernel; then the split merge.
+cudaError_t launch_attention(const pkv::SplitPlan& plan, const void* pool, int64_t num_pages,
+                             const pkv_bf16* q, const int32_t* block_table, int max_blocks,
+                             const int32_t* seq_lens, int batch, float scale, pkv_bf16* out,
+                             void* workspace, int32_t* dev_err, cudaStream_t stream,
+                             const pkv::AppendArgs* append) {
+  pkv::AttnArgs args = {};
+  args.q = q;
+  args.block_table = block_table;
+  args.seq_lens = seq_lens;
+  args.out = out;
+  const size_t need = pkv::workspace_bytes_for(batch, kNumQHeads, kHeadDim, plan);
+  float* ws = static_cast<float*>(workspace);
+  const size_t acc_elems = static_cast<size_t>(batch) * kNumQHeads * plan.num_splits * kHeadDim;
+  args.part_acc = need > 0 ? ws : nullptr;
+  args.part_ml = need > 0 ? ws + acc_elems : nullptr;
+  args.dev_err = dev_err;
+  args.num_pages = num_pages;
+  args.max_blocks = max_blocks;
+  args.batch = batch;
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.plan = plan;
+  CUtensorMap map;
+  if (use_pagebox(static_cast<long long>(batch) * plan.num_splits, plan.pages_per_split)) {
+    if (!pool_page_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
+    const cudaError_t err =
+        pkv::launch_pagebox_attention(map, args, 0, plan.pages_per_split, stream, append);
+    if (err != cudaSuccess) return err;
+    return pkv::launch_split_merge(args, 0, stream);
+  }
+  if (!pool_tensor_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
+  return pkv::launch_paged_decode_attention(map, args, stream, append);
 }
 
 }  // namespace
@@ -285,12 +349,9 @@ PKV_API int pkv_paged_decode_attention(const pkv_bf16* q, const pkv_bf16* pool,
   if (!make_plan(batch, max_blocks, num_splits, &plan)) return PKV_ECUDA;
   const size_t need = plan_workspace(batch, plan);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
-  CUtensorMap map;
-  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
   const cudaError_t err =
-      launch_attention(plan, map, q, block_table, max_blocks, seq_lens, batch, scale, out,
-                       workspace, dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream),
-                       nullptr);
+      launch_attention(plan, pool, num_pages, q, block_table, max_blocks, seq_lens, batch, scale,
+                       out, workspace, dev_err, reinterpret_cast<cudaStream_t>(stream), nullptr);
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -315,8 +376,6 @@ PKV_API int pkv_decode_step(const pkv_bf16* q, const pkv_bf16* k_new, const pkv_
   if (!make_plan(batch, max_blocks, num_splits, &plan)) return PKV_ECUDA;
   const size_t need = plan_workspace(batch, plan);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
-  CUtensorMap map;
-  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
   pkv::AppendArgs app;
   app.k_new = k_new;
   app.v_new = v_new;
@@ -325,9 +384,8 @@ PKV_API int pkv_decode_step(const pkv_bf16* q, const pkv_bf16* k_new, const pkv_
       cudaSuccess)
     return PKV_ECUDA;
   const cudaError_t err =
-      launch_attention(plan, map, q, block_table, max_blocks, seq_lens, batch, scale, out,
-                       workspace, dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream),
-                       &app);
+      launch_attention(plan, pool, num_pages, q, block_table, max_blocks, seq_lens, batch, scale,
+                       out, workspace, dev_err, reinterpret_cast<cudaStream_t>(stream), &app);
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -386,11 +444,9 @@ extern "C" PKV_API int pkv_paged_decode_attention_static_ws(
     ws = static_cast<float*>(static_scratch_address(device));
     if (ws == nullptr) return PKV_ECUDA;
   }
-  CUtensorMap map;
-  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
   const cudaError_t err =
-      launch_attention(plan, map, q, block_table, max_blocks, seq_lens, batch, scale, out, ws,
-                       dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream), nullptr);
+      launch_attention(plan, pool, num_pages, q, block_table, max_blocks, seq_lens, batch, scale,
+                       out, ws, dev_err, reinterpret_cast<cudaStream_t>(stream), nullptr);
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -419,10 +475,20 @@ size_t plan_slots_bytes(const PlanHeader& h) {
   return static_cast<size_t>(h.num_slots) * kNumQHeads * (kHeadDim + 2) * sizeof(float);
 }
 
-cudaError_t launch_planned(const PlanHeader& h, const CUtensorMap& map, const pkv_bf16* q,
-                           const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                           int batch, float scale, pkv_bf16* out, const void* plan_dev,
-                           void* workspace, int32_t* dev_err, int64_t num_pages,
+// True when every item of the plan is a range (no packed sequences).
+bool plan_has_only_ranges(const PlanHeader& h) {
+  const int32_t* item = reinterpret_cast<const int32_t*>(&h) + pkv::kPlanHeaderWords;
+  for (int i = 0; i < h.num_items; ++i, item += pkv::kPlanItemWords)
+    if (item[0] != pkv::kPlanKindRange) return false;
+  return true;
+}
+
+// Launch a planned call: the whole-page kernel when the plan is all ranges
+// and fills the SMs, else the per-(item, kv head) kernel; then the merge.
+cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pages,
+                           const pkv_bf16* q, const int32_t* block_table, int max_blocks,
+                           const int32_t* seq_lens, int batch, float scale, pkv_bf16* out,
+                           const void* plan_dev, void* workspace, int32_t* dev_err,
                            cudaStream_t stream, const pkv::AppendArgs* append) {
   pkv::AttnArgs args = {};
   args.q = q;
@@ -444,6 +510,15 @@ cudaError_t launch_planned(const PlanHeader& h, const CUtensorMap& map, const pk
   args.scale_log2 = scale * 1.4426950408889634f;
   args.plan.num_splits = 1;
   args.plan.pages_per_split = h.range_pages;
+  CUtensorMap map;
+  if (use_pagebox(h.num_items, h.range_pages) && plan_has_only_ranges(h)) {
+    if (!pool_page_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
+    const cudaError_t err = pkv::launch_pagebox_attention(map, args, h.num_items, h.range_pages,
+                                                          stream, append);
+    if (err != cudaSuccess) return err;
+    return pkv::launch_split_merge(args, h.num_merges, stream);
+  }
+  if (!pool_tensor_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
   return pkv::launch_planned_decode_attention(map, args, h.num_items, h.num_merges,
                                               h.range_pages, stream, append);
 }
@@ -451,6 +526,27 @@ cudaError_t launch_planned(const PlanHeader& h, const CUtensorMap& map, const pk
 }  // namespace
 
 extern "C" {
+
+PKV_API const char* pkv_attention_kernels(int batch, int max_blocks, int num_splits,
+                                          const void* plan) {
+  if (batch < 1 || max_blocks < 1 || num_splits < 0) return nullptr;
+  if (plan != nullptr) {
+    const PlanHeader* h = plan_header(plan, batch, max_blocks);
+    if (h == nullptr) return nullptr;
+    const bool pb = use_pagebox(h->num_items, h->range_pages) && plan_has_only_ranges(*h);
+    if (h->num_merges > 0)
+      return pb ? "paged_decode_pagebox_kernel+merge_plan_kernel"
+                : "paged_decode_kernel+merge_plan_kernel";
+    return pb ? "paged_decode_pagebox_kernel" : "paged_decode_kernel";
+  }
+  pkv::SplitPlan p;
+  if (!make_plan(batch, max_blocks, num_splits, &p)) return nullptr;
+  const bool pb = use_pagebox(static_cast<long long>(batch) * p.num_splits, p.pages_per_split);
+  if (p.num_splits > 1)
+    return pb ? "paged_decode_pagebox_kernel+merge_splits_kernel"
+              : "paged_decode_kernel+merge_splits_kernel";
+  return pb ? "paged_decode_pagebox_kernel" : "paged_decode_kernel";
+}
 
 PKV_API size_t pkv_plan_bytes(int batch, int max_blocks) {
   return pkv::plan_bytes(batch, max_blocks);
@@ -495,11 +591,9 @@ PKV_API int pkv_paged_decode_attention_planned(
   if (h == nullptr) return PKV_EINVAL;
   const size_t need = plan_slots_bytes(*h);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
-  CUtensorMap map;
-  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
   const cudaError_t err =
-      launch_planned(*h, map, q, block_table, max_blocks, seq_lens, batch, scale, out, plan_dev,
-                     workspace, dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream),
+      launch_planned(*h, pool, num_pages, q, block_table, max_blocks, seq_lens, batch, scale, out,
+                     plan_dev, workspace, dev_err, reinterpret_cast<cudaStream_t>(stream),
                      nullptr);
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
@@ -527,8 +621,6 @@ PKV_API int pkv_decode_step_planned(
   if (h == nullptr) return PKV_EINVAL;
   const size_t need = plan_slots_bytes(*h);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_EWORKSPACE;
-  CUtensorMap map;
-  if (!pool_tensor_map(pool, num_pages, &map)) return PKV_ECUDA;
   pkv::AppendArgs app;
   app.k_new = k_new;
   app.v_new = v_new;
@@ -537,8 +629,8 @@ PKV_API int pkv_decode_step_planned(
       cudaSuccess)
     return PKV_ECUDA;
   const cudaError_t err =
-      launch_planned(*h, map, q, block_table, max_blocks, seq_lens, batch, scale, out, plan_dev,
-                     workspace, dev_err, num_pages, reinterpret_cast<cudaStream_t>(stream), &app);
+      launch_planned(*h, pool, num_pages, q, block_table, max_blocks, seq_lens, batch, scale, out,
+                     plan_dev, workspace, dev_err, reinterpret_cast<cudaStream_t>(stream), &app);
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 

@@ -138,6 +138,19 @@ cudaError_t launch_planned_decode_attention(const CUtensorMap& pool_map,
                                             cudaStream_t stream,
                                             const AppendArgs* append = nullptr);
 
+// The same attention (fixed plan: args.plan_items == nullptr, grid (S, B);
+// work plan: range items only, grid (num_items)) with one CTA per (sequence,
+// range) covering all kv heads, each page fetched as one 32 KiB box through
+// page_map (decode_pagebox.cu).  The caller launches the split merge.
+cudaError_t launch_pagebox_attention(const CUtensorMap& page_map, const AttnArgs& args,
+                                     int num_items, int range_pages, cudaStream_t stream,
+                                     const AppendArgs* append = nullptr);
+int pagebox_max_range_pages();
+
+// Launch the split merge of a plan (fixed: merge_splits_kernel when S > 1;
+// work plan: merge_plan_kernel over num_merges sequences).
+cudaError_t launch_split_merge(const AttnArgs& args, int num_merges, cudaStream_t stream);
+
 // Largest logical page range one attention CTA handles.
 int max_pages_per_split();
 
