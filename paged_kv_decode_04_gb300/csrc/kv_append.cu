@@ -138,7 +138,7 @@ constexpr int kPfStageBytes = 2 * kPfHalfStage;
 constexpr int kPrefillSmemBatch = 2048;
 constexpr size_t kPfSmemBytes =
     static_cast<size_t>(kPfStages) * kPfStageBytes + 8 * kPfStages +
-    sizeof(int32_t) * (kPrefillSmemBatch + 1);
+    sizeof(int32_t) * (kPrefillSmemBatch + 1) + sizeof(int32_t) * kPfStages;
 
 // Where token t goes: its pool page (-1: skip), slot and position.
 struct PfDest {
@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(kPfThreads)
   extern __shared__ __align__(16) uint8_t pf_smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(pf_smem + kPfStages * kPfStageBytes);
   int32_t* s_off = reinterpret_cast<int32_t*>(bars + kPfStages);
+  int32_t* done = s_off + kPrefillSmemBatch + 1;  // warps finished with each stage
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -299,7 +300,10 @@ __global__ void __launch_bounds__(kPfThreads)
   const uint32_t bar0 = smem_addr(bars);
   const uint32_t stage0 = smem_addr(pf_smem);
   if (tid == 0) {
-    for (int s = 0; s < kPfStages; ++s) mbar_init(bar0 + 8 * s, 1);
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(bar0 + 8 * s, 1);
+      done[s] = 0;
+    }
     fence_barrier_init();
   }
   wait_for_prior_grids();
@@ -351,14 +355,10 @@ __global__ void __launch_bounds__(kPfThreads)
                          num_pages, dev_err);
     const int st = it % kPfStages;
     const bool ready = mbar_wait_bounded(bar0 + 8 * st, (it / kPfStages) & 1);
-    if (!__syncthreads_and(ready)) {
-      // give the copies still in flight a bounded time to land, then stop
-      if (tid == 0) {
-        record_error(dev_err, kErrTimeout);
-        for (int j = it; j < it + kPfStages && j < my_chunks; ++j)
-          mbar_wait_bounded(bar0 + 8 * (j % kPfStages), (j / kPfStages) & 1);
-      }
-      return;
+    if (!__all_sync(0xFFFFFFFFu, ready)) {
+      // stop; the copies still in flight are drained below
+      if (lane == 0) record_error(dev_err, kErrTimeout);
+      break;
     }
     const uint32_t kst = stage0 + st * kPfStageBytes;
     for (int q = 0; q < kPfChunk / kPfWarps; ++q) {
@@ -381,12 +381,29 @@ __global__ void __launch_bounds__(kPfThreads)
       if (__any_sync(0xFFFFFFFFu, bad != 0))
         rope_redo_pairs(freqs, table_ok, pos, bad, ks + x1_off, kd + x1_off, lane_q);
     }
-    __syncthreads();  // every warp is done with stage st
-    if (tid == 0 && it + kPfStages < my_chunks) {
-      fence_proxy_async_smem();
-      issue(it + kPfStages);
+    // release the stage; the last of the warps refills it, so no warp waits
+    // for the others (one may be redoing a rotation in FP64)
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(done + st, 1) == kPfWarps - 1) {
+        done[st] = 0;
+        __threadfence_block();
+        if (it + kPfStages < my_chunks) {
+          fence_proxy_async_smem();
+          issue(it + kPfStages);
+        }
+      }
     }
   }
+  // before the CTA exits, every copy it issued has landed (after a timeout,
+  // each wait is bounded again)
+  __syncthreads();
+  if (tid == 0)
+    for (int s = 0; s < kPfStages && s < my_chunks; ++s) {
+      const int last = s + ((my_chunks - 1 - s) / kPfStages) * kPfStages;
+      mbar_wait_bounded(bar0 + 8 * s, (last / kPfStages) & 1);
+    }
 }
 
 // Device addresses of this device's table, looked up once per device.
