@@ -26,6 +26,13 @@
 //  * kAppend: the fused decode step.  The warp that owns the sequence's last
 //    page computes the new token's K/V row for head g, writes it to the pool
 //    and patches its copy of the page before the math.
+//  * kPlanned: the work comes from a host-built plan (planner.cpp): CTA
+//    (g, i) takes item i, either a range of one sequence (as above) or up to
+//    4 short sequences, one per warp, each warp writing its own rows.
+//  * kStages: the per-warp ring depth -- 4 tiles (3 CTAs per SM) when it can
+//    hold every page a warp gets, else 3 tiles at 4 CTAs per SM.
+//  * Batches that fill the SMs go to decode_pagebox.cu instead (one CTA per
+//    sequence range for all heads, whole-page boxes).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
