@@ -24,6 +24,7 @@ import copy
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -92,10 +93,15 @@ def measured_hbm_peak():
 
 
 def kernel_sha() -> str:
+    """Hash of the kernel sources' code: comments and whitespace do not count,
+    so a comment edit does not orphan the recorded counters."""
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 
