@@ -19,7 +19,7 @@ from _gpu_util import assert_close, binding, cuda_or_skip
 
 pytestmark = pytest.mark.gpu
 
-B = 160            # >= the SM count: the whole-page kernel's territory
+B = 160            # >= the SM count (152 on GB300): the whole-page kernel's territory
 
 
 def workload(lo, hi, seed):
@@ -137,12 +137,15 @@ def test_bad_pages_and_lengths_reported():
 def test_kernel_choice_is_reported():
     cuda_or_skip()
     b = binding()
-    assert b.attention_kernels(B, 128, 1) == "paged_decode_pagebox_kernel"
-    assert b.attention_kernels(B, 128, 2) == "paged_decode_pagebox_kernel+merge_splits_kernel"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    big = max(B, sms)                      # one CTA per SM: the whole-page kernel
+    assert b.attention_kernels(big, 128, 1) == "paged_decode_pagebox_kernel"
+    assert b.attention_kernels(big, 128, 2) == "paged_decode_pagebox_kernel+merge_splits_kernel"
+    assert b.attention_kernels(sms - 1, 128, 1) == "paged_decode_kernel"
     assert b.attention_kernels(8, 128, 1) == "paged_decode_kernel"
     assert b.attention_kernels(1, 128, 0) == "paged_decode_kernel+merge_splits_kernel"
-    lens = np.full(B, 2048, np.int32)
-    assert b.attention_kernels(B, 128, 0, b.Plan(lens, 128)) == "paged_decode_pagebox_kernel"
+    lens = np.full(big, 2048, np.int32)
+    assert b.attention_kernels(big, 128, 0, b.Plan(lens, 128)) == "paged_decode_pagebox_kernel"
     mixed = np.concatenate([np.full(13, 2000), np.full(115, 60)]).astype(np.int32)
     assert b.attention_kernels(128, 128, 0, b.Plan(mixed, 128)) == \
         "paged_decode_kernel+merge_plan_kernel"
