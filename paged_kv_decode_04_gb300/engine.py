@@ -53,36 +53,55 @@ class Engine:
             return x.to(torch.bfloat16).to(self.dev)
         return torch.randn(shape, generator=self.gen, device=self.dev).to(torch.bfloat16)
 
+    def _upload_i32(self, *arrays):
+        """Copy int32 host arrays to the device in one transfer through pinned
+        memory, without waiting for the work already queued; returns views."""
+        sizes = [a.size for a in arrays]
+        staged = torch.empty(sum(sizes), dtype=torch.int32, pin_memory=True)
+        flat = staged.numpy()
+        at = 0
+        for a, k in zip(arrays, sizes):
+            flat[at:at + k] = a.reshape(-1)
+            at += k
+        dev = staged.to(self.dev, non_blocking=True)
+        views, at = [], 0
+        for a, k in zip(arrays, sizes):
+            views.append(dev[at:at + k].view(a.shape))
+            at += k
+        return views
+
     def step(self, on_prefill=None, on_decode=None) -> int:
         """One scheduling point; returns the decode batch size."""
         self.sched.admit()
         got = self.sched.next_prefill()
         if got is not None:
             rid, plen, bt = got
-            off = torch.tensor([0, plen], dtype=torch.int32, device=self.dev)
-            st = torch.zeros(1, dtype=torch.int32, device=self.dev)
+            dbt, off, st = self._upload_i32(np.ascontiguousarray(bt, dtype=np.int32)[:, None],
+                                            np.array([0, plen], np.int32),
+                                            np.zeros(1, np.int32))
+            ks = self._normal((self.layers, plen, HKV, D))   # one draw per prompt
+            vs = self._normal((self.layers, plen, HKV, D))
             for layer in range(self.layers):
-                k = self._normal((plen, HKV, D))
-                v = self._normal((plen, HKV, D))
-                btl = torch.from_numpy(bt[layer:layer + 1].copy()).to(self.dev)
-                binding.kv_write_prefill(k, v, off, st, self.pool, btl, dev_err=self.err)
+                binding.kv_write_prefill(ks[layer], vs[layer], off, st, self.pool, dbt[layer],
+                                         dev_err=self.err)
                 if on_prefill is not None:
-                    on_prefill(layer, rid, k, v, bt[layer])
+                    on_prefill(layer, rid, ks[layer], vs[layer], bt[layer])
         ids, lens, bts = self.sched.decode_batch(self.max_batch)
         n = len(ids)
         if n:
-            dlens = torch.from_numpy(lens).to(self.dev)
+            # one transfer per step: every layer's block table and the lengths
+            dbts, dlens = self._upload_i32(bts, lens)
             plan = None
             if self.use_plan:
                 plan = binding.Plan(lens, self.max_blocks, device=self.dev)
                 if plan.workspace_bytes > self.ws.numel():
                     self.ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8,
                                           device=self.dev)
+            qs = self._normal((self.layers, n, HQ, D))   # one draw per step
+            kns = self._normal((self.layers, n, HKV, D))
+            vns = self._normal((self.layers, n, HKV, D))
             for layer in range(self.layers):
-                q = self._normal((n, HQ, D))
-                kn = self._normal((n, HKV, D))
-                vn = self._normal((n, HKV, D))
-                btl = torch.from_numpy(bts[layer]).to(self.dev)
+                q, kn, vn, btl = qs[layer], kns[layer], vns[layer], dbts[layer]
                 if plan is not None:
                     out = binding.decode_step_planned(q, kn, vn, self.pool, btl, dlens, plan,
                                                       workspace=self.ws, dev_err=self.err)
