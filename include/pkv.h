@@ -319,6 +319,22 @@ PKV_API int pkv_decode_step_planned(
     size_t workspace_bytes, int32_t* dev_err, pkv_stream_t stream);
 
 /*
+ * pkv_decode_step_planned for `layers` layers of one decode step in one call:
+ * layer l takes q + l*batch*Hq*D, k_new / v_new + l*batch*Hkv*D, block_tables
+ * + l*batch*max_blocks and writes out + l*batch*Hq*D (every array holding the
+ * layers back to back), with the same lengths, plan and workspace; the layers
+ * are launched in order on `stream`, exactly as `layers` separate calls would
+ * be.  Arguments are checked once, before anything is enqueued.
+ */
+PKV_API int pkv_decode_steps_planned(
+    int layers, const pkv_bf16* q, const pkv_bf16* k_new, const pkv_bf16* v_new,
+    pkv_bf16* pool, int64_t num_pages, const int32_t* block_tables, int max_blocks,
+    const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+    int page_size, double rope_theta, float scale, pkv_bf16* out, const void* plan_host,
+    const void* plan_dev, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+    pkv_stream_t stream);
+
+/*
  * The kernels pkv_paged_decode_attention (plan == NULL, with num_splits as
  * given) or the _planned calls (plan = a built plan; num_splits ignored) launch
  * for this batch on the current device, joined by '+': the attention kernel

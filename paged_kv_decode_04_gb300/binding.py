@@ -88,6 +88,8 @@ def _load():
     L.pkv_decode_step_planned.argtypes = [vp, vp, vp, vp, i64, vp, i32, vp, i32, i32, i32, i32,
                                           i32, f64, f32, vp, vp, vp, vp, sz, vp, vp]
     L.pkv_decode_step_planned.restype = i32
+    L.pkv_decode_steps_planned.argtypes = [i32] + L.pkv_decode_step_planned.argtypes
+    L.pkv_decode_steps_planned.restype = i32
     return L
 
 
@@ -433,4 +435,44 @@ def decode_step_planned(q, k_new, v_new, pool, block_table, seq_lens, plan, out=
         _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
     if rc != PKV_OK:
         raise PkvError(rc, "pkv_decode_step_planned")
+    return out
+
+
+def decode_steps_planned(qs, k_news, v_news, pool, block_tables, seq_lens, plan, out=None, *,
+                         rope_theta: float = 500000.0, scale: float = None, workspace=None,
+                         dev_err=None, stream=None) -> torch.Tensor:
+    """decode_step_planned for every layer of one step in one native call:
+    qs [layers][B][Hq][D], k_news / v_news [layers][B][Hkv][D], block_tables
+    [layers][B][max_blocks]; the lengths, plan and workspace are shared."""
+    num_pages = _pool_pages(pool)
+    dev = pool.device
+    _check(qs, "qs", torch.bfloat16, 4, dev)
+    _check(k_news, "k_news", torch.bfloat16, 4, dev)
+    _check(v_news, "v_news", torch.bfloat16, 4, dev)
+    _check(block_tables, "block_tables", torch.int32, 3, dev)
+    _check(seq_lens, "seq_lens", torch.int32, 1, dev)
+    layers, B, Hq, D = qs.shape
+    if k_news.shape[0] != layers or v_news.shape[0] != layers or block_tables.shape[0] != layers:
+        raise ValueError("qs, k_news, v_news and block_tables must hold the same layers")
+    if tuple(k_news.shape[1:]) != (B, NUM_KV_HEADS, D) or v_news.shape != k_news.shape:
+        raise ValueError("k_news and v_news must be [layers][B][8][64]")
+    if block_tables.shape[1] != B:
+        raise ValueError("block_tables must be [layers][B][max_blocks]")
+    if out is None:
+        out = torch.empty_like(qs)
+    _check(out, "out", torch.bfloat16, 4, dev)
+    if out.shape != qs.shape:
+        raise ValueError("out must have the shape of qs")
+    if scale is None:
+        scale = D ** -0.5
+    workspace, ws_bytes = _plan_workspace(plan, workspace, dev)
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, None, dev)
+    rc = _lib.pkv_decode_steps_planned(
+        layers, _ptr(qs), _ptr(k_news), _ptr(v_news), _ptr(pool), num_pages, _ptr(block_tables),
+        block_tables.shape[2], _ptr(seq_lens), B, Hq, k_news.shape[2], D, PAGE_SIZE,
+        float(rope_theta), float(scale), _ptr(out), plan._host_ptr(), _ptr(plan.dev),
+        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    if rc != PKV_OK:
+        raise PkvError(rc, "pkv_decode_steps_planned")
     return out

@@ -634,4 +634,29 @@ PKV_API int pkv_decode_step_planned(
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
+PKV_API int pkv_decode_steps_planned(
+    int layers, const pkv_bf16* q, const pkv_bf16* k_new, const pkv_bf16* v_new, pkv_bf16* pool,
+    int64_t num_pages, const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+    int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size, double rope_theta,
+    float scale, pkv_bf16* out, const void* plan_host, const void* plan_dev, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, pkv_stream_t stream) {
+  if (layers < 1) return PKV_EINVAL;
+  // the first layer's checks cover every layer: the strides keep alignment
+  // (whole rows of 64 elements) and every other argument is shared
+  const size_t q_stride = static_cast<size_t>(batch) * kNumQHeads * kHeadDim;
+  const size_t kv_stride = static_cast<size_t>(batch) * kNumKvHeads * kHeadDim;
+  const size_t bt_stride = static_cast<size_t>(batch) * static_cast<size_t>(max_blocks);
+  for (int l = 0; l < layers; ++l) {
+    const int rc = pkv_decode_step_planned(
+        q == nullptr ? nullptr : q + l * q_stride, k_new == nullptr ? nullptr : k_new + l * kv_stride,
+        v_new == nullptr ? nullptr : v_new + l * kv_stride, pool, num_pages,
+        block_tables == nullptr ? nullptr : block_tables + l * bt_stride, max_blocks, seq_lens,
+        batch, num_q_heads, num_kv_heads, head_dim, page_size, rope_theta, scale,
+        out == nullptr ? nullptr : out + l * q_stride, plan_host, plan_dev, workspace,
+        workspace_bytes, dev_err, stream);
+    if (rc != PKV_OK) return rc;  // only the first layer can fail its checks
+  }
+  return PKV_OK;
+}
+
 }  // extern "C"

@@ -100,16 +100,18 @@ class Engine:
             qs = self._normal((self.layers, n, HQ, D))   # one draw per step
             kns = self._normal((self.layers, n, HKV, D))
             vns = self._normal((self.layers, n, HKV, D))
-            for layer in range(self.layers):
-                q, kn, vn, btl = qs[layer], kns[layer], vns[layer], dbts[layer]
-                if plan is not None:
-                    out = binding.decode_step_planned(q, kn, vn, self.pool, btl, dlens, plan,
-                                                      workspace=self.ws, dev_err=self.err)
-                else:
-                    out = binding.decode_step(q, kn, vn, self.pool, btl, dlens,
-                                              workspace=self.ws, dev_err=self.err)
-                if on_decode is not None:
-                    on_decode(layer, ids, lens, bts[layer], q, kn, vn, out)
+            if plan is not None:
+                # every layer in one native call, launched in layer order
+                outs = binding.decode_steps_planned(qs, kns, vns, self.pool, dbts, dlens, plan,
+                                                    workspace=self.ws, dev_err=self.err)
+            else:
+                outs = [binding.decode_step(qs[layer], kns[layer], vns[layer], self.pool,
+                                            dbts[layer], dlens, workspace=self.ws,
+                                            dev_err=self.err) for layer in range(self.layers)]
+            if on_decode is not None:
+                for layer in range(self.layers):
+                    on_decode(layer, ids, lens, bts[layer], qs[layer], kns[layer], vns[layer],
+                              outs[layer])
         return n
 
     def run(self, requests, max_iters: int = 1_000_000, on_prefill=None, on_decode=None):

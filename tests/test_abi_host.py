@@ -141,3 +141,25 @@ def test_decode_step_and_prefill_argument_errors(lib):
     assert pre(d=128) == B.PKV_EUNSUPPORTED
     assert pre(pool=ctypes.c_void_p(0x10004)) == B.PKV_EALIGN
     assert pre(n=0) == B.PKV_OK
+
+
+def test_multi_layer_planned_step_argument_errors(lib):
+    import numpy as np
+    from paged_kv_decode_04_gb300 import binding as B
+    plan = B.Plan(np.array([40], np.int32), 128, num_sms=152)
+    f = lib.pkv_decode_steps_planned
+
+    def steps(**kw):
+        args = dict(layers=2, q=A, k=A, v=A, pool=A, num_pages=64, bt=A, max_blocks=128, lens=A,
+                    batch=1, hq=32, hkv=8, d=64, ps=16, theta=500000.0, scale=0.125, out=A,
+                    plan_host=plan._host_ptr(), plan_dev=A, ws=None, ws_bytes=0, err=None,
+                    stream=None)
+        args.update(kw)
+        return f(*args.values())
+    assert steps(layers=0) == B.PKV_EINVAL
+    assert steps(layers=-3) == B.PKV_EINVAL
+    assert steps(k=None) == B.PKV_EINVAL
+    assert steps(plan_host=None) == B.PKV_EINVAL
+    assert steps(batch=2) == B.PKV_EINVAL                # the plan is for one sequence
+    assert steps(hkv=4) == B.PKV_EUNSUPPORTED
+    assert steps(v=ctypes.c_void_p(0x10002)) == B.PKV_EALIGN

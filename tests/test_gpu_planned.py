@@ -219,3 +219,49 @@ def test_graph_replays_reuse_the_plan():
         g.replay()
         torch.cuda.synchronize()
         assert np.array_equal(synth.bits(out), want_bits)
+
+
+def test_all_layers_in_one_call_equal_per_layer_calls():
+    # pkv_decode_steps_planned: the mix workload's 16 layers in one native call
+    # give the bits of 16 single-layer calls, outputs and appended pages alike
+    dev = cuda_or_skip()
+    w = synth.make_workload("mix", 1)
+    b = binding()
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    d = synth.device_inputs(w, dev)
+    one = [b.decode_step_planned(d["q"][layer], d["k_new"][layer], d["v_new"][layer], d["pool"],
+                                 d["block_tables"][layer], d["seq_lens"], plan,
+                                 rope_theta=w.rope_theta, scale=w.scale, dev_err=err)
+           for layer in range(w.layers)]
+    one = np.stack([synth.bits(o) for o in one])
+    pool_one = synth.bits(d["pool"])
+    del d
+    d = synth.device_inputs(w, dev)
+    many = b.decode_steps_planned(d["q"], d["k_new"], d["v_new"], d["pool"], d["block_tables"],
+                                  d["seq_lens"], plan, rope_theta=w.rope_theta, scale=w.scale,
+                                  dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(synth.bits(many), one)
+    assert np.array_equal(synth.bits(d["pool"]), pool_one)
+    from _gpu_util import oracle_step
+    seqs = np.sort(np.concatenate([np.nonzero(w.seq_lens >= 1536)[0][:4],
+                                   np.nonzero(w.seq_lens <= 128)[0][:4]]))
+    ref, _ = oracle_step(w, 7, seqs)
+    assert_close(one[7][seqs], ref, "mix layer 7 through the multi-layer call")
+
+
+def test_multi_layer_call_checks_its_shapes():
+    dev = cuda_or_skip()
+    w = synth.make_workload("edge", 3, seq_lens=np.array([40, 17], np.int32), layers=2,
+                            num_pages=64)
+    d = synth.device_inputs(w, dev)
+    b = binding()
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev)
+    with pytest.raises(ValueError):
+        b.decode_steps_planned(d["q"], d["k_new"][:1].contiguous(), d["v_new"], d["pool"],
+                               d["block_tables"], d["seq_lens"], plan)
+    with pytest.raises(b.PkvError):                 # a plan built for another batch
+        b.decode_steps_planned(d["q"], d["k_new"], d["v_new"], d["pool"], d["block_tables"],
+                               d["seq_lens"], b.Plan([40, 17, 5], w.max_blocks, device=dev))
