@@ -132,6 +132,47 @@ __device__ __forceinline__ int pick(int4 v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
+// Before griddepcontrol.wait: prefetch into L2 the head-g tiles that the
+// CTA's first ring fill will load, so that a CTA made resident while the
+// previous grid drains finds them there.  Every word read here may still be
+// written by that grid, so the values are only addresses for the prefetch:
+// reads bypass L1, every index is range-checked, nothing is recorded, and the
+// kernel reads everything again after the wait.  (A mixed 16..2048-token
+// batch, 16 layers: 267.5 -> 252.4 us per step; prefetching twice the ring
+// fill: 257.0 us.)
+template <int kStages, bool kPlanned>
+__device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map, const AttnArgs& a,
+                                                     int g, int tid) {
+  int b = -1, p = -1;  // this thread's tile: sequence b, logical page p
+  if constexpr (kPlanned) {
+    const int4* it = a.plan_items + static_cast<int64_t>(blockIdx.y) * (kPlanItemWords / 4);
+    const int4 head = ld_cg(it);
+    if (head.x == kPlanKindPacked) {
+      const int w = tid >> 5, l = tid & 31;
+      if (l < kStages) {
+        b = pick(ld_cg(it + 1), w);
+        if (l * kPageSize < pick(ld_cg(it + 2), w)) p = l;
+      }
+    } else if (tid < kWarps * kStages && tid < head.w) {
+      b = ld_cg(it + 1).x;
+      p = head.z + tid;
+    }
+  } else {
+    const int split = blockIdx.x / kNumKvHeads;
+    const int pps = a.plan.pages_per_split;
+    const int L = ld_cg(a.seq_lens + blockIdx.y);
+    const int np = (min(max(L, 0), a.max_blocks * kPageSize) + kPageSize - 1) / kPageSize;
+    if (tid < kWarps * kStages && tid < pps && split * pps + tid < np) {
+      b = blockIdx.y;
+      p = split * pps + tid;
+    }
+  }
+  if (b >= 0 && b < a.batch && p >= 0 && p < a.max_blocks) {
+    const int pid = ld_cg(a.block_table + static_cast<int64_t>(b) * a.max_blocks + p);
+    if (pid >= 0 && pid < a.num_pages) tma_prefetch_l2_3d(map, g * kHeadDim, 0, pid);
+  }
+}
+
 template <bool kAppend, int kStages, bool kPlanned>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
     paged_decode_kernel(const __grid_constant__ CUtensorMap pool_map,
@@ -147,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
   const int warp = tid >> 5;
   const int g = blockIdx.x % kNumKvHeads;
   if (tid == 0) tma_prefetch_desc(&pool_map);
+  prefetch_first_tiles<kStages, kPlanned>(&pool_map, a, g, tid);
   wait_for_prior_grids();
   allow_dependent_grids();
 
@@ -390,8 +432,8 @@ __global__ void __launch_bounds__(32) merge_splits_kernel(const AttnArgs a) {
   const int j = blockIdx.x;
   const int b = blockIdx.y;
   const int pps = a.plan.pages_per_split;
+  allow_dependent_grids();  // the next grid may launch; it waits for this one itself
   wait_for_prior_grids();
-  allow_dependent_grids();
   int L = a.seq_lens[b];
   const int Lmax = a.max_blocks * kPageSize;
   L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
@@ -405,8 +447,8 @@ __global__ void __launch_bounds__(32) merge_splits_kernel(const AttnArgs a) {
 // Work plan: combine the ranges of the split sequences the plan lists;
 // grid (Hq, merges), one warp per (sequence, query row).
 __global__ void __launch_bounds__(32) merge_plan_kernel(const AttnArgs a) {
+  allow_dependent_grids();  // the next grid may launch; it waits for this one itself
   wait_for_prior_grids();
-  allow_dependent_grids();
   const int4 e = a.plan_merges[blockIdx.y];  // (b, first slot, ranges, 0)
   const int j = blockIdx.x;
   const int64_t row = static_cast<int64_t>(e.x) * kNumQHeads + j;

@@ -17,10 +17,11 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // Programmatic dependent launch.  Every library kernel is launched allowed to
 // start before the previous kernel on its stream has finished; it calls
-// wait_for_prior_grids() before its first read of global memory (which
-// returns once the prior grids have completed and their writes are visible,
-// and at once when there is no such dependency), then
-// allow_dependent_grids() so that the next kernel may be scheduled in turn.
+// wait_for_prior_grids() (which returns once the prior grids have completed
+// and their writes are visible, and at once when there is no such dependency)
+// before it reads anything it uses, and allow_dependent_grids() so that the
+// next kernel may be scheduled in turn.  Before the wait, the attention
+// kernels only prefetch into L2 (the addresses read there serve as hints).
 __device__ __forceinline__ void wait_for_prior_grids() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -99,6 +100,39 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar,
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// Loads that bypass L1 (cached in L2 only).  The attention kernels use them
+// for the reads they make before griddepcontrol.wait: the previous grid may
+// still be writing those words, and a stale line must not stay in L1 for the
+// reads made after the wait.
+__device__ __forceinline__ int ld_cg(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int4 ld_cg(const int4* p) {
+  int4 v;
+  asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Prefetch of one tensor-map box into L2 (no shared memory, no barrier).  L2
+// is coherent for every SM, so a prefetch can never make a later read stale:
+// a write that lands after it updates the same L2 lines.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int x, int y, int z,
+                                                   int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   map),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
 }
 
 // 3-D tiled tensor copy global -> shared, completion signalled on `bar`
