@@ -335,6 +335,21 @@ PKV_API int pkv_decode_steps_planned(
     pkv_stream_t stream);
 
 /*
+ * pkv_kv_write_prefill for `layers` layers of the same prompts in one call:
+ * layer l writes k + l*num_tokens*Hkv*D and v + l*num_tokens*Hkv*D through
+ * block_tables + l*batch*max_blocks (the arrays holding the layers back to
+ * back), with the same offsets and positions; launched in layer order on
+ * `stream`.  Arguments are checked once, before anything is enqueued.
+ */
+PKV_API int pkv_kv_write_prefill_layers(int layers, const pkv_bf16* k, const pkv_bf16* v,
+                                        int num_tokens, const int32_t* token_offsets,
+                                        const int32_t* start_positions, pkv_bf16* pool,
+                                        int64_t num_pages, const int32_t* block_tables,
+                                        int max_blocks, int batch, int num_kv_heads,
+                                        int head_dim, int page_size, double rope_theta,
+                                        int32_t* dev_err, pkv_stream_t stream);
+
+/*
  * The kernels pkv_paged_decode_attention (plan == NULL, with num_splits as
  * given) or the _planned calls (plan = a built plan; num_splits ignored) launch
  * for this batch on the current device, joined by '+': the attention kernel

@@ -113,6 +113,10 @@ PKV_API int pkv_sched_next_prefill(pkv_scheduler* s, int64_t* id, int32_t* promp
 PKV_API int pkv_sched_decode_batch(pkv_scheduler* s, int max_batch, int64_t* ids,
                                    int32_t* seq_lens, int32_t* block_tables);
 
+/* The number of prefilled, unfinished requests: the size of the next decode
+ * batch before its max_batch cap (so that a caller can size its buffers). */
+PKV_API int pkv_sched_running(const pkv_scheduler* s);
+
 /* Early finish (e.g. an end-of-sequence token): the request leaves the next
  * decode batches; its pages and unused credits return at the next admit. */
 PKV_API int pkv_sched_finish(pkv_scheduler* s, int64_t id);

@@ -90,6 +90,8 @@ def _load():
     L.pkv_decode_step_planned.restype = i32
     L.pkv_decode_steps_planned.argtypes = [i32] + L.pkv_decode_step_planned.argtypes
     L.pkv_decode_steps_planned.restype = i32
+    L.pkv_kv_write_prefill_layers.argtypes = [i32] + L.pkv_kv_write_prefill.argtypes
+    L.pkv_kv_write_prefill_layers.restype = i32
     return L
 
 
@@ -283,6 +285,32 @@ def kv_write_prefill(k, v, token_offsets, start_positions, pool, block_table, *,
         raise PkvError(rc, "pkv_kv_write_prefill")
 
 
+def kv_write_prefill_layers(ks, vs, token_offsets, start_positions, pool, block_tables, *,
+                            rope_theta: float = 500000.0, dev_err=None, stream=None) -> None:
+    """kv_write_prefill for every layer in one native call: ks, vs
+    [layers][num_tokens][Hkv][D], block_tables [layers][B][max_blocks]."""
+    num_pages = _pool_pages(pool)
+    dev = pool.device
+    _check(ks, "ks", torch.bfloat16, 4, dev)
+    _check(vs, "vs", torch.bfloat16, 4, dev)
+    _check(token_offsets, "token_offsets", torch.int32, 1, dev)
+    _check(start_positions, "start_positions", torch.int32, 1, dev)
+    _check(block_tables, "block_tables", torch.int32, 3, dev)
+    layers, B = block_tables.shape[0], start_positions.shape[0]
+    if (token_offsets.shape[0] != B + 1 or block_tables.shape[1] != B or vs.shape != ks.shape
+            or ks.shape[0] != layers):
+        raise ValueError("token_offsets must have batch + 1 entries; ks/vs/block_tables must "
+                         "hold the same layers")
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, None, dev)
+    rc = _lib.pkv_kv_write_prefill_layers(
+        layers, _ptr(ks), _ptr(vs), ks.shape[1], _ptr(token_offsets), _ptr(start_positions),
+        _ptr(pool), num_pages, _ptr(block_tables), block_tables.shape[2], B, ks.shape[2],
+        ks.shape[3], PAGE_SIZE, float(rope_theta), _ptr(dev_err), _stream(stream))
+    if rc != PKV_OK:
+        raise PkvError(rc, "pkv_kv_write_prefill_layers")
+
+
 def attention_kernels(batch: int, max_blocks: int, num_splits: int = 0, plan=None) -> str:
     """The kernels an attention call launches for these sizes ('+'-joined)."""
     r = _lib.pkv_attention_kernels(batch, max_blocks, num_splits,
@@ -323,16 +351,28 @@ class Plan:
     HEADER = ("magic", "batch", "max_blocks", "num_items", "num_merges", "num_slots",
               "range_pages", "bytes_used")
 
-    def __init__(self, seq_lens_host, max_blocks: int, *, num_sms: int = 0, device=None):
+    def __init__(self, seq_lens_host, max_blocks: int, *, num_sms: int = 0, device=None,
+                 out=None):
+        """out: an int32 array of at least plan_bytes(len(seq_lens_host), max_blocks)
+        bytes, 16-byte aligned, to build the plan in (e.g. a view of pinned
+        staging memory); by default the plan gets a buffer of its own."""
         lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
         if lens.ndim != 1:
             raise ValueError("seq_lens_host must be one-dimensional")
         nbytes = _lib.pkv_plan_bytes(lens.shape[0], max_blocks)
         if nbytes == 0:
             raise PkvError(PKV_EINVAL, "pkv_plan_bytes")
-        raw = np.zeros(nbytes // 4 + 4, dtype=np.int32)
-        off = (-raw.ctypes.data % 16) // 4      # 16-byte aligned view
-        buf = raw[off:off + nbytes // 4]
+        if out is None:
+            raw = np.zeros(nbytes // 4 + 4, dtype=np.int32)
+            off = (-raw.ctypes.data % 16) // 4      # 16-byte aligned view
+            buf = raw[off:off + nbytes // 4]
+        else:
+            if (out.dtype != np.int32 or out.ndim != 1 or out.shape[0] * 4 < nbytes
+                    or out.ctypes.data % 16 or not out.flags.c_contiguous):
+                raise ValueError("out must be a contiguous, 16-byte aligned int32 array of at "
+                                 "least plan_bytes() bytes")
+            raw = out
+            buf = out[: nbytes // 4]
         rc = _lib.pkv_plan_build(lens.ctypes.data_as(ctypes.c_void_p), lens.shape[0], max_blocks,
                                  num_sms, buf.ctypes.data_as(ctypes.c_void_p), nbytes)
         if rc != PKV_OK:
@@ -365,6 +405,11 @@ class Plan:
 
     def _host_ptr(self):
         return self.host.ctypes.data_as(ctypes.c_void_p)
+
+
+def plan_bytes(batch: int, max_blocks: int) -> int:
+    """Bytes a plan for this batch and table width can take (pkv_plan_bytes)."""
+    return int(_lib.pkv_plan_bytes(batch, max_blocks))
 
 
 def _plan_workspace(plan, workspace, dev):

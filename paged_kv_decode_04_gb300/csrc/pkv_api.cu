@@ -641,20 +641,56 @@ PKV_API int pkv_decode_steps_planned(
     float scale, pkv_bf16* out, const void* plan_host, const void* plan_dev, void* workspace,
     size_t workspace_bytes, int32_t* dev_err, pkv_stream_t stream) {
   if (layers < 1) return PKV_EINVAL;
-  // the first layer's checks cover every layer: the strides keep alignment
-  // (whole rows of 64 elements) and every other argument is shared
+  // layer 0 through the single-layer call checks every argument (the layer
+  // strides keep each array's alignment: whole rows of 64 elements) and
+  // prepares the RoPE table; the other layers only launch
+  const int rc = pkv_decode_step_planned(q, k_new, v_new, pool, num_pages, block_tables,
+                                         max_blocks, seq_lens, batch, num_q_heads, num_kv_heads,
+                                         head_dim, page_size, rope_theta, scale, out, plan_host,
+                                         plan_dev, workspace, workspace_bytes, dev_err, stream);
+  if (rc != PKV_OK || layers == 1) return rc;
+  const PlanHeader* h = plan_header(plan_host, batch, max_blocks);
+  pkv::AppendArgs app;
+  app.pool = pool;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (pkv::prepare_rope(rope_theta, &app.freqs, st) != cudaSuccess) return PKV_ECUDA;
   const size_t q_stride = static_cast<size_t>(batch) * kNumQHeads * kHeadDim;
   const size_t kv_stride = static_cast<size_t>(batch) * kNumKvHeads * kHeadDim;
   const size_t bt_stride = static_cast<size_t>(batch) * static_cast<size_t>(max_blocks);
-  for (int l = 0; l < layers; ++l) {
-    const int rc = pkv_decode_step_planned(
-        q == nullptr ? nullptr : q + l * q_stride, k_new == nullptr ? nullptr : k_new + l * kv_stride,
-        v_new == nullptr ? nullptr : v_new + l * kv_stride, pool, num_pages,
-        block_tables == nullptr ? nullptr : block_tables + l * bt_stride, max_blocks, seq_lens,
-        batch, num_q_heads, num_kv_heads, head_dim, page_size, rope_theta, scale,
-        out == nullptr ? nullptr : out + l * q_stride, plan_host, plan_dev, workspace,
-        workspace_bytes, dev_err, stream);
-    if (rc != PKV_OK) return rc;  // only the first layer can fail its checks
+  for (int l = 1; l < layers; ++l) {
+    app.k_new = k_new + l * kv_stride;
+    app.v_new = v_new + l * kv_stride;
+    const cudaError_t err =
+        launch_planned(*h, pool, num_pages, q + l * q_stride, block_tables + l * bt_stride,
+                       max_blocks, seq_lens, batch, scale, out + l * q_stride, plan_dev,
+                       workspace, dev_err, st, &app);
+    if (err != cudaSuccess) return PKV_ECUDA;
+  }
+  return PKV_OK;
+}
+
+PKV_API int pkv_kv_write_prefill_layers(int layers, const pkv_bf16* k, const pkv_bf16* v,
+                                        int num_tokens, const int32_t* token_offsets,
+                                        const int32_t* start_positions, pkv_bf16* pool,
+                                        int64_t num_pages, const int32_t* block_tables,
+                                        int max_blocks, int batch, int num_kv_heads,
+                                        int head_dim, int page_size, double rope_theta,
+                                        int32_t* dev_err, pkv_stream_t stream) {
+  if (layers < 1) return PKV_EINVAL;
+  const int rc = pkv_kv_write_prefill(k, v, num_tokens, token_offsets, start_positions, pool,
+                                      num_pages, block_tables, max_blocks, batch, num_kv_heads,
+                                      head_dim, page_size, rope_theta, dev_err, stream);
+  if (rc != PKV_OK || layers == 1 || num_tokens == 0) return rc;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  pkv::RopeFreqs freqs;
+  if (pkv::prepare_rope(rope_theta, &freqs, st) != cudaSuccess) return PKV_ECUDA;
+  const size_t kv_stride = static_cast<size_t>(num_tokens) * kNumKvHeads * kHeadDim;
+  const size_t bt_stride = static_cast<size_t>(batch) * static_cast<size_t>(max_blocks);
+  for (int l = 1; l < layers; ++l) {
+    const cudaError_t err = pkv::launch_kv_write_prefill(
+        k + l * kv_stride, v + l * kv_stride, num_tokens, token_offsets, start_positions, pool,
+        num_pages, block_tables + l * bt_stride, max_blocks, batch, freqs, dev_err, st);
+    if (err != cudaSuccess) return PKV_ECUDA;
   }
   return PKV_OK;
 }

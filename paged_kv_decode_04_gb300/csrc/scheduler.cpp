@@ -210,10 +210,11 @@ PKV_API int pkv_sched_decode_batch(pkv_scheduler* s, int max_batch, int64_t* ids
     ids[n] = r.id;
     seq_lens[n] = r.len;
     const int blocks = static_cast<int>(r.pages[0].size());
-    for (int l = 0; l < s->layers; ++l)
-      for (int k = 0; k < s->max_blocks; ++k)
-        block_tables[(static_cast<int64_t>(l) * max_batch + n) * s->max_blocks + k] =
-            k < blocks ? r.pages[l][k] : -1;
+    for (int l = 0; l < s->layers; ++l) {
+      int32_t* row = block_tables + (static_cast<int64_t>(l) * max_batch + n) * s->max_blocks;
+      std::copy(r.pages[l].begin(), r.pages[l].begin() + blocks, row);
+      std::fill(row + blocks, row + s->max_blocks, -1);
+    }
     if (r.generated >= r.budget_new) {
       r.state = State::kFinished;
       s->st.finished++;
@@ -222,6 +223,14 @@ PKV_API int pkv_sched_decode_batch(pkv_scheduler* s, int max_batch, int64_t* ids
     ++n;
   }
   s->st.largest_decode_batch = std::max<int64_t>(s->st.largest_decode_batch, n);
+  return n;
+}
+
+PKV_API int pkv_sched_running(const pkv_scheduler* s) {
+  if (s == nullptr) return 0;
+  int n = 0;
+  for (int64_t rid : s->admitted)
+    if (s->reqs.at(rid).state == State::kRunning) ++n;
   return n;
 }
 

@@ -51,7 +51,7 @@ class Engine:
         if self.host_inputs:
             x = torch.from_numpy(self.rng.standard_normal(shape).astype(np.float32))
             return x.to(torch.bfloat16).to(self.dev)
-        return torch.randn(shape, generator=self.gen, device=self.dev).to(torch.bfloat16)
+        return torch.randn(shape, generator=self.gen, device=self.dev, dtype=torch.bfloat16)
 
     def _upload_i32(self, *arrays):
         """Copy int32 host arrays to the device in one transfer through pinned
@@ -79,39 +79,58 @@ class Engine:
             dbt, off, st = self._upload_i32(np.ascontiguousarray(bt, dtype=np.int32)[:, None],
                                             np.array([0, plen], np.int32),
                                             np.zeros(1, np.int32))
-            ks = self._normal((self.layers, plen, HKV, D))   # one draw per prompt
-            vs = self._normal((self.layers, plen, HKV, D))
-            for layer in range(self.layers):
-                binding.kv_write_prefill(ks[layer], vs[layer], off, st, self.pool, dbt[layer],
-                                         dev_err=self.err)
-                if on_prefill is not None:
-                    on_prefill(layer, rid, ks[layer], vs[layer], bt[layer])
-        ids, lens, bts = self.sched.decode_batch(self.max_batch)
-        n = len(ids)
-        if n:
-            # one transfer per step: every layer's block table and the lengths
-            dbts, dlens = self._upload_i32(bts, lens)
-            plan = None
-            if self.use_plan:
-                plan = binding.Plan(lens, self.max_blocks, device=self.dev)
-                if plan.workspace_bytes > self.ws.numel():
-                    self.ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8,
-                                          device=self.dev)
-            qs = self._normal((self.layers, n, HQ, D))   # one draw per step
-            kns = self._normal((self.layers, n, HKV, D))
-            vns = self._normal((self.layers, n, HKV, D))
-            if plan is not None:
-                # every layer in one native call, launched in layer order
-                outs = binding.decode_steps_planned(qs, kns, vns, self.pool, dbts, dlens, plan,
-                                                    workspace=self.ws, dev_err=self.err)
-            else:
-                outs = [binding.decode_step(qs[layer], kns[layer], vns[layer], self.pool,
-                                            dbts[layer], dlens, workspace=self.ws,
-                                            dev_err=self.err) for layer in range(self.layers)]
-            if on_decode is not None:
+            kv = self._normal((2, self.layers, plen, HKV, D))   # one draw per prompt
+            ks, vs = kv[0], kv[1]
+            binding.kv_write_prefill_layers(ks, vs, off, st, self.pool, dbt, dev_err=self.err)
+            if on_prefill is not None:
                 for layer in range(self.layers):
-                    on_decode(layer, ids, lens, bts[layer], qs[layer], kns[layer], vns[layer],
-                              outs[layer])
+                    on_prefill(layer, rid, ks[layer], vs[layer], bt[layer])
+        n = min(self.max_batch, self.sched.running())
+        if n == 0:
+            return 0
+        # One pinned staging buffer per step: the scheduler writes every
+        # layer's block table and the lengths straight into it, the plan is
+        # built behind them, and one copy moves all of it to the device.
+        L, mb = self.layers, self.max_blocks
+        nt = L * n * mb
+        plan_at = (nt + n + 3) // 4 * 4                  # 16-byte aligned
+        plan_words = binding.plan_bytes(n, mb) // 4 if self.use_plan else 0
+        staged = torch.empty(plan_at + plan_words, dtype=torch.int32, pin_memory=True)
+        flat = staged.numpy()
+        bts = flat[:nt].reshape(L, n, mb)
+        lens = flat[nt:nt + n]
+        ids = np.empty(n, np.int64)
+        if self.sched.decode_batch_into(ids, lens, bts) != n:
+            raise RuntimeError("the scheduler's decode batch does not match its running count")
+        plan = None
+        upto = nt + n
+        if self.use_plan:
+            plan = binding.Plan(lens, mb, out=flat[plan_at:])
+            upto = plan_at + plan.bytes_used // 4
+            if plan.workspace_bytes > self.ws.numel():
+                self.ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=self.dev)
+        dev = staged[:upto].to(self.dev, non_blocking=True)
+        dbts = dev[:nt].view(L, n, mb)
+        dlens = dev[nt:nt + n]
+        if plan is not None:
+            plan.dev = dev[plan_at:upto]
+        a, b = L * n * HQ * D, L * n * HKV * D
+        x = self._normal((a + 2 * b,))                   # one draw per step
+        qs = x[:a].view(L, n, HQ, D)
+        kns = x[a:a + b].view(L, n, HKV, D)
+        vns = x[a + b:].view(L, n, HKV, D)
+        if plan is not None:
+            # every layer in one native call, launched in layer order
+            outs = binding.decode_steps_planned(qs, kns, vns, self.pool, dbts, dlens, plan,
+                                                workspace=self.ws, dev_err=self.err)
+        else:
+            outs = [binding.decode_step(qs[layer], kns[layer], vns[layer], self.pool,
+                                        dbts[layer], dlens, workspace=self.ws,
+                                        dev_err=self.err) for layer in range(L)]
+        if on_decode is not None:
+            for layer in range(L):
+                on_decode(layer, ids, lens, bts[layer], qs[layer], kns[layer], vns[layer],
+                          outs[layer])
         return n
 
     def run(self, requests, max_iters: int = 1_000_000, on_prefill=None, on_decode=None):

@@ -44,6 +44,8 @@ def _lib():
         L.pkv_sched_next_prefill.restype = i32
         L.pkv_sched_decode_batch.argtypes = [vp, i32, vp, vp, vp]
         L.pkv_sched_decode_batch.restype = i32
+        L.pkv_sched_running.argtypes = [vp]
+        L.pkv_sched_running.restype = i32
         L.pkv_sched_finish.argtypes = [vp, i64]
         L.pkv_sched_finish.restype = i32
         L.pkv_sched_seq_len.argtypes = [vp, i64]
@@ -99,6 +101,26 @@ class Scheduler:
         got = self._L.pkv_sched_next_prefill(self._h, ctypes.byref(rid), ctypes.byref(plen),
                                              bt.ctypes.data_as(ctypes.c_void_p))
         return (rid.value, plen.value, bt) if got else None
+
+    def running(self) -> int:
+        """Prefilled, unfinished requests: the next decode batch's size before its cap."""
+        return self._L.pkv_sched_running(self._h)
+
+    def decode_batch_into(self, ids, seq_lens, block_tables) -> int:
+        """decode_batch writing into caller arrays of capacity n = len(ids): ids
+        int64 [n], seq_lens int32 [n], block_tables int32 [layers][n][max_blocks]
+        (C-contiguous; when the batch is n long, its tables are exactly these)."""
+        n = ids.shape[0]
+        if (ids.dtype != np.int64 or seq_lens.dtype != np.int32 or block_tables.dtype != np.int32
+                or seq_lens.shape != (n,) or block_tables.shape != (self.layers, n, self.max_blocks)
+                or not (ids.flags.c_contiguous and seq_lens.flags.c_contiguous
+                        and block_tables.flags.c_contiguous)):
+            raise ValueError("decode_batch_into: wrong array types or shapes")
+        if n == 0:
+            return 0
+        return self._L.pkv_sched_decode_batch(self._h, n, ids.ctypes.data_as(ctypes.c_void_p),
+                                              seq_lens.ctypes.data_as(ctypes.c_void_p),
+                                              block_tables.ctypes.data_as(ctypes.c_void_p))
 
     def decode_batch(self, max_batch: int):
         """(ids [n], seq_lens [n], block_tables [layers][n][max_blocks])."""

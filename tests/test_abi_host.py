@@ -163,3 +163,20 @@ def test_multi_layer_planned_step_argument_errors(lib):
     assert steps(batch=2) == B.PKV_EINVAL                # the plan is for one sequence
     assert steps(hkv=4) == B.PKV_EUNSUPPORTED
     assert steps(v=ctypes.c_void_p(0x10002)) == B.PKV_EALIGN
+
+
+def test_multi_layer_prefill_argument_errors(lib):
+    from paged_kv_decode_04_gb300 import binding as B
+    f = lib.pkv_kv_write_prefill_layers
+
+    def pre(**kw):
+        args = dict(layers=3, k=A, v=A, n=10, off=A, st=A, pool=A, num_pages=64, bt=A,
+                    max_blocks=128, batch=1, hkv=8, d=64, ps=16, theta=500000.0, err=None,
+                    stream=None)
+        args.update(kw)
+        return f(*args.values())
+    assert pre(layers=0) == B.PKV_EINVAL
+    assert pre(off=None) == B.PKV_EINVAL
+    assert pre(d=128) == B.PKV_EUNSUPPORTED
+    assert pre(v=ctypes.c_void_p(0x10004)) == B.PKV_EALIGN
+    assert pre(n=0) == B.PKV_OK

@@ -165,3 +165,36 @@ def test_prefill_special_values_bit_exact(theta):
     assert mism.size == 0, f"{len(mism)} mismatching elements, first {mism[:3].tolist()}"
     assert int(err.item()) == 0
     assert is_nan_bf16(want).any() and (want == 0).any()
+
+
+def test_multi_layer_prefill_equals_per_layer_calls():
+    # pkv_kv_write_prefill_layers: 3 layers of the same ragged prompts through
+    # their own tables, in one call, write the bits the oracle writes
+    dev = cuda_or_skip()
+    counts, starts = [20, 0, 5, 300], [0, 3, 15, 100]
+    layers = 3
+    rng = np.random.default_rng(77)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    T = int(off[-1])
+    ks = bf16_normal(rng, (layers, T, 8, 64))
+    vs = bf16_normal(rng, (layers, T, 8, 64))
+    bts = np.full((layers, len(counts), 128), -1, np.int32)
+    perm = rng.permutation(512)
+    cur = 0
+    for layer in range(layers):
+        for b, (c, s0) in enumerate(zip(counts, starts)):
+            if c:
+                first, last = s0 // 16, (s0 + c - 1) // 16
+                bts[layer, b, first:last + 1] = perm[cur:cur + last - first + 1]
+                cur += last - first + 1
+    st = np.asarray(starts, np.int32)
+    want = np.full((512, 2, 16, 8, 64), POISON, dtype=np.uint16)
+    for layer in range(layers):
+        assert oracle.kv_write_prefill(ks[layer], vs[layer], off, st, want, bts[layer]) == 0
+    dpool = to_dev(np.full((512, 2, 16, 8, 64), POISON, dtype=np.uint16), dev, bf=True)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    binding().kv_write_prefill_layers(to_dev(ks, dev, True), to_dev(vs, dev, True),
+                                      to_dev(off, dev), to_dev(st, dev), dpool, to_dev(bts, dev),
+                                      dev_err=err)
+    assert np.array_equal(synth.bits(dpool), want)
+    assert int(err.item()) == 0

@@ -178,3 +178,42 @@ def test_matches_oracle_on_random_traces(seed, static):
     # every accepted request ends finished (after admission, or cancelled while waiting)
     assert st["finished"] + st["rejected"] == st["submitted"]
     assert st["admitted"] <= st["finished"]
+
+
+def test_running_count_and_decode_batch_into_match_decode_batch():
+    # two schedulers fed the same trace: decode_batch_into (caller arrays sized
+    # by running()) fills exactly what decode_batch returns
+    rng = np.random.default_rng(21)
+    reqs = [(int(rng.integers(1, 80)), int(rng.integers(1, 60))) for _ in range(12)]
+    a, b = Scheduler(400, 3, CTX), Scheduler(400, 3, CTX)
+    for p, n in reqs:
+        a.submit(p, n)
+        b.submit(p, n)
+    for _ in range(200):
+        a.admit()
+        b.admit()
+        ga, gb = a.next_prefill(), b.next_prefill()
+        assert (ga is None) == (gb is None)
+        n = min(5, b.running())
+        ids_a, lens_a, bt_a = a.decode_batch(5)
+        ids = np.empty(n, np.int64)
+        lens = np.empty(n, np.int32)
+        bt = np.empty((3, n, CTX // 16), np.int32)
+        assert b.decode_batch_into(ids, lens, bt) == n == len(ids_a)
+        assert np.array_equal(ids, ids_a) and np.array_equal(lens, lens_a)
+        assert np.array_equal(bt, bt_a)
+        if a.stats()["finished"] == len(reqs):
+            break
+    assert b.stats()["finished"] == len(reqs) and b.running() == 0
+
+
+def test_decode_batch_into_rejects_bad_arrays():
+    s = Scheduler(100, 2, CTX)
+    with pytest.raises(ValueError):
+        s.decode_batch_into(np.empty(2, np.int32), np.empty(2, np.int32),
+                            np.empty((2, 2, CTX // 16), np.int32))
+    with pytest.raises(ValueError):
+        s.decode_batch_into(np.empty(2, np.int64), np.empty(2, np.int32),
+                            np.empty((3, 2, CTX // 16), np.int32))
+    assert s.decode_batch_into(np.empty(0, np.int64), np.empty(0, np.int32),
+                               np.empty((2, 0, CTX // 16), np.int32)) == 0
