@@ -39,6 +39,13 @@
  *  - Query head j uses kv head j / (num_q_heads / num_kv_heads).
  *  - Supported sizes: num_q_heads = 32, num_kv_heads = 8, head_dim = 64,
  *    page_size = 16 (other values return PKV_EUNSUPPORTED).
+ *  - Kernels are launched with programmatic dependent launch: a kernel may
+ *    start while the previous kernel on `stream` is still running, and waits
+ *    for it (griddepcontrol.wait) before it reads anything it uses.  Before
+ *    that wait the attention kernels only prefetch pool pages into L2, with
+ *    addresses taken from the plan, lengths and block tables as they stand
+ *    (every index range-checked); those words are read again after the wait,
+ *    so a caller's kernel that writes them just before a call is safe.
  *  - Return value: PKV_OK or a PKV_E* code (see pkv_strerror).  Argument
  *    errors are detected on the host before anything is enqueued.  Bad DEVICE
  *    data (a page id outside [0, num_pages), a length or position outside the
