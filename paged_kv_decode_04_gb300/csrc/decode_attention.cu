@@ -31,6 +31,9 @@
 //    4 short sequences, one per warp, each warp writing its own rows.
 //  * kStages: the per-warp ring depth -- 4 tiles (3 CTAs per SM) when it can
 //    hold every page a warp gets, else 3 tiles at 4 CTAs per SM.
+//  * Before griddepcontrol.wait a CTA only prefetches its first ring fill
+//    into L2 (prefetch_first_tiles), so that a CTA made resident while the
+//    previous grid drains already pulls its pages.
 //  * Batches that fill the SMs go to decode_pagebox.cu instead (one CTA per
 //    sequence range for all heads, whole-page boxes).
 #include <cuda.h>
