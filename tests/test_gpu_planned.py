@@ -265,3 +265,22 @@ def test_multi_layer_call_checks_its_shapes():
     with pytest.raises(b.PkvError):                 # a plan built for another batch
         b.decode_steps_planned(d["q"], d["k_new"], d["v_new"], d["pool"], d["block_tables"],
                                d["seq_lens"], b.Plan([40, 17, 5], w.max_blocks, device=dev))
+
+
+def test_one_layer_multi_call_equals_the_single_layer_call():
+    dev = cuda_or_skip()
+    lens = mixed_lengths(np.random.default_rng(9), 30, 3)
+    w = synth.make_workload("edge", 9, seq_lens=lens, num_pages=2048)
+    b = binding()
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev)
+    outs = []
+    for multi in (False, True):
+        d = synth.device_inputs(w, dev)
+        if multi:
+            out = b.decode_steps_planned(d["q"][:1], d["k_new"][:1], d["v_new"][:1], d["pool"],
+                                         d["block_tables"][:1], d["seq_lens"], plan)[0]
+        else:
+            out = b.decode_step_planned(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"],
+                                        d["block_tables"][0], d["seq_lens"], plan)
+        outs.append((synth.bits(out), synth.bits(d["pool"])))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])

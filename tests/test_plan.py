@@ -216,3 +216,20 @@ def test_check_tables_names_the_first_bad_entry(case):
     with pytest.raises(B.PkvError) as e:
         B.check_tables(bt, lens, 64)
     assert want in str(e.value) and e.value.status == B.PKV_EINVAL
+
+
+def test_plan_built_into_a_caller_buffer_is_the_same_plan():
+    lens = np.random.default_rng(31).integers(0, 2049, 90).astype(np.int32)
+    nbytes = B.plan_bytes(len(lens), 128)
+    raw = np.zeros(nbytes // 4 + 8, np.int32)
+    off = (-raw.ctypes.data % 16) // 4
+    p = B.Plan(lens, 128, num_sms=SMS, out=raw[off:])
+    q = B.Plan(lens, 128, num_sms=SMS)
+    assert np.array_equal(p.host, q.host) and p.workspace_bytes == q.workspace_bytes
+    assert np.shares_memory(p.host, raw)
+    with pytest.raises(ValueError):                 # too small
+        B.Plan(lens, 128, num_sms=SMS, out=raw[off:off + 8])
+    with pytest.raises(ValueError):                 # misaligned
+        B.Plan(lens, 128, num_sms=SMS, out=raw[off + 1:])
+    with pytest.raises(ValueError):                 # wrong type
+        B.Plan(lens, 128, num_sms=SMS, out=raw[off:].view(np.float32))
