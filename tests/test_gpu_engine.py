@@ -4,7 +4,6 @@ oracle and compared (appended pages bit-exact at the end, outputs within
 tolerance at every step)."""
 import numpy as np
 import pytest
-import torch
 
 import oracle
 from paged_kv_decode_04_gb300 import synth

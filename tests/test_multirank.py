@@ -7,7 +7,6 @@ times and the sum of their bytes.  The reference arm prints from rank 0 only.
 import os
 import socket
 
-import pytest
 import torch.distributed as dist
 import torch.multiprocessing as mp
 

@@ -5,7 +5,6 @@ Sources of the rules: "Hours of YouTube and 85 handtyped pages of notes on LLM
 Inference - Start here", section "現在のスコープ" (page-credit admission, FIFO
 wait, rejection, lazy pages, --stats) and the batching item of "これまでの進捗".
 """
-import math
 
 import numpy as np
 import pytest
