@@ -42,8 +42,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_attention_peak_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_decode_04_gb300", "csrc", f)
-                  for f in ("decode_attention.cu", "decode_pagebox.cu", "decode_page.cuh",
-                            "pkv_device.cuh", "pkv_internal.h")]
+                  for f in ("decode_attention.cu", "decode_pagebox.cu", "decode_shared.cu",
+                            "decode_page.cuh", "pkv_device.cuh", "pkv_internal.h")]
 # The traffic file holds a list of records {workload, kernel, kernel_sha, dram_bytes_per_launch}.
 
 WORKLOAD_TEXT = {
@@ -313,14 +313,18 @@ def run_ours(args, world, rank, local):
     d = synth.device_inputs(w, dev)
     B, layers = w.batch, w.layers
     stream = torch.cuda.current_stream(dev)
-    planned = args.plan == "host"
-    plan = binding.Plan(w.seq_lens, w.max_blocks, device=dev) if planned else None
+    planned = args.plan in ("host", "lengths")
+    # the host plan is built from the lengths and layer 0's tables (shared
+    # prefixes become shared-prefix items); the workloads share the same runs
+    # of pages in every layer, so it serves every layer
+    plan_kw = {"block_tables": w.block_tables[0]} if args.plan == "host" else {}
+    plan = binding.Plan(w.seq_lens, w.max_blocks, device=dev, **plan_kw) if planned else None
     plan_build_us = None
     if planned:
         # host cost of planning one step (a serving loop builds one plan per step)
         t = time.perf_counter()
         for _ in range(200):
-            binding.Plan(w.seq_lens, w.max_blocks)
+            binding.Plan(w.seq_lens, w.max_blocks, **plan_kw)
         plan_build_us = round((time.perf_counter() - t) / 200 * 1e6, 2)
     if planned:
         d["plan"] = plan.dev
@@ -328,6 +332,9 @@ def run_ours(args, world, rank, local):
         ws_bytes = plan.workspace_bytes
         split_text = (f"host work plan: {plan.num_items} items of at most {plan.range_pages} "
                       f"pages or 4 packed sequences, {plan.num_merges} merged sequences")
+        if plan.num_shared:
+            split_text += (f", {plan.num_shared} shared-prefix items of at most "
+                           f"{plan.shared_pages} pages")
     else:
         splits = binding.plan_splits(B, w.max_blocks, args.splits)
         ws_bytes = binding.workspace_bytes(B, w.max_blocks, args.splits)
@@ -338,7 +345,8 @@ def run_ours(args, world, rank, local):
     fused = args.path == "fused"
     merges = (plan.num_merges > 0) if planned else (splits > 1)
     launched = binding.attention_kernels(B, w.max_blocks, args.splits, plan)
-    kernels_per_layer = (1 if fused else 2) + (1 if merges else 0)
+    kernels_per_layer = ((1 if fused else 2) + (1 if merges else 0)
+                         + (1 if planned and plan.num_shared else 0))
 
     def plan_for(dset):
         """The plan whose device copy is dset["plan"] (one per input set)."""
@@ -764,10 +772,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="peak")
     ap.add_argument("--splits", type=int, default=0, help="0 = automatic split plan")
-    ap.add_argument("--plan", choices=["auto", "host"], default="host",
-                    help="host (default): a work plan built on the host from the lengths "
-                         "(pkv_plan_build) and passed to the planned entry points, as the "
-                         "serving engine does; auto: the fixed automatic split plan")
+    ap.add_argument("--plan", choices=["auto", "host", "lengths"], default="host",
+                    help="host (default): a work plan built on the host from the lengths and "
+                         "the block tables, shared prefixes as shared-prefix items "
+                         "(pkv_plan_build_shared), passed to the planned entry points; "
+                         "lengths: the plan from the lengths alone (pkv_plan_build), as the "
+                         "serving engine builds it; auto: the fixed automatic split plan")
     ap.add_argument("--path", choices=["fused", "separate"], default="fused",
                     help="fused: one pkv_decode_step launch per layer; separate: pkv_kv_append "
                          "then pkv_paged_decode_attention")

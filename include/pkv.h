@@ -270,18 +270,21 @@ PKV_API int pkv_check_tables(const int32_t* block_table, int max_blocks,
  * whose plan fits in one wave of four CTAs per SM; when none does, the
  * ranges take the whole table width (a batch of long sequences then gets
  * one range each, as with num_splits = 1).
- * The plan is plain data: 8 header words
+ * The plan is plain data: 12 header words
  *   {PKV_PLAN_MAGIC, batch, max_blocks, num_items, num_merges, num_slots,
- *    range_pages, bytes_used},
+ *    range_pages, bytes_used, num_shared, shared_pages, 0, 0},
  * then num_items items of 16 int32 words
  *   {kind (0 range, 1 packed), slot (-1: not split), p_begin, n,
  *    seq[4], len[4], 0, 0, 0, 0}
  * (a range item repeats its sequence in all four seq/len words; a packed
  * item holds one sequence per warp, -1 for none), then num_merges entries
- * {b, first slot, ranges, 0}.  The results follow the same numerics as the
- * calls above (same tolerance, bit-identical on repeated runs of a plan).
+ * {b, first slot, ranges, 0}, then num_shared shared-prefix items of 36
+ * words {members, p_begin, n, 0, seq[16], slot[16]} (plans from
+ * pkv_plan_build_shared only; shared_pages is the longest one's n).  The
+ * results follow the same numerics as the calls above (same tolerance,
+ * bit-identical on repeated runs of a plan).
  */
-#define PKV_PLAN_MAGIC 0x31564b50 /* "PKV1" */
+#define PKV_PLAN_MAGIC 0x32564b50 /* "PKV2" */
 
 /* Bytes a plan for this batch and table width can take (host buffer). */
 PKV_API size_t pkv_plan_bytes(int batch, int max_blocks);
@@ -296,6 +299,24 @@ PKV_API size_t pkv_plan_bytes(int batch, int max_blocks);
  */
 PKV_API int pkv_plan_build(const int32_t* seq_lens_host, int batch, int max_blocks,
                            int num_sms, void* plan, size_t plan_bytes);
+
+/*
+ * A plan for a batch whose sequences share prompt prefixes (block tables
+ * naming the same physical pages; "Tiny-vLLMでゼロから構築する高性能LLM推論
+ * エンジン", section "KV Cache").  block_tables_host: the host copy of this
+ * layer's tables, int32 [batch][max_blocks].  Runs of up to 16 consecutive
+ * sequences whose tables start with the same min_shared_pages or more page
+ * ids form a group; its common pages (never a member's last page) become
+ * shared-prefix items, each attended once for all members by
+ * paged_decode_shared_kernel, which writes one partial per member.  Each
+ * member's own pages become ranges writing partials too, and one merge
+ * combines a member's partials.  Sequences in no group are planned as by
+ * pkv_plan_build.  Same returns as pkv_plan_build (PKV_EUNSUPPORTED also for
+ * more than 65535 shared-prefix items).  Pure host code.
+ */
+PKV_API int pkv_plan_build_shared(const int32_t* seq_lens_host, const int32_t* block_tables_host,
+                                  int batch, int max_blocks, int num_sms, int min_shared_pages,
+                                  void* plan, size_t plan_bytes);
 
 /* Device workspace bytes a built plan needs (0 when nothing is split). */
 PKV_API size_t pkv_plan_workspace_bytes(const void* plan);

@@ -30,7 +30,8 @@ DEVERR_POSITION = 4
 DEVERR_TIMEOUT = 8
 DEVERR_OFFSETS = 16
 DEVERR_PLAN = 32
-PLAN_MAGIC = 0x31564B50
+PLAN_MAGIC = 0x32564B50
+PLAN_HEADER_WORDS = 12
 
 NUM_Q_HEADS = 32
 NUM_KV_HEADS = 8
@@ -80,6 +81,8 @@ def _load():
     L.pkv_plan_bytes.restype = sz
     L.pkv_plan_build.argtypes = [vp, i32, i32, i32, vp, sz]
     L.pkv_plan_build.restype = i32
+    L.pkv_plan_build_shared.argtypes = [vp, vp, i32, i32, i32, i32, vp, sz]
+    L.pkv_plan_build_shared.restype = i32
     L.pkv_plan_workspace_bytes.argtypes = [vp]
     L.pkv_plan_workspace_bytes.restype = sz
     L.pkv_paged_decode_attention_planned.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32,
@@ -349,13 +352,17 @@ class Plan:
     planned calls take the plan object itself."""
 
     HEADER = ("magic", "batch", "max_blocks", "num_items", "num_merges", "num_slots",
-              "range_pages", "bytes_used")
+              "range_pages", "bytes_used", "num_shared", "shared_pages")
 
     def __init__(self, seq_lens_host, max_blocks: int, *, num_sms: int = 0, device=None,
-                 out=None):
+                 out=None, block_tables=None, min_shared_pages: int = 16):
         """out: an int32 array of at least plan_bytes(len(seq_lens_host), max_blocks)
         bytes, 16-byte aligned, to build the plan in (e.g. a view of pinned
-        staging memory); by default the plan gets a buffer of its own."""
+        staging memory); by default the plan gets a buffer of its own.
+        block_tables: the host copy of this layer's tables [B][max_blocks];
+        when given, runs of consecutive sequences whose tables start with the
+        same min_shared_pages or more pages get them as shared-prefix items
+        (pkv_plan_build_shared)."""
         lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
         if lens.ndim != 1:
             raise ValueError("seq_lens_host must be one-dimensional")
@@ -373,10 +380,22 @@ class Plan:
                                  "least plan_bytes() bytes")
             raw = out
             buf = out[: nbytes // 4]
-        rc = _lib.pkv_plan_build(lens.ctypes.data_as(ctypes.c_void_p), lens.shape[0], max_blocks,
-                                 num_sms, buf.ctypes.data_as(ctypes.c_void_p), nbytes)
+        if block_tables is None:
+            rc = _lib.pkv_plan_build(lens.ctypes.data_as(ctypes.c_void_p), lens.shape[0],
+                                     max_blocks, num_sms, buf.ctypes.data_as(ctypes.c_void_p),
+                                     nbytes)
+            what = "pkv_plan_build"
+        else:
+            bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+            if bt.shape != (lens.shape[0], max_blocks):
+                raise ValueError("block_tables must be [batch][max_blocks] int32")
+            rc = _lib.pkv_plan_build_shared(lens.ctypes.data_as(ctypes.c_void_p),
+                                            bt.ctypes.data_as(ctypes.c_void_p), lens.shape[0],
+                                            max_blocks, num_sms, int(min_shared_pages),
+                                            buf.ctypes.data_as(ctypes.c_void_p), nbytes)
+            what = "pkv_plan_build_shared"
         if rc != PKV_OK:
-            raise PkvError(rc, "pkv_plan_build")
+            raise PkvError(rc, what)
         self._raw = raw
         self.host = buf[: int(buf[7]) // 4]
         for i, name in enumerate(self.HEADER):
@@ -388,12 +407,18 @@ class Plan:
 
     def items(self) -> np.ndarray:
         """[num_items][16] int32: kind, slot, p_begin, n, seq[4], len[4], 0 x 4."""
-        return self.host[8:8 + 16 * self.num_items].reshape(self.num_items, 16)
+        o = PLAN_HEADER_WORDS
+        return self.host[o:o + 16 * self.num_items].reshape(self.num_items, 16)
 
     def merges(self) -> np.ndarray:
         """[num_merges][4] int32: sequence, first slot, ranges, 0."""
-        o = 8 + 16 * self.num_items
+        o = PLAN_HEADER_WORDS + 16 * self.num_items
         return self.host[o:o + 4 * self.num_merges].reshape(self.num_merges, 4)
+
+    def shared(self) -> np.ndarray:
+        """[num_shared][36] int32: members, p_begin, n, 0, seq[16], slot[16]."""
+        o = PLAN_HEADER_WORDS + 16 * self.num_items + 4 * self.num_merges
+        return self.host[o:o + 36 * self.num_shared].reshape(self.num_shared, 36)
 
     def to(self, device):
         """Copy the plan to `device`, asynchronously on the current stream (through

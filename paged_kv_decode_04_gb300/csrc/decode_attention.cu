@@ -85,6 +85,8 @@ __host__ __device__ constexpr size_t smem_bytes(int stages, int pages_per_split)
 // order (deterministic).  Splits that saw no valid key (sum 0) get weight 0.
 // The partials are read through L2 (ld.global.cg).
 constexpr int kMergeBatch = 16;
+constexpr int kMergeRowsMax = 4;  // query rows (warps) per CTA of merge_plan_kernel
+static_assert(kNumQHeads % kMergeRowsMax == 0, "merge CTAs cover whole sequences");
 
 __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t base, int64_t stride,
                                           int nr, uint16_t* out_row, int lane) {
@@ -448,15 +450,45 @@ __global__ void __launch_bounds__(32) merge_splits_kernel(const AttnArgs a) {
 }
 
 // Work plan: combine the ranges of the split sequences the plan lists;
-// grid (Hq, merges), one warp per (sequence, query row).
-__global__ void __launch_bounds__(32) merge_plan_kernel(const AttnArgs a) {
+// grid (Hq / rows, merges), one warp per (sequence, query row), `rows` =
+// blockDim.x / 32 query rows per CTA.
+__global__ void __launch_bounds__(kMergeRowsMax * 32) merge_plan_kernel(const AttnArgs a) {
   allow_dependent_grids();  // the next grid may launch; it waits for this one itself
   wait_for_prior_grids();
   const int4 e = a.plan_merges[blockIdx.y];  // (b, first slot, ranges, 0)
-  const int j = blockIdx.x;
+  const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t row = static_cast<int64_t>(e.x) * kNumQHeads + j;
   merge_row(a, static_cast<int64_t>(e.y) * kNumQHeads + j, kNumQHeads, e.z,
-            a.out + row * kHeadDim, threadIdx.x);
+            a.out + row * kHeadDim, threadIdx.x & 31);
+}
+
+// Query rows per merge CTA: one (more CTAs, for few merged sequences) or
+// kMergeRowsMax once there are at least as many merged sequences as SMs.
+// Measured: 256 merged sequences 82.4 -> 78.7 us per step with 4 rows, one
+// 16-range sequence 88.1 -> 90.1 us, so the switch.
+int merge_rows_per_cta(int num_merges) {
+  static std::atomic<int> sms_of[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  std::atomic<int>& c = sms_of[dev & 63];
+  int sms = c.load(std::memory_order_relaxed);
+  if (sms == 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 1;
+    }
+    c.store(sms, std::memory_order_relaxed);
+  }
+  return num_merges >= sms ? kMergeRowsMax : 1;
+}
+
+cudaError_t launch_merge_plan(const AttnArgs& args, int num_merges, cudaStream_t stream) {
+  const int rows = merge_rows_per_cta(num_merges);
+  return launch_pdl(merge_plan_kernel, dim3(kNumQHeads / rows, num_merges), dim3(32 * rows), 0,
+                    stream, args);
 }
 
 }  // namespace
@@ -538,9 +570,7 @@ cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
 
 cudaError_t launch_split_merge(const AttnArgs& args, int num_merges, cudaStream_t stream) {
   if (args.plan_items != nullptr)
-    return num_merges > 0 ? launch_pdl(merge_plan_kernel, dim3(kNumQHeads, num_merges), dim3(32),
-                                       0, stream, args)
-                          : cudaSuccess;
+    return num_merges > 0 ? launch_merge_plan(args, num_merges, stream) : cudaSuccess;
   return args.plan.num_splits > 1 ? launch_pdl(merge_splits_kernel,
                                                dim3(kNumQHeads, args.batch), dim3(32), 0, stream,
                                                args)
@@ -558,9 +588,7 @@ cudaError_t launch_planned_decode_attention(const CUtensorMap& pool_map,
   err = launch_attention_kernel<true>(pool_map, args, append, dim3(kNumKvHeads, num_items),
                                       range_pages, page_list, device, stream);
   if (err != cudaSuccess) return err;
-  if (num_merges > 0)
-    err = launch_pdl(merge_plan_kernel, dim3(kNumQHeads, num_merges), dim3(32), 0, stream,
-                     args);
+  if (num_merges > 0) err = launch_merge_plan(args, num_merges, stream);
   return err;
 }
 

@@ -458,7 +458,9 @@ namespace {
 
 struct PlanHeader {
   int32_t magic, batch, max_blocks, num_items, num_merges, num_slots, range_pages, bytes_used;
+  int32_t num_shared, shared_pages, reserved0, reserved1;
 };
+static_assert(sizeof(PlanHeader) == 4 * pkv::kPlanHeaderWords, "plan header layout");
 
 // The plan's header when it is well formed for this batch and table, else nullptr.
 const PlanHeader* plan_header(const void* plan, int batch, int max_blocks) {
@@ -466,7 +468,9 @@ const PlanHeader* plan_header(const void* plan, int batch, int max_blocks) {
   const PlanHeader* h = static_cast<const PlanHeader*>(plan);
   if (h->magic != static_cast<int32_t>(PKV_PLAN_MAGIC) || h->batch != batch ||
       h->max_blocks != max_blocks || h->num_items < 1 || h->num_items > 65535 ||
-      h->num_merges < 0 || h->num_slots < 0 || h->range_pages < 1 || h->range_pages > 1024)
+      h->num_merges < 0 || h->num_slots < 0 || h->range_pages < 1 || h->range_pages > 1024 ||
+      h->num_shared < 0 || h->num_shared > 65535 ||
+      (h->num_shared > 0 && (h->shared_pages < 1 || h->shared_pages > 1024)))
     return nullptr;
   return h;
 }
@@ -503,6 +507,9 @@ cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pa
   args.plan_items = reinterpret_cast<const int4*>(words + pkv::kPlanHeaderWords);
   args.plan_merges = reinterpret_cast<const int4*>(
       words + pkv::kPlanHeaderWords + static_cast<size_t>(h.num_items) * pkv::kPlanItemWords);
+  args.plan_shared = reinterpret_cast<const int4*>(
+      words + pkv::kPlanHeaderWords + static_cast<size_t>(h.num_items) * pkv::kPlanItemWords +
+      static_cast<size_t>(h.num_merges) * pkv::kPlanMergeWords);
   args.dev_err = dev_err;
   args.num_pages = num_pages;
   args.max_blocks = max_blocks;
@@ -511,6 +518,14 @@ cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pa
   args.plan.num_splits = 1;
   args.plan.pages_per_split = h.range_pages;
   CUtensorMap map;
+  if (h.num_shared > 0) {
+    // shared prefixes first: their partials join the members' own ones in
+    // the merge that follows the attention kernel
+    if (!pool_tensor_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
+    const cudaError_t err =
+        pkv::launch_shared_prefix_attention(map, args, h.num_shared, h.shared_pages, stream);
+    if (err != cudaSuccess) return err;
+  }
   if (use_pagebox(h.num_items, h.range_pages) && plan_has_only_ranges(h)) {
     if (!pool_page_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
     const cudaError_t err = pkv::launch_pagebox_attention(map, args, h.num_items, h.range_pages,
@@ -534,6 +549,9 @@ PKV_API const char* pkv_attention_kernels(int batch, int max_blocks, int num_spl
     const PlanHeader* h = plan_header(plan, batch, max_blocks);
     if (h == nullptr) return nullptr;
     const bool pb = use_pagebox(h->num_items, h->range_pages) && plan_has_only_ranges(*h);
+    if (h->num_shared > 0)  // a plan with shared groups always merges
+      return pb ? "paged_decode_shared_kernel+paged_decode_pagebox_kernel+merge_plan_kernel"
+                : "paged_decode_shared_kernel+paged_decode_kernel+merge_plan_kernel";
     if (h->num_merges > 0)
       return pb ? "paged_decode_pagebox_kernel+merge_plan_kernel"
                 : "paged_decode_kernel+merge_plan_kernel";
@@ -561,6 +579,18 @@ PKV_API int pkv_plan_build(const int32_t* seq_lens_host, int batch, int max_bloc
   }
   return pkv::build_plan(seq_lens_host, batch, max_blocks, num_sms, static_cast<int32_t*>(plan),
                          plan_bytes);
+}
+
+PKV_API int pkv_plan_build_shared(const int32_t* seq_lens_host, const int32_t* block_tables_host,
+                                  int batch, int max_blocks, int num_sms, int min_shared_pages,
+                                  void* plan, size_t plan_bytes) {
+  if (num_sms < 0) return PKV_EINVAL;
+  if (num_sms == 0) {
+    num_sms = current_sm_count();
+    if (num_sms <= 0) return PKV_ECUDA;
+  }
+  return pkv::build_plan_shared(seq_lens_host, block_tables_host, batch, max_blocks, num_sms,
+                                min_shared_pages, static_cast<int32_t*>(plan), plan_bytes);
 }
 
 PKV_API size_t pkv_plan_workspace_bytes(const void* plan) {

@@ -25,19 +25,31 @@ constexpr int kErrOffsets = 16;
 constexpr int kErrPlan = 32;
 
 // Work plans (include/pkv.h): header words, item and merge entry sizes.
-constexpr int kPlanHeaderWords = 8;
+constexpr int kPlanHeaderWords = 12;
 constexpr int kPlanItemWords = 16;
 constexpr int kPlanMergeWords = 4;
 constexpr int kPlanKindRange = 0;   // 4 warps share pages [p_begin, p_begin + n) of one sequence
 constexpr int kPlanKindPacked = 1;  // one whole sequence per warp
 constexpr int kPackPages = 16;      // most pages a packed sequence may have
 constexpr int kPlanWarps = 4;       // warps per attention CTA: one packed sequence each
+// Shared-prefix items (a plan's last section): one CTA per (item, kv head)
+// attends pages [p_begin, p_begin + n) that the item's members' tables all
+// hold, warp w for members 2w and 2w + 1: {members, p_begin, n, 0, seq[16],
+// slot[16]}.
+constexpr int kSharedMembers = 16;
+constexpr int kPlanSharedWords = 4 + 2 * kSharedMembers;
 
 // Host side of the work plans (planner.cpp): an upper bound on a plan's
 // bytes, and the plan itself from host lengths (PKV_* status).
 size_t plan_bytes(int batch, int max_blocks);
 int build_plan(const int32_t* lens, int batch, int max_blocks, int num_sms, int32_t* out,
                size_t out_bytes);
+// The same with shared prefixes: runs of consecutive sequences whose host
+// block tables start with the same min_shared_pages or more entries get
+// those pages as shared-prefix items (PKV_* status).
+int build_plan_shared(const int32_t* lens, const int32_t* block_tables, int batch,
+                      int max_blocks, int num_sms, int min_shared_pages, int32_t* out,
+                      size_t out_bytes);
 
 // Positions covered by the per-device cos/sin table (the 2048-token context).
 constexpr int kRopeTablePositions = 2048;
@@ -107,6 +119,7 @@ struct AttnArgs {
   float* part_ml;   // [B][Hq][S][2] fp32, (max in log2 units, sum)
   const int4* plan_items;   // work plan items (kPlanItemWords words each), or nullptr
   const int4* plan_merges;  // work plan merge entries (b, first slot, ranges, 0)
+  const int4* plan_shared;  // work plan shared-prefix items (kPlanSharedWords words each)
   int32_t* dev_err;
   int64_t num_pages;
   int max_blocks;
@@ -150,6 +163,11 @@ int pagebox_max_range_pages();
 // Launch the split merge of a plan (fixed: merge_splits_kernel when S > 1;
 // work plan: merge_plan_kernel over num_merges sequences).
 cudaError_t launch_split_merge(const AttnArgs& args, int num_merges, cudaStream_t stream);
+
+// Shared-prefix items of a work plan: grid (Hkv, num_shared), each CTA
+// writing its members' partials (decode_shared.cu).
+cudaError_t launch_shared_prefix_attention(const CUtensorMap& pool_map, const AttnArgs& args,
+                                           int num_shared, int range_pages, cudaStream_t stream);
 
 // Largest logical page range one attention CTA handles.
 int max_pages_per_split();

@@ -37,8 +37,10 @@ size_t plan_bytes(int batch, int max_blocks) {
   if (batch < 1 || max_blocks < 1) return 0;
   const int rmin = max_blocks < kMinRangePages ? max_blocks : kMinRangePages;
   const size_t items = static_cast<size_t>(batch) * ceil_div(max_blocks, rmin) + 1;
+  // shared-prefix items: at most one per (group of two or more, range)
+  const size_t shared = static_cast<size_t>(batch / 2) * ceil_div(max_blocks, rmin);
   return 4 * (kPlanHeaderWords + items * kPlanItemWords +
-              static_cast<size_t>(batch) * kPlanMergeWords);
+              static_cast<size_t>(batch) * kPlanMergeWords + shared * kPlanSharedWords);
 }
 
 // Sizes for work unit u (the pages one warp streams): ranges of R = 4 u
@@ -69,6 +71,13 @@ long long count_items(const std::vector<int>& pages, Sizes z) {
   return items + (packed + kPlanWarps - 1) / kPlanWarps;
 }
 
+// A run of consecutive sequences whose block tables start with the same k
+// pages (k at least the minimum asked for, and below every member's last
+// page, which takes the step's append and so stays its own).
+struct SharedGroup {
+  int first, members, k;
+};
+
 // The work unit U: the smallest whose plan fits in one wave of resident
 // CTAs (kResidentPerSm per SM, 8 kv heads each item), starting from
 // ceil(P / (2 SMs)), the unit at which the ranges alone would fill that
@@ -77,54 +86,96 @@ long long count_items(const std::vector<int>& pages, Sizes z) {
 // ones are cut into ceil(p / R) ranges of near-equal size, which the merge
 // kernel combines.  Items run in order of the pages their busiest warp
 // streams, most first (ranges before packed items on ties).
-int build_plan(const int32_t* lens, int batch, int max_blocks, int num_sms, int32_t* out,
-               size_t out_bytes) {
-  if (lens == nullptr || out == nullptr || batch < 1 || max_blocks < 1 || num_sms < 1)
-    return PKV_EINVAL;
-  if (reinterpret_cast<uintptr_t>(out) % 16 != 0) return PKV_EALIGN;
-  if (out_bytes < plan_bytes(batch, max_blocks)) return PKV_EINVAL;
+//
+// With shared groups, a member attends only its own pages [k, pages) in
+// range items (never packed) and every range writes a partial; the group's
+// pages [0, k) become shared-prefix items (ns near-equal ranges per group,
+// ns the most that keeps these CTAs within one wave of two per SM) whose CTAs write one
+// partial per member; each member's partials sit in consecutive slots,
+// shared ranges first, and one merge entry combines them.
+int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
+               const std::vector<SharedGroup>& groups, int32_t* out, size_t out_bytes) {
   const long long Lmax = static_cast<long long>(max_blocks) * kPageSize;
-  std::vector<int> pages(batch);
-  long long total = 0;
+  std::vector<int> pages(batch), start(batch, 0), group_of(batch, -1);
   for (int b = 0; b < batch; ++b) {
     if (lens[b] < 0 || lens[b] > Lmax) return PKV_EINVAL;
     pages[b] = ceil_div(lens[b], kPageSize);
-    total += pages[b];
   }
+  for (size_t gi = 0; gi < groups.size(); ++gi)
+    for (int m = 0; m < groups[gi].members; ++m) {
+      start[groups[gi].first + m] = groups[gi].k;
+      group_of[groups[gi].first + m] = static_cast<int>(gi);
+    }
+  // what the per-sequence items attend: own pages; members never packed
+  std::vector<int> own(batch), asc;
+  long long total = 0;
+  for (int b = 0; b < batch; ++b) {
+    own[b] = pages[b] - start[b];
+    total += own[b];
+    if (group_of[b] < 0) asc.push_back(own[b]);
+  }
+  std::sort(asc.begin(), asc.end());
+  auto count = [&](Sizes z) {
+    long long items = count_items(asc, z);
+    for (int b = 0; b < batch; ++b)
+      if (group_of[b] >= 0) items += (own[b] + z.range - 1) / z.range;
+    return items;
+  };
   const long long wave = static_cast<long long>(kResidentPerSm) * num_sms;  // CTAs
   const long long u0 = std::max<long long>(1, (total + 2LL * num_sms - 1) / (2LL * num_sms));
   const long long umax = std::max<long long>(u0, (max_blocks + kPlanWarps - 1) / kPlanWarps);
   long long lo = u0, hi = umax;  // smallest u in [u0, umax] that fits, else umax
   while (lo < hi) {
     const long long mid = (lo + hi) / 2;
-    if (count_items(pages, sizes_for(mid, max_blocks)) * kNumKvHeads <= wave) hi = mid;
+    if (count(sizes_for(mid, max_blocks)) * kNumKvHeads <= wave) hi = mid;
     else lo = mid + 1;
   }
   const Sizes z = sizes_for(lo, max_blocks);
   const int range = z.range;
   const int pack_max = z.pack_max;
 
+  // shared ranges per group: as many as keep the shared-prefix CTAs within
+  // one wave of two per SM, ranges of at least kMinRangePages pages
+  int ns_target = 1;
+  if (!groups.empty()) {
+    const long long per = static_cast<long long>(groups.size()) * kNumKvHeads;
+    ns_target = static_cast<int>(std::max<long long>(1, (2LL * num_sms) / per));
+  }
+  std::vector<int> shared_ranges(groups.size());
+  int shared_max = 0;  // pages of the longest shared range
+  for (size_t gi = 0; gi < groups.size(); ++gi) {
+    const int k = groups[gi].k;
+    int ns = std::max(1, std::min(ns_target, ceil_div(k, kMinRangePages)));
+    ns = std::max(ns, ceil_div(k, kMaxRangePages));  // the kernel's page list
+    shared_ranges[gi] = ns;
+    shared_max = std::max(shared_max, ceil_div(k, ns));
+  }
+
   std::vector<Range> ranges;
   std::vector<int> packed;
   std::vector<int32_t> merges;  // (b, first slot, ranges, 0) per split sequence
+  std::vector<int> slot_base(batch, -1);
   int slots = 0;
   for (int b = 0; b < batch; ++b) {
-    const int p = pages[b];
-    if (p <= pack_max) {
+    const int p = own[b];
+    const bool member = group_of[b] >= 0;
+    if (!member && p <= pack_max) {
       packed.push_back(b);
-    } else if (p <= range) {
+    } else if (!member && p <= range) {
       ranges.push_back({b, lens[b], 0, p, -1});
     } else {
+      const int ns = member ? shared_ranges[group_of[b]] : 0;
       const int nr = ceil_div(p, range);
       const int base = p / nr, extra = p % nr;
-      int begin = 0;
+      int begin = start[b];
       for (int r = 0; r < nr; ++r) {
         const int n = base + (r < extra ? 1 : 0);
-        ranges.push_back({b, lens[b], begin, n, slots + r});
+        ranges.push_back({b, lens[b], begin, n, slots + ns + r});
         begin += n;
       }
-      merges.insert(merges.end(), {b, slots, nr, 0});
-      slots += nr;
+      merges.insert(merges.end(), {b, slots, ns + nr, 0});
+      slot_base[b] = slots;
+      slots += ns + nr;
     }
   }
   std::stable_sort(packed.begin(), packed.end(),
@@ -144,9 +195,13 @@ int build_plan(const int32_t* lens, int batch, int max_blocks, int num_sms, int3
   });
   const size_t num_items = order.size();
   const size_t num_merges = merges.size() / kPlanMergeWords;
-  if (num_items > 65535) return PKV_EUNSUPPORTED;  // grid y limit
+  size_t num_shared = 0;
+  for (int ns : shared_ranges) num_shared += static_cast<size_t>(ns);
+  if (num_items > 65535 || num_shared > 65535) return PKV_EUNSUPPORTED;  // grid y limit
 
-  const size_t words = kPlanHeaderWords + num_items * kPlanItemWords + merges.size();
+  const size_t words = kPlanHeaderWords + num_items * kPlanItemWords + merges.size() +
+                       num_shared * kPlanSharedWords;
+  if (words * 4 > out_bytes) return PKV_EINVAL;
   memset(out, 0, words * 4);
   out[0] = static_cast<int32_t>(PKV_PLAN_MAGIC);
   out[1] = batch;
@@ -156,6 +211,8 @@ int build_plan(const int32_t* lens, int batch, int max_blocks, int num_sms, int3
   out[5] = slots;
   out[6] = range;
   out[7] = static_cast<int32_t>(words * 4);
+  out[8] = static_cast<int32_t>(num_shared);
+  out[9] = shared_max;
   int32_t* item = out + kPlanHeaderWords;
   for (const Item& o : order) {
     if (o.kind == kPlanKindRange) {
@@ -181,7 +238,85 @@ int build_plan(const int32_t* lens, int batch, int max_blocks, int num_sms, int3
     item += kPlanItemWords;
   }
   if (!merges.empty()) memcpy(item, merges.data(), merges.size() * 4);
+  item += merges.size();
+  // shared-prefix items: {members, p_begin, n, 0, seq[16], slot[16]}
+  for (size_t gi = 0; gi < groups.size(); ++gi) {
+    const SharedGroup& g = groups[gi];
+    const int ns = shared_ranges[gi];
+    const int base = g.k / ns, extra = g.k % ns;
+    int begin = 0;
+    for (int r = 0; r < ns; ++r) {
+      const int n = base + (r < extra ? 1 : 0);
+      item[0] = g.members;
+      item[1] = begin;
+      item[2] = n;
+      for (int m = 0; m < kSharedMembers; ++m) {
+        const bool has = m < g.members;
+        item[4 + m] = has ? g.first + m : -1;
+        item[4 + kSharedMembers + m] = has ? slot_base[g.first + m] + r : -1;
+      }
+      begin += n;
+      item += kPlanSharedWords;
+    }
+  }
   return PKV_OK;
+}
+
+int check_plan_args(const int32_t* lens, int batch, int max_blocks, int num_sms,
+                    const int32_t* out, size_t out_bytes) {
+  if (lens == nullptr || out == nullptr || batch < 1 || max_blocks < 1 || num_sms < 1)
+    return PKV_EINVAL;
+  if (reinterpret_cast<uintptr_t>(out) % 16 != 0) return PKV_EALIGN;
+  if (out_bytes < plan_bytes(batch, max_blocks)) return PKV_EINVAL;
+  return PKV_OK;
+}
+
+int build_plan(const int32_t* lens, int batch, int max_blocks, int num_sms, int32_t* out,
+               size_t out_bytes) {
+  const int rc = check_plan_args(lens, batch, max_blocks, num_sms, out, out_bytes);
+  if (rc != PKV_OK) return rc;
+  return build_core(lens, batch, max_blocks, num_sms, {}, out, out_bytes);
+}
+
+// Groups are found in batch order: a run starts at sequence s and takes the
+// next sequences while their tables agree with s's on at least the first
+// min_shared_pages entries (each a valid page id) and it has fewer than
+// kSharedMembers members; k is the shortest agreement, also kept below
+// every member's last page.  A run of one sequence is no group.
+int build_plan_shared(const int32_t* lens, const int32_t* block_tables, int batch,
+                      int max_blocks, int num_sms, int min_shared_pages, int32_t* out,
+                      size_t out_bytes) {
+  const int rc = check_plan_args(lens, batch, max_blocks, num_sms, out, out_bytes);
+  if (rc != PKV_OK) return rc;
+  if (block_tables == nullptr || min_shared_pages < 1) return PKV_EINVAL;
+  const long long Lmax = static_cast<long long>(max_blocks) * kPageSize;
+  std::vector<int> pages(batch);
+  for (int b = 0; b < batch; ++b) {
+    if (lens[b] < 0 || lens[b] > Lmax) return PKV_EINVAL;
+    pages[b] = ceil_div(lens[b], kPageSize);
+  }
+  auto row = [&](int b) { return block_tables + static_cast<size_t>(b) * max_blocks; };
+  std::vector<SharedGroup> groups;
+  int b = 0;
+  while (b < batch) {
+    int k = pages[b] - 1;  // the leader's last page stays its own
+    int e = b + 1;
+    while (e < batch && e - b < kSharedMembers) {
+      int c = std::min(k, pages[e] - 1);
+      int agree = 0;
+      while (agree < c && row(b)[agree] == row(e)[agree] && row(b)[agree] >= 0) ++agree;
+      if (agree < min_shared_pages) break;
+      k = agree;
+      ++e;
+    }
+    if (e - b >= 2 && k >= min_shared_pages) {
+      groups.push_back({b, e - b, k});
+      b = e;
+    } else {
+      ++b;
+    }
+  }
+  return build_core(lens, batch, max_blocks, num_sms, groups, out, out_bytes);
 }
 
 }  // namespace pkv

@@ -68,3 +68,107 @@ def test_prefix_full_size_sampled():
     seqs = np.array([0, 1, 15, 16, 130, 255])
     ref, _ = oracle_step(w, 0, seqs)
     assert_close(out[seqs], ref, "prefix 256 x 2048 sampled")
+
+
+# ------------------------------------------------ shared-prefix work plans --
+
+def planned(w, d, plan, fused_step=True, **kw):
+    b = binding()
+    bt = d["block_tables"][0]
+    if fused_step:
+        return b.decode_step_planned(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"], bt,
+                                     d["seq_lens"], plan, rope_theta=w.rope_theta, scale=w.scale,
+                                     **kw)
+    return b.paged_decode_attention_planned(d["q"][0], d["pool"], bt, d["seq_lens"], plan,
+                                            scale=w.scale, **kw)
+
+
+def test_shared_plan_matches_oracle_fused_and_unfused():
+    # 48 sequences in groups of 16 sharing 96 pages: the plan makes groups of 8
+    dev = cuda_or_skip()
+    b = binding()
+    w = synth.make_workload("prefix", 2, batch=48, num_pages=12000)
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, block_tables=w.block_tables[0])
+    assert plan.num_shared > 0
+    assert b.attention_kernels(w.batch, w.max_blocks, 0, plan).startswith(
+        "paged_decode_shared_kernel+")
+    ref, c = oracle_step(w, 0)
+    outs = []
+    for fused_step in (True, False):
+        d = synth.device_inputs(w, dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        if not fused_step:
+            binding().kv_append(d["k_new"][0], d["v_new"][0], d["pool"], d["block_tables"][0],
+                                d["positions"], rope_theta=w.rope_theta, dev_err=err)
+        out = synth.bits(planned(w, d, plan, fused_step, dev_err=err))
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_close(out, ref, f"shared plan, fused={fused_step}")
+        outs.append(out)
+    assert np.array_equal(outs[0], outs[1])
+    # repeated calls give the same bits
+    d = synth.device_inputs(w, dev)
+    again = [synth.bits(planned(w, d, plan)) for _ in range(3)]
+    assert all(np.array_equal(x, outs[0]) for x in again)
+
+
+def test_shared_plan_full_size_sampled():
+    # the prefix workload itself: 256 x 2048, 16-way shared 1536-token prefixes
+    dev = cuda_or_skip()
+    b = binding()
+    w = synth.make_workload("prefix", 0)
+    d = synth.device_inputs(w, dev)
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, block_tables=w.block_tables[0])
+    assert plan.num_shared > 0
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = synth.bits(planned(w, d, plan, dev_err=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    seqs = np.array([0, 1, 7, 8, 15, 16, 130, 255])
+    ref, _ = oracle_step(w, 0, seqs)
+    assert_close(out[seqs], ref, "prefix 256 x 2048 under a shared plan, sampled")
+
+
+def test_shared_plan_ragged_groups():
+    # groups of different sizes and prefix lengths, sequences in no group,
+    # short own tails: every output against the oracle, fused
+    import oracle
+    from _gpu_util import bf16_normal
+    dev = cuda_or_skip()
+    b = binding()
+    rng = np.random.default_rng(5)
+    lens, rows, nxt = [], [], 0
+    for size, k in [(3, 20), (1, 0), (8, 40), (2, 16), (5, 17), (1, 0)]:
+        common = list(range(nxt, nxt + k))
+        nxt += k
+        for _ in range(size):
+            o = int(rng.integers(1, 30))
+            rows.append(common + list(range(nxt, nxt + o)))
+            nxt += o
+            lens.append(16 * (k + o) - int(rng.integers(0, 16)))
+    lens = np.asarray(lens, np.int32)
+    B = len(lens)
+    perm = rng.permutation(nxt + 32).astype(np.int32)
+    bt = np.full((B, 128), -1, np.int32)
+    for i, r in enumerate(rows):
+        bt[i, :len(r)] = perm[r]
+    pool = bf16_normal(rng, (nxt + 32, 2, 16, 8, 64))
+    q = bf16_normal(rng, (B, 32, 64))
+    kn = bf16_normal(rng, (B, 8, 64))
+    vn = bf16_normal(rng, (B, 8, 64))
+    ref_pool = pool.copy()
+    assert oracle.kv_append(kn, vn, ref_pool, bt, lens - 1) == 0
+    ref = oracle.decode_attention(q, ref_pool, bt, lens)
+    u16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    plan = b.Plan(lens, 128, device=dev, block_tables=bt)
+    assert plan.num_shared > 0
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    dpool = u16(pool)
+    out = b.decode_step_planned(u16(q), u16(kn), u16(vn), dpool, torch.from_numpy(bt).to(dev),
+                                torch.from_numpy(lens).to(dev), plan, dev_err=err)
+    got = synth.bits(out)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(got, ref, "ragged shared groups")
+    assert np.array_equal(synth.bits(dpool), ref_pool)    # appended slots, nothing else

@@ -78,7 +78,8 @@ def test_every_page_once_and_merges_consistent(lens):
     assert plan.workspace_bytes == plan.num_slots * 32 * 66 * 4
     for it in plan.items():                        # words 12..15 are reserved zeros
         assert not it[12:].any()
-    assert plan.bytes_used == 4 * (8 + 16 * plan.num_items + 4 * plan.num_merges)
+    assert plan.num_shared == 0
+    assert plan.bytes_used == 4 * (12 + 16 * plan.num_items + 4 * plan.num_merges)
 
 
 def expected_sizes(lens, sms, max_blocks=128):
@@ -233,3 +234,90 @@ def test_plan_built_into_a_caller_buffer_is_the_same_plan():
         B.Plan(lens, 128, num_sms=SMS, out=raw[off + 1:])
     with pytest.raises(ValueError):                 # wrong type
         B.Plan(lens, 128, num_sms=SMS, out=raw[off:].view(np.float32))
+
+
+# ------------------------------------------- shared prefixes (pkv_plan_build_shared) --
+
+def shared_case(seed, groups, own, mb=128):
+    """Consecutive groups of sequences whose tables start with the same pages:
+    groups = [(size, shared pages)], own = each sequence's own pages count
+    range; returns lens, tables."""
+    rng = np.random.default_rng(seed)
+    lens, rows, nxt = [], [], 0
+    for size, k in groups:
+        common = list(range(nxt, nxt + k))
+        nxt += k
+        for _ in range(size):
+            o = int(rng.integers(own[0], own[1] + 1))
+            row = common + list(range(nxt, nxt + o))
+            nxt += o
+            lens.append(16 * (k + o) - int(rng.integers(0, 16)))
+            rows.append(row + [-1] * (mb - len(row)))
+    return np.asarray(lens, np.int32), np.asarray(rows, np.int32)
+
+
+def shared_coverage(plan, lens, bt):
+    pieces, slots = coverage(plan, lens)
+    for it in plan.shared().tolist():
+        members, p0, n = it[0], it[1], it[2]
+        seqs, sl = it[4:4 + members], it[20:20 + members]
+        assert 2 <= members <= 16 and all(x == -1 for x in it[4 + members:20])
+        assert seqs == list(range(seqs[0], seqs[0] + members))       # consecutive
+        for m, (b, slot) in enumerate(zip(seqs, sl)):
+            assert np.array_equal(bt[b, p0:p0 + n], bt[seqs[0], p0:p0 + n])
+            assert p0 + n <= -(-int(lens[b]) // 16) - 1                # never the last page
+            assert slot not in slots
+            slots[slot] = (b, p0)
+            pieces[b].append((p0, n))
+    return pieces, slots
+
+
+@pytest.mark.parametrize("seed,groups,own", [
+    (0, [(16, 96)] * 4, (32, 32)),            # the prefix workload's shape
+    (1, [(3, 20), (1, 5), (8, 40), (2, 16)], (1, 60)),
+    (2, [(5, 1000)], (1, 3)),                 # long prefixes: several shared ranges
+])
+def test_shared_plan_covers_every_page_once(seed, groups, own):
+    mb = 2048 if seed == 2 else 128
+    lens, bt = shared_case(seed, groups, own, mb)
+    plan = B.Plan(lens, mb, num_sms=SMS, block_tables=bt, min_shared_pages=16)
+    assert plan.num_shared > 0
+    pieces, slots = shared_coverage(plan, lens, bt)
+    for b, L in enumerate(lens.tolist()):
+        covered = []
+        for p0, n in sorted(pieces[b]):
+            covered += list(range(p0, p0 + n))
+        assert covered == list(range(-(-L // 16))), b
+    merged = {}
+    for b, first, nr, zero in plan.merges().tolist():
+        assert zero == 0 and b not in merged
+        merged[b] = [slots[first + r] for r in range(nr)]
+        assert all(x[0] == b for x in merged[b])
+        assert [x[1] for x in merged[b]] == sorted(x[1] for x in merged[b])
+    members = {int(x) for it in plan.shared() for x in it[4:4 + it[0]]}
+    assert members <= set(merged)                  # every member is merged
+    assert plan.num_slots == len(slots)
+    assert plan.bytes_used == 4 * (12 + 16 * plan.num_items + 4 * plan.num_merges
+                                   + 36 * plan.num_shared)
+    assert plan.shared_pages == max(int(n) for n in plan.shared()[:, 2])
+
+
+def test_shared_groups_follow_the_rule():
+    lens, bt = shared_case(3, [(20, 30), (2, 10), (3, 17)], (2, 5))
+    plan = B.Plan(lens, 128, num_sms=SMS, block_tables=bt, min_shared_pages=16)
+    sh = plan.shared()
+    firsts = sorted({(int(it[4]), int(it[0])) for it in sh})
+    # 20 sharing 30 pages: groups of 16 and 4; 2 sharing 10 < 16 pages: none;
+    # 3 sharing 17: one group
+    assert firsts == [(0, 16), (16, 4), (22, 3)]
+    ends = sorted(int(it[1]) + int(it[2]) for it in sh if it[4] == 22)
+    assert ends[-1] == 17 and int(min(it[1] for it in sh if it[4] == 22)) == 0
+
+
+def test_without_tables_or_sharing_the_plan_is_the_plain_one():
+    lens = np.random.default_rng(4).integers(1, 2049, 60).astype(np.int32)
+    bt = np.arange(60 * 128, dtype=np.int32).reshape(60, 128)     # nothing shared
+    a = B.Plan(lens, 128, num_sms=SMS)
+    b = B.Plan(lens, 128, num_sms=SMS, block_tables=bt)
+    assert a.num_shared == b.num_shared == 0
+    assert np.array_equal(a.host, b.host)
