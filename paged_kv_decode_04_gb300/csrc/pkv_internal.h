@@ -35,8 +35,10 @@ constexpr int kPlanWarps = 4;       // warps per attention CTA: one packed seque
 // Shared-prefix items (a plan's last section): one CTA per (item, kv head)
 // attends pages [p_begin, p_begin + n) that the item's members' tables all
 // hold, warp w for members 2w and 2w + 1: {members, p_begin, n, 0, seq[16],
-// slot[16]}.
+// slot[16]}.  The planner sizes their ranges for one wave of
+// kSharedCtasPerSm CTAs per SM.
 constexpr int kSharedMembers = 16;
+constexpr int kSharedCtasPerSm = 3;
 constexpr int kPlanSharedWords = 4 + 2 * kSharedMembers;
 
 // Host side of the work plans (planner.cpp): an upper bound on a plan's

@@ -90,7 +90,7 @@ struct SharedGroup {
 // With shared groups, a member attends only its own pages [k, pages) in
 // range items (never packed) and every range writes a partial; the group's
 // pages [0, k) become shared-prefix items (ns near-equal ranges per group,
-// ns the most that keeps these CTAs within one wave of two per SM) whose CTAs write one
+// ns the most that keeps these CTAs within one wave of three per SM) whose CTAs write one
 // partial per member; each member's partials sit in consecutive slots,
 // shared ranges first, and one merge entry combines them.
 int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
@@ -135,11 +135,12 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
   const int pack_max = z.pack_max;
 
   // shared ranges per group: as many as keep the shared-prefix CTAs within
-  // one wave of two per SM, ranges of at least kMinRangePages pages
+  // one wave of kSharedCtasPerSm per SM, ranges of at least kMinRangePages pages
   int ns_target = 1;
   if (!groups.empty()) {
     const long long per = static_cast<long long>(groups.size()) * kNumKvHeads;
-    ns_target = static_cast<int>(std::max<long long>(1, (2LL * num_sms) / per));
+    ns_target = static_cast<int>(
+        std::max<long long>(1, (static_cast<long long>(kSharedCtasPerSm) * num_sms) / per));
   }
   std::vector<int> shared_ranges(groups.size());
   int shared_max = 0;  // pages of the longest shared range
