@@ -1,5 +1,6 @@
 // decode_shared.cu -- paged decode attention over pages that a group of
-// sequences shares (a common prompt prefix), each page read once per group.
+// sequences shares (a common prompt prefix), each page read once per group,
+// on the fifth-generation tensor cores (tcgen05, accumulators in TMEM).
 //
 // Tiny-vLLM README ("Hours of YouTube and 85 handtyped pages of notes on LLM
 // Inference - Start here"), section "これまでの進捗": attention streams each
@@ -10,18 +11,53 @@
 // A host work plan (planner.cpp, pkv_plan_build_shared) finds runs of
 // consecutive sequences whose block tables start with the same pages and
 // emits shared-prefix items: pages [p_begin, p_begin + n) common to up to 16
-// members.  One CTA per (item, kv head g): warp w holds the 4 query rows of
-// head g of members 2w and 2w + 1 as the 8 columns of its tensor-core tiles
-// (the per-page math computes 8 query rows anyway; a group of 4 rows uses
-// half of them).  The CTA streams head g's 4 KiB tile of each page once into
-// a shared ring (the last warp done with a stage refills it, as in the
-// whole-page kernel), and every warp folds that tile into its two members'
-// online-softmax states.  Each warp then writes its members' unnormalised
-// (max, sum, acc) partials to the slots the plan gives them; the members' own
-// pages are attended by the ordinary planned kernels into the following
-// slots, and the merge kernel combines them.  A shared page is never a
-// member's last page, so every shared page is full and none takes the
-// step's append.
+// members.  One CTA per (item, kv head g).  The members' 4 query rows of head
+// g stack into 64 rows, so a batch of 4 pages (64 tokens) is two small dense
+// contractions, run by tcgen05.mma with M = 128 and the A operand in TMEM:
+//
+//   S = Q K^T   (128 x 64 tokens, K = 64 head dims: 4 MMAs; Q in TMEM, the
+//                batch's K rows in shared memory)
+//   O += P V    (128 x 64 dims, K = 16 tokens per MMA: 2 per page, P as hi
+//                and lo bf16 terms in TMEM, V rows in shared memory)
+//
+// With N = 64 an MMA whose A operand came from shared memory would spend most
+// of its time re-reading A; from TMEM only B is read.
+//
+// Rows 0..63 and 64..127 hold the same 64 query rows.  The two copies split
+// each batch's tokens: a row of the upper half weighs pages 0, 1 of the
+// batch, its copy in the lower half pages 2, 3 (its P is zero elsewhere),
+// each with its own online-softmax state and O row; the two are combined at
+// the end like two split-K partials.  So all four softmax warps work (TMEM
+// lane 32w + i belongs to warp w), on 32 scores each.
+//
+// TMEM (256 columns): X0 = 0..63 and X1 = 64..127 take S_b for batches
+// b = 0, 1 mod 2 and then, written over it by the softmax, P_b (hi for page p
+// in columns 8p..8p+7, lo in 32 + 8p..); O = 128..191; Q = 192..223.
+//
+// Roles (8 warps; one thread of each of warps 4..7 works):
+//   warp 6: K producer.  Per batch, head g's K rows of its 4 pages into one
+//     8 KiB region (64 rows: the N = 64 K-major B operand of S), in a ring of
+//     6 regions freed as soon as the batch's S has been computed.
+//   warp 7: V producer.  The V rows likewise into a ring of 6 regions (four
+//     MN-major B operands of PV), freed once the batch's PV is done.  Both
+//     128B-swizzled by TMA, which is the operand layout the MMA reads.
+//   warp 5: issues S_b = Q K_b^T into X(b mod 2) once K_b has landed and
+//     PV_{b-2} (which read P_{b-2} from there) is done.
+//   warp 4: allocates the TMEM and issues PV_j once P_j is written and V_j
+//     has landed.
+//   warps 0..3: the softmax, thread = TMEM lane = MMA row.  Per batch: wait
+//     for S_j, read the row's 32 scores, take the FP32 online-softmax step (a
+//     lazily updated reference maximum), and write P_j as hi = bf16(p) and
+//     lo = bf16(p - hi) (about 16 significant bits together) over S_j.  Only
+//     when the maximum moves does the row wait for PV_{j-1} and rescale its O
+//     row in TMEM.  At the end each query row's (max, sum, acc) partial,
+//     unnormalised, goes to the slot the plan gives its member; the members'
+//     own pages are attended by the ordinary planned kernels into the
+//     following slots, and the merge kernel combines them.
+// A shared page is never a member's last page, so every shared page is full
+// and none takes the step's append.  Every wait is bounded (kWaitLimitNs):
+// past it the kernel records PKV_DEVERR_TIMEOUT, lets outstanding copies and
+// MMAs finish (bounded too), frees its TMEM and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -37,55 +73,111 @@ namespace pkv {
 
 namespace {
 
-constexpr int kShWarps = kSharedMembers / 2;  // warp w <-> members 2w, 2w + 1
-constexpr int kShRows = 2 * kGroup;            // query rows per warp
-constexpr int kShThreads = kShWarps * 32;
-// Eight 4 KiB tiles in the ring (32 KiB per CTA).  Three CTAs per SM (78
-// registers) against two (88): 79.3 -> 75.9 us per step on 256 x 2048
-// tokens with 16-way shared 1536-token prefixes; the kernel is bound by its
-// per-page math, so more resident warps help.
-constexpr int kShStages = 8;
-constexpr int kShCtasPerSm = kSharedCtasPerSm;
-constexpr int kShRingBytes = kShStages * kTileBytes;
-constexpr int kShMaxPages = 1024;
+constexpr int kTcRows = kSharedMembers * kGroup;  // 64 query rows
+constexpr int kTcM = 2 * kTcRows;                 // MMA rows: two copies
+constexpr int kTcBatch = 4;                       // pages per S / P batch
+constexpr int kTcCols = kTcBatch * kPageSize;     // 64 score columns per S
+constexpr int kTcHalfCols = kTcCols / 2;          // a row's share of them
+constexpr int kKSlots = 6;                        // K regions in flight
+constexpr int kVSlots = 6;                        // V regions in flight
+constexpr int kTcSoftmaxWarps = 4;
+constexpr int kPvWarp = 4;
+constexpr int kSWarp = 5;
+constexpr int kKLoadWarp = 6;
+constexpr int kVLoadWarp = 7;
+constexpr int kTcThreads = 32 * (kTcSoftmaxWarps + 4);
+constexpr int kTcCtasPerSm = kSharedCtasPerSm;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemO = 2 * kTcCols;           // X0: 0, X1: 64, O: 128
+constexpr uint32_t kTmemQ = kTmemO + kHeadDim;     // Q: 192 (32 columns)
+constexpr uint32_t kPLo = kTcHalfCols;             // P lo terms: X + 32
+constexpr int kMaxPagesPerItem = 1024;
 
-static_assert(kShWarps * (2 * kShRows + kShRows * kHeadDim) * 4 <= kShRingBytes,
-              "end-of-CTA scratch must fit in the ring");
+// Shared memory, from a 1024-byte aligned base.
+constexpr int kHalfTileBytes = kPageSize * kRowBytes;    // 2 KiB: one head's K (or V) rows
+constexpr int kRegionBytes = kTcBatch * kHalfTileBytes;  // 8 KiB: a batch's K (or V) rows
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kKSlots * kRegionBytes;
+constexpr int kOffBars = kOffV + kVSlots * kRegionBytes;
+// k_full[6], k_empty[6], v_full[6], v_empty[6], s_ready[2], x_free[2],
+// p_ready, pv_done, s_fin, pv_fin, q_ready
+constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 9;
+constexpr int kPrefetchBatches = 2;  // pulled into L2 before the grid dependency wait
+constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
+constexpr int kOffPages = kOffTmemSlot + 16;
+
+static_assert(kTcM == 128 && 32 * kTcSoftmaxWarps == kTcM, "one softmax thread per TMEM lane");
+static_assert(kTmemQ + kHeadDim / 2 <= kTmemCols, "X0, X1, O and Q fit the allocation");
+static_assert(kTcRows * (kHeadDim + 2) * 4 <= kKSlots * kRegionBytes, "end-of-CTA exchange fits");
+// Shared memory alone keeps more than kTcCtasPerSm CTAs of this kernel off
+// one SM (228 KiB per SM, 1 KiB reserved per CTA), so their TMEM
+// allocations always fit the 512 columns and tcgen05.alloc never waits.
+static_assert((kTcCtasPerSm + 1) * (kOffPages + 1024 + 1024) > 228 * 1024,
+              "at most kTcCtasPerSm CTAs per SM");
+static_assert(kTcCtasPerSm * kTmemCols <= 512, "TMEM columns of the resident CTAs");
+static_assert(kTcCtasPerSm * (kOffPages + 1024 + 1024 + 4 * 64) <= 228 * 1024,
+              "kTcCtasPerSm CTAs per SM fit for ranges of up to 64 pages");
+
+constexpr uint32_t kIdescS = tc_idesc_bf16(kTcM, kTcCols, false);   // K: K-major
+constexpr uint32_t kIdescPV = tc_idesc_bf16(kTcM, kHeadDim, true);  // V: MN-major
 
 __host__ __device__ constexpr size_t sh_smem_bytes(int pages) {
-  return 1024 /* alignment slack */ + kShRingBytes + 8 * kShStages /* bars */ +
-         4 * kShStages /* counters */ + static_cast<size_t>(pages) * 4;
+  return 1024 /* alignment slack */ + kOffPages + static_cast<size_t>(pages) * 4;
 }
 
-// Q^T of two members as the B operand of S^T = K Q^T: columns 0..3 are
-// member a's 4 rows, 4..7 member b's (qa / qb: their [4][64] bf16 rows, or
-// nullptr for zeros).
-__device__ __forceinline__ void load_q_frags_pair(const uint16_t* qa, const uint16_t* qb,
-                                                  const LaneGeom& G, uint32_t (&f)[4][2]) {
-  const uint16_t* base = G.fg < kGroup ? qa : qb;
-  const uint32_t* qw =
-      base != nullptr ? reinterpret_cast<const uint32_t*>(base + (G.fg & 3) * kHeadDim) : nullptr;
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    f[kk][0] = qw != nullptr ? qw[kk * 8 + G.ft] : 0u;
-    f[kk][1] = qw != nullptr ? qw[kk * 8 + 4 + G.ft] : 0u;
+// Before the grid dependency wait: pull the first kPrefetchBatches batches'
+// K and V rows into L2.  The plan item and the leader's table entries read
+// here may still be being written by the previous grid, so they serve only
+// as prefetch addresses (L1-bypassing loads, every index range-checked,
+// nothing recorded); the kernel reads all of it again after the wait.
+__device__ __forceinline__ void prefetch_first_batches(const CUtensorMap* map, const AttnArgs& a,
+                                                       int g, int tid) {
+  constexpr int kPages = kPrefetchBatches * kTcBatch;
+  if (tid >= 2 * kPages) return;
+  const int4* itp = a.plan_shared + static_cast<int64_t>(blockIdx.y) * (kPlanSharedWords / 4);
+  const int4 head = ld_cg(itp);      // members, p_begin, n, 0
+  const int leader = ld_cg(itp + 1).x;
+  const int i = tid >> 1;            // page of the range; even tid: K rows, odd: V rows
+  if (i < head.z && leader >= 0 && leader < a.batch && head.y >= 0 && head.y + i < a.max_blocks) {
+    const int pid = ld_cg(a.block_table + static_cast<int64_t>(leader) * a.max_blocks + head.y + i);
+    if (pid >= 0 && pid < a.num_pages)
+      tma_prefetch_l2_3d(map, g * kHeadDim, (tid & 1) ? kPageSize : 0, pid);
   }
 }
 
-__global__ void __launch_bounds__(kShThreads, kShCtasPerSm)
-    paged_decode_shared_kernel(const __grid_constant__ CUtensorMap pool_map, const AttnArgs a) {
+// Named barrier of the softmax warps (id 1; 0 is __syncthreads).
+__device__ __forceinline__ void softmax_warps_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kTcSoftmaxWarps) : "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
+    paged_decode_shared_kernel(const __grid_constant__ CUtensorMap half_map, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kShRingBytes);
-  int32_t* done = reinterpret_cast<int32_t*>(full + kShStages);  // warps finished per stage
-  int32_t* s_pages = done + kShStages;
+  const uint32_t sb = smem_addr(smem);
+  const uint32_t bars = sb + kOffBars;
+  auto k_full = [&](int b) { return bars + 8u * (b % kKSlots); };
+  auto k_empty = [&](int b) { return bars + 8u * (kKSlots + b % kKSlots); };
+  auto v_full = [&](int b) { return bars + 8u * (2 * kKSlots + b % kVSlots); };
+  auto v_empty = [&](int b) { return bars + 8u * (2 * kKSlots + kVSlots + b % kVSlots); };
+  const uint32_t bars2 = bars + 8u * (2 * kKSlots + 2 * kVSlots);
+  auto s_ready = [&](int b) { return bars2 + 8u * (b & 1); };
+  auto x_free = [&](int b) { return bars2 + 16u + 8u * (b & 1); };
+  const uint32_t p_ready = bars2 + 32u;
+  const uint32_t pv_done = bars2 + 40u;
+  const uint32_t s_fin = bars2 + 48u;
+  const uint32_t pv_fin = bars2 + 56u;
+  const uint32_t q_ready = bars2 + 64u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+  int32_t* s_pages = reinterpret_cast<int32_t*>(smem + kOffPages);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int warp = tid >> 5;  // this warp's members: 2 warp, 2 warp + 1
-  const int g = blockIdx.x;   // kv head
-  if (tid == 0) tma_prefetch_desc(&pool_map);
+  const int warp = tid >> 5;
+  const int g = blockIdx.x;  // kv head
+  if (tid == 0) tma_prefetch_desc(&half_map);
+  prefetch_first_batches(&half_map, a, g, tid);
   wait_for_prior_grids();
   allow_dependent_grids();
 
@@ -94,16 +186,10 @@ __global__ void __launch_bounds__(kShThreads, kShCtasPerSm)
                       static_cast<int64_t>(blockIdx.y) * kPlanSharedWords;
   const int members = it[0], p_begin = it[1], n = it[2];
   const int leader = it[4];
-  int mseq[2], mslot[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int m = 2 * warp + h;
-    mseq[h] = m < members ? it[4 + m] : -1;
-    mslot[h] = m < members ? it[4 + kSharedMembers + m] : -1;
-  }
+  const int nb = (n + kTcBatch - 1) / kTcBatch;
 
   // page ids: the leader's table (every member's holds the same ones here)
-  for (int i = tid; i < n; i += kShThreads) {
+  for (int i = tid; i < n; i += kTcThreads) {
     int32_t pid = a.block_table[static_cast<int64_t>(leader) * a.max_blocks + p_begin + i];
     if (pid < 0 || pid >= a.num_pages) {
       record_error(a.dev_err, kErrPage);
@@ -111,114 +197,323 @@ __global__ void __launch_bounds__(kShThreads, kShCtasPerSm)
     }
     s_pages[i] = pid;
   }
-  const uint32_t bar0 = smem_addr(full);
-  const uint32_t ring0 = smem_addr(smem);
+  // Q rows into registers now, into TMEM once it is allocated: MMA row L
+  // holds query row (L mod 64) = 4 m + i, query row i of head g of member m
+  // (absent members: zeros), 64 dims as 32 packed columns
+  uint32_t qw[2][16];
+  if (warp < kTcSoftmaxWarps) {
+    const int qr = tid & (kTcRows - 1), m = qr >> 2;
+    const uint4* src = m < members
+                           ? reinterpret_cast<const uint4*>(
+                                 a.q + (static_cast<int64_t>(it[4 + m]) * kNumQHeads + g * kGroup +
+                                        (qr & 3)) * kHeadDim)
+                           : nullptr;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = src != nullptr ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      qw[c >> 2][4 * (c & 3) + 0] = v.x;
+      qw[c >> 2][4 * (c & 3) + 1] = v.y;
+      qw[c >> 2][4 * (c & 3) + 2] = v.z;
+      qw[c >> 2][4 * (c & 3) + 3] = v.w;
+    }
+  }
   if (tid == 0) {
-    for (int s = 0; s < kShStages; ++s) {
-      mbar_init(bar0 + 8 * s, 1);
-      done[s] = 0;
+    for (int i = 0; i < kNumBars; ++i) {
+      const uint32_t bar = bars + 8u * i;  // the softmax rows arrive on two
+      mbar_init(bar, (bar == p_ready || bar == q_ready) ? kTcM : 1);
     }
     fence_barrier_init();
   }
-  __syncthreads();
-
-  const uint64_t policy = l2_policy_evict_first();
-  auto issue = [&](int k) {  // one thread
-    const int st = k % kShStages;
-    const int pid = s_pages[k];
-    const uint32_t bar = bar0 + 8 * st;
-    if (pid >= 0) {
-      mbar_arrive_expect_tx(bar, kTileBytes);
-      tma_load_3d(ring0 + st * kTileBytes, &pool_map, bar, g * kHeadDim, 0, pid, policy);
-    } else {
-      mbar_arrive(bar);  // keep the stage's phase sequence in step
-    }
-  };
-  if (tid == 0)
-    for (int k = 0; k < kShStages && k < n; ++k) issue(k);
-
-  const LaneGeom G(lane);
-  uint32_t qb[4][2];
-  auto qrows = [&](int seq) {
-    return seq >= 0 ? a.q + (static_cast<int64_t>(seq) * kNumQHeads + g * kGroup) * kHeadDim
-                    : nullptr;
-  };
-  load_q_frags_pair(qrows(mseq[0]), qrows(mseq[1]), G, qb);
-  const float c = a.scale_log2;
-
-  AttnState S;
-  S.reset();
-  for (int k = 0; k < n; ++k) {
-    const int st = k % kShStages;
-    const bool ready = mbar_wait_bounded(bar0 + 8 * st, (k / kShStages) & 1);
-    if (!__all_sync(kFullMask, ready)) {
-      // stop; the copies this CTA issued are still to be drained (below)
-      if (lane == 0) record_error(a.dev_err, kErrTimeout);
-      break;
-    }
-    if (mseq[0] >= 0 && s_pages[k] >= 0)
-      attend_page(ring0 + st * kTileBytes, kPageSize, qb, c, G, lane, S);
+  if (warp == kPvWarp) {
     __syncwarp();
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  if (warp < kTcSoftmaxWarps) {
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    tmem_st16(t_lane + kTmemQ, qw[0]);
+    tmem_st16(t_lane + kTmemQ + 16, qw[1]);
+    tmem_wait_st();
+    tc_fence_before_sync();
+    mbar_arrive(q_ready);  // S_0 may read Q
+  }
+
+  auto page_live = [&](int k) { return k < n && s_pages[k] >= 0; };
+  auto batch_live = [&](int b) {
+    int live = 0;
+    for (int p = 0; p < kTcBatch; ++p) live += page_live(b * kTcBatch + p) ? 1 : 0;
+    return live;
+  };
+  int issued = 0;  // batches whose copies this producer issued
+
+  if (warp == kKLoadWarp || warp == kVLoadWarp) {
+    // ----------------------------------------------------- TMA producers
     if (lane == 0) {
-      // release the stage; the last of the warps refills it
-      __threadfence_block();
-      if (atomicAdd(done + st, 1) == kShWarps - 1) {
-        done[st] = 0;
-        __threadfence_block();
-        if (k + kShStages < n) {
-          fence_proxy_async_smem();
-          issue(k + kShStages);
+      const bool is_k = warp == kKLoadWarp;
+      const int slots = is_k ? kKSlots : kVSlots;
+      const uint64_t policy = l2_policy_evict_first();
+      for (int b = 0; b < nb; ++b) {
+        const uint32_t empty = is_k ? k_empty(b) : v_empty(b);
+        const uint32_t full = is_k ? k_full(b) : v_full(b);
+        if (b >= slots && !mbar_wait_bounded(empty, ((b / slots) - 1) & 1)) {
+          record_error(a.dev_err, kErrTimeout);
+          break;
         }
+        const int live = batch_live(b);
+        if (live > 0)
+          mbar_arrive_expect_tx(full, live * kHalfTileBytes);
+        else
+          mbar_arrive(full);
+        const uint32_t region =
+            sb + (is_k ? kOffK + (b % kKSlots) * kRegionBytes : kOffV + (b % kVSlots) * kRegionBytes);
+        for (int p = 0; p < kTcBatch; ++p) {
+          const int k = b * kTcBatch + p;
+          if (page_live(k))
+            tma_load_3d(region + p * kHalfTileBytes, &half_map, full, g * kHeadDim,
+                        is_k ? 0 : kPageSize, s_pages[k], policy);
+        }
+        issued = b + 1;
       }
     }
+  } else if (warp == kSWarp) {
+    // -------------------------------------------- S = Q K^T, 64 tokens
+    if (lane == 0) {
+      bool ok = mbar_wait_bounded(q_ready, 0);
+      tc_fence_after_sync();
+      for (int b = 0; b < nb && ok; ++b) {
+        if (b >= 2) {  // PV_{b-2} has read P_{b-2} out of X(b mod 2)
+          if (!mbar_wait_bounded(x_free(b), ((b - 2) >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+        }
+        if (!mbar_wait_bounded(k_full(b), (b / kKSlots) & 1)) {
+          ok = false;
+          break;
+        }
+        if (batch_live(b) > 0) {  // else the softmax masks every column
+          const uint32_t kr = sb + kOffK + (b % kKSlots) * kRegionBytes;
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            tc_mma_bf16_ta(tmem + (b & 1) * kTcCols, tmem + kTmemQ + 8 * kk,
+                           sw128_desc(kr + 32 * kk), kIdescS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_ready(b));
+        tc_commit(k_empty(b));  // the K region may be refilled
+      }
+      if (!ok) record_error(a.dev_err, kErrTimeout);
+      tc_commit(s_fin);
+      if (!mbar_wait_bounded(s_fin, 0)) record_error(a.dev_err, kErrTimeout);
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------- O += P V
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t o_init = 0;
+      for (int j = 0; j < nb; ++j) {
+        if (!mbar_wait_bounded(p_ready, j & 1) || !mbar_wait_bounded(v_full(j), (j / kVSlots) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t vr = sb + kOffV + (j % kVSlots) * kRegionBytes;
+        const uint32_t x = tmem + (j & 1) * kTcCols;
+        for (int p = 0; p < kTcBatch; ++p) {
+          if (!page_live(j * kTcBatch + p)) continue;
+          const uint64_t v_op = sw128_desc(vr + p * kHalfTileBytes);
+          tc_mma_bf16_ta(tmem + kTmemO, x + 8 * p, v_op, kIdescPV, o_init);
+          o_init = 1;
+          tc_mma_bf16_ta(tmem + kTmemO, x + kPLo + 8 * p, v_op, kIdescPV, 1u);
+        }
+        tc_commit(pv_done);     // O holds batches 0..j
+        tc_commit(x_free(j));   // X(j mod 2) may take S_{j+2}
+        tc_commit(v_empty(j));  // the V region may be refilled
+      }
+      if (!ok) record_error(a.dev_err, kErrTimeout);
+      tc_commit(pv_fin);
+      if (!mbar_wait_bounded(pv_fin, 0)) record_error(a.dev_err, kErrTimeout);
+    }
+  } else {
+    // --------------------------------------------------------- softmax
+    const int L = tid;          // TMEM lane = MMA row
+    const int h = L / kTcRows;  // 0: pages 0, 1 of each batch; 1: pages 2, 3
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float c = a.scale_log2;
+    float m_ref = -INFINITY, l_run = 0.f;
+    bool o_live = false;  // a PV MMA has been issued (O initialised)
+    bool ok = true;
+    const uint32_t zero16[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    for (int j = 0; j < nb; ++j) {
+      const bool ready = mbar_wait_bounded(s_ready(j), (j >> 1) & 1);
+      if (!__all_sync(kFullMask, ready)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t x = t_lane + (j & 1) * kTcCols;
+      uint32_t sr[2][16];  // this row's 32 scores: pages 2h, 2h + 1
+      tmem_ld16(x + h * kTcHalfCols, sr[0]);
+      tmem_ld16(x + h * kTcHalfCols + 16, sr[1]);
+      tmem_wait_ld();
+      reg_after_wait(sr[0]);
+      reg_after_wait(sr[1]);
+      bool live[2], any_live = false;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) live[q] = page_live(j * kTcBatch + 2 * h + q);
+#pragma unroll
+      for (int p = 0; p < kTcBatch; ++p) any_live = any_live || page_live(j * kTcBatch + p);
+      // row maximum as a tree (independent chains)
+      float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        if (live[q])
+#pragma unroll
+          for (int t = 0; t < kPageSize; ++t)
+            mxs[t & 3] = fmaxf(mxs[t & 3], __uint_as_float(sr[q][t]));
+      const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * c;
+      // (branch-free: the TMEM accesses below are warp-collective)
+      const bool grow = mx > m_ref + kRescaleLog2;
+      const float m_new = grow ? fmaxf(m_ref, mx) : m_ref;
+      const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;  // 0 on the first live page
+      m_ref = m_new;
+      // P = 2^(s c - m_ref) as hi + lo bf16 terms; word w of page q packs
+      // tokens 2w, 2w + 1
+      uint32_t hi[16], lo[16];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          float x0 = 0.f, x1 = 0.f;
+          if (live[q]) {
+            x0 = fast_exp2(fmaf(__uint_as_float(sr[q][2 * w]), c, -m_ref));
+            x1 = fast_exp2(fmaf(__uint_as_float(sr[q][2 * w + 1]), c, -m_ref));
+          }
+          ls[w & 3] += x0 + x1;
+          const uint32_t hw = pack_bf16x2(x0, x1);
+          hi[8 * q + w] = hw;
+          lo[8 * q + w] = pack_bf16x2(x0 - __uint_as_float(hw << 16),
+                                      x1 - __uint_as_float(hw & 0xFFFF0000u));
+        }
+      l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      if (__any_sync(kFullMask, grow && o_live)) {
+        // O row *= alpha, once PV_{j-1} is done (every lane takes part in the
+        // collective TMEM accesses; rows that did not move multiply by 1).
+        // S_j needed PV_{j-2} done and PV_j needs this row's P_j, so pv_done
+        // is within one phase of j - 1 here and its parity is unambiguous.
+        const bool done = j == 0 || mbar_wait_bounded(pv_done, (j - 1) & 1);
+        if (!__all_sync(kFullMask, done)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int q = 0; q < kHeadDim / 16; ++q) {
+          uint32_t o[16];
+          tmem_ld16(t_lane + kTmemO + 16 * q, o);
+          tmem_wait_ld();
+          reg_after_wait(o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st16(t_lane + kTmemO + 16 * q, o);
+        }
+      }
+      // P over S: hi in X + 16h, lo in X + 32 + 16h; the other half's
+      // columns of this row are zero
+      tmem_st16(x + h * 16, hi);
+      tmem_st16(x + (1 - h) * 16, zero16);
+      tmem_st16(x + kPLo + h * 16, lo);
+      tmem_st16(x + kPLo + (1 - h) * 16, zero16);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(p_ready);
+      o_live = o_live || any_live;
+    }
+    // ---- epilogue: combine the two copies of each query row, then write
+    // the row's partial (max, sum, acc) to its member's slot
+    if (ok) {
+      // every PV done: pv_fin completes once, after the last of them (two
+      // phases of pv_done may still be pending here, which a parity wait
+      // could not tell from none)
+      const bool done = mbar_wait_bounded(pv_fin, 0);
+      ok = __all_sync(kFullMask, done);
+    }
+    if (!ok && lane == 0) record_error(a.dev_err, kErrTimeout);
+    uint32_t o[kHeadDim / 16][16];
+    tc_fence_after_sync();
+#pragma unroll
+    for (int q = 0; q < kHeadDim / 16; ++q) tmem_ld16(t_lane + kTmemO + 16 * q, o[q]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < kHeadDim / 16; ++q) reg_after_wait(o[q]);
+    if (!o_live) {
+#pragma unroll
+      for (int q = 0; q < kHeadDim / 16; ++q)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[q][e] = 0u;
+      l_run = 0.f;
+    }
+    // the lower copies hand (m, l, acc) to the upper ones through the K ring
+    // (every S, the only reader of it, has completed): [64 rows][66 floats]
+    float* xch = reinterpret_cast<float*>(smem + kOffK);
+    const int qr = L & (kTcRows - 1);
+    if (h == 1) {
+      float* row = xch + qr * (kHeadDim + 2);
+      row[0] = m_ref;
+      row[1] = l_run;
+#pragma unroll
+      for (int q = 0; q < kHeadDim / 16; ++q)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) row[2 + 16 * q + e] = __uint_as_float(o[q][e]);
+    }
+    softmax_warps_sync();
+    const int m = qr >> 2;
+    if (h == 0 && m < members) {
+      const float* row = xch + qr * (kHeadDim + 2);
+      const float m1 = row[0], l1 = row[1];
+      const float M = fmaxf(m_ref, m1);
+      const float w0 = M == -INFINITY ? 0.f : fast_exp2(m_ref - M);
+      const float w1 = M == -INFINITY ? 0.f : fast_exp2(m1 - M);
+      const int64_t part =
+          static_cast<int64_t>(it[4 + kSharedMembers + m]) * kNumQHeads + g * kGroup + (qr & 3);
+      float4* dst = reinterpret_cast<float4*>(a.part_acc + part * kHeadDim);
+#pragma unroll
+      for (int q = 0; q < kHeadDim / 16; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = 16 * q + 4 * e;
+          dst[d / 4] = make_float4(__uint_as_float(o[q][4 * e]) * w0 + row[2 + d] * w1,
+                                   __uint_as_float(o[q][4 * e + 1]) * w0 + row[3 + d] * w1,
+                                   __uint_as_float(o[q][4 * e + 2]) * w0 + row[4 + d] * w1,
+                                   __uint_as_float(o[q][4 * e + 3]) * w0 + row[5 + d] * w1);
+        }
+      *reinterpret_cast<float2*>(a.part_ml + part * 2) = make_float2(M, l_run * w0 + l1 * w1);
+    }
   }
 
-  // ---- each warp writes its members' partials (state through shared
-  // memory, once every copy of the ring has landed)
-  reduce_row_sums(S);
+  // ---- teardown: every copy landed and every MMA done before the shared
+  // memory and the TMEM columns are given back
   __syncthreads();
-  if (tid == 0) {
-    // after a timeout some tiles may still be in flight: wait for each
-    // stage's outstanding phase (bounded) before the ring is reused
-    for (int s = 0; s < kShStages && s < n; ++s) {
-      const int last_k = s + ((n - 1 - s) / kShStages) * kShStages;  // last page of stage s
-      mbar_wait_bounded(bar0 + 8 * s, (last_k / kShStages) & 1);
+  if ((warp == kKLoadWarp || warp == kVLoadWarp) && lane == 0) {
+    const bool is_k = warp == kKLoadWarp;
+    const int slots = is_k ? kKSlots : kVSlots;
+    for (int s = 0; s < slots && s < issued; ++s) {
+      const int last_b = s + ((issued - 1 - s) / slots) * slots;
+      if (!mbar_wait_bounded(is_k ? k_full(last_b) : v_full(last_b), (last_b / slots) & 1))
+        record_error(a.dev_err, kErrTimeout);
     }
   }
+  tc_fence_before_sync();
   __syncthreads();
-  if (mseq[0] < 0) return;
-  float* sm_m = reinterpret_cast<float*>(smem);
-  float* sm_l = sm_m + kShWarps * kShRows;
-  float* sm_o = sm_l + kShWarps * kShRows;
-  if (G.fg == 0) {
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      sm_m[warp * kShRows + 2 * G.ft + rr] = S.m_ref[rr];
-      sm_l[warp * kShRows + 2 * G.ft + rr] = S.l_run[rr];
-    }
-  }
-#pragma unroll
-  for (int mt = 0; mt < 4; ++mt) {
-    float* o0 = sm_o + (warp * kShRows + 2 * G.ft) * kHeadDim + 16 * mt + G.fg;
-    o0[0] = S.oacc[mt][0];
-    o0[kHeadDim] = S.oacc[mt][1];
-    o0[8] = S.oacc[mt][2];
-    o0[kHeadDim + 8] = S.oacc[mt][3];
-  }
-  __syncwarp();
-  const int d = 2 * lane;
-#pragma unroll
-  for (int r = 0; r < kShRows; ++r) {
-    const int h = r / kGroup;  // member 2 warp + h
-    if (mseq[h] < 0) continue;
-    const float M = sm_m[warp * kShRows + r];
-    const float Ls = M == -INFINITY ? 0.f : sm_l[warp * kShRows + r];
-    const float2 O = M == -INFINITY ? make_float2(0.f, 0.f)
-                                    : *reinterpret_cast<const float2*>(
-                                          sm_o + (warp * kShRows + r) * kHeadDim + d);
-    const int64_t part = static_cast<int64_t>(mslot[h]) * kNumQHeads + g * kGroup + (r & 3);
-    *reinterpret_cast<float2*>(a.part_acc + part * kHeadDim + d) = O;
-    if (lane == 0) *reinterpret_cast<float2*>(a.part_ml + part * 2) = make_float2(M, Ls);
+  if (warp == kPvWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -228,7 +523,7 @@ cudaError_t configure_sh_once(int device) {
   if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
   const cudaError_t err =
       cudaFuncSetAttribute(paged_decode_shared_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sh_smem_bytes(kShMaxPages)));
+                           static_cast<int>(sh_smem_bytes(kMaxPagesPerItem)));
   if (err == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
@@ -237,13 +532,14 @@ cudaError_t configure_sh_once(int device) {
 
 cudaError_t launch_shared_prefix_attention(const CUtensorMap& pool_map, const AttnArgs& args,
                                            int num_shared, int range_pages, cudaStream_t stream) {
-  if (num_shared < 1 || range_pages < 1 || range_pages > kShMaxPages) return cudaErrorInvalidValue;
+  if (num_shared < 1 || range_pages < 1 || range_pages > kMaxPagesPerItem)
+    return cudaErrorInvalidValue;
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
   err = configure_sh_once(device);
   if (err != cudaSuccess) return err;
-  return launch_pdl(paged_decode_shared_kernel, dim3(kNumKvHeads, num_shared), dim3(kShThreads),
+  return launch_pdl(paged_decode_shared_kernel, dim3(kNumKvHeads, num_shared), dim3(kTcThreads),
                     sh_smem_bytes(range_pages), stream, pool_map, args);
 }
 

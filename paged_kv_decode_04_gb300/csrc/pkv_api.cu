@@ -104,20 +104,25 @@ EncodeTiledFn encode_fn() {
 }
 
 // TMA descriptor of the pool viewed as [num_pages][32 rows (K|V x slot)][512]
-// bf16 with a 64 x 32 x 1 box (one kv head's K and V rows of one page),
-// 128-byte swizzled.  Cached per thread for the last (device, pool, pages).
-bool pool_tensor_map(const void* pool, int64_t num_pages, CUtensorMap* out) {
+// bf16, 128-byte swizzled, with a box of one kv head's rows of one page:
+// box_rows = 32 takes its K and V rows (a 4 KiB tile), box_rows = 16 its K
+// rows (row coordinate 0) or its V rows (row coordinate 16), 2 KiB each.
+// Cached per thread for the last (device, pool, pages) of each box height.
+bool pool_tensor_map(const void* pool, int64_t num_pages, CUtensorMap* out,
+                     int box_rows = 2 * kPageSize) {
   struct Entry {
     int device = -1;
     const void* pool = nullptr;
     int64_t num_pages = 0;
     CUtensorMap map;
   };
-  thread_local Entry cached;
+  thread_local Entry cached[2];
+  if (box_rows != kPageSize && box_rows != 2 * kPageSize) return false;
+  Entry& c = cached[box_rows == kPageSize ? 1 : 0];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (cached.device == dev && cached.pool == pool && cached.num_pages == num_pages) {
-    *out = cached.map;
+  if (c.device == dev && c.pool == pool && c.num_pages == num_pages) {
+    *out = c.map;
     return true;
   }
   EncodeTiledFn enc = encode_fn();
@@ -129,7 +134,7 @@ bool pool_tensor_map(const void* pool, int64_t num_pages, CUtensorMap* out) {
       static_cast<cuuint64_t>(kNumKvHeads * kHeadDim * 2),
       static_cast<cuuint64_t>(2 * kPageSize * kNumKvHeads * kHeadDim * 2)};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim),
-                             static_cast<cuuint32_t>(2 * kPageSize), 1};
+                             static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMap m;
   const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool),
@@ -137,10 +142,10 @@ bool pool_tensor_map(const void* pool, int64_t num_pages, CUtensorMap* out) {
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
-  cached.device = dev;
-  cached.pool = pool;
-  cached.num_pages = num_pages;
-  cached.map = m;
+  c.device = dev;
+  c.pool = pool;
+  c.num_pages = num_pages;
+  c.map = m;
   *out = m;
   return true;
 }
@@ -521,7 +526,7 @@ cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pa
   if (h.num_shared > 0) {
     // shared prefixes first: their partials join the members' own ones in
     // the merge that follows the attention kernel
-    if (!pool_tensor_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
+    if (!pool_tensor_map(pool, num_pages, &map, kPageSize)) return cudaErrorInvalidValue;
     const cudaError_t err =
         pkv::launch_shared_prefix_attention(map, args, h.num_shared, h.shared_pages, stream);
     if (err != cudaSuccess) return err;

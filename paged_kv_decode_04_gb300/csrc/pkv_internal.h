@@ -34,11 +34,11 @@ constexpr int kPackPages = 16;      // most pages a packed sequence may have
 constexpr int kPlanWarps = 4;       // warps per attention CTA: one packed sequence each
 // Shared-prefix items (a plan's last section): one CTA per (item, kv head)
 // attends pages [p_begin, p_begin + n) that the item's members' tables all
-// hold, warp w for members 2w and 2w + 1: {members, p_begin, n, 0, seq[16],
-// slot[16]}.  The planner sizes their ranges for one wave of
+// hold, for the 4 query rows of every member at once: {members, p_begin, n,
+// 0, seq[16], slot[16]}.  The planner sizes their ranges for one wave of
 // kSharedCtasPerSm CTAs per SM.
 constexpr int kSharedMembers = 16;
-constexpr int kSharedCtasPerSm = 3;
+constexpr int kSharedCtasPerSm = 2;
 constexpr int kPlanSharedWords = 4 + 2 * kSharedMembers;
 
 // Host side of the work plans (planner.cpp): an upper bound on a plan's
