@@ -102,13 +102,14 @@ constexpr int kOffBars = kOffV + kVSlots * kRegionBytes;
 // k_full[6], k_empty[6], v_full[6], v_empty[6], s_ready[2], x_free[2],
 // p_ready, pv_done, s_fin, pv_fin, q_ready
 constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 9;
-constexpr int kPrefetchBatches = 2;  // pulled into L2 before the grid dependency wait
+constexpr int kPrefetchBatches = 4;  // pulled into L2 before the grid dependency wait
 constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
 constexpr int kOffPages = kOffTmemSlot + 16;
 
 static_assert(kTcM == 128 && 32 * kTcSoftmaxWarps == kTcM, "one softmax thread per TMEM lane");
 static_assert(kTmemQ + kHeadDim / 2 <= kTmemCols, "X0, X1, O and Q fit the allocation");
-static_assert(kTcRows * (kHeadDim + 2) * 4 <= kKSlots * kRegionBytes, "end-of-CTA exchange fits");
+constexpr int kXchStride = kHeadDim + 4;  // floats per exchanged row: acc, then (m, l), 16-B aligned
+static_assert(kTcRows * kXchStride * 4 <= kKSlots * kRegionBytes, "end-of-CTA exchange fits");
 // Shared memory alone keeps more than kTcCtasPerSm CTAs of this kernel off
 // one SM (228 KiB per SM, 1 KiB reserved per CTA), so their TMEM
 // allocations always fit the 512 columns and tcgen05.alloc never waits.
@@ -458,24 +459,26 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         for (int e = 0; e < 16; ++e) o[q][e] = 0u;
       l_run = 0.f;
     }
-    // the lower copies hand (m, l, acc) to the upper ones through the K ring
-    // (every S, the only reader of it, has completed): [64 rows][66 floats]
-    float* xch = reinterpret_cast<float*>(smem + kOffK);
+    // the lower copies hand (acc, m, l) to the upper ones through the K ring
+    // (every S, the only reader of it, has completed): [64 rows][68 floats]
+    float4* xch = reinterpret_cast<float4*>(smem + kOffK);
     const int qr = L & (kTcRows - 1);
+    float4* xrow = xch + qr * (kXchStride / 4);
     if (h == 1) {
-      float* row = xch + qr * (kHeadDim + 2);
-      row[0] = m_ref;
-      row[1] = l_run;
 #pragma unroll
       for (int q = 0; q < kHeadDim / 16; ++q)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) row[2 + 16 * q + e] = __uint_as_float(o[q][e]);
+        for (int e = 0; e < 4; ++e)
+          xrow[4 * q + e] = make_float4(__uint_as_float(o[q][4 * e]), __uint_as_float(o[q][4 * e + 1]),
+                                        __uint_as_float(o[q][4 * e + 2]),
+                                        __uint_as_float(o[q][4 * e + 3]));
+      xrow[kHeadDim / 4] = make_float4(m_ref, l_run, 0.f, 0.f);
     }
     softmax_warps_sync();
     const int m = qr >> 2;
     if (h == 0 && m < members) {
-      const float* row = xch + qr * (kHeadDim + 2);
-      const float m1 = row[0], l1 = row[1];
+      const float4 ml = xrow[kHeadDim / 4];
+      const float m1 = ml.x, l1 = ml.y;
       const float M = fmaxf(m_ref, m1);
       const float w0 = M == -INFINITY ? 0.f : fast_exp2(m_ref - M);
       const float w1 = M == -INFINITY ? 0.f : fast_exp2(m1 - M);
@@ -486,19 +489,27 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       for (int q = 0; q < kHeadDim / 16; ++q)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int d = 16 * q + 4 * e;
-          dst[d / 4] = make_float4(__uint_as_float(o[q][4 * e]) * w0 + row[2 + d] * w1,
-                                   __uint_as_float(o[q][4 * e + 1]) * w0 + row[3 + d] * w1,
-                                   __uint_as_float(o[q][4 * e + 2]) * w0 + row[4 + d] * w1,
-                                   __uint_as_float(o[q][4 * e + 3]) * w0 + row[5 + d] * w1);
+          const float4 u = xrow[4 * q + e];
+          dst[4 * q + e] = make_float4(__uint_as_float(o[q][4 * e]) * w0 + u.x * w1,
+                                       __uint_as_float(o[q][4 * e + 1]) * w0 + u.y * w1,
+                                       __uint_as_float(o[q][4 * e + 2]) * w0 + u.z * w1,
+                                       __uint_as_float(o[q][4 * e + 3]) * w0 + u.w * w1);
         }
       *reinterpret_cast<float2*>(a.part_ml + part * 2) = make_float2(M, l_run * w0 + l1 * w1);
     }
   }
 
-  // ---- teardown: every copy landed and every MMA done before the shared
-  // memory and the TMEM columns are given back
+  // ---- teardown.  Past this barrier every MMA is done (the issuers waited
+  // for their last commits) and every TMEM read has completed, so the
+  // columns go back at once; the producers still wait for any copy in
+  // flight (only after a timeout) before the shared memory is released.
+  tc_fence_before_sync();
   __syncthreads();
+  if (warp == kPvWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
   if ((warp == kKLoadWarp || warp == kVLoadWarp) && lane == 0) {
     const bool is_k = warp == kKLoadWarp;
     const int slots = is_k ? kKSlots : kVSlots;
@@ -507,13 +518,6 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       if (!mbar_wait_bounded(is_k ? k_full(last_b) : v_full(last_b), (last_b / slots) & 1))
         record_error(a.dev_err, kErrTimeout);
     }
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == kPvWarp) {
-    __syncwarp();
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
