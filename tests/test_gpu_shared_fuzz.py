@@ -1,0 +1,91 @@
+"""Seeded fuzz parity of shared-prefix plans (GPU).
+
+Each case draws groups of consecutive sequences whose block tables start with
+the same physical pages: group sizes 2..16, shared prefixes of 16..100 pages
+(so shared ranges end on any page of a 4-page batch), singletons between the
+groups, private tails of 1..27 pages whose last page is partly filled, and a
+random minimum shared extent.  The decode step runs fused and as append +
+attention under the plan built from the lengths and tables.  Every output is
+checked against the FP64 oracle, every appended slot bit for bit, and fused
+against unfused bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_04_gb300 import synth
+from _gpu_util import assert_close, bf16_normal, binding, cuda_or_skip
+
+pytestmark = pytest.mark.gpu
+
+MAX_BLOCKS = 128
+
+
+def draw_case(seed):
+    rng = np.random.default_rng(7000 + seed)
+    min_shared = int(rng.choice([16, 24, 32]))
+    lens, rows, nxt, expect_shared = [], [], 0, False
+    for _ in range(int(rng.integers(1, 6))):
+        groups = [(1, 0)] if rng.random() < 0.5 else []
+        groups.append((int(rng.integers(2, 17)), int(rng.integers(16, 101))))
+        for size, k in groups:
+            expect_shared |= size >= 2 and k >= min_shared
+            common = list(range(nxt, nxt + k))
+            nxt += k
+            for _ in range(size):
+                o = int(rng.integers(1, 28))
+                rows.append(common + list(range(nxt, nxt + o)))
+                nxt += o
+                lens.append(16 * (k + o) - int(rng.integers(0, 16)))
+    lens = np.asarray(lens, np.int32)
+    B = len(lens)
+    perm = rng.permutation(nxt + 16).astype(np.int32)
+    bt = np.full((B, MAX_BLOCKS), -1, np.int32)
+    for i, r in enumerate(rows):
+        bt[i, :len(r)] = perm[r]
+    pool = bf16_normal(rng, (nxt + 16, 2, 16, 8, 64))
+    q = bf16_normal(rng, (B, 32, 64))
+    kn = bf16_normal(rng, (B, 8, 64))
+    vn = bf16_normal(rng, (B, 8, 64))
+    return lens, bt, pool, q, kn, vn, min_shared, expect_shared
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shared_groups(seed):
+    dev = cuda_or_skip()
+    b = binding()
+    lens, bt, pool, q, kn, vn, min_shared, expect_shared = draw_case(seed)
+    ref_pool = pool.copy()
+    assert oracle.kv_append(kn, vn, ref_pool, bt, lens - 1) == 0
+    ref = oracle.decode_attention(q, ref_pool, bt, lens)
+
+    def u16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+            torch.bfloat16)
+
+    plan = b.Plan(lens, MAX_BLOCKS, device=dev, block_tables=bt, min_shared_pages=min_shared)
+    assert (plan.num_shared > 0) == expect_shared
+    if expect_shared:
+        assert b.attention_kernels(len(lens), MAX_BLOCKS, 0, plan).startswith(
+            "paged_decode_shared_kernel+")
+    dbt, dl = torch.from_numpy(bt).to(dev), torch.from_numpy(lens).to(dev)
+    outs, pools = [], []
+    for fused in (True, False):
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        dpool = u16(pool)
+        if fused:
+            out = b.decode_step_planned(u16(q), u16(kn), u16(vn), dpool, dbt, dl, plan,
+                                        dev_err=err)
+        else:
+            b.kv_append(u16(kn), u16(vn), dpool, dbt, dl - 1, dev_err=err)
+            out = b.paged_decode_attention_planned(u16(q), dpool, dbt, dl, plan, dev_err=err)
+        got = synth.bits(out)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_close(got, ref, f"shared fuzz seed {seed}, fused={fused}")
+        outs.append(got)
+        pools.append(synth.bits(dpool))
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(pools[0], ref_pool)  # appended slots, nothing else
+    assert np.array_equal(pools[1], ref_pool)
