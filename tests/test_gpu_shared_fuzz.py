@@ -89,3 +89,36 @@ def test_random_shared_groups(seed):
     assert np.array_equal(outs[0], outs[1])
     assert np.array_equal(pools[0], ref_pool)  # appended slots, nothing else
     assert np.array_equal(pools[1], ref_pool)
+
+
+def test_bad_page_in_shared_prefix_is_reported():
+    # every member of a group names the same out-of-range page inside the
+    # shared prefix: the shared-prefix kernel records PKV_DEVERR_PAGE, skips
+    # that page and finishes (no timeout); outputs stay finite
+    dev = cuda_or_skip()
+    b = binding()
+    lens, bt, pool, q, kn, vn, min_shared, _ = draw_case(3)
+    plan0 = b.Plan(lens, MAX_BLOCKS, block_tables=bt, min_shared_pages=min_shared)
+    sh = plan0.shared()
+    assert len(sh) > 0
+    members, p_begin = int(sh[0][0]), int(sh[0][1])
+    seqs = [int(x) for x in sh[0][4:4 + members]]
+    bad = bt.copy()
+    for s in seqs:
+        bad[s, p_begin + 2] = pool.shape[0] + 5
+    plan = b.Plan(lens, MAX_BLOCKS, device=dev, block_tables=bad, min_shared_pages=min_shared)
+    assert plan.num_shared == plan0.num_shared
+
+    def u16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+            torch.bfloat16)
+
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = b.paged_decode_attention_planned(u16(q), u16(pool), torch.from_numpy(bad).to(dev),
+                                           torch.from_numpy(lens).to(dev), plan, dev_err=err)
+    got = synth.bits(out)
+    torch.cuda.synchronize()
+    e = int(err.item())
+    assert e & b.DEVERR_PAGE
+    assert not e & b.DEVERR_TIMEOUT
+    assert np.all(np.isfinite(oracle.bf16_to_f64(got)))
