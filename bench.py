@@ -41,10 +41,20 @@ METRIC = "paged decode-attn achieved HBM GB/s (% of peak); decode steps/s at bs=
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_attention_peak_traffic.json")
-KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_decode_04_gb300", "csrc", f)
-                  for f in ("decode_attention.cu", "decode_pagebox.cu", "decode_shared.cu",
-                            "decode_page.cuh", "pkv_device.cuh", "pkv_internal.h")]
-# The traffic file holds a list of records {workload, kernel, kernel_sha, dram_bytes_per_launch}.
+CSRC = os.path.join(ROOT, "paged_kv_decode_04_gb300", "csrc")
+# The source file of each decode kernel; every one of them also includes these headers.
+KERNEL_FILES = {
+    "paged_decode_kernel": "decode_attention.cu",
+    "merge_plan_kernel": "decode_attention.cu",
+    "merge_splits_kernel": "decode_attention.cu",
+    "paged_decode_pagebox_kernel": "decode_pagebox.cu",
+    "paged_decode_shared_kernel": "decode_shared.cu",
+}
+COMMON_SOURCES = ("decode_page.cuh", "pkv_device.cuh", "pkv_internal.h")
+KERNEL_SOURCES = [os.path.join(CSRC, f)
+                  for f in sorted(set(KERNEL_FILES.values())) + list(COMMON_SOURCES)]
+# The traffic file holds a list of records {workload, kernel, kernel_sha, dram_bytes_per_launch};
+# kernel_sha covers the sources of the kernels the record names.
 
 WORKLOAD_TEXT = {
     "peak": "peak: 256 seqs x 2048 ctx, 1 layer, 32q/8kv/64 bf16, 32768 live pages (1 GiB K/V) "
@@ -92,11 +102,22 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sha() -> str:
-    """Hash of the kernel sources' code: comments and whitespace do not count,
-    so a comment edit does not orphan the recorded counters."""
+def kernel_sources(kernel: str = None):
+    """Source files of the kernels named in `kernel` ("a+b (fused step)"), or of all of them."""
+    if kernel is None:
+        return KERNEL_SOURCES
+    names = kernel.split(" (")[0].split("+")
+    files = sorted({KERNEL_FILES[n] for n in names if n in KERNEL_FILES})
+    return [os.path.join(CSRC, f) for f in files + list(COMMON_SOURCES)]
+
+
+def kernel_sha(kernel: str = None) -> str:
+    """Hash of the code of the sources `kernel` is built from (all kernel
+    sources if None): comments and whitespace do not count, so a comment edit
+    does not orphan the recorded counters, and a change to one kernel's file
+    does not orphan another kernel's."""
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in kernel_sources(kernel):
         with open(p, encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -113,7 +134,7 @@ def recorded_traffic(workload: str, kernel: str):
     except Exception:
         return None
     for rec in recs if isinstance(recs, list) else [recs]:
-        if (rec.get("kernel_sha") == kernel_sha() and rec.get("workload") == workload
+        if (rec.get("kernel_sha") == kernel_sha(kernel) and rec.get("workload") == workload
                 and rec.get("kernel") == kernel):
             return rec.get("dram_bytes_per_launch")
     return None
