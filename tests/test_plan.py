@@ -321,3 +321,25 @@ def test_without_tables_or_sharing_the_plan_is_the_plain_one():
     b = B.Plan(lens, 128, num_sms=SMS, block_tables=bt)
     assert a.num_shared == b.num_shared == 0
     assert np.array_equal(a.host, b.host)
+
+
+@pytest.mark.parametrize("sms", [1, 132, 152])
+def test_shared_ranges_fill_one_wave_of_two_ctas_per_sm(sms):
+    # the prefix workload: 16 groups of 16 sequences sharing 96 pages.  Each
+    # group's prefix is cut into as many near-equal ranges as keep the
+    # shared-prefix CTAs (one per item and kv head, two resident per SM)
+    # within one wave: 2 ranges of 48 pages at 132 or 152 SMs, 1 of 96 at 1
+    from paged_kv_decode_04_gb300 import synth
+    w = synth.make_workload("prefix", 0)
+    plan = B.Plan(w.seq_lens, w.max_blocks, num_sms=sms, block_tables=w.block_tables[0])
+    sh = plan.shared()
+    ranges = 1 if sms == 1 else 2
+    assert plan.num_shared == 16 * ranges
+    assert all(int(it[0]) == 16 for it in sh)
+    assert sorted({int(it[2]) for it in sh}) == [96 // ranges]
+    if sms > 1:
+        assert plan.num_shared * 8 <= 2 * sms
+    for g in range(16):   # each group's ranges tile its 96 shared pages
+        mine = sorted((int(it[1]), int(it[2])) for it in sh if int(it[4]) == 16 * g)
+        assert mine[0][0] == 0 and all(a + n == b for (a, n), (b, _) in zip(mine, mine[1:]))
+        assert mine[-1][0] + mine[-1][1] == 96
