@@ -90,7 +90,7 @@ struct SharedGroup {
 // With shared groups, a member attends only its own pages [k, pages) in
 // range items (never packed) and every range writes a partial; the group's
 // pages [0, k) become shared-prefix items (ns near-equal ranges per group,
-// ns the most that keeps these CTAs within one wave of three per SM) whose CTAs write one
+// ns the most that keeps these CTAs within one wave of two per SM) whose CTAs write one
 // partial per member; each member's partials sit in consecutive slots,
 // shared ranges first, and one merge entry combines them.
 int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
