@@ -9,7 +9,9 @@ What is pinned, and by what (none of these re-type the oracle's own loops):
   * invariants: permuting physical pages with a remapped table, the online
     recurrence vs the two-pass form, split partials merged vs the whole;
   * structure: the GQA head map, poison never read, the append touching only
-    its slot.
+    its slot;
+  * aliasing: sequences whose tables share prefix pages equal the same batch
+    with private copies, and an append never writes the shared pages.
 Source of the computation: "Hours of YouTube and 85 handtyped pages of notes on
 LLM Inference - Start here", section "これまでの進捗" (paged decode attention
 item; KV page pool item).
@@ -317,3 +319,57 @@ def test_prefill_bad_positions_are_skipped():
     assert not np.array_equal(pool[1, :, 15], before[1, :, 15])
     changed = np.argwhere(np.any(pool != before, axis=(3, 4)))
     assert {tuple(c) for c in changed.tolist()} == {(1, 0, 15), (1, 1, 15)}
+
+
+def aliased_prefix_case(seed, group=3, shared_pages=2, own=(5, 20, 33)):
+    """`group` sequences whose tables name the same `shared_pages` physical
+    pages first (a common prompt prefix), then pages of their own."""
+    rng = np.random.default_rng(seed)
+    num_pages = shared_pages + sum(-(-o // P) for o in own) + 4
+    pool = np.full((num_pages, 2, P, HKV, D), POISON, dtype=np.uint16)
+    perm = rng.permutation(num_pages)
+    shared = perm[:shared_pages]
+    pool[shared] = bf16(rng.standard_normal((shared_pages, 2, P, HKV, D)))
+    bt = np.full((group, 8), -1, dtype=np.int32)
+    cur = shared_pages
+    lens = []
+    for b in range(group):
+        n_own = -(-own[b] // P)
+        bt[b, :shared_pages] = shared
+        bt[b, shared_pages:shared_pages + n_own] = perm[cur:cur + n_own]
+        for k in range(n_own):
+            valid = min(P, own[b] - k * P)
+            pool[perm[cur + k], :, :valid] = bf16(rng.standard_normal((2, valid, HKV, D)))
+        cur += n_own
+        lens.append(shared_pages * P + own[b])
+    q = bf16(rng.standard_normal((group, HQ, D)))
+    return q, pool, bt, np.asarray(lens, dtype=np.int32), shared
+
+
+def test_aliased_prefix_equals_private_copies():
+    # prefix sharing is pure aliasing: copying the shared pages out to private
+    # pages for every follower changes no output bit, and both agree with the
+    # brute-force gather
+    q, pool, bt, L, shared = aliased_prefix_case(21)
+    base = oracle.decode_attention(q, pool, bt, L)
+    S = len(shared)
+    pool2 = np.concatenate([pool, np.empty((S * (len(L) - 1),) + pool.shape[1:], pool.dtype)])
+    bt2 = bt.copy()
+    nxt = pool.shape[0]
+    for b in range(1, len(L)):
+        for k in range(S):
+            pool2[nxt] = pool[shared[k]]
+            bt2[b, k] = nxt
+            nxt += 1
+    assert np.array_equal(oracle.decode_attention(q, pool2, bt2, L), base)
+    np.testing.assert_allclose(base, brute_force(q, pool, bt, L), rtol=1e-12, atol=1e-12)
+
+
+def test_append_to_an_aliased_batch_leaves_the_shared_pages():
+    q, pool, bt, L, shared = aliased_prefix_case(22)
+    rng = np.random.default_rng(23)
+    kn = bf16(rng.standard_normal((len(L), HKV, D)))
+    vn = bf16(rng.standard_normal((len(L), HKV, D)))
+    before = pool[shared].copy()
+    assert oracle.kv_append(kn, vn, pool, bt, L - 1) == 0
+    assert np.array_equal(pool[shared], before)
