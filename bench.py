@@ -10,12 +10,16 @@ one layer, 32 query / 8 kv heads, head dim 64, 32768 live pages randomly
 scattered in a 40000-page pool.
 
 Prints one JSON line.  `value` is achieved algorithmic HBM GB/s of the whole
-step with all inputs resident in device memory; `e2e` repeats the measurement
-with the per-step inputs copied from pinned host memory and the output copied
-back inside the timed region.  `--impl reference` times the FP64 CPU oracle on
-the host cores instead (a deliberately slow baseline, not a target).
-Multi-GPU runs (torchrun) are independent replicas, one per rank (weak
-scaling): the path has no exchange step.
+step with all inputs resident in device memory (the median of repeated timed
+regions of K steps); `e2e` repeats the measurement through the same public
+calls with the per-step work plan built on the host, the per-step inputs
+copied from pinned host memory and the output copied back inside the timed
+region.  `per_workload` measures the other workloads (tiny, long, small, mix,
+prefix, the prefill write) the same way, each checked element by element
+against the FP64 oracle on every output.  `--impl reference` times the FP64
+CPU oracle on the host cores instead (a deliberately slow baseline, not a
+target).  Multi-GPU runs (torchrun) are independent replicas, one per rank
+(weak scaling): the path has no exchange step.
 """
 from __future__ import annotations
 
@@ -23,6 +27,7 @@ import argparse
 import copy
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -55,6 +60,11 @@ KERNEL_SOURCES = [os.path.join(CSRC, f)
                   for f in sorted(set(KERNEL_FILES.values())) + list(COMMON_SOURCES)]
 # The traffic file holds a list of records {workload, kernel, kernel_sha, dram_bytes_per_launch};
 # kernel_sha covers the sources of the kernels the record names.
+# Every kernel of the library, for the per-kernel shares of a step.
+LIBRARY_KERNELS = ("paged_decode_pagebox_kernel", "paged_decode_shared_kernel",
+                   "paged_decode_kernel", "merge_plan_kernel", "merge_splits_kernel",
+                   "kv_append_kernel", "kv_write_prefill_kernel", "rope_table_kernel",
+                   "rope_tag_kernel")
 
 WORKLOAD_TEXT = {
     "peak": "peak: 256 seqs x 2048 ctx, 1 layer, 32q/8kv/64 bf16, 32768 live pages (1 GiB K/V) "
@@ -65,9 +75,17 @@ WORKLOAD_TEXT = {
     "small": "small: 8 seqs, lengths U[1,2048], 1 layer, 4096-page pool",
     "tiny": "tiny: 1 seq x 37 ctx, 1 layer, 64-page pool",
     "prefix": "prefix: 256 seqs x 2048 ctx, groups of 16 share a 1536-token prefix (96 aliased "
-              "pages) + 32 private pages each, 9728 live pages in a 40000-page pool; K/V bytes "
-              "are counted per sequence (effective bandwidth: shared pages may hit in L2)",
+              "pages) + 32 private pages each, 9728 live pages in a 40000-page pool",
 }
+# The workloads measured next to the headline (in this order), then the prefill write.
+PER_WORKLOADS = ("tiny", "long", "small", "mix", "prefix")
+PREFILL_TEXT = "prefill write: 256 prompts x 2047 tokens, 8 kv heads x 64 bf16, 40000-page pool"
+# Repeated timed regions: at least this many, and for at least this long (the
+# clock sampler then sees the whole span).
+MIN_REPEATS = 10
+MIN_TIMED_SECONDS = 1.5
+MAX_REPEATS = 5000
+TOL_ABS, TOL_REL = 1e-3, 8e-3
 
 
 # ------------------------------------------------------------------ bytes --
@@ -89,6 +107,23 @@ def algorithmic_bytes(w, part: str = "step") -> int:
     app = B * Hkv * D * 2 * 2 * 2 + B * 4
     per_layer = {"attention": attn, "append": app, "step": attn + app}[part]
     return per_layer * w.layers
+
+
+def unique_bytes(w) -> int:
+    """algorithmic_bytes(w) with each physical page's K/V counted once per
+    layer (the tokens it holds for the longest sequence naming it): the bytes
+    a step must read from DRAM when sequences share prefix pages."""
+    Hkv, D, P = w.num_kv_heads, w.head_dim, w.page_size
+    total = algorithmic_bytes(w, "step") - int(w.seq_lens.astype(np.int64).sum()) * Hkv * D * 4 \
+        * w.layers
+    for layer in range(w.layers):
+        tokens = {}
+        for b in range(w.batch):
+            L = int(w.seq_lens[b])
+            for k, p in enumerate(w.pages_of(layer, b)):
+                tokens[int(p)] = max(tokens.get(int(p), 0), min(P, L - k * P))
+        total += sum(tokens.values()) * Hkv * D * 4
+    return total
 
 
 # ------------------------------------------------------------- utilities --
@@ -138,6 +173,15 @@ def recorded_traffic(workload: str, kernel: str):
                 and rec.get("kernel") == kernel):
             return rec.get("dram_bytes_per_launch")
     return None
+
+
+def spread(times_ms, steps):
+    """Median / min / max of per-step times (ms) over repeated timed regions."""
+    per = sorted(t / steps for t in times_ms)
+    med = statistics.median(per)
+    return {"repeats": len(per), "steps_per_repeat": steps, "ms_per_step_median": round(med, 6),
+            "ms_per_step_min": round(per[0], 6), "ms_per_step_max": round(per[-1], 6),
+            "spread_pct": round(100.0 * (per[-1] - per[0]) / med, 2)}
 
 
 class ClockSampler:
@@ -196,6 +240,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": reasons, "samples": len(rows),
+                "span_s": round(t1 - t0, 3),
                 "power_w_max": max(power) if power else None}
 
 
@@ -258,16 +303,22 @@ def sum_over_ranks(x: float, world: int, device) -> float:
 
 # ------------------------------------------------------------ CPU oracle --
 
-def oracle_sample_run(w, n_seqs: int, rng_seed: int = 0, threads: int = 0):
+def oracle_sample_run(w, n_seqs: int, rng_seed: int = 0, threads: int = 0,
+                      want_slots: bool = False):
     """Time the FP64 oracle on n_seqs sequences of every layer (append + attention).
 
     The sample's inputs are relabelled into compact host copies first (not
     timed).  Returns (seconds, algorithmic bytes of the sample, threads, number
-    of sequences, the sampled sequence ids, the oracle's outputs per layer)."""
+    of sequences, the sampled sequence ids, the oracle's outputs per layer);
+    with want_slots, also the appended K and V rows per layer ([n][2][Hkv][D]
+    bits, from the oracle's pool after its append)."""
     import oracle
     from paged_kv_decode_04_gb300 import synth
-    rng = np.random.default_rng(rng_seed)
-    seqs = np.sort(rng.choice(w.batch, size=min(n_seqs, w.batch), replace=False))
+    if n_seqs >= w.batch:
+        seqs = np.arange(w.batch)
+    else:
+        rng = np.random.default_rng(rng_seed)
+        seqs = np.sort(rng.choice(w.batch, size=n_seqs, replace=False))
     threads = threads or oracle.default_threads()
     comps = [synth.compact(w, layer, seqs) for layer in range(w.layers)]
     refs = []
@@ -284,7 +335,602 @@ def oracle_sample_run(w, n_seqs: int, rng_seed: int = 0, threads: int = 0):
         seq_lens=w.seq_lens[seqs], block_tables=w.block_tables[:, seqs], live_pages=w.live_pages,
         page_data=w.page_data[:0], q=w.q[:, seqs], k_new=w.k_new[:, seqs],
         v_new=w.v_new[:, seqs])
-    return dt, algorithmic_bytes(sub, "step"), threads, len(seqs), seqs, refs
+    res = (dt, algorithmic_bytes(sub, "step"), threads, len(seqs), seqs, refs)
+    if not want_slots:
+        return res
+    slots = []
+    for c in comps:
+        rows = np.zeros((len(seqs), 2, w.num_kv_heads, w.head_dim), dtype=np.uint16)
+        for r in range(len(seqs)):
+            pos = int(c.positions[r])
+            if pos >= 0:
+                rows[r] = c.pool[c.block_table[r, pos // w.page_size], :, pos % w.page_size]
+        slots.append(rows)
+    return res + (slots,)
+
+
+def parity_report(got_bits, refs):
+    """Element-wise check of bf16 outputs against the oracle (float64)."""
+    got = (got_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = np.stack(refs)
+    err = np.abs(got - ref)
+    with np.errstate(invalid="ignore"):
+        over = err / (TOL_ABS + TOL_REL * np.abs(ref))
+    worst = float(np.nanmax(over)) if over.size else 0.0
+    if not np.all(np.isfinite(got)):
+        worst = float("inf")
+    return {"outputs_checked": int(ref.size), "max_abs_err": float(np.nanmax(err)) if err.size
+            else 0.0, "worst_err_over_tolerance": round(worst, 5),
+            "tolerance": "|err| <= 1e-3 + 8e-3 |ref|", "within_tolerance": bool(worst <= 1.0)}
+
+
+# ------------------------------------------------------------ the decode --
+
+class DecodeBench:
+    """One workload resident on the device with everything a timed step needs:
+    the plan, workspace, outputs, the step as a CUDA graph, and the
+    measurements (repeated timed regions, per-launch events, e2e)."""
+
+    def __init__(self, w, args, dev, *, world=1, plan_mode=None):
+        import torch
+        from paged_kv_decode_04_gb300 import binding, synth
+        self.torch, self.binding, self.synth = torch, binding, synth
+        self.w, self.args, self.dev, self.world = w, args, dev, world
+        self.d = synth.device_inputs(w, dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.plan_mode = plan_mode or args.plan
+        self.planned = self.plan_mode in ("host", "lengths")
+        # the host plan is built from the lengths and layer 0's tables (shared
+        # prefixes become shared-prefix items); the workloads share the same
+        # runs of pages in every layer, so it serves every layer
+        self.plan_kw = ({"block_tables": w.block_tables[0]} if self.plan_mode == "host" else {})
+        B = w.batch
+        if self.planned:
+            self.plan = binding.Plan(w.seq_lens, w.max_blocks, device=dev, **self.plan_kw)
+            self.d["plan"] = self.plan.dev
+            ws_bytes = self.plan.workspace_bytes
+            p = self.plan
+            self.split_text = (f"host work plan: {p.num_items} items of at most {p.range_pages} "
+                               f"pages or 4 packed sequences, {p.num_merges} merged sequences")
+            if p.num_shared:
+                self.split_text += (f", {p.num_shared} shared-prefix items of at most "
+                                    f"{p.shared_pages} pages")
+            self.splits = max(1, max((int(m[2]) for m in p.merges()), default=1))
+        else:
+            self.plan = None
+            self.splits = binding.plan_splits(B, w.max_blocks, args.splits)
+            ws_bytes = binding.workspace_bytes(B, w.max_blocks, args.splits)
+            self.split_text = f"fixed: {self.splits} ranges per sequence"
+        self.workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        self.outs = torch.empty((w.layers, B, w.num_q_heads, w.head_dim), dtype=torch.bfloat16,
+                                device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.fused = args.path == "fused"
+        merges = (self.plan.num_merges > 0) if self.planned else (self.splits > 1)
+        self.launched = binding.attention_kernels(B, w.max_blocks, args.splits, self.plan)
+        self.kernels_per_layer = ((1 if self.fused else 2) + (1 if merges else 0)
+                                  + (1 if self.planned and self.plan.num_shared else 0))
+        self.run_step = self.launch_step
+
+    # -- launches
+    def plan_for(self, dset):
+        """The plan whose device copy is dset["plan"] (one per input set)."""
+        if not self.planned:
+            return None
+        if dset["plan"] is self.plan.dev:
+            return self.plan
+        p2 = copy.copy(self.plan)
+        p2.dev = dset["plan"]
+        return p2
+
+    def fused_on(self, dset, layer, out):
+        w, b, d = self.w, self.binding, self.d
+        if self.planned:
+            b.decode_step_planned(
+                dset["q"][layer], dset["k_new"][layer], dset["v_new"][layer], d["pool"],
+                dset["block_tables"][layer], dset["seq_lens"], self.plan_for(dset), out,
+                rope_theta=w.rope_theta, scale=w.scale, workspace=self.workspace,
+                dev_err=self.err)
+        else:
+            b.decode_step(
+                dset["q"][layer], dset["k_new"][layer], dset["v_new"][layer], d["pool"],
+                dset["block_tables"][layer], dset["seq_lens"], out, rope_theta=w.rope_theta,
+                scale=w.scale, workspace=self.workspace, num_splits=self.args.splits,
+                dev_err=self.err)
+
+    def append_on(self, dset, layer):
+        self.binding.kv_append(dset["k_new"][layer], dset["v_new"][layer], self.d["pool"],
+                               dset["block_tables"][layer], dset["positions"],
+                               rope_theta=self.w.rope_theta, dev_err=self.err)
+
+    def attend_on(self, dset, layer, out):
+        w, b, d = self.w, self.binding, self.d
+        if self.planned:
+            b.paged_decode_attention_planned(
+                dset["q"][layer], d["pool"], dset["block_tables"][layer], dset["seq_lens"],
+                self.plan_for(dset), out, scale=w.scale, workspace=self.workspace,
+                dev_err=self.err)
+        else:
+            b.paged_decode_attention(
+                dset["q"][layer], d["pool"], dset["block_tables"][layer], dset["seq_lens"], out,
+                scale=w.scale, workspace=self.workspace, num_splits=self.args.splits,
+                dev_err=self.err)
+
+    def launch_on(self, dset, out):
+        """Enqueue one whole step (every layer) on the current stream."""
+        for layer in range(self.w.layers):
+            if self.fused:
+                self.fused_on(dset, layer, out[layer])
+            else:
+                self.append_on(dset, layer)
+                self.attend_on(dset, layer, out[layer])
+
+    def launch_step(self):
+        self.launch_on(self.d, self.outs)
+
+    def warm_and_capture(self, warmup, graph):
+        torch = self.torch
+        for _ in range(warmup):
+            self.launch_step()
+        torch.cuda.synchronize(self.dev)
+        self.check_err("warm-up")
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.launch_step()
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize(self.dev)
+            self.graph = g
+            self.run_step = g.replay
+
+    def check_err(self, when):
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(self.err.item())} during the {when}")
+
+    # -- timing
+    def one_region(self, steps, flush=None):
+        """CUDA-event time (ms) of `steps` steps on the launching stream, with a
+        barrier and a synchronize on both sides; with `flush` (a device buffer
+        larger than L2), L2 is flushed before every step, outside the per-step
+        event pairs, and the region's time is the sum of the step events."""
+        torch = self.torch
+        barrier(self.world)
+        torch.cuda.synchronize(self.dev)
+        if flush is None:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for _ in range(steps):
+                self.run_step()
+            e1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            ms = e0.elapsed_time(e1)
+        else:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+            for i in range(steps):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(self.stream)
+                self.run_step()
+                ev[i][1].record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            ms = sum(a.elapsed_time(b) for a, b in ev)
+        barrier(self.world)
+        return max_over_ranks(ms, self.world, self.dev)
+
+    def timed(self, steps, flush=None, min_seconds=MIN_TIMED_SECONDS):
+        """Repeated timed regions of `steps` steps: at least MIN_REPEATS of them
+        and at least min_seconds in all (the count is fixed from a probe region,
+        the same on every rank).  Returns (region times in ms, wall t0, t1)."""
+        probe = self.one_region(steps, flush)
+        per_region_s = max(probe, 1e-3) / 1e3
+        if flush is not None:
+            per_region_s += steps * 1.2e-4         # the flushes between steps
+        reps = int(min(MAX_REPEATS, max(MIN_REPEATS, math.ceil(min_seconds / per_region_s))))
+        t0 = time.time()
+        times = [self.one_region(steps, flush) for _ in range(reps)]
+        return times, t0, time.time()
+
+    def per_launch(self, steps):
+        """Per-launch CUDA events in a separate pass of the same loop (the
+        launches queued behind a short busy kernel so the events time
+        back-to-back kernels, not the host's launch pace)."""
+        torch = self.torch
+        layers = self.w.layers
+        n_prof = min(steps, max(50, steps // 4))
+        chunk = 64
+        kern = {}
+
+        def prequeue(i):
+            if i % chunk == 0:
+                torch.cuda._sleep(int(2e9 * 100e-6 * min(chunk, n_prof - i) * layers))
+
+        if self.fused:
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_prof)]
+            for i in range(n_prof):
+                prequeue(i)
+                ev[i][0].record(self.stream)
+                for layer in range(layers):
+                    self.fused_on(self.d, layer, self.outs[layer])
+                ev[i][1].record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            per = [e[0].elapsed_time(e[1]) / layers for e in ev]
+            dom_ms = statistics.mean(per)
+            kern["decode_step_median"] = round(statistics.median(per) * 1e3, 2)
+            kern["decode_step"] = round(dom_ms * 1e3, 2)
+            dom_bytes = algorithmic_bytes(self.w, "step") / layers
+            dom_name = self.launched + " (fused step)"
+        else:
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_prof)]
+            for i in range(n_prof):
+                prequeue(i)
+                ev[i][0].record(self.stream)
+                for layer in range(layers):
+                    self.append_on(self.d, layer)
+                ev[i][1].record(self.stream)
+                for layer in range(layers):
+                    self.attend_on(self.d, layer, self.outs[layer])
+                ev[i][2].record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            app_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / layers
+            dom_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) / layers
+            kern["kv_append"] = round(app_ms * 1e3, 2)
+            kern["paged_decode_attention"] = round(dom_ms * 1e3, 2)
+            dom_bytes = algorithmic_bytes(self.w, "attention") / layers
+            dom_name = self.launched + " (attention)"
+        return kern, dom_ms, dom_bytes, dom_name
+
+    def kernel_shares(self, n=20):
+        """Each library kernel's share of the device time of n eager steps, from
+        the CUPTI kernel records torch.profiler collects (a ratio; no duration
+        taken under the profiler is reported)."""
+        torch = self.torch
+        try:
+            from torch.profiler import ProfilerActivity, profile
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                for _ in range(n):
+                    self.launch_step()
+                torch.cuda.synchronize(self.dev)
+            totals = {}
+            for ev in prof.key_averages():
+                t = getattr(ev, "device_time_total", None)
+                if t is None:
+                    t = getattr(ev, "cuda_time_total", 0.0)
+                m = re.search(r"\b(" + "|".join(LIBRARY_KERNELS) + r")\b", ev.key)
+                if m and t:
+                    totals[m.group(1)] = totals.get(m.group(1), 0.0) + float(t)
+            s = sum(totals.values())
+            if s <= 0:
+                return None
+            return {k: round(v / s, 4) for k, v in sorted(totals.items(), key=lambda x: -x[1])}
+        except Exception as exc:  # the profiler is optional on a box
+            return {"unavailable": str(exc)[:120]}
+
+    # -- end to end
+    def e2e(self, steps, warmup):
+        """The same step through the public calls with every per-step input
+        coming from pinned host memory: the work plan is built on the host
+        from the host lengths (and tables) each step, packed with q, k_new,
+        v_new, positions, seq_lens and the block tables into one pinned buffer
+        and copied in one transfer; the output is copied back.  Two input sets
+        alternate so that the copies of step k+1 and the read-back of step k
+        overlap step k."""
+        torch, w = self.torch, self.w
+        names = ["q", "k_new", "v_new", "positions", "seq_lens", "block_tables"]
+        if self.planned:
+            names.append("plan")
+        layout, total = [], 0
+        for k in names:
+            nb = self.d[k].numel() * self.d[k].element_size()
+            layout.append((k, total, nb, self.d[k].dtype, tuple(self.d[k].shape)))
+            total += (nb + 255) // 256 * 256
+        plan_off = dict((k, off) for k, off, _, _, _ in layout).get("plan")
+        plan_cap = 0
+        if self.planned:
+            plan_cap = self.binding.plan_bytes(w.batch, w.max_blocks)
+            total = plan_off + (plan_cap + 255) // 256 * 256
+        host_bufs = [torch.empty(total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        for hb in host_bufs:
+            for k, off, nb, _, _ in layout:
+                hb[off:off + nb].copy_(self.d[k].reshape(-1).view(torch.uint8).cpu())
+        lens_host = np.ascontiguousarray(w.seq_lens.astype(np.int32))
+        plan_kw = dict(self.plan_kw)
+
+        def build_plan(i):
+            """This step's plan, built by the host into set i's pinned buffer."""
+            view = host_bufs[i][plan_off:plan_off + plan_cap].numpy().view(np.int32)
+            return self.binding.Plan(lens_host, w.max_blocks, out=view, **plan_kw)
+
+        dev_bufs = [torch.empty(total, dtype=torch.uint8, device=self.dev) for _ in range(2)]
+        sets = [{k: buf[off:off + nb].view(dt).view(shape) for k, off, nb, dt, shape in layout}
+                for buf in dev_bufs]
+        plans = [None, None]
+        for i, dset in enumerate(sets):
+            for k in names:
+                if k != "plan":
+                    dset[k].copy_(self.d[k])
+            if self.planned:
+                plans[i] = build_plan(i)
+                n_words = plans[i].host.shape[0]
+                dset["plan"] = dev_bufs[i][plan_off:plan_off + 4 * n_words].view(torch.int32)
+                dset["plan"].copy_(torch.from_numpy(plans[i].host.copy()))
+        out_host = [torch.empty(self.outs.shape, dtype=self.outs.dtype).pin_memory()
+                    for _ in range(2)]
+        d2h = out_host[0].numel() * out_host[0].element_size()
+        set_outs = [self.outs, torch.empty_like(self.outs)]
+
+        def make_step(i):
+            dset, out = sets[i], set_outs[i]
+
+            def launch():
+                for layer in range(w.layers):
+                    if self.fused:
+                        self.fused_on(dset, layer, out[layer])
+                    else:
+                        self.append_on(dset, layer)
+                        self.attend_on(dset, layer, out[layer])
+            if not self.args.graph:
+                return launch
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                launch()
+            return g.replay
+
+        steps_e2e = [make_step(i) for i in range(2)]
+        copy_stream = torch.cuda.Stream(self.dev)
+        in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+        computed = [torch.cuda.Event(), torch.cuda.Event()]
+        out_done = [torch.cuda.Event(), torch.cuda.Event()]
+        for e_ in in_ready + computed + out_done:
+            e_.record(self.stream)
+        plan_us = []
+
+        moved = []
+
+        def h2d_into(i):
+            n = total
+            if self.planned:
+                in_ready[i].synchronize()     # the last copy out of this host buffer is done
+                t = time.perf_counter()
+                p = build_plan(i)             # the step's plan, into the pinned buffer
+                plan_us.append((time.perf_counter() - t) * 1e6)
+                n = plan_off + (p.bytes_used + 255) // 256 * 256
+            moved.append(n)
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(computed[i])     # the last step that read set i is done
+                dev_bufs[i][:n].copy_(host_bufs[i][:n], non_blocking=True)
+                in_ready[i].record(copy_stream)
+
+        def run_e2e(n):
+            h2d_into(0)
+            for k in range(n):
+                i = k % 2
+                self.stream.wait_event(in_ready[i])
+                self.stream.wait_event(out_done[i])      # read-back of step k-2 left set_outs[i]
+                steps_e2e[i]()
+                computed[i].record(self.stream)
+                if k + 1 < n:
+                    h2d_into(1 - i)
+                with torch.cuda.stream(copy_stream):
+                    copy_stream.wait_event(computed[i])
+                    out_host[i].copy_(set_outs[i], non_blocking=True)
+                    out_done[i].record(copy_stream)
+            self.stream.wait_stream(copy_stream)
+
+        run_e2e(max(3, min(warmup, 20)))
+        torch.cuda.synchronize(self.dev)
+        plan_us.clear()
+        moved.clear()
+        barrier(self.world)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(self.stream)
+        run_e2e(steps)
+        f1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        barrier(self.world)
+        e2e_ms = max_over_ranks(f0.elapsed_time(f1), self.world, self.dev)
+        self.check_err("end-to-end runs")
+        step_bytes = algorithmic_bytes(w, "step")
+        value = sum_over_ranks(step_bytes * steps, self.world, self.dev) / (e2e_ms / 1e3) / 1e9
+        rec = {"value": round(value, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(round(statistics.mean(moved))) if moved else total,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / steps, 5),
+               "pipelining": "copies of step k+1 and read-back of step k overlap step k; a "
+                             "step's inputs travel as one packed copy"}
+        if self.planned:
+            rec["plan_built_per_step"] = True
+            rec["plan_build_us_host_median"] = round(statistics.median(plan_us), 2) \
+                if plan_us else None
+        return rec
+
+    # -- results
+    def output_bits(self):
+        return self.synth.bits(self.outs)
+
+    def appended_rows(self):
+        """The pool's K and V rows at every sequence's appended slot, per layer:
+        uint16 [layers][B][2][Hkv][D]."""
+        torch, w = self.torch, self.w
+        pos = torch.from_numpy(w.positions.astype(np.int64)).to(self.dev)
+        bt = self.d["block_tables"].long()
+        blk = (pos // w.page_size).clamp(min=0)
+        pages = bt.gather(2, blk.view(1, -1, 1).expand(w.layers, -1, 1)).squeeze(2)
+        slot = (pos % w.page_size).view(1, -1).expand(w.layers, -1)
+        pool = self.d["pool"]
+        rows = pool[pages.clamp(min=0), :, slot]          # [layers][B][2][Hkv][D]
+        return self.synth.bits(rows)
+
+    def close(self):
+        for k in list(vars(self)):
+            if k not in ("torch", "binding", "synth", "w", "args", "dev", "world"):
+                delattr(self, k)
+        self.torch.cuda.synchronize(self.dev)
+        self.torch.cuda.empty_cache()
+
+
+def l2_flush_buffer(dev):
+    """A device buffer twice the L2 size, written between steps of the
+    L2-resident workloads."""
+    import torch
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (132 << 20)
+    return torch.empty(2 * l2, dtype=torch.uint8, device=dev), l2
+
+
+def measure_workload(name, args, dev, peak):
+    """One per-workload record: the step timed like the headline (repeated
+    regions of K steps; L2 flushed between steps when the workload fits in
+    L2), its roofline on the step's algorithmic bytes, the kernels' shares,
+    the oracle's time, and every output against the oracle."""
+    import torch
+    from paged_kv_decode_04_gb300 import synth
+    t_start = time.time()
+    w = synth.make_workload(name, args.seed)
+    db = DecodeBench(w, args, dev)
+    db.warm_and_capture(args.warmup, args.graph)
+    fits_l2 = w.kv_bytes() <= 96 * 2 ** 20
+    flush, l2 = l2_flush_buffer(dev) if fits_l2 else (None, 0)
+    times, _, _ = db.timed(args.steps, flush, min_seconds=0.5)
+    db.check_err("timed runs")
+    sp = spread(times, args.steps)
+    ms = sp["ms_per_step_median"]
+    step_bytes = algorithmic_bytes(w, "step")
+    gbs = step_bytes / (ms / 1e3) / 1e9
+    shares = db.kernel_shares()
+    got = db.output_bits()
+    rows = db.appended_rows()
+    rec = {
+        "workload": WORKLOAD_TEXT[name], "layers_per_step": w.layers,
+        "split_plan": db.split_text, "kernels": db.launched,
+        "algorithmic_bytes_per_step": step_bytes,
+        "ms_per_step": ms, "timing": sp,
+        "value": round(gbs, 2), "unit": "GB/s", "steps_per_s": round(1e3 / ms, 1),
+        "l2": (f"flushed: {2 * l2 >> 20} MiB written between steps, outside the per-step "
+               f"CUDA-event pairs (K/V {w.kv_bytes() / 2 ** 20:.1f} MiB per step fits in L2)"
+               if fits_l2 else f"inputs larger than L2: {w.kv_bytes() / 2 ** 30:.2f} GiB of "
+               f"K/V streamed per step; no flush"),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                     "frac": round(gbs / peak, 4), "unit": "GB/s",
+                     "basis": "the whole step's algorithmic bytes / its median CUDA-event time"},
+        "kernel_shares": shares,
+        "gpu_launches": db.kernels_per_layer * w.layers * args.steps * sp["repeats"],
+    }
+    if shares and "unavailable" not in shares:
+        dom = next(iter(shares))
+        rec["dominant_kernel"] = {"name": dom, "share": shares[dom]}
+        rec["roofline"]["traffic"] = recorded_traffic(name, db.launched + " (fused step)")
+    if name == "prefix":
+        ub = unique_bytes(w)
+        ug = ub / (ms / 1e3) / 1e9
+        rec["unique_bytes_per_step"] = ub
+        rec["roofline"] = {"bound": "hbm", "achieved": round(ug, 1), "peak": peak,
+                           "frac": round(ug / peak, 4), "unit": "GB/s",
+                           "basis": "bytes with every shared prefix page counted once per step "
+                                    "(what DRAM must deliver) / the median CUDA-event time",
+                           "traffic": recorded_traffic(name, db.launched + " (fused step)")}
+        rec["value"] = round(ug, 2)
+        rec["dedup_work_rate"] = {
+            "value": round(gbs, 2), "unit": "GB/s",
+            "what": "per-sequence algorithmic bytes (shared pages counted once per sequence "
+                    "that attends them) / step time: deduplicated work, not a bandwidth"}
+    db.close()
+    del flush
+    torch.cuda.empty_cache()
+    # the oracle: every sequence of every layer, all host cores; tiny and small
+    # also on one thread
+    dt, nb, threads, used, seqs, refs, slots = oracle_sample_run(w, w.batch, want_slots=True)
+    orc = {"seconds": round(dt, 4), "threads": threads, "value": round(nb / dt / 1e9, 4),
+           "unit": "GB/s", "sample": f"all {used} sequences x {w.layers} layer(s)"}
+    if name in ("tiny", "small"):
+        dt1, nb1, _, _, _, _ = oracle_sample_run(w, w.batch, threads=1)
+        orc["single_thread_seconds"] = round(dt1, 4)
+        orc["single_thread_value"] = round(nb1 / dt1 / 1e9, 4)
+    rec["oracle"] = orc
+    rec["speedup_vs_oracle"] = round(dt / (ms / 1e3), 1)
+    par = parity_report(got, refs)
+    par["appended_slots_bit_exact"] = bool(np.array_equal(rows, np.stack(slots)))
+    par["sequences"] = f"all {w.batch} x {w.layers} layer(s)"
+    rec["parity_vs_oracle"] = par
+    rec["wall_s"] = round(time.time() - t_start, 1)
+    return rec
+
+
+def measure_prefill(args, dev, peak):
+    """The paged prefill write (256 prompts x 2047 tokens) timed in repeated
+    regions; 4 prompts' pages compared bit for bit with the oracle's write."""
+    import torch
+    import oracle
+    from paged_kv_decode_04_gb300 import binding, synth
+    t_start = time.time()
+    p = synth.make_prefill(args.seed)
+    B, L = p.batch, p.prompt_len
+    k = synth.to_device_bf16(p.k, dev)
+    v = synth.to_device_bf16(p.v, dev)
+    off = torch.from_numpy(p.token_offsets).to(dev)
+    st = torch.from_numpy(p.start_positions).to(dev)
+    bt = torch.from_numpy(p.block_table).to(dev)
+    pool = torch.full((p.num_pages, 2, 16, 8, 64), -1, dtype=torch.int16,
+                      device=dev).view(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        binding.kv_write_prefill(k, v, off, st, pool, bt, dev_err=err)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    def region():
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    probe = region()
+    reps = int(min(MAX_REPEATS, max(MIN_REPEATS, math.ceil(0.5 / max(probe / 1e3, 1e-6)))))
+    times = [region() for _ in range(reps)]
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} in the prefill write")
+    sp = spread(times, args.steps)
+    ms = sp["ms_per_step_median"]
+    T = B * L
+    step_bytes = T * 8 * 64 * 2 * 2 * 2 + (B + 1) * 4 + B * 4 + B * p.block_table.shape[1] * 4
+    gbs = step_bytes / (ms / 1e3) / 1e9
+    # oracle: the write of 4 prompts into a compact pool of their pages
+    sample = [0, 1, B // 2, B - 1]
+    c = synth.compact_prefill(p, sample)
+    t0 = time.perf_counter()
+    rc = oracle.kv_write_prefill(c.k, c.v, c.token_offsets, c.start_positions, c.pool,
+                                 c.block_table)
+    dt = time.perf_counter() - t0
+    got = synth.bits(pool[torch.from_numpy(c.pages).to(dev)])
+    exact = rc == 0 and bool(np.array_equal(got, c.pool))
+    rec = {
+        "workload": PREFILL_TEXT, "algorithmic_bytes_per_step": step_bytes, "ms_per_step": ms,
+        "timing": sp, "value": round(gbs, 2), "unit": "GB/s",
+        "l2": "inputs larger than L2: 1.07 GB of new K/V read and written per call; no flush",
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                     "frac": round(gbs / peak, 4), "unit": "GB/s",
+                     "basis": "bytes of the call (new K/V read + pool write + offsets, positions, "
+                              "tables) / its median CUDA-event time"},
+        "dominant_kernel": {"name": "kv_write_prefill_kernel", "share": 1.0},
+        "oracle": {"seconds": round(dt, 4), "threads": 1,
+                   "value": round(len(sample) * L * 8 * 64 * 2 * 2 * 2 / dt / 1e9, 4),
+                   "unit": "GB/s", "sample": f"{len(sample)} of {B} prompts"},
+        "parity_vs_oracle": {"pages_compared": int(len(c.pages)),
+                             "bit_exact": exact, "sequences": f"{len(sample)} of {B} prompts"},
+        "gpu_launches": args.steps * sp["repeats"],
+    }
+    del pool, k, v
+    torch.cuda.empty_cache()
+    rec["wall_s"] = round(time.time() - t_start, 1)
+    return rec
 
 
 # ------------------------------------------------------------------ main --
@@ -325,299 +971,62 @@ def run_reference(args, world, rank):
 
 def run_ours(args, world, rank, local):
     import torch
-    from paged_kv_decode_04_gb300 import binding, synth
+    from paged_kv_decode_04_gb300 import synth
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
     w = synth.make_workload(args.workload, args.seed, num_pages=args.pool_pages)
-    d = synth.device_inputs(w, dev)
-    B, layers = w.batch, w.layers
-    stream = torch.cuda.current_stream(dev)
-    planned = args.plan in ("host", "lengths")
-    # the host plan is built from the lengths and layer 0's tables (shared
-    # prefixes become shared-prefix items); the workloads share the same runs
-    # of pages in every layer, so it serves every layer
-    plan_kw = {"block_tables": w.block_tables[0]} if args.plan == "host" else {}
-    plan = binding.Plan(w.seq_lens, w.max_blocks, device=dev, **plan_kw) if planned else None
+    db = DecodeBench(w, args, dev, world=world)
     plan_build_us = None
-    if planned:
+    if db.planned:
         # host cost of planning one step (a serving loop builds one plan per step)
+        from paged_kv_decode_04_gb300 import binding
         t = time.perf_counter()
         for _ in range(200):
-            binding.Plan(w.seq_lens, w.max_blocks, **plan_kw)
+            binding.Plan(w.seq_lens, w.max_blocks, **db.plan_kw)
         plan_build_us = round((time.perf_counter() - t) / 200 * 1e6, 2)
-    if planned:
-        d["plan"] = plan.dev
-        splits = max(1, max((int(m[2]) for m in plan.merges()), default=1))
-        ws_bytes = plan.workspace_bytes
-        split_text = (f"host work plan: {plan.num_items} items of at most {plan.range_pages} "
-                      f"pages or 4 packed sequences, {plan.num_merges} merged sequences")
-        if plan.num_shared:
-            split_text += (f", {plan.num_shared} shared-prefix items of at most "
-                           f"{plan.shared_pages} pages")
-    else:
-        splits = binding.plan_splits(B, w.max_blocks, args.splits)
-        ws_bytes = binding.workspace_bytes(B, w.max_blocks, args.splits)
-        split_text = f"fixed: {splits} ranges per sequence"
-    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    outs = torch.empty((layers, B, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    fused = args.path == "fused"
-    merges = (plan.num_merges > 0) if planned else (splits > 1)
-    launched = binding.attention_kernels(B, w.max_blocks, args.splits, plan)
-    kernels_per_layer = ((1 if fused else 2) + (1 if merges else 0)
-                         + (1 if planned and plan.num_shared else 0))
+    db.warm_and_capture(args.warmup, args.graph)
+    layers = w.layers
 
-    def plan_for(dset):
-        """The plan whose device copy is dset["plan"] (one per input set)."""
-        if not planned:
-            return None
-        if dset["plan"] is plan.dev:
-            return plan
-        p2 = copy.copy(plan)
-        p2.dev = dset["plan"]
-        return p2
-
-    def attend_on(dset, layer, out):
-        if planned:
-            binding.paged_decode_attention_planned(
-                dset["q"][layer], d["pool"], dset["block_tables"][layer], dset["seq_lens"],
-                plan_for(dset), out, scale=w.scale, workspace=workspace, dev_err=err)
-        else:
-            binding.paged_decode_attention(
-                dset["q"][layer], d["pool"], dset["block_tables"][layer], dset["seq_lens"], out,
-                scale=w.scale, workspace=workspace, num_splits=args.splits, dev_err=err)
-
-    def fused_on(dset, layer, out):
-        if planned:
-            binding.decode_step_planned(
-                dset["q"][layer], dset["k_new"][layer], dset["v_new"][layer], d["pool"],
-                dset["block_tables"][layer], dset["seq_lens"], plan_for(dset), out,
-                rope_theta=w.rope_theta, scale=w.scale, workspace=workspace, dev_err=err)
-        else:
-            binding.decode_step(
-                dset["q"][layer], dset["k_new"][layer], dset["v_new"][layer], d["pool"],
-                dset["block_tables"][layer], dset["seq_lens"], out, rope_theta=w.rope_theta,
-                scale=w.scale, workspace=workspace, num_splits=args.splits, dev_err=err)
-
-    def append_on(dset, layer):
-        binding.kv_append(dset["k_new"][layer], dset["v_new"][layer], d["pool"],
-                          dset["block_tables"][layer], dset["positions"], rope_theta=w.rope_theta,
-                          dev_err=err)
-
-    def attend(layer):
-        attend_on(d, layer, outs[layer])
-
-    def append(layer):
-        append_on(d, layer)
-
-    def fused_layer(layer):
-        fused_on(d, layer, outs[layer])
-
-    def launch_step():
-        """Enqueue one whole step (every layer) on the current stream."""
-        for layer in range(layers):
-            if fused:
-                fused_layer(layer)
-            else:
-                append(layer)
-                attend(layer)
-
-    # ---- warm-up (eager), then optionally capture one step as a CUDA graph
-    for _ in range(args.warmup):
-        launch_step()
-    torch.cuda.synchronize(dev)
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
-    if args.graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            launch_step()
-        for _ in range(3):
-            graph.replay()
-        torch.cuda.synchronize(dev)
-        run_step = graph.replay
-    else:
-        run_step = launch_step
-
-    # ---- timed region: K whole steps, device-resident inputs
+    # ---- timed: repeated regions of K whole steps, device-resident inputs
     sampler = ClockSampler(gpu_selector(local)) if rank == 0 else None
     if sampler:
         time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    e0.record(stream)
-    for _ in range(args.steps):
-        run_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    t_wall1 = time.time()
-    barrier(world)
+    times, t_wall0, t_wall1 = db.timed(args.steps)
     if sampler:
         sampler.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    db.check_err("timed runs")
+    sp = spread(times, args.steps)
+    ms_per_step = sp["ms_per_step_median"]
     step_bytes = algorithmic_bytes(w, "step")
-    total_bytes = sum_over_ranks(step_bytes * args.steps, world, dev)
-    value = total_bytes / (ms / 1e3) / 1e9
-    ms_per_step = ms / args.steps
+    total_bytes = sum_over_ranks(step_bytes, world, dev)
+    value = total_bytes / (ms_per_step / 1e3) / 1e9
 
-    # ---- per-kernel durations: CUDA events around each launch on the same stream.
-    # The launches are queued in chunks behind a short fixed-length busy kernel
-    # (torch.cuda._sleep) so that the host is ahead of the GPU and the events
-    # see back-to-back kernels, not the host's launch pace.
-    n_prof = min(args.steps, max(50, args.steps // 4))
-    kern = {}
-    chunk = 64
-
-    def prequeue(i):
-        if i % chunk == 0:
-            torch.cuda._sleep(int(2e9 * 100e-6 * min(chunk, n_prof - i) * layers))
-
-    if fused:
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_prof)]
-        for i in range(n_prof):
-            prequeue(i)
-            ev[i][0].record(stream)
-            for layer in range(layers):
-                fused_layer(layer)
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        per = [e[0].elapsed_time(e[1]) / layers for e in ev]
-        dom_ms = statistics.mean(per)
-        kern["decode_step_median"] = round(statistics.median(per) * 1e3, 2)
-        dom_bytes = algorithmic_bytes(w, "step") / layers
-        kern["decode_step"] = round(dom_ms * 1e3, 2)
-        dom_name = launched + " (fused step)"
-    else:
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_prof)]
-        for i in range(n_prof):
-            prequeue(i)
-            ev[i][0].record(stream)
-            for layer in range(layers):
-                append(layer)
-            ev[i][1].record(stream)
-            for layer in range(layers):
-                attend(layer)
-            ev[i][2].record(stream)
-        torch.cuda.synchronize(dev)
-        app_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / layers
-        dom_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) / layers
-        dom_bytes = algorithmic_bytes(w, "attention") / layers
-        kern["kv_append"] = round(app_ms * 1e3, 2)
-        kern["paged_decode_attention"] = round(dom_ms * 1e3, 2)
-        dom_name = launched + " (attention)"
+    # ---- per-kernel durations: CUDA events around each launch on the same stream
+    kern, dom_ms, dom_bytes, dom_name = db.per_launch(args.steps)
     peak, peak_kind = measured_hbm_peak()
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     duration_source = "CUDA events around each launch, in a separate pass of the same loop"
-    if fused and kernels_per_layer == 1:
+    if db.fused and db.kernels_per_layer == 1:
         # the timed steps are this one kernel, `layers` launches per step back to back: its
-        # average launch duration is the timed region's own CUDA-event time per launch (the
+        # average launch duration is the timed regions' own CUDA-event time per launch (the
         # separate pass above puts an event record between launches, which keeps each launch
         # from starting before the previous one has finished)
         dom_ms = ms_per_step / layers
         kern["decode_step_timed_region"] = round(dom_ms * 1e3, 2)
         achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-        duration_source = "timed region: CUDA events around the K steps, which are this kernel alone"
+        duration_source = ("timed regions: the median of the repeated CUDA-event regions of K "
+                           "steps, which are this kernel alone")
 
-    # ---- end to end: per-step inputs from pinned host memory, output back to host.
-    # Two device copies of the per-step inputs and outputs alternate, so the
-    # copies of step k+1 (and the read-back of step k) run on a copy stream
-    # while step k computes; every step still moves its own inputs in and its
-    # output out inside the timed region.  (Three sets on separate upload and
-    # read-back streams measured no better: short steps are bound by the
-    # host's per-step stream calls.)
-    names = ["q", "k_new", "v_new", "positions", "seq_lens", "block_tables"]
-    if planned:
-        names.append("plan")                  # the step's work plan travels with its inputs
-    # One pinned host buffer holds all of a step's inputs, each at a 256-byte
-    # aligned offset; a step moves it with one copy into one of two device
-    # buffers, and the step's graph reads views of that buffer.
-    layout, total = [], 0
-    for k in names:
-        nb = d[k].numel() * d[k].element_size()
-        layout.append((k, total, nb, d[k].dtype, tuple(d[k].shape)))
-        total += (nb + 255) // 256 * 256
-    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
-    for k, off, nb, _, _ in layout:
-        host_buf[off:off + nb].copy_(d[k].reshape(-1).view(torch.uint8).cpu())
-    dev_bufs = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
-    sets = [{k: buf[off:off + nb].view(dt).view(shape) for k, off, nb, dt, shape in layout}
-            for buf in dev_bufs]
-    for dset in sets:
-        for k in names:
-            dset[k].copy_(d[k])
-    out_host = [torch.empty(outs.shape, dtype=outs.dtype).pin_memory() for _ in range(2)]
-    h2d = total
-    d2h = out_host[0].numel() * out_host[0].element_size()
-    set_outs = [outs, torch.empty_like(outs)]
+    # ---- end to end: per-step plan built on the host, inputs from pinned host
+    # memory, output back to the host
+    e2e = db.e2e(args.steps, args.warmup)
 
-    def make_step(dset, out):
-        def launch():
-            for layer in range(layers):
-                if fused:
-                    fused_on(dset, layer, out[layer])
-                else:
-                    append_on(dset, layer)
-                    attend_on(dset, layer, out[layer])
-        if not args.graph:
-            return launch
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            launch()
-        return g.replay
-
-    steps_e2e = [make_step(sets[i], set_outs[i]) for i in range(2)]
-    copy_stream = torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event()
-    in_ready, computed, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-    for e_ in computed + out_done:
-        e_.record(stream)
-
-    def h2d_into(i):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(computed[i])     # the last step that read set i is done
-            dev_bufs[i].copy_(host_buf, non_blocking=True)
-            in_ready[i].record(copy_stream)
-
-    def run_e2e(n):
-        h2d_into(0)
-        for k in range(n):
-            i = k % 2
-            stream.wait_event(in_ready[i])
-            stream.wait_event(out_done[i])           # read-back of step k-2 left set_outs[i]
-            steps_e2e[i]()
-            computed[i].record(stream)
-            if k + 1 < n:
-                h2d_into(1 - i)
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(computed[i])
-                out_host[i].copy_(set_outs[i], non_blocking=True)
-                out_done[i].record(copy_stream)
-        stream.wait_stream(copy_stream)
-
-    run_e2e(max(3, min(args.warmup, 20)))
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    run_e2e(args.steps)
-    f1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
-    e2e_value = sum_over_ranks(step_bytes * args.steps, world, dev) / (e2e_ms / 1e3) / 1e9
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error bits {int(err.item())} during the timed runs")
-
-    # ---- CPU baseline: the oracle on a bounded sample of the same workload
+    # ---- CPU baseline: the oracle on a bounded sample of the same workload, and
+    # the same sample set against the GPU's outputs of the timed steps
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # repeat the bounded sample until it has used about 10 s of CPU time
         dt, nb, threads, used, seqs, refs = oracle_sample_run(w, args.cpu_seqs)
         reps = 1
         while dt * threads < 10.0 and reps < 30:
@@ -628,16 +1037,21 @@ def run_ours(args, world, rank, local):
                "sample": f"{used} of {w.batch} sequences x {w.layers} layer(s), {reps} time(s): "
                          f"FP64 append + two-pass attention, {dt:.2f} s wall on {threads} "
                          f"threads ({dt * threads:.1f} CPU-s)"}
-        # the same sample, set against the GPU's outputs of the timed steps
-        # (every step recomputes the same outputs from the same inputs)
-        got = outs.view(torch.int16).cpu().numpy().view(np.uint16)[:, seqs]
-        got = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-        ref = np.stack(refs)
-        err = np.abs(got - ref)
-        cpu["parity_vs_gpu"] = {
-            "max_abs_err": float(err.max()),
-            "worst_err_over_tolerance": float((err / (1e-3 + 8e-3 * np.abs(ref))).max()),
-            "tolerance": "|err| <= 1e-3 + 8e-3 |ref|"}
+        got = db.output_bits()[:, seqs]
+        cpu["parity_vs_gpu"] = parity_report(got, refs)
+    launched, kernels_per_layer, split_text, splits = (db.launched, db.kernels_per_layer,
+                                                       db.split_text, db.splits)
+    fused = db.fused
+    db.close()
+
+    # ---- the other workloads, each the same way (N = 1 only)
+    per = None
+    if rank == 0 and world == 1 and args.per_workload:
+        per = {}
+        for name in PER_WORKLOADS:
+            if name != args.workload:
+                per[name] = measure_workload(name, args, dev, peak)
+        per["prefill"] = measure_prefill(args, dev, peak)
 
     if rank != 0:
         return 0
@@ -661,6 +1075,7 @@ def run_ours(args, world, rank, local):
                   "working set fits in L2 (no flush): L2-resident figure",
             "parallelism": f"replicas x{world}",
         },
+        "timing": sp,
         "steps_per_s": round(1e3 / ms_per_step * world, 1),
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_copy": round(100 * value / world / peak, 2),
@@ -671,73 +1086,34 @@ def run_ours(args, world, rank, local):
                      "kernel": dom_name, "peak_kind": f"{peak_kind} copy bandwidth",
                      "bytes_per_launch": dom_bytes, "duration_source": duration_source},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 5),
-                "pipelining": "copies of step k+1 and read-back of step k overlap step k; "
-                              "a step's inputs travel as one packed copy"},
-        "gpu_launches": kernels_per_layer * layers * args.steps,
+        "e2e": e2e,
+        "gpu_launches": kernels_per_layer * layers * args.steps * sp["repeats"],
+        "gpu_launches_note": "library kernels launched in all the repeated timed regions",
         "clocks": clocks,
     }
+    if per is not None:
+        line["per_workload"] = per
     print(json.dumps(line), flush=True)
     return 0
 
 
 def run_prefill(args, world, rank, local):
-    """Throughput of the paged prefill write: 256 prompts x 2047 tokens per call."""
+    """Throughput of the paged prefill write alone: 256 prompts x 2047 tokens per call."""
     import torch
-    from paged_kv_decode_04_gb300 import binding
-
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
-    B, L, num_pages = 256, 2047, 40000
-    g = torch.Generator(device=dev).manual_seed(args.seed)
-    perm = torch.randperm(num_pages, generator=g, device=dev)[:B * 128].view(B, 128).int()
-    k = torch.randn((B * L, 8, 64), generator=g, device=dev).to(torch.bfloat16)
-    v = torch.randn((B * L, 8, 64), generator=g, device=dev).to(torch.bfloat16)
-    off = torch.arange(0, B * L + 1, L, dtype=torch.int32, device=dev)
-    st = torch.zeros(B, dtype=torch.int32, device=dev)
-    pool = torch.full((num_pages, 2, 16, 8, 64), -1, dtype=torch.int16, device=dev).view(
-        torch.bfloat16)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-
-    def step():
-        binding.kv_write_prefill(k, v, off, st, pool, perm, dev_err=err)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    T = B * L
-    step_bytes = T * 8 * 64 * 2 * 2 * 2 + (B + 1) * 4 + B * 4 + B * 128 * 4
-    value = sum_over_ranks(step_bytes * args.steps, world, dev) / (ms / 1e3) / 1e9
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error bits {int(err.item())}")
+    peak, _ = measured_hbm_peak()
+    rec = measure_prefill(args, dev, peak)
     if rank == 0:
-        peak, kind = measured_hbm_peak()
-        print(json.dumps({
-            "metric": "paged prefill write achieved HBM GB/s", "value": round(value, 2),
-            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "storage_dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": f"prefill write: {B} prompts x {L} tokens, 32q/8kv/64 bf16, "
-                                   f"{num_pages}-page pool", "seed": args.seed},
-            "algorithmic_bytes_per_step": step_bytes,
-            "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(value / world / peak, 4),
-                         "traffic": None, "kernel": "kv_write_prefill_kernel",
-                         "peak_kind": f"{kind} copy bandwidth"},
-            "gpu_launches": args.steps}), flush=True)
+        line = {"metric": "paged prefill write achieved HBM GB/s", "value": rec["value"],
+                "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": rec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "storage_dtype": "bf16",
+                "data": "synthetic", "config": {"workload": PREFILL_TEXT, "seed": args.seed}}
+        line.update({k: rec[k] for k in ("timing", "algorithmic_bytes_per_step", "roofline",
+                                         "parity_vs_oracle", "gpu_launches")})
+        print(json.dumps(line), flush=True)
     return 0
 
 
@@ -810,7 +1186,10 @@ def main(argv=None):
     ap.add_argument("--ref-seqs", type=int, default=1,
                     help="sequences per step of the --impl reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["decode", "prefill", "serve"], default="decode",
+    ap.add_argument("--per-workload", action=argparse.BooleanOptionalAction, default=True,
+                    help="after the headline, measure the other workloads and the prefill "
+                         "write the same way, each against the oracle (N = 1 only)")
+    ap.add_argument("--op",choices=["decode", "prefill", "serve"], default="decode",
                     help="decode: the decode step (headline); prefill: the paged prefill write; "
                          "serve: scheduler-driven serving simulation")
     ap.add_argument("--serve-requests", type=int, default=512)

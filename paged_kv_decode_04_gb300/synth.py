@@ -97,7 +97,7 @@ def _lengths(name: str, rng: np.random.Generator, batch: int) -> np.ndarray:
     raise ValueError(f"unknown workload {name!r}")
 
 
-# name -> (layers, batch, pool pages); see the design doc's input recipe.
+# name -> (layers, batch, pool pages) of each named workload.
 WORKLOADS = {
     "tiny": (1, 1, 64),
     "long": (16, 1, 4096),
@@ -228,14 +228,21 @@ class Compact:
 
 def compact(w: Workload, layer: int, seqs=None) -> Compact:
     seqs = np.arange(w.batch) if seqs is None else np.asarray(seqs, dtype=np.int64)
-    index_of = {int(p): i for i, p in enumerate(w.live_pages)}
+    # index of each physical page in page_data (-1: not live)
+    index_of = np.full(w.num_pages, -1, dtype=np.int64)
+    index_of[w.live_pages] = np.arange(len(w.live_pages), dtype=np.int64)
     bt = np.full((len(seqs), w.max_blocks), -1, dtype=np.int32)
-    pages = []
+    chunks = []
+    count = 0
     for r, b in enumerate(seqs):
-        for k, p in enumerate(w.pages_of(layer, int(b))):
-            bt[r, k] = len(pages)
-            pages.append(index_of[int(p)])
-    pool = w.page_data[np.asarray(pages, dtype=np.int64)] if pages else np.zeros(
+        ids = w.pages_of(layer, int(b)).astype(np.int64)
+        bt[r, :len(ids)] = np.arange(count, count + len(ids), dtype=np.int32)
+        chunks.append(index_of[ids])
+        count += len(ids)
+    pages = np.concatenate(chunks) if count else np.zeros(0, dtype=np.int64)
+    if np.any(pages < 0):
+        raise ValueError("a block table names a page that holds no live data")
+    pool = w.page_data[pages] if count else np.zeros(
         (0, 2, w.page_size, w.num_kv_heads, w.head_dim), dtype=np.uint16)
     pool = np.ascontiguousarray(pool)
     return Compact(seqs=seqs, pool=pool, block_table=bt,
@@ -245,7 +252,81 @@ def compact(w: Workload, layer: int, seqs=None) -> Compact:
                    v_new=np.ascontiguousarray(w.v_new[layer][seqs]))
 
 
+# --------------------------------------------------------------- prefill --
+
+@dataclass
+class Prefill:
+    """A ragged prefill batch: prompt b's tokens [token_offsets[b],
+    token_offsets[b+1]) of k and v go to positions start_positions[b] + i
+    through block_table row b (the prompt's pages, randomly scattered)."""
+    batch: int
+    prompt_len: int
+    num_pages: int
+    k: np.ndarray                 # uint16 [tokens][Hkv][D]
+    v: np.ndarray                 # uint16 [tokens][Hkv][D]
+    token_offsets: np.ndarray     # int32 [B + 1]
+    start_positions: np.ndarray   # int32 [B]
+    block_table: np.ndarray       # int32 [B][max_blocks]
+
+
+def make_prefill(seed: int = 0, batch: int = 256, prompt_len: int = 2047,
+                 num_pages: int = 40000, max_blocks: int = MAX_BLOCKS) -> Prefill:
+    """batch prompts of prompt_len tokens each, written from position 0; every
+    prompt owns ceil(prompt_len / 16) pages of a random permutation of the pool."""
+    full_seed = int(seed) * 1000 + 96
+    gen = torch.Generator().manual_seed(full_seed)
+    blocks = _num_blocks(prompt_len, PAGE_SIZE)
+    if batch * blocks > num_pages or blocks > max_blocks:
+        raise ValueError("the prompts do not fit the pool or the block table")
+    perm = torch.randperm(num_pages, generator=gen).numpy().astype(np.int32)
+    bt = np.full((batch, max_blocks), -1, dtype=np.int32)
+    bt[:, :blocks] = perm[:batch * blocks].reshape(batch, blocks)
+    n = batch * prompt_len * NUM_KV_HEADS * HEAD_DIM
+    k = _bf16_normal(gen, n).reshape(batch * prompt_len, NUM_KV_HEADS, HEAD_DIM)
+    v = _bf16_normal(gen, n).reshape(batch * prompt_len, NUM_KV_HEADS, HEAD_DIM)
+    offsets = np.arange(0, batch * prompt_len + 1, prompt_len, dtype=np.int32)
+    return Prefill(batch=batch, prompt_len=prompt_len, num_pages=num_pages, k=k, v=v,
+                   token_offsets=offsets, start_positions=np.zeros(batch, dtype=np.int32),
+                   block_table=bt)
+
+
+@dataclass
+class CompactPrefill:
+    """Some prompts of a Prefill relabelled onto a pool of only their pages
+    (poison-filled), for the oracle: pages[i] is the physical page of compact
+    page i."""
+    pages: np.ndarray
+    pool: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    token_offsets: np.ndarray
+    start_positions: np.ndarray
+    block_table: np.ndarray
+
+
+def compact_prefill(p: Prefill, prompts) -> CompactPrefill:
+    prompts = [int(b) for b in prompts]
+    blocks = _num_blocks(p.prompt_len, PAGE_SIZE)
+    bt = np.full((len(prompts), p.block_table.shape[1]), -1, dtype=np.int32)
+    bt[:, :blocks] = np.arange(len(prompts) * blocks, dtype=np.int32).reshape(-1, blocks)
+    pages = np.concatenate([p.block_table[b, :blocks] for b in prompts]).astype(np.int64)
+    ks = np.concatenate([p.k[p.token_offsets[b]:p.token_offsets[b + 1]] for b in prompts])
+    vs = np.concatenate([p.v[p.token_offsets[b]:p.token_offsets[b + 1]] for b in prompts])
+    lens = [int(p.token_offsets[b + 1] - p.token_offsets[b]) for b in prompts]
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    pool = np.full((len(pages), 2, PAGE_SIZE, NUM_KV_HEADS, HEAD_DIM), POISON, dtype=np.uint16)
+    return CompactPrefill(pages=pages, pool=pool, k=np.ascontiguousarray(ks),
+                          v=np.ascontiguousarray(vs), token_offsets=offsets,
+                          start_positions=p.start_positions[prompts].copy(), block_table=bt)
+
+
 # ---------------------------------------------------------- device views --
+
+def to_device_bf16(a: np.ndarray, device) -> torch.Tensor:
+    """uint16 bf16 bit patterns -> a bf16 tensor on `device`."""
+    return _to_bf16_tensor(a, device)
+
+
 
 def _to_bf16_tensor(a: np.ndarray, device) -> torch.Tensor:
     t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))

@@ -60,6 +60,9 @@ def test_static_scratch_matches_workspace_entry_point_twice():
             a = out.float().cpu().numpy()
             b = want.float().cpu().numpy()
             assert np.all(np.abs(a - b) <= TOL_ABS + TOL_REL * np.abs(b)), (splits, call)
+            # the same plan and kernels as the workspace entry point: the same bits,
+            # so a partial left in the buffer by an earlier call cannot hide
+            assert torch.equal(out.view(torch.int16), want.view(torch.int16)), (splits, call)
 
 
 def test_static_scratch_rejects_oversized_plans_before_launch():
