@@ -2,10 +2,8 @@
 FP64 CPU oracle, through the C-ABI binding.
 
 Appended K/V slots must match the oracle bit for bit; attention outputs must be
-within |err| <= 1e-3 + 8e-3 * |ref| element-wise.  Small workloads are checked
-on every output; the full-size ones (256 x 2048, and the 16-layer 8 GiB-pool
-mix) run the whole step on the GPU in the benchmark's launch configuration and
-are checked on sampled sequences plus size-independent properties.
+within |err| <= 1e-3 + 8e-3 * |ref| element-wise, on every output, the
+full-size workloads (256 x 2048, and the 16-layer 8 GiB-pool mix) included.
 """
 import functools
 
@@ -118,20 +116,14 @@ def test_page_permutation_is_bit_invisible():
 
 # ------------------------------------------------------------ full size, sampled --
 
-def test_peak_full_size_sampled():
+def test_peak_full_size_every_output():
     w = workload("peak")
     d = upload(w)
     err = new_err()
-    out = gpu_step(w, d, 0, dev_err=err)   # 256 x 2048, auto split plan as benchmarked
+    out = gpu_step(w, d, 0, dev_err=err)   # 256 x 2048, the two-kernel path, automatic split plan
     got = synth.bits(out)
-    rng = np.random.default_rng(0)
-    seqs = np.sort(rng.choice(w.batch, size=24, replace=False))
-    ref, _ = oracle_step(w, 0, seqs)
-    assert_close(got[seqs], ref, "peak sampled")
-    # size-independent properties on every output: finite, and inside the hull of V
-    vals = oracle.bf16_to_f64(got)
-    assert np.all(np.isfinite(vals))
-    assert np.abs(vals).max() <= 6.0   # |V| <= max |N(0,1) draw| (~5.8 for 2^30 draws)
+    ref, _ = oracle_step(w, 0)             # every sequence, all host cores
+    assert_close(got, ref, "peak, every output")
     # the appended slots of all 256 sequences, bit for bit
     kexp, vexp = appended_slots_expected(w, 0, range(w.batch))
     pos = torch.from_numpy(w.positions.astype(np.int64)).cuda()
@@ -143,19 +135,14 @@ def test_peak_full_size_sampled():
     assert int(err.item()) == 0
 
 
-def test_mix_full_size_sampled():
+def test_mix_full_size_every_output():
     w = workload("mix")
     d = upload(w)
     err = new_err()
     outs = [synth.bits(gpu_step(w, d, layer, dev_err=err)) for layer in range(w.layers)]
-    long_seqs = np.nonzero(w.seq_lens >= 1536)[0]
-    short_seqs = np.nonzero(w.seq_lens <= 128)[0][:8]
-    seqs = np.sort(np.concatenate([long_seqs, short_seqs]))
-    for layer in (0, 7, 15):
-        ref, _ = oracle_step(w, layer, seqs)
-        assert_close(outs[layer][seqs], ref, f"mix layer {layer}")
-    for layer in range(w.layers):
-        assert np.all(np.isfinite(oracle.bf16_to_f64(outs[layer])))
+    for layer in range(w.layers):          # every sequence of every layer
+        ref, _ = oracle_step(w, layer)
+        assert_close(outs[layer], ref, f"mix layer {layer}")
     torch.cuda.synchronize()
     assert int(err.item()) == 0
 

@@ -60,14 +60,13 @@ def test_shared_prefix_matches_oracle_and_private_copies(splits):
     assert int(err.item()) == 0
 
 
-def test_prefix_full_size_sampled():
+def test_prefix_full_size_every_output():
     dev = cuda_or_skip()
     w = synth.make_workload("prefix", 0)
     d = synth.device_inputs(w, dev)
     out = synth.bits(fused(w, d, d["block_tables"][0]))
-    seqs = np.array([0, 1, 15, 16, 130, 255])
-    ref, _ = oracle_step(w, 0, seqs)
-    assert_close(out[seqs], ref, "prefix 256 x 2048 sampled")
+    ref, _ = oracle_step(w, 0)
+    assert_close(out, ref, "prefix 256 x 2048, every sequence")
 
 
 # ------------------------------------------------ shared-prefix work plans --
@@ -112,8 +111,10 @@ def test_shared_plan_matches_oracle_fused_and_unfused():
     assert all(np.array_equal(x, outs[0]) for x in again)
 
 
-def test_shared_plan_full_size_sampled():
-    # the prefix workload itself: 256 x 2048, 16-way shared 1536-token prefixes
+def test_shared_plan_full_size_every_output():
+    # the prefix workload itself, in the benchmark's launch configuration:
+    # 256 x 2048, 16-way shared 1536-token prefixes, the fused step under the
+    # shared-prefix plan; every output and every appended slot
     dev = cuda_or_skip()
     b = binding()
     w = synth.make_workload("prefix", 0)
@@ -124,9 +125,38 @@ def test_shared_plan_full_size_sampled():
     out = synth.bits(planned(w, d, plan, dev_err=err))
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    seqs = np.array([0, 1, 7, 8, 15, 16, 130, 255])
-    ref, _ = oracle_step(w, 0, seqs)
-    assert_close(out[seqs], ref, "prefix 256 x 2048 under a shared plan, sampled")
+    ref, c = oracle_step(w, 0)
+    assert_close(out, ref, "prefix 256 x 2048 under a shared plan, every sequence")
+    pos = w.positions
+    pages = w.block_tables[0, np.arange(w.batch), pos // 16]
+    got = synth.bits(d["pool"][torch.from_numpy(pages).long().to(dev), :,
+                               torch.from_numpy(pos % 16).long().to(dev)])
+    want = c.pool[c.block_table[np.arange(w.batch), pos // 16], :, pos % 16]
+    assert np.array_equal(got, want)
+
+
+def test_shared_plan_with_a_diverging_member_table_is_reported():
+    # A shared plan says that every member's table holds the leader's page ids
+    # over the shared ranges.  A member whose table says otherwise (a plan
+    # built from another layer's tables, or tables changed since) would attend
+    # the leader's pages; the kernel compares the tables and reports it.
+    dev = cuda_or_skip()
+    b = binding()
+    w = synth.make_workload("prefix", 6, batch=32, num_pages=4096, share_group=16,
+                            share_blocks=64)
+    d = synth.device_inputs(w, dev)
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, block_tables=w.block_tables[0])
+    assert plan.num_shared > 0
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    planned(w, d, plan, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    bt = d["block_tables"][0]
+    bt[5, 10] = bt[20, 100]          # a valid page, but not the leader's shared one
+    planned(w, d, plan, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & b.DEVERR_PLAN
+    assert not int(err.item()) & (b.DEVERR_PAGE | b.DEVERR_TIMEOUT)
 
 
 def test_shared_plan_ragged_groups():
