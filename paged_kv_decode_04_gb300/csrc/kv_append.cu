@@ -32,21 +32,27 @@ constexpr int kAppendThreads = 256;
 constexpr int kHalf = kHeadDim / 2;
 constexpr int kRopeEntries = kRopeTablePositions * kHalf;
 
-// This device's cos/sin table and the theta it holds (NaN = none).
-__device__ __align__(16) float2 g_rope32[kRopeEntries];
-__device__ __align__(16) double2 g_rope64[kRopeEntries];
-__device__ double g_rope_theta;
+// This device's cos/sin tables: kRopeSlots slots, each built once for one
+// rope_theta and tagged with it afterwards (a tag of 0 = not built yet; a
+// valid theta is > 0).  A slot that holds a theta is never rewritten, so a
+// kernel that has read its tag can read its table while calls with other
+// thetas run on other streams; once every slot is taken, calls with a new
+// theta evaluate sincos in the kernels (the same values).
+constexpr int kRopeSlots = 4;
+__device__ __align__(16) float2 g_rope32[kRopeSlots][kRopeEntries];
+__device__ __align__(16) double2 g_rope64[kRopeSlots][kRopeEntries];
+__device__ double g_rope_theta[kRopeSlots];
 
-__global__ void rope_tag_kernel(double value) { g_rope_theta = value; }
+__global__ void rope_tag_kernel(int slot, double value) { g_rope_theta[slot] = value; }
 
-__global__ void __launch_bounds__(256) rope_table_kernel(RopeFreqs f) {
+__global__ void __launch_bounds__(256) rope_table_kernel(RopeFreqs f, int slot) {
   const int e = blockIdx.x * 256 + threadIdx.x;
   if (e >= kRopeEntries) return;
   const int pos = e / kHalf, i = e % kHalf;
   double sn, cs;
   sincos(__dmul_rn(static_cast<double>(pos), f.inv_freq[i]), &sn, &cs);
-  g_rope64[e] = make_double2(cs, sn);
-  g_rope32[e] = make_float2(static_cast<float>(cs), static_cast<float>(sn));
+  g_rope64[slot][e] = make_double2(cs, sn);
+  g_rope32[slot][e] = make_float2(static_cast<float>(cs), static_cast<float>(sn));
 }
 
 // One CTA per sequence, thread (h, i) rotates pair i of kv head h (and of
@@ -138,7 +144,7 @@ constexpr int kPfStageBytes = 2 * kPfHalfStage;
 constexpr int kPrefillSmemBatch = 2048;
 constexpr size_t kPfSmemBytes =
     static_cast<size_t>(kPfStages) * kPfStageBytes + 8 * kPfStages +
-    sizeof(int32_t) * (kPrefillSmemBatch + 1) + sizeof(int32_t) * kPfStages;
+    sizeof(int32_t) * (kPrefillSmemBatch + 1) + 2 * sizeof(int32_t) * kPfStages;
 
 // Where token t goes: its pool page (-1: skip), slot and position.
 struct PfDest {
@@ -286,11 +292,12 @@ __global__ void __launch_bounds__(kPfThreads)
                             const int32_t* __restrict__ start_positions,
                             uint16_t* __restrict__ pool, int64_t num_pages,
                             const int32_t* __restrict__ block_table, int max_blocks, int batch,
-                            RopeFreqs freqs, int32_t* dev_err) {
+                            RopeFreqs freqs, int32_t* dev_err, unsigned long long wait_ns) {
   extern __shared__ __align__(16) uint8_t pf_smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(pf_smem + kPfStages * kPfStageBytes);
   int32_t* s_off = reinterpret_cast<int32_t*>(bars + kPfStages);
   int32_t* done = s_off + kPrefillSmemBatch + 1;  // warps finished with each stage
+  int32_t* last_issued = done + kPfStages;       // the last chunk each stage was given
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -303,6 +310,7 @@ __global__ void __launch_bounds__(kPfThreads)
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(bar0 + 8 * s, 1);
       done[s] = 0;
+      last_issued[s] = -1;
     }
     fence_barrier_init();
   }
@@ -317,6 +325,7 @@ __global__ void __launch_bounds__(kPfThreads)
     const uint32_t bar = bar0 + 8 * st;
     const uint32_t dst = stage0 + st * kPfStageBytes;
     const int64_t src = static_cast<int64_t>(t0) * (kRowBytes / 2);
+    last_issued[st] = it;
     mbar_arrive_expect_tx(bar, 2 * bytes);
     bulk_load(dst, k + src, bytes, bar, policy);
     bulk_load(dst + kPfHalfStage, v + src, bytes, bar, policy);
@@ -354,7 +363,7 @@ __global__ void __launch_bounds__(kPfThreads)
       dst = prefill_dest(t0 + my_j, off, batch, start_positions, block_table, max_blocks,
                          num_pages, dev_err);
     const int st = it % kPfStages;
-    const bool ready = mbar_wait_bounded(bar0 + 8 * st, (it / kPfStages) & 1);
+    const bool ready = mbar_wait_bounded(bar0 + 8 * st, (it / kPfStages) & 1, wait_ns);
     if (!__all_sync(0xFFFFFFFFu, ready)) {
       // stop; the copies still in flight are drained below
       if (lane == 0) record_error(dev_err, kErrTimeout);
@@ -396,22 +405,23 @@ __global__ void __launch_bounds__(kPfThreads)
       }
     }
   }
-  // before the CTA exits, every copy it issued has landed (after a timeout,
-  // each wait is bounded again)
+  // before the CTA exits, every copy it issued has landed: after a timeout
+  // the phase of the last chunk each stage was given may still be pending (a
+  // stage is refilled only once every warp released its previous chunk, so
+  // it is the only one), waited for by the full limit
   __syncthreads();
   if (tid == 0)
-    for (int s = 0; s < kPfStages && s < my_chunks; ++s) {
-      const int last = s + ((my_chunks - 1 - s) / kPfStages) * kPfStages;
-      mbar_wait_bounded(bar0 + 8 * s, (last / kPfStages) & 1);
-    }
+    for (int s = 0; s < kPfStages; ++s)
+      if (last_issued[s] >= 0) mbar_wait_bounded(bar0 + 8 * s, (last_issued[s] / kPfStages) & 1);
 }
 
-// Device addresses of this device's table, looked up once per device.
+// Device addresses of this device's table slots (looked up once per device)
+// and the theta each slot was given (NaN: free).
 struct RopeTableAddrs {
   float2* t32 = nullptr;
   double2* t64 = nullptr;
   double* theta = nullptr;
-  double built_for = NAN;  // theta of the last rebuild enqueued on this device
+  double slot_theta[kRopeSlots] = {NAN, NAN, NAN, NAN};
 };
 
 std::mutex g_rope_mutex;
@@ -441,17 +451,23 @@ cudaError_t prepare_rope(double theta, RopeFreqs* f, cudaStream_t stream) {
     a.t64 = static_cast<double2*>(p64);
     a.theta = static_cast<double*>(pt);
   }
-  if (!(a.built_for == theta)) {
-    // invalidate, rebuild, then publish the theta -- in stream order
-    rope_tag_kernel<<<1, 1, 0, stream>>>(NAN);
-    rope_table_kernel<<<(kRopeEntries + 255) / 256, 256, 0, stream>>>(*f);
-    rope_tag_kernel<<<1, 1, 0, stream>>>(theta);
+  int slot = -1;
+  for (int s = 0; s < kRopeSlots && slot < 0; ++s)
+    if (a.slot_theta[s] == theta) slot = s;
+  if (slot < 0) {
+    for (int s = 0; s < kRopeSlots && slot < 0; ++s)
+      if (isnan(a.slot_theta[s])) slot = s;
+    if (slot < 0) return cudaSuccess;  // every slot holds another theta: sincos
+    // build, then tag -- in stream order; readers on any stream use the slot
+    // only once they read the tag
+    rope_table_kernel<<<(kRopeEntries + 255) / 256, 256, 0, stream>>>(*f, slot);
+    rope_tag_kernel<<<1, 1, 0, stream>>>(slot, theta);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    a.built_for = theta;
+    a.slot_theta[slot] = theta;
   }
-  f->table32 = a.t32;
-  f->table64 = a.t64;
-  f->table_theta = a.theta;
+  f->table32 = a.t32 + static_cast<size_t>(slot) * kRopeEntries;
+  f->table64 = a.t64 + static_cast<size_t>(slot) * kRopeEntries;
+  f->table_theta = a.theta + slot;
   return cudaSuccess;
 }
 
@@ -460,7 +476,8 @@ cudaError_t launch_kv_write_prefill(const uint16_t* k, const uint16_t* v, int nu
                                     const int32_t* start_positions, uint16_t* pool,
                                     int64_t num_pages, const int32_t* block_table,
                                     int max_blocks, int batch, const RopeFreqs& freqs,
-                                    int32_t* dev_err, cudaStream_t stream) {
+                                    int32_t* dev_err, unsigned long long wait_ns,
+                                    cudaStream_t stream) {
   if (num_tokens <= 0) return cudaSuccess;
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
@@ -488,7 +505,7 @@ cudaError_t launch_kv_write_prefill(const uint16_t* k, const uint16_t* v, int nu
   const int ctas = nchunks < cap ? nchunks : cap;
   return launch_pdl(kv_write_prefill_kernel, dim3(ctas), dim3(kPfThreads), kPfSmemBytes, stream,
                     k, v, num_tokens, token_offsets, start_positions, pool, num_pages,
-                    block_table, max_blocks, batch, freqs, dev_err);
+                    block_table, max_blocks, batch, freqs, dev_err, wait_ns);
 }
 
 cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new,

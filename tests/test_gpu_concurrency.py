@@ -65,3 +65,56 @@ def test_threads_on_their_own_streams_match_a_sequential_run():
     assert not errors, errors
     for i in range(THREADS):
         assert all(np.array_equal(a, c) for a, c in zip(results[i], want)), i
+
+
+def test_two_thetas_on_two_streams_interleaved_are_bit_exact():
+    # Appends with two rope_theta values, never seen before in this process,
+    # run interleaved on two streams with nothing ordering one stream against
+    # the other: each theta's first call builds its cos/sin table on its own
+    # stream while the other stream's kernels run.  Every appended K row must
+    # equal the oracle's rotation with its own theta, and every V row the new
+    # V, bit for bit (a table rewritten under a reader would give another
+    # theta's angles).
+    import oracle
+    from _gpu_util import bf16_normal
+    dev = cuda_or_skip()
+    b = binding()
+    thetas = (31415.5, 271828.25)
+    iters, batch, pages = 12, 64, 64 * 12
+    rng = np.random.default_rng(11)
+    pos = rng.integers(0, 2048, (2, iters, batch)).astype(np.int32)
+    k_new = bf16_normal(rng, (2, iters, batch, 8, 64))
+    v_new = bf16_normal(rng, (2, iters, batch, 8, 64))
+    # iteration i of stream s writes sequence r's token into page i * batch + r
+    bt = np.full((2, iters, batch, 128), -1, np.int32)
+    for i in range(iters):
+        bt[:, i, np.arange(batch), pos[0, i] // 16] = i * batch + np.arange(batch)
+        bt[1, i] = -1
+        bt[1, i, np.arange(batch), pos[1, i] // 16] = i * batch + np.arange(batch)
+    u16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    pools = [torch.full((pages, 2, 16, 8, 64), -1, dtype=torch.int16, device=dev).view(
+        torch.bfloat16) for _ in range(2)]
+    ks, vs = u16(k_new), u16(v_new)
+    bts = torch.from_numpy(bt).to(dev)
+    ps = torch.from_numpy(pos).to(dev)
+    errs = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in range(2)]
+    torch.cuda.synchronize(dev)
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    for i in range(iters):
+        for s in range(2):
+            with torch.cuda.stream(streams[s]):
+                b.kv_append(ks[s, i], vs[s, i], pools[s], bts[s, i], ps[s, i],
+                            rope_theta=thetas[s], dev_err=errs[s])
+    torch.cuda.synchronize(dev)
+    assert int(errs[0].item()) == 0 and int(errs[1].item()) == 0
+    for s in range(2):
+        pool = synth.bits(pools[s])
+        for i in range(iters):
+            for r in range(batch):
+                p = i * batch + r
+                slot = int(pos[s, i, r]) % 16
+                want_k = np.stack([oracle.rope_rotate(k_new[s, i, r, h], int(pos[s, i, r]),
+                                                      thetas[s]) for h in range(8)])
+                assert np.array_equal(pool[p, 0, slot], want_k), (s, i, r)
+                assert np.array_equal(pool[p, 1, slot], v_new[s, i, r]), (s, i, r)
