@@ -486,7 +486,8 @@ class DecodeBench:
 
     def check_err(self, when):
         if int(self.err.item()) != 0:
-            raise RuntimeError(f"device error bits {int(self.err.item())} during the {when}")
+            raise RuntimeError(f"device error bits {int(self.err.item())} during the {when} "
+                               f"({self.w.name} workload)")
 
     # -- timing
     def one_region(self, steps, flush=None):
@@ -582,51 +583,68 @@ class DecodeBench:
         return kern, dom_ms, dom_bytes, dom_name
 
     def kernel_shares(self, n=20):
-        """Each library kernel's share of the device time of n eager steps, from
-        the CUPTI kernel records torch.profiler collects (a ratio; no duration
-        taken under the profiler is reported)."""
+        """Each library kernel's share of the device time of n eager steps,
+        from the CUPTI kernel records torch.profiler collects (a ratio; no
+        duration taken under the profiler is reported).  Kernels launched with
+        programmatic dependent launch start before the previous kernel ends and
+        wait for it on the device, so a kernel is charged only for the time
+        after every earlier-started kernel has ended (the serialised
+        timeline)."""
         torch = self.torch
         try:
+            from torch.autograd import DeviceType
             from torch.profiler import ProfilerActivity, profile
+            with profile(activities=[ProfilerActivity.CUDA]):   # initialises CUPTI
+                self.launch_step()
+                torch.cuda.synchronize(self.dev)
             with profile(activities=[ProfilerActivity.CUDA]) as prof:
                 for _ in range(n):
                     self.launch_step()
                 torch.cuda.synchronize(self.dev)
-            totals = {}
-            for ev in prof.key_averages():
-                t = getattr(ev, "device_time_total", None)
-                if t is None:
-                    t = getattr(ev, "cuda_time_total", 0.0)
-                m = re.search(r"\b(" + "|".join(LIBRARY_KERNELS) + r")\b", ev.key)
-                if m and t:
-                    totals[m.group(1)] = totals.get(m.group(1), 0.0) + float(t)
-            s = sum(totals.values())
+            pat = re.compile(r"\b(" + "|".join(LIBRARY_KERNELS) + r")\b")
+            spans = []
+            for ev in prof.events():
+                if getattr(ev, "device_type", DeviceType.CUDA) != DeviceType.CUDA:
+                    continue
+                m = pat.search(ev.name)
+                if m:
+                    spans.append((ev.time_range.start, ev.time_range.end, m.group(1)))
+            spans.sort()
+            excl, last_end = {}, -math.inf
+            for t0, t1, name in spans:
+                s0 = max(t0, last_end)
+                excl[name] = excl.get(name, 0.0) + max(0.0, t1 - s0)
+                last_end = max(last_end, t1)
+            s = sum(excl.values())
             if s <= 0:
                 return None
-            return {k: round(v / s, 4) for k, v in sorted(totals.items(), key=lambda x: -x[1])}
+            return {k: round(v / s, 4) for k, v in sorted(excl.items(), key=lambda x: -x[1])}
         except Exception as exc:  # the profiler is optional on a box
             return {"unavailable": str(exc)[:120]}
 
     # -- end to end
     def e2e(self, steps, warmup):
-        """The same step through the public calls with every per-step input
-        coming from pinned host memory: the work plan is built on the host
-        from the host lengths (and tables) each step, packed with q, k_new,
-        v_new, positions, seq_lens and the block tables into one pinned buffer
-        and copied in one transfer; the output is copied back.  Two input sets
-        alternate so that the copies of step k+1 and the read-back of step k
-        overlap step k."""
+        """The same step with every per-step input coming from pinned host
+        memory and the output going back to it.  Each step the host builds the
+        step's work plan from the host lengths (and tables) through the C ABI,
+        straight into the pinned buffer that holds the step's packed inputs
+        (q, k_new, v_new, positions, seq_lens, block tables, plan), then
+        launches the step.  Two input sets alternate; the step of set s is one
+        CUDA graph: the upload of the NEXT step's packed inputs (set 1 - s,
+        one copy) runs beside this step's kernels, which are followed by the
+        read-back of this step's output.  So every step moves its own inputs
+        in and its output out, and the copies overlap the compute."""
         torch, w = self.torch, self.w
         names = ["q", "k_new", "v_new", "positions", "seq_lens", "block_tables"]
-        if self.planned:
-            names.append("plan")
         layout, total = [], 0
         for k in names:
             nb = self.d[k].numel() * self.d[k].element_size()
             layout.append((k, total, nb, self.d[k].dtype, tuple(self.d[k].shape)))
             total += (nb + 255) // 256 * 256
-        plan_off = dict((k, off) for k, off, _, _, _ in layout).get("plan")
-        plan_cap = 0
+        plan_off, plan_cap = total, 0
+        lens_host = np.ascontiguousarray(w.seq_lens.astype(np.int32))
+        bt_host = (np.ascontiguousarray(w.block_tables[0].astype(np.int32))
+                   if self.plan_mode == "host" else None)
         if self.planned:
             plan_cap = self.binding.plan_bytes(w.batch, w.max_blocks)
             total = plan_off + (plan_cap + 255) // 256 * 256
@@ -634,94 +652,80 @@ class DecodeBench:
         for hb in host_bufs:
             for k, off, nb, _, _ in layout:
                 hb[off:off + nb].copy_(self.d[k].reshape(-1).view(torch.uint8).cpu())
-        lens_host = np.ascontiguousarray(w.seq_lens.astype(np.int32))
-        plan_kw = dict(self.plan_kw)
-
-        def build_plan(i):
-            """This step's plan, built by the host into set i's pinned buffer."""
-            view = host_bufs[i][plan_off:plan_off + plan_cap].numpy().view(np.int32)
-            return self.binding.Plan(lens_host, w.max_blocks, out=view, **plan_kw)
-
+        plans = [None, None]
+        if self.planned:
+            for i in range(2):
+                view = host_bufs[i][plan_off:plan_off + plan_cap].numpy().view(np.int32)
+                plans[i] = self.binding.Plan(lens_host, w.max_blocks, out=view, **self.plan_kw)
+        n_copy = total if not self.planned else \
+            plan_off + (plans[0].bytes_used + 255) // 256 * 256
         dev_bufs = [torch.empty(total, dtype=torch.uint8, device=self.dev) for _ in range(2)]
         sets = [{k: buf[off:off + nb].view(dt).view(shape) for k, off, nb, dt, shape in layout}
                 for buf in dev_bufs]
-        plans = [None, None]
         for i, dset in enumerate(sets):
-            for k in names:
-                if k != "plan":
-                    dset[k].copy_(self.d[k])
+            dev_bufs[i][:n_copy].copy_(host_bufs[i][:n_copy])
             if self.planned:
-                plans[i] = build_plan(i)
-                n_words = plans[i].host.shape[0]
-                dset["plan"] = dev_bufs[i][plan_off:plan_off + 4 * n_words].view(torch.int32)
-                dset["plan"].copy_(torch.from_numpy(plans[i].host.copy()))
+                dset["plan"] = dev_bufs[i][plan_off:plan_off + plans[i].bytes_used].view(
+                    torch.int32)
         out_host = [torch.empty(self.outs.shape, dtype=self.outs.dtype).pin_memory()
                     for _ in range(2)]
         d2h = out_host[0].numel() * out_host[0].element_size()
         set_outs = [self.outs, torch.empty_like(self.outs)]
+        side = torch.cuda.Stream(self.dev)
 
-        def make_step(i):
-            dset, out = sets[i], set_outs[i]
+        def step_body(s):
+            """Upload set 1 - s (the next step's inputs) beside the kernels of
+            set s, then read set s's output back."""
+            cur = torch.cuda.current_stream(self.dev)   # the capture stream when capturing
+            fork = torch.cuda.Event()
+            fork.record(cur)
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                dev_bufs[1 - s][:n_copy].copy_(host_bufs[1 - s][:n_copy], non_blocking=True)
+            dset, out = sets[s], set_outs[s]
+            for layer in range(w.layers):
+                if self.fused:
+                    self.fused_on(dset, layer, out[layer])
+                else:
+                    self.append_on(dset, layer)
+                    self.attend_on(dset, layer, out[layer])
+            out_host[s].copy_(out, non_blocking=True)
+            cur.wait_stream(side)
 
-            def launch():
-                for layer in range(w.layers):
-                    if self.fused:
-                        self.fused_on(dset, layer, out[layer])
-                    else:
-                        self.append_on(dset, layer)
-                        self.attend_on(dset, layer, out[layer])
-            if not self.args.graph:
-                return launch
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                launch()
-            return g.replay
-
-        steps_e2e = [make_step(i) for i in range(2)]
-        copy_stream = torch.cuda.Stream(self.dev)
-        in_ready = [torch.cuda.Event(), torch.cuda.Event()]
-        computed = [torch.cuda.Event(), torch.cuda.Event()]
-        out_done = [torch.cuda.Event(), torch.cuda.Event()]
-        for e_ in in_ready + computed + out_done:
-            e_.record(self.stream)
+        graphs = []
+        for s in range(2):
+            if self.args.graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    step_body(s)
+                graphs.append(g.replay)
+            else:
+                graphs.append(lambda s=s: step_body(s))
+        done = [torch.cuda.Event(), torch.cuda.Event()]
         plan_us = []
 
-        moved = []
-
-        def h2d_into(i):
-            n = total
-            if self.planned:
-                in_ready[i].synchronize()     # the last copy out of this host buffer is done
-                t = time.perf_counter()
-                p = build_plan(i)             # the step's plan, into the pinned buffer
-                plan_us.append((time.perf_counter() - t) * 1e6)
-                n = plan_off + (p.bytes_used + 255) // 256 * 256
-            moved.append(n)
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(computed[i])     # the last step that read set i is done
-                dev_bufs[i][:n].copy_(host_bufs[i][:n], non_blocking=True)
-                in_ready[i].record(copy_stream)
-
         def run_e2e(n):
-            h2d_into(0)
+            # the first step's inputs (set 0), then each step uploads the next one's
+            dev_bufs[0][:n_copy].copy_(host_bufs[0][:n_copy], non_blocking=True)
+            done[1].record(self.stream)
             for k in range(n):
-                i = k % 2
-                self.stream.wait_event(in_ready[i])
-                self.stream.wait_event(out_done[i])      # read-back of step k-2 left set_outs[i]
-                steps_e2e[i]()
-                computed[i].record(self.stream)
-                if k + 1 < n:
-                    h2d_into(1 - i)
-                with torch.cuda.stream(copy_stream):
-                    copy_stream.wait_event(computed[i])
-                    out_host[i].copy_(set_outs[i], non_blocking=True)
-                    out_done[i].record(copy_stream)
-            self.stream.wait_stream(copy_stream)
+                s = k % 2
+                if self.planned:
+                    # host buffer 1 - s is about to be uploaded again: its last
+                    # upload (step k - 2's graph; for step 1 the first copy
+                    # above) must be over before the plan of step k + 1 is
+                    # built into it
+                    if k >= 1:
+                        done[s].synchronize()
+                    t = time.perf_counter()
+                    plans[1 - s].rebuild(lens_host, bt_host)
+                    plan_us.append((time.perf_counter() - t) * 1e6)
+                graphs[s]()
+                done[s].record(self.stream)
 
         run_e2e(max(3, min(warmup, 20)))
         torch.cuda.synchronize(self.dev)
         plan_us.clear()
-        moved.clear()
         barrier(self.world)
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
@@ -732,13 +736,16 @@ class DecodeBench:
         barrier(self.world)
         e2e_ms = max_over_ranks(f0.elapsed_time(f1), self.world, self.dev)
         self.check_err("end-to-end runs")
+        if self.planned:
+            for p in plans:       # the rebuilt plans are the plan the graphs were made with
+                assert np.array_equal(p.host, self.plan.host)
         step_bytes = algorithmic_bytes(w, "step")
         value = sum_over_ranks(step_bytes * steps, self.world, self.dev) / (e2e_ms / 1e3) / 1e9
-        rec = {"value": round(value, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(round(statistics.mean(moved))) if moved else total,
+        rec = {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": n_copy,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / steps, 5),
-               "pipelining": "copies of step k+1 and read-back of step k overlap step k; a "
-                             "step's inputs travel as one packed copy"}
+               "pipelining": "each step is one CUDA graph per input set: the upload of the next "
+                             "step's packed inputs runs beside this step's kernels, followed "
+                             "by the read-back of its output"}
         if self.planned:
             rec["plan_built_per_step"] = True
             rec["plan_build_us_host_median"] = round(statistics.median(plan_us), 2) \
@@ -1050,7 +1057,11 @@ def run_ours(args, world, rank, local):
         per = {}
         for name in PER_WORKLOADS:
             if name != args.workload:
+                print(f"[bench] {name} ...", file=sys.stderr, flush=True)
                 per[name] = measure_workload(name, args, dev, peak)
+                print(f"[bench] {name}: {per[name]['ms_per_step'] * 1e3:.2f} us per step, "
+                      f"{per[name]['value']} GB/s", file=sys.stderr, flush=True)
+        print("[bench] prefill ...", file=sys.stderr, flush=True)
         per["prefill"] = measure_prefill(args, dev, peak)
 
     if rank != 0:

@@ -21,15 +21,26 @@
  *  - Every tensor pointer is DEVICE memory owned by the caller, unless the
  *    comment says otherwise.  The library never allocates, frees or
  *    synchronizes; all work is enqueued on `stream` (NULL = the legacy
- *    default stream) and returns before it runs.  Calls are thread-safe.
- *    State kept between calls: a per-thread cache of TMA descriptors, the
- *    device's SM count, and one RoPE cos/sin table per device for positions
- *    below 2048 (1.5 MiB of static device memory).  The table is rebuilt on
- *    the calling stream whenever a call brings a rope_theta different from
- *    the last one seen on that device; kernels use it only while it holds
- *    their theta and otherwise evaluate sincos themselves, with identical
- *    results.  Calls with different rope_theta values must not run
- *    concurrently on one device (a rebuild would race with the readers).
+ *    default stream) and returns before it runs.  Calls are thread-safe,
+ *    also across streams.  State kept between calls: a per-thread cache of
+ *    TMA descriptors and of the wait limit (pkv_set_wait_limit_ns), the
+ *    device's SM count, and per device up to four RoPE cos/sin tables for
+ *    positions below 2048 (6 MiB of static device memory).  The first call
+ *    with a rope_theta not seen before on a device builds a table for it in
+ *    a free slot, on the calling stream, and tags the slot afterwards; a
+ *    tagged slot is never rewritten.  Kernels read a table only once they
+ *    have read its tag, and otherwise (table not built yet, or all four
+ *    slots taken by other thetas) evaluate sincos themselves.  So calls with
+ *    different thetas may run concurrently on any streams.  The library's
+ *    device state (these tables, the static scratch buffer below) belongs to
+ *    the CUDA context it was set up in: do not reset a device
+ *    (cudaDeviceReset) between calls.
+ *  - RoPE bit-exactness: keys are rotated in FP64 and rounded once to bf16,
+ *    as the oracle does.  cos and sin come from CUDA's FP64 sincos on the
+ *    device and from the C library on the oracle's side; where the two
+ *    libraries differ in the last FP64 bit, a bf16 rounding could flip (about
+ *    2^-44 per element, never observed over every position below 4096 for
+ *    the thetas tested).  "Bit-exact" below is relative to that.
  *  - Pool layout: [num_pages][2 (K, V)][page_size][num_kv_heads][head_dim]
  *    bf16, i.e. element ((page*2 + kv)*page_size + slot)*Hkv*D + h*D + d.
  *    The pool must be 16-byte aligned.
@@ -90,6 +101,23 @@ typedef struct CUstream_st* pkv_stream_t; /* same type as cudaStream_t */
 
 /* Library ABI version (bumped when a signature changes). */
 PKV_API int pkv_abi_version(void);
+
+/*
+ * Limit, in nanoseconds, of each wait a kernel makes on its own progress (a
+ * page copy landing, another warp role's hand-off, an MMA completing) for the
+ * kernels that the CALLING THREAD launches from now on; returns the previous
+ * value.  The default is 2,000,000,000 (2 s).  Past the limit a kernel stops
+ * waiting, ORs PKV_DEVERR_TIMEOUT into *dev_err, lets every copy and MMA it
+ * has started finish (those waits always take the full 2 s limit, so nothing
+ * it started is still running when it exits), frees what it holds and
+ * returns, so a stalled copy never hangs the stream; the outputs of a call
+ * that timed out are finite but not the attention result.  0 means a single
+ * look: a copy that has not landed when first waited for counts as a
+ * timeout (useful to exercise that path on normal inputs).  A CUDA graph
+ * keeps the value its captured launches were made with.  Host code only.
+ * (The source pages have no counterpart: failure handling of this library.)
+ */
+PKV_API unsigned long long pkv_set_wait_limit_ns(unsigned long long ns);
 
 /* Static description of a status code; never NULL. */
 PKV_API const char* pkv_strerror(int status);
@@ -412,8 +440,12 @@ PKV_API const char* pkv_attention_kernels(int batch, int max_blocks, int num_spl
  * num_splits (1 needs no scratch at all) or use the workspace entry point.
  *
  * The first call on each device looks up the device address of the scratch
- * buffer with that device current (cudaGetSymbolAddress) and caches it; make
- * that first call outside any stream capture.  All calls on a device share
+ * buffer with that device current (cudaGetSymbolAddress) and caches it; with
+ * lazy module loading that first call may also be the one that loads the
+ * library's device code and places the buffer.  So make one call on each
+ * device before any stream capture, and do not reset the device
+ * (cudaDeviceReset) or destroy its primary context between calls: the
+ * cached address belongs to the context it was taken in.  All calls on a device share
  * the one buffer: two calls whose kernels overlap in time on the GPU (for
  * example on two streams without an ordering between them) race on it and
  * produce garbage.  Calls ordered on one stream are safe.  The buffer keeps

@@ -55,6 +55,8 @@ def _load():
                                   ctypes.c_float, ctypes.c_double, ctypes.c_size_t)
     L.pkv_abi_version.argtypes = []
     L.pkv_abi_version.restype = i32
+    L.pkv_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    L.pkv_set_wait_limit_ns.restype = ctypes.c_ulonglong
     L.pkv_strerror.argtypes = [i32]
     L.pkv_strerror.restype = ctypes.c_char_p
     L.pkv_plan_splits.argtypes = [i32, i32, i32, i32]
@@ -111,6 +113,17 @@ def abi_version() -> int:
 
 def strerror(status: int) -> str:
     return _lib.pkv_strerror(status).decode()
+
+
+DEFAULT_WAIT_NS = 2_000_000_000
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of each in-kernel wait for the kernels this thread launches from
+    now on (pkv_set_wait_limit_ns); returns the previous limit."""
+    if ns < 0:
+        raise ValueError("the wait limit is a number of nanoseconds >= 0")
+    return int(_lib.pkv_set_wait_limit_ns(int(ns)))
 
 
 def plan_splits(batch: int, max_blocks: int, num_splits: int = 0,
@@ -397,13 +410,37 @@ class Plan:
         if rc != PKV_OK:
             raise PkvError(rc, what)
         self._raw = raw
-        self.host = buf[: int(buf[7]) // 4]
-        for i, name in enumerate(self.HEADER):
-            setattr(self, name, int(buf[i]))
-        self.workspace_bytes = int(_lib.pkv_plan_workspace_bytes(buf.ctypes.data_as(ctypes.c_void_p)))
+        self._buf = buf
+        self._args = (lens.shape[0], max_blocks, num_sms, int(min_shared_pages),
+                      buf.ctypes.data, nbytes)
+        self._read_header()
         self.dev = None
         if device is not None:
             self.to(device)
+
+    def _read_header(self):
+        buf = self._buf
+        self.host = buf[: int(buf[7]) // 4]
+        for i, name in enumerate(self.HEADER):
+            setattr(self, name, int(buf[i]))
+        self.workspace_bytes = int(_lib.pkv_plan_workspace_bytes(self._args[4]))
+
+    def rebuild(self, seq_lens_host, block_tables=None):
+        """Build this step's plan into the same buffer (what a serving loop does
+        every step): seq_lens_host and block_tables must be C-contiguous int32
+        numpy arrays of this plan's batch ([B], [B][max_blocks]); no copies are
+        made.  The device copy (``dev``) is not touched."""
+        B, max_blocks, num_sms, min_shared, buf_ptr, nbytes = self._args
+        if block_tables is None:
+            rc = _lib.pkv_plan_build(seq_lens_host.ctypes.data, B, max_blocks, num_sms, buf_ptr,
+                                     nbytes)
+        else:
+            rc = _lib.pkv_plan_build_shared(seq_lens_host.ctypes.data, block_tables.ctypes.data,
+                                            B, max_blocks, num_sms, min_shared, buf_ptr, nbytes)
+        if rc != PKV_OK:
+            raise PkvError(rc, "pkv_plan_build")
+        self._read_header()
+        return self
 
     def items(self) -> np.ndarray:
         """[num_items][16] int32: kind, slot, p_begin, n, seq[4], len[4], 0 x 4."""

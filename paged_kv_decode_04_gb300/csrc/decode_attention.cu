@@ -330,11 +330,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
   S.reset();
   for (int k = 0; k < nw; ++k) {
     const int st = k % kStages;
-    const bool ready = mbar_wait_bounded(bar0 + 8 * st, (k / kStages) & 1);
+    const bool ready = mbar_wait_bounded(bar0 + 8 * st, (k / kStages) & 1, a.wait_ns);
     if (!__all_sync(kFullMask, ready)) {
       // give up on this warp's pages, but not before the copies it issued
-      // (pages k .. k + kStages - 1) have landed -- each wait bounded again --
-      // since the epilogue reuses the stage buffers
+      // (pages k .. k + kStages - 1, one in flight per stage) have landed --
+      // each wait bounded again, by the full limit -- since the epilogue
+      // reuses the stage buffers
       if (lane == 0) {
         record_error(a.dev_err, kErrTimeout);
         for (int j = k; j < k + kStages && j < nw; ++j)

@@ -58,7 +58,7 @@ static_assert(kPbWarps * (2 * kGroup + kGroup * kHeadDim) * 4 <= kPbRingBytes,
 
 __host__ __device__ constexpr size_t pb_smem_bytes(int range_pages) {
   return 1024 /* alignment slack */ + kPbRingBytes + 8 * kPbStages /* bars */ +
-         4 * kPbStages /* counters */ + static_cast<size_t>(range_pages) * 4;
+         8 * kPbStages /* counters, last pages issued */ + static_cast<size_t>(range_pages) * 4;
 }
 
 // 4-D tiled copy of one whole page (coordinates {0, 0, 0, page}).
@@ -111,7 +111,8 @@ __global__ void __launch_bounds__(kPbThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPbRingBytes);
   int32_t* done = reinterpret_cast<int32_t*>(full + kPbStages);  // warps finished per stage
-  int32_t* s_pages = done + kPbStages;
+  int32_t* last_issued = done + kPbStages;  // the last page each stage was given (-1: none)
+  int32_t* s_pages = last_issued + kPbStages;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -178,6 +179,7 @@ __global__ void __launch_bounds__(kPbThreads, 2)
     for (int s = 0; s < kPbStages; ++s) {
       mbar_init(bar0 + 8 * s, 1);
       done[s] = 0;
+      last_issued[s] = -1;
     }
     fence_barrier_init();
   }
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(kPbThreads, 2)
     const int st = k % kPbStages;
     const int pid = s_pages[k];
     const uint32_t bar = bar0 + 8 * st;
+    last_issued[st] = k;
     if (pid >= 0) {
       mbar_arrive_expect_tx(bar, kPageBoxBytes);
       tma_load_page(ring0 + st * kPageBoxBytes, &page_map, bar, pid, policy);
@@ -219,9 +222,11 @@ __global__ void __launch_bounds__(kPbThreads, 2)
   S.reset();
   for (int k = 0; k < n; ++k) {
     const int st = k % kPbStages;
-    const bool ready = mbar_wait_bounded(bar0 + 8 * st, (k / kPbStages) & 1);
+    const bool ready = mbar_wait_bounded(bar0 + 8 * st, (k / kPbStages) & 1, a.wait_ns);
     if (!__all_sync(kFullMask, ready)) {
-      // stop; the copies this CTA issued are still to be drained (below)
+      // stop; the copies this CTA issued are still to be drained (below).
+      // This warp never releases stage st again, so the other warps time out
+      // on it in turn.
       if (lane == 0) record_error(a.dev_err, kErrTimeout);
       break;
     }
@@ -251,12 +256,14 @@ __global__ void __launch_bounds__(kPbThreads, 2)
   reduce_row_sums(S);
   __syncthreads();
   if (tid == 0) {
-    // after a timeout some boxes may still be in flight: wait for each stage's
-    // outstanding phase (bounded) before the ring is reused
-    for (int s = 0; s < kPbStages && s < n; ++s) {
-      const int last_k = s + ((n - 1 - s) / kPbStages) * kPbStages;  // last page of stage s
-      mbar_wait_bounded(bar0 + 8 * s, (last_k / kPbStages) & 1);
-    }
+    // after a timeout a box may still be in flight: wait (bounded by the full
+    // limit) for the phase of the last page each stage was given -- a stage
+    // is refilled only once every warp has released its previous page, so
+    // that is its only phase that can be outstanding -- before the ring is
+    // reused and the CTA exits
+    for (int s = 0; s < kPbStages; ++s)
+      if (last_issued[s] >= 0)
+        mbar_wait_bounded(bar0 + 8 * s, (last_issued[s] / kPbStages) & 1);
   }
   __syncthreads();
   float* sm_m = reinterpret_cast<float*>(smem);

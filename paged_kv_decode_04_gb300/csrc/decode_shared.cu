@@ -55,9 +55,11 @@
 //     own pages are attended by the ordinary planned kernels into the
 //     following slots, and the merge kernel combines them.
 // A shared page is never a member's last page, so every shared page is full
-// and none takes the step's append.  Every wait is bounded (kWaitLimitNs):
-// past it the kernel records PKV_DEVERR_TIMEOUT, lets outstanding copies and
-// MMAs finish (bounded too), frees its TMEM and returns.
+// and none takes the step's append.  Every wait is bounded: a wait on
+// another role's progress by the call's limit (2 s unless the caller set
+// another, pkv_set_wait_limit_ns); past it the kernel records
+// PKV_DEVERR_TIMEOUT, lets its outstanding copies and MMAs finish (waits
+// bounded by the full 2 s), frees its TMEM and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -243,6 +245,25 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     mbar_arrive(q_ready);  // S_0 may read Q
   }
 
+  // The plan says every member's table holds the leader's page ids over
+  // [p_begin, p_begin + n) in this layer; a member whose table says
+  // otherwise (a plan built from another layer's tables, or tables changed
+  // since) would silently attend the leader's K/V.  The idle lanes of the
+  // two issuer warps compare the entries while the stream runs and report a
+  // difference as PKV_DEVERR_PLAN.
+  auto check_members = [&](int t, int nt) {
+    bool differs = false;
+    const int total = (members - 1) * n;
+    for (int x = t; x < total; x += nt) {
+      const int m = 1 + x / n, i = x % n;
+      const int32_t pid =
+          a.block_table[static_cast<int64_t>(it[4 + m]) * a.max_blocks + p_begin + i];
+      const int32_t lead = s_pages[i];
+      if (lead >= 0 && pid != lead) differs = true;
+    }
+    if (differs) record_error(a.dev_err, kErrPlan);
+  };
+
   auto page_live = [&](int k) { return k < n && s_pages[k] >= 0; };
   auto batch_live = [&](int b) {
     int live = 0;
@@ -250,6 +271,14 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     return live;
   };
   int issued = 0;  // batches whose copies this producer issued
+  // softmax state (warps 0..3: thread = TMEM lane = MMA row), kept past the
+  // role loops for the epilogue
+  const int L = tid;
+  const int h = (L / kTcRows) & 1;  // 0: pages 0, 1 of each batch; 1: pages 2, 3
+  const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  float m_ref = -INFINITY, l_run = 0.f;
+  bool o_live = false;  // a PV MMA has been issued (O initialised)
+  bool ok = true;       // no wait of this softmax row timed out
 
   if (warp == kKLoadWarp || warp == kVLoadWarp) {
     // ----------------------------------------------------- TMA producers
@@ -260,7 +289,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       for (int b = 0; b < nb; ++b) {
         const uint32_t empty = is_k ? k_empty(b) : v_empty(b);
         const uint32_t full = is_k ? k_full(b) : v_full(b);
-        if (b >= slots && !mbar_wait_bounded(empty, ((b / slots) - 1) & 1)) {
+        if (b >= slots && !mbar_wait_bounded(empty, ((b / slots) - 1) & 1, a.wait_ns)) {
           record_error(a.dev_err, kErrTimeout);
           break;
         }
@@ -283,17 +312,17 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   } else if (warp == kSWarp) {
     // -------------------------------------------- S = Q K^T, 64 tokens
     if (lane == 0) {
-      bool ok = mbar_wait_bounded(q_ready, 0);
+      bool ok = mbar_wait_bounded(q_ready, 0, a.wait_ns);
       tc_fence_after_sync();
       for (int b = 0; b < nb && ok; ++b) {
         if (b >= 2) {  // PV_{b-2} has read P_{b-2} out of X(b mod 2)
-          if (!mbar_wait_bounded(x_free(b), ((b - 2) >> 1) & 1)) {
+          if (!mbar_wait_bounded(x_free(b), ((b - 2) >> 1) & 1, a.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
         }
-        if (!mbar_wait_bounded(k_full(b), (b / kKSlots) & 1)) {
+        if (!mbar_wait_bounded(k_full(b), (b / kKSlots) & 1, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -310,6 +339,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       if (!ok) record_error(a.dev_err, kErrTimeout);
       tc_commit(s_fin);
       if (!mbar_wait_bounded(s_fin, 0)) record_error(a.dev_err, kErrTimeout);
+    } else {
+      check_members(lane - 1, 62);
     }
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------- O += P V
@@ -317,7 +348,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       bool ok = true;
       uint32_t o_init = 0;
       for (int j = 0; j < nb; ++j) {
-        if (!mbar_wait_bounded(p_ready, j & 1) || !mbar_wait_bounded(v_full(j), (j / kVSlots) & 1)) {
+        if (!mbar_wait_bounded(p_ready, j & 1, a.wait_ns) ||
+            !mbar_wait_bounded(v_full(j), (j / kVSlots) & 1, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -338,19 +370,15 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       if (!ok) record_error(a.dev_err, kErrTimeout);
       tc_commit(pv_fin);
       if (!mbar_wait_bounded(pv_fin, 0)) record_error(a.dev_err, kErrTimeout);
+    } else {
+      check_members(31 + (lane - 1), 62);
     }
   } else {
     // --------------------------------------------------------- softmax
-    const int L = tid;          // TMEM lane = MMA row
-    const int h = L / kTcRows;  // 0: pages 0, 1 of each batch; 1: pages 2, 3
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const float c = a.scale_log2;
-    float m_ref = -INFINITY, l_run = 0.f;
-    bool o_live = false;  // a PV MMA has been issued (O initialised)
-    bool ok = true;
     const uint32_t zero16[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     for (int j = 0; j < nb; ++j) {
-      const bool ready = mbar_wait_bounded(s_ready(j), (j >> 1) & 1);
+      const bool ready = mbar_wait_bounded(s_ready(j), (j >> 1) & 1, a.wait_ns);
       if (!__all_sync(kFullMask, ready)) {
         ok = false;
         break;
@@ -407,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         // collective TMEM accesses; rows that did not move multiply by 1).
         // S_j needed PV_{j-2} done and PV_j needs this row's P_j, so pv_done
         // is within one phase of j - 1 here and its parity is unambiguous.
-        const bool done = j == 0 || mbar_wait_bounded(pv_done, (j - 1) & 1);
+        const bool done = j == 0 || mbar_wait_bounded(pv_done, (j - 1) & 1, a.wait_ns);
         if (!__all_sync(kFullMask, done)) {
           ok = false;
           break;
@@ -435,15 +463,30 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       mbar_arrive(p_ready);
       o_live = o_live || any_live;
     }
+  }
+
+  // ---- drain.  After a timeout a producer's copies may still be in flight:
+  // wait for the last batch each ring slot was given (a slot is refilled only
+  // after its previous batch was consumed, so that is the only one that can
+  // be pending), by the full limit.  Past the barrier below no copy and no
+  // MMA of this CTA is in flight (the issuers waited for their last commits,
+  // s_fin and pv_fin), so the epilogue may read O from TMEM and reuse the K
+  // ring for the row exchange.
+  if ((warp == kKLoadWarp || warp == kVLoadWarp) && lane == 0) {
+    const bool is_k = warp == kKLoadWarp;
+    const int slots = is_k ? kKSlots : kVSlots;
+    for (int s = 0; s < slots && s < issued; ++s) {
+      const int last_b = s + ((issued - 1 - s) / slots) * slots;
+      if (!mbar_wait_bounded(is_k ? k_full(last_b) : v_full(last_b), (last_b / slots) & 1))
+        record_error(a.dev_err, kErrTimeout);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+
+  if (warp < kTcSoftmaxWarps) {
     // ---- epilogue: combine the two copies of each query row, then write
     // the row's partial (max, sum, acc) to its member's slot
-    if (ok) {
-      // every PV done: pv_fin completes once, after the last of them (two
-      // phases of pv_done may still be pending here, which a parity wait
-      // could not tell from none)
-      const bool done = mbar_wait_bounded(pv_fin, 0);
-      ok = __all_sync(kFullMask, done);
-    }
     if (!ok && lane == 0) record_error(a.dev_err, kErrTimeout);
     uint32_t o[kHeadDim / 16][16];
     tc_fence_after_sync();
@@ -499,25 +542,13 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     }
   }
 
-  // ---- teardown.  Past this barrier every MMA is done (the issuers waited
-  // for their last commits) and every TMEM read has completed, so the
-  // columns go back at once; the producers still wait for any copy in
-  // flight (only after a timeout) before the shared memory is released.
+  // ---- teardown: every TMEM read is done, so the columns go back
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kPvWarp) {
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
-  }
-  if ((warp == kKLoadWarp || warp == kVLoadWarp) && lane == 0) {
-    const bool is_k = warp == kKLoadWarp;
-    const int slots = is_k ? kKSlots : kVSlots;
-    for (int s = 0; s < slots && s < issued; ++s) {
-      const int last_b = s + ((issued - 1 - s) / slots) * slots;
-      if (!mbar_wait_bounded(is_k ? k_full(last_b) : v_full(last_b), (last_b / slots) & 1))
-        record_error(a.dev_err, kErrTimeout);
-    }
   }
 }
 

@@ -18,6 +18,18 @@ using pkv::kNumKvHeads;
 using pkv::kNumQHeads;
 using pkv::kPageSize;
 
+namespace pkv {
+
+// The calling thread's limit on each in-kernel wait (pkv_set_wait_limit_ns).
+unsigned long long& t_wait_ns_ref() {
+  thread_local unsigned long long ns = kDefaultWaitNs;
+  return ns;
+}
+
+unsigned long long wait_limit_ns() { return t_wait_ns_ref(); }
+
+}  // namespace pkv
+
 namespace {
 
 bool aligned(const void* p, uintptr_t a) {
@@ -227,6 +239,7 @@ cudaError_t launch_attention(const pkv::SplitPlan& plan, const void* pool, int64
   args.batch = batch;
   args.scale_log2 = scale * 1.4426950408889634f;
   args.plan = plan;
+  args.wait_ns = pkv::wait_limit_ns();
   CUtensorMap map;
   if (use_pagebox(static_cast<long long>(batch) * plan.num_splits, plan.pages_per_split)) {
     if (!pool_page_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
@@ -244,6 +257,12 @@ cudaError_t launch_attention(const pkv::SplitPlan& plan, const void* pool, int64
 extern "C" {
 
 PKV_API int pkv_abi_version(void) { return 1; }
+
+PKV_API unsigned long long pkv_set_wait_limit_ns(unsigned long long ns) {
+  const unsigned long long prev = pkv::t_wait_ns_ref();
+  pkv::t_wait_ns_ref() = ns;
+  return prev;
+}
 
 PKV_API const char* pkv_strerror(int status) {
   switch (status) {
@@ -328,7 +347,7 @@ PKV_API int pkv_kv_write_prefill(const pkv_bf16* k, const pkv_bf16* v, int num_t
     return PKV_ECUDA;
   const cudaError_t err = pkv::launch_kv_write_prefill(
       k, v, num_tokens, token_offsets, start_positions, pool, num_pages, block_table, max_blocks,
-      batch, freqs, dev_err, reinterpret_cast<cudaStream_t>(stream));
+      batch, freqs, dev_err, pkv::wait_limit_ns(), reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -467,16 +486,67 @@ struct PlanHeader {
 };
 static_assert(sizeof(PlanHeader) == 4 * pkv::kPlanHeaderWords, "plan header layout");
 
+// True when every index a kernel takes from the plan's body stays inside the
+// buffers it addresses: sequences in [0, batch), page ranges inside the table
+// and within the page list the launch sizes (range_pages, shared_pages),
+// partial slots in [0, num_slots), shared items with 1..16 members.  A plan
+// from pkv_plan_build / pkv_plan_build_shared always passes; a hand-made or
+// damaged one is refused before anything is launched.
+bool plan_body_valid(const PlanHeader& h) {
+  const int32_t* w = reinterpret_cast<const int32_t*>(&h) + pkv::kPlanHeaderWords;
+  auto seq_ok = [&](int32_t b) { return b >= 0 && b < h.batch; };
+  auto range_ok = [&](int32_t p, int32_t n, int32_t cap) {
+    return p >= 0 && n >= 0 && n <= cap && static_cast<int64_t>(p) + n <= h.max_blocks;
+  };
+  const int64_t lmax = static_cast<int64_t>(h.max_blocks) * kPageSize;
+  for (int i = 0; i < h.num_items; ++i, w += pkv::kPlanItemWords) {
+    if (w[0] == pkv::kPlanKindRange) {
+      if (!seq_ok(w[4]) || !range_ok(w[2], w[3], h.range_pages)) return false;
+      if (w[1] != -1 && (w[1] < 0 || w[1] >= h.num_slots)) return false;
+    } else if (w[0] == pkv::kPlanKindPacked) {
+      if (w[1] != -1) return false;
+      for (int k = 0; k < pkv::kPlanWarps; ++k)
+        if (w[4 + k] != -1 && (!seq_ok(w[4 + k]) || w[8 + k] < 0 || w[8 + k] > lmax))
+          return false;
+    } else {
+      return false;
+    }
+  }
+  for (int i = 0; i < h.num_merges; ++i, w += pkv::kPlanMergeWords)
+    if (!seq_ok(w[0]) || w[1] < 0 || w[2] < 1 ||
+        static_cast<int64_t>(w[1]) + w[2] > h.num_slots)
+      return false;
+  for (int i = 0; i < h.num_shared; ++i, w += pkv::kPlanSharedWords) {
+    const int members = w[0];
+    if (members < 1 || members > pkv::kSharedMembers || w[2] < 1 ||
+        !range_ok(w[1], w[2], h.shared_pages))
+      return false;
+    for (int m = 0; m < members; ++m)
+      if (!seq_ok(w[4 + m]) || w[4 + pkv::kSharedMembers + m] < 0 ||
+          w[4 + pkv::kSharedMembers + m] >= h.num_slots)
+        return false;
+  }
+  return true;
+}
+
 // The plan's header when it is well formed for this batch and table, else nullptr.
 const PlanHeader* plan_header(const void* plan, int batch, int max_blocks) {
   if (plan == nullptr || !aligned(plan, 16)) return nullptr;
   const PlanHeader* h = static_cast<const PlanHeader*>(plan);
   if (h->magic != static_cast<int32_t>(PKV_PLAN_MAGIC) || h->batch != batch ||
       h->max_blocks != max_blocks || h->num_items < 1 || h->num_items > 65535 ||
-      h->num_merges < 0 || h->num_slots < 0 || h->range_pages < 1 || h->range_pages > 1024 ||
-      h->num_shared < 0 || h->num_shared > 65535 ||
+      h->num_merges < 0 || h->num_merges > batch || h->num_slots < 0 ||
+      h->range_pages < 1 || h->range_pages > 1024 || h->num_shared < 0 ||
+      h->num_shared > 65535 ||
       (h->num_shared > 0 && (h->shared_pages < 1 || h->shared_pages > 1024)))
     return nullptr;
+  // bytes_used is exactly the header and the three sections the counts imply
+  const int64_t words = pkv::kPlanHeaderWords +
+                        static_cast<int64_t>(h->num_items) * pkv::kPlanItemWords +
+                        static_cast<int64_t>(h->num_merges) * pkv::kPlanMergeWords +
+                        static_cast<int64_t>(h->num_shared) * pkv::kPlanSharedWords;
+  if (static_cast<int64_t>(h->bytes_used) != 4 * words) return nullptr;
+  if (!plan_body_valid(*h)) return nullptr;
   return h;
 }
 
@@ -522,6 +592,7 @@ cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pa
   args.scale_log2 = scale * 1.4426950408889634f;
   args.plan.num_splits = 1;
   args.plan.pages_per_split = h.range_pages;
+  args.wait_ns = pkv::wait_limit_ns();
   CUtensorMap map;
   if (h.num_shared > 0) {
     // shared prefixes first: their partials join the members' own ones in
@@ -724,7 +795,8 @@ PKV_API int pkv_kv_write_prefill_layers(int layers, const pkv_bf16* k, const pkv
   for (int l = 1; l < layers; ++l) {
     const cudaError_t err = pkv::launch_kv_write_prefill(
         k + l * kv_stride, v + l * kv_stride, num_tokens, token_offsets, start_positions, pool,
-        num_pages, block_tables + l * bt_stride, max_blocks, batch, freqs, dev_err, st);
+        num_pages, block_tables + l * bt_stride, max_blocks, batch, freqs, dev_err,
+        pkv::wait_limit_ns(), st);
     if (err != cudaSuccess) return PKV_ECUDA;
   }
   return PKV_OK;

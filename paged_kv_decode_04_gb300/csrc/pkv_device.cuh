@@ -12,8 +12,11 @@
 namespace pkv {
 
 // Upper bound for one in-kernel wait on a page copy: past it the kernel
-// records kErrTimeout and stops waiting instead of spinning forever.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// records kErrTimeout and stops waiting instead of spinning forever.  The
+// waits on a kernel's progress take the per-call limit (AttnArgs::wait_ns,
+// this value unless the caller set another); the drains after a timeout
+// always take this one.
+constexpr unsigned long long kWaitLimitNs = kDefaultWaitNs;
 
 // Programmatic dependent launch.  Every library kernel is launched allowed to
 // start before the previous kernel on its stream has finished; it calls
@@ -85,14 +88,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for phase `parity` of a barrier, giving up after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar,
-                                                  uint32_t parity) {
+// Non-blocking look at phase `parity` of a barrier.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for phase `parity` of a barrier, giving up after limit_ns nanoseconds
+// (0: a single non-blocking look, so a phase that has not completed by then
+// counts as a timeout).  The kernels' waits on their own progress take the
+// caller's limit (pkv_set_wait_limit_ns, 2 s by default); the waits that
+// drain a CTA's own copies and MMAs after a timeout always take
+// kWaitLimitNs, so nothing the CTA started is still running when it exits.
+//
+// The time waited is the sum of the forward steps of %globaltimer between
+// looks, each counted up to kTimerStepCapNs: the global timer is kept in step
+// with the host clock, and a step back (which an unsigned difference from a
+// start time would read as an enormous wait) or a jump forward must not end a
+// wait early.
+constexpr unsigned long long kTimerStepCapNs = 1000000ull;  // 1 ms
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns == 0) return mbar_test_wait(bar, parity);
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
+  unsigned long long last = global_timer_ns(), waited = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 7u) == 0u) {
+      const unsigned long long now = global_timer_ns();
+      if (now > last) waited += min(now - last, kTimerStepCapNs);
+      last = now;
+      if (waited > limit_ns) return false;
+    }
   }
 }
 

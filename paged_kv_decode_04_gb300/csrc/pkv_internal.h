@@ -16,6 +16,10 @@ constexpr int kNumKvHeads = 8;
 constexpr int kNumQHeads = 32;
 constexpr int kGroup = kNumQHeads / kNumKvHeads;  // 4 query rows per kv head
 
+// Default limit of a kernel's wait on its own progress (a page copy, an MMA,
+// another role's hand-off), in nanoseconds: 2 s (pkv_set_wait_limit_ns).
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+
 // Device error bits (mirror PKV_DEVERR_* in pkv.h).
 constexpr int kErrPage = 1;
 constexpr int kErrSeqLen = 2;
@@ -110,7 +114,8 @@ cudaError_t launch_kv_write_prefill(const uint16_t* k, const uint16_t* v, int nu
                                     const int32_t* start_positions, uint16_t* pool,
                                     int64_t num_pages, const int32_t* block_table,
                                     int max_blocks, int batch, const RopeFreqs& freqs,
-                                    int32_t* dev_err, cudaStream_t stream);
+                                    int32_t* dev_err, unsigned long long wait_ns,
+                                    cudaStream_t stream);
 
 struct AttnArgs {
   const uint16_t* q;
@@ -128,7 +133,11 @@ struct AttnArgs {
   int batch;
   float scale_log2;  // softmax scale * log2(e)
   SplitPlan plan;
+  unsigned long long wait_ns;  // limit of each wait on the kernel's progress
 };
+
+// The calling thread's wait limit (pkv_set_wait_limit_ns), for the launches.
+unsigned long long wait_limit_ns();
 
 // Extra inputs of the fused decode step: the new token of every sequence is
 // appended at position seq_lens[b] - 1 by the attention kernel itself.

@@ -31,6 +31,19 @@ struct Range {
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
+// Stable counting sort of v by key(x) in [0, nkeys), ascending; the keys here
+// are small page counts, so this is a few linear passes (a comparison sort of
+// a 256-sequence batch took most of the plan's host time).
+template <typename T, typename Key>
+void counting_sort(std::vector<T>& v, int nkeys, Key key) {
+  std::vector<int> first(static_cast<size_t>(nkeys) + 1, 0);
+  for (const T& x : v) ++first[static_cast<size_t>(key(x)) + 1];
+  for (int k = 0; k < nkeys; ++k) first[k + 1] += first[k];
+  std::vector<T> out(v.size());
+  for (const T& x : v) out[first[key(x)]++] = x;
+  v.swap(out);
+}
+
 }  // namespace
 
 size_t plan_bytes(int batch, int max_blocks) {
@@ -107,16 +120,16 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
       group_of[groups[gi].first + m] = static_cast<int>(gi);
     }
   // what the per-sequence items attend: own pages; members never packed
-  std::vector<int> own(batch), asc;
+  std::vector<int> own(batch), solo;  // solo: pages of the sequences in no group
+  solo.reserve(batch);
   long long total = 0;
   for (int b = 0; b < batch; ++b) {
     own[b] = pages[b] - start[b];
     total += own[b];
-    if (group_of[b] < 0) asc.push_back(own[b]);
+    if (group_of[b] < 0) solo.push_back(own[b]);
   }
-  std::sort(asc.begin(), asc.end());
   auto count = [&](Sizes z) {
-    long long items = count_items(asc, z);
+    long long items = count_items(solo, z);
     for (int b = 0; b < batch; ++b)
       if (group_of[b] >= 0) items += (own[b] + z.range - 1) / z.range;
     return items;
@@ -155,6 +168,8 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
   std::vector<Range> ranges;
   std::vector<int> packed;
   std::vector<int32_t> merges;  // (b, first slot, ranges, 0) per split sequence
+  ranges.reserve(batch);
+  packed.reserve(batch);
   std::vector<int> slot_base(batch, -1);
   int slots = 0;
   for (int b = 0; b < batch; ++b) {
@@ -179,21 +194,28 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
       slots += ns + nr;
     }
   }
-  std::stable_sort(packed.begin(), packed.end(),
-                   [&](int x, int y) { return pages[x] > pages[y]; });
-  // work items with the pages of their busiest warp, then a stable sort
+  // packed sequences by pages, most first (stable); packed ones have at most
+  // pack_max <= kPackPages pages
+  counting_sort(packed, kPackPages + 1, [&](int b) { return kPackPages - pages[b]; });
+  // work items with the pages of their busiest warp, most first, ranges
+  // before packed items on ties (stable)
   struct Item {
     int work, kind, index;  // index into ranges or into packed (first of 4)
   };
   std::vector<Item> order;
-  for (size_t i = 0; i < ranges.size(); ++i)
+  order.reserve(ranges.size() + packed.size() / kPlanWarps + 1);
+  int max_work = 0;
+  for (size_t i = 0; i < ranges.size(); ++i) {
     order.push_back({(ranges[i].n + kPlanWarps - 1) / kPlanWarps, kPlanKindRange,
                      static_cast<int>(i)});
-  for (size_t i = 0; i < packed.size(); i += kPlanWarps)
+    max_work = std::max(max_work, order.back().work);
+  }
+  for (size_t i = 0; i < packed.size(); i += kPlanWarps) {
     order.push_back({pages[packed[i]], kPlanKindPacked, static_cast<int>(i)});
-  std::stable_sort(order.begin(), order.end(), [](const Item& x, const Item& y) {
-    return x.work != y.work ? x.work > y.work : x.kind < y.kind;
-  });
+    max_work = std::max(max_work, order.back().work);
+  }
+  counting_sort(order, 2 * (max_work + 1),
+                [&](const Item& x) { return 2 * (max_work - x.work) + x.kind; });
   const size_t num_items = order.size();
   const size_t num_merges = merges.size() / kPlanMergeWords;
   size_t num_shared = 0;

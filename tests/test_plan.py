@@ -343,3 +343,83 @@ def test_shared_ranges_fill_one_wave_of_two_ctas_per_sm(sms):
         mine = sorted((int(it[1]), int(it[2])) for it in sh if int(it[4]) == 16 * g)
         assert mine[0][0] == 0 and all(a + n == b for (a, n), (b, _) in zip(mine, mine[1:]))
         assert mine[-1][0] + mine[-1][1] == 96
+
+
+def _kernels_for(plan_words, batch, mb=128):
+    """pkv_attention_kernels on a copy of the plan words (host code only):
+    None when the library refuses the plan."""
+    import ctypes
+    raw = np.zeros(plan_words.shape[0] + 4, dtype=np.int32)
+    off = (-raw.ctypes.data % 16) // 4
+    buf = raw[off:off + plan_words.shape[0]]
+    buf[:] = plan_words
+    return B.lib().pkv_attention_kernels(batch, mb, 0, buf.ctypes.data_as(ctypes.c_void_p))
+
+
+def test_damaged_plans_are_refused_before_any_launch():
+    # a plan is plain data: every index a kernel would take from it (sequence,
+    # page range, partial slot, member count) and the byte count its header
+    # states are checked on the host, so a hand-made or damaged plan is
+    # refused instead of sending a kernel outside its buffers
+    lens, bt = shared_case(0, [(16, 96)] * 2, (32, 32))
+    lens = np.concatenate([lens, np.array([2048, 40, 3], np.int32)])
+    extra = np.arange(3 * 128, dtype=np.int32).reshape(3, 128) + 100000
+    bt = np.concatenate([bt, extra])
+    plan = B.Plan(lens, 128, num_sms=SMS, block_tables=bt, min_shared_pages=16)
+    batch = len(lens)
+    assert plan.num_shared > 0 and plan.num_merges > 0
+    kinds = plan.items()[:, 0]
+    assert (kinds == 0).any() and (kinds == 1).any()
+    good = plan.host.copy()
+    assert _kernels_for(good, batch) is not None
+    it0 = B.PLAN_HEADER_WORDS
+    rng_i = it0 + 16 * int(np.flatnonzero(kinds == 0)[0])
+    pk_i = it0 + 16 * int(np.flatnonzero(kinds == 1)[0])
+    mg = it0 + 16 * plan.num_items
+    sh = mg + 4 * plan.num_merges
+    damage = {
+        "bytes_used": (7, int(good[7]) - 4),
+        "range item sequence": (rng_i + 4, batch),
+        "range item negative sequence": (rng_i + 4, -1),
+        "range longer than the page list": (rng_i + 3, plan.range_pages + 1),
+        "range past the table": (rng_i + 2, 128),
+        "range item slot": (rng_i + 1, plan.num_slots),
+        "unknown item kind": (rng_i, 2),
+        "packed item sequence": (pk_i + 4, batch + 7),
+        "packed item length": (pk_i + 8, 128 * 16 + 1),
+        "merge sequence": (mg, batch),
+        "merge slots": (mg + 2, plan.num_slots + 1),
+        "shared members": (sh, 17),
+        "no shared members": (sh, 0),
+        "shared range": (sh + 2, plan.shared_pages + 1),
+        "shared member sequence": (sh + 5, batch),
+        "shared member slot": (sh + 21, plan.num_slots),
+        "merges beyond the batch": (4, batch + 1),
+    }
+    for what, (idx, value) in damage.items():
+        bad = good.copy()
+        bad[idx] = value
+        assert _kernels_for(bad, batch) is None, what
+
+
+def test_rebuild_in_place_gives_the_plan_of_the_new_lengths():
+    # a serving loop rebuilds the step's plan into the same (pinned) buffer
+    rng = np.random.default_rng(9)
+    a = rng.integers(1, 2049, 100).astype(np.int32)
+    b = rng.integers(1, 2049, 100).astype(np.int32)
+    p = B.Plan(a, 128, num_sms=SMS)
+    buf = p.host.base if p.host.base is not None else p.host
+    p.rebuild(b)
+    q = B.Plan(b, 128, num_sms=SMS)
+    assert np.array_equal(p.host, q.host)
+    assert (p.num_items, p.num_merges, p.workspace_bytes) == (q.num_items, q.num_merges,
+                                                              q.workspace_bytes)
+    assert np.shares_memory(p.host, buf)
+    # with shared prefixes: the tables' groups are found again
+    lens, bt = shared_case(1, [(3, 20), (1, 5), (8, 40), (2, 16)], (1, 60))
+    p = B.Plan(lens, 128, num_sms=SMS, block_tables=bt)
+    lens2 = lens.copy()
+    lens2[-1] += 1
+    p.rebuild(np.ascontiguousarray(lens2), np.ascontiguousarray(bt))
+    q = B.Plan(lens2, 128, num_sms=SMS, block_tables=bt)
+    assert np.array_equal(p.host, q.host) and p.num_shared == q.num_shared > 0
