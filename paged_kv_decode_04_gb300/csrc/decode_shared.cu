@@ -102,8 +102,8 @@ constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKSlots * kRegionBytes;
 constexpr int kOffBars = kOffV + kVSlots * kRegionBytes;
 // k_full[6], k_empty[6], v_full[6], v_empty[6], s_ready[2], x_free[2],
-// p_ready, pv_done, s_fin, pv_fin, q_ready
-constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 9;
+// p_ready[2], pv_done, s_fin, pv_fin, q_ready
+constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 10;
 constexpr int kPrefetchBatches = 4;  // pulled into L2 before the grid dependency wait
 constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
 constexpr int kOffPages = kOffTmemSlot + 16;
@@ -167,11 +167,17 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   const uint32_t bars2 = bars + 8u * (2 * kKSlots + 2 * kVSlots);
   auto s_ready = [&](int b) { return bars2 + 8u * (b & 1); };
   auto x_free = [&](int b) { return bars2 + 16u + 8u * (b & 1); };
-  const uint32_t p_ready = bars2 + 32u;
-  const uint32_t pv_done = bars2 + 40u;
-  const uint32_t s_fin = bars2 + 48u;
-  const uint32_t pv_fin = bars2 + 56u;
-  const uint32_t q_ready = bars2 + 64u;
+  // One p_ready per S/P buffer, like s_ready and x_free: the softmax may
+  // finish batches j and j + 1 (S_{j+1} needs only PV_{j-1}) before the PV
+  // issuer looks for batch j, and one barrier for all batches would then be
+  // two phases ahead with batch j's parity, so its parity wait would wait
+  // for batch j + 2, which needs PV_j.  Per buffer, batch j + 2 needs PV_j
+  // first, so a waiter is never more than one phase behind.
+  auto p_ready = [&](int j) { return bars2 + 32u + 8u * (j & 1); };
+  const uint32_t pv_done = bars2 + 48u;
+  const uint32_t s_fin = bars2 + 56u;
+  const uint32_t pv_fin = bars2 + 64u;
+  const uint32_t q_ready = bars2 + 72u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
   int32_t* s_pages = reinterpret_cast<int32_t*>(smem + kOffPages);
 
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       const uint32_t bar = bars + 8u * i;  // the softmax rows arrive on two
-      mbar_init(bar, (bar == p_ready || bar == q_ready) ? kTcM : 1);
+      mbar_init(bar, (bar == p_ready(0) || bar == p_ready(1) || bar == q_ready) ? kTcM : 1);
     }
     fence_barrier_init();
   }
@@ -248,9 +254,9 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   // The plan says every member's table holds the leader's page ids over
   // [p_begin, p_begin + n) in this layer; a member whose table says
   // otherwise (a plan built from another layer's tables, or tables changed
-  // since) would silently attend the leader's K/V.  The idle lanes of the
-  // two issuer warps compare the entries while the stream runs and report a
-  // difference as PKV_DEVERR_PLAN.
+  // since) would silently attend the leader's K/V.  The softmax warps
+  // compare the entries while the first batch loads and report a difference
+  // as PKV_DEVERR_PLAN.
   auto check_members = [&](int t, int nt) {
     bool differs = false;
     const int total = (members - 1) * n;
@@ -339,8 +345,6 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       if (!ok) record_error(a.dev_err, kErrTimeout);
       tc_commit(s_fin);
       if (!mbar_wait_bounded(s_fin, 0)) record_error(a.dev_err, kErrTimeout);
-    } else {
-      check_members(lane - 1, 62);
     }
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------- O += P V
@@ -348,7 +352,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       bool ok = true;
       uint32_t o_init = 0;
       for (int j = 0; j < nb; ++j) {
-        if (!mbar_wait_bounded(p_ready, j & 1, a.wait_ns) ||
+        if (!mbar_wait_bounded(p_ready(j), (j >> 1) & 1, a.wait_ns) ||
             !mbar_wait_bounded(v_full(j), (j / kVSlots) & 1, a.wait_ns)) {
           ok = false;
           break;
@@ -370,11 +374,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       if (!ok) record_error(a.dev_err, kErrTimeout);
       tc_commit(pv_fin);
       if (!mbar_wait_bounded(pv_fin, 0)) record_error(a.dev_err, kErrTimeout);
-    } else {
-      check_members(31 + (lane - 1), 62);
     }
   } else {
     // --------------------------------------------------------- softmax
+    // (idle until S_0 lands: compare the members' tables meanwhile)
+    check_members(tid, 32 * kTcSoftmaxWarps);
     const float c = a.scale_log2;
     const uint32_t zero16[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     for (int j = 0; j < nb; ++j) {
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       tmem_st16(x + kPLo + (1 - h) * 16, zero16);
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(p_ready);
+      mbar_arrive(p_ready(j));
       o_live = o_live || any_live;
     }
   }
