@@ -54,6 +54,7 @@ KERNEL_FILES = {
     "merge_splits_kernel": "decode_attention.cu",
     "paged_decode_pagebox_kernel": "decode_pagebox.cu",
     "paged_decode_shared_kernel": "decode_shared.cu",
+    "paged_decode_segments_kernel": "decode_segments.cu",
 }
 COMMON_SOURCES = ("decode_page.cuh", "pkv_device.cuh", "pkv_internal.h")
 KERNEL_SOURCES = [os.path.join(CSRC, f)
@@ -61,7 +62,8 @@ KERNEL_SOURCES = [os.path.join(CSRC, f)
 # The traffic file holds a list of records {workload, kernel, kernel_sha, dram_bytes_per_launch};
 # kernel_sha covers the sources of the kernels the record names.
 # Every kernel of the library, for the per-kernel shares of a step.
-LIBRARY_KERNELS = ("paged_decode_pagebox_kernel", "paged_decode_shared_kernel",
+LIBRARY_KERNELS = ("paged_decode_segments_kernel", "paged_decode_pagebox_kernel",
+                   "paged_decode_shared_kernel",
                    "paged_decode_kernel", "merge_plan_kernel", "merge_splits_kernel",
                    "kv_append_kernel", "kv_write_prefill_kernel", "rope_table_kernel",
                    "rope_tag_kernel")
@@ -520,15 +522,19 @@ class DecodeBench:
         barrier(self.world)
         return max_over_ranks(ms, self.world, self.dev)
 
-    def timed(self, steps, flush=None, min_seconds=MIN_TIMED_SECONDS):
-        """Repeated timed regions of `steps` steps: at least MIN_REPEATS of them
-        and at least min_seconds in all (the count is fixed from a probe region,
-        the same on every rank).  Returns (region times in ms, wall t0, t1)."""
+    def timed(self, steps, flush=None, min_seconds=None):
+        """Repeated timed regions of `steps` steps: at least --min-repeats of
+        them and at least min_seconds (--repeat-seconds) in all (the count is
+        fixed from a probe region, the same on every rank).  Returns (region
+        times in ms, wall t0, t1)."""
+        if min_seconds is None:
+            min_seconds = self.args.repeat_seconds
         probe = self.one_region(steps, flush)
         per_region_s = max(probe, 1e-3) / 1e3
         if flush is not None:
             per_region_s += steps * 1.2e-4         # the flushes between steps
-        reps = int(min(MAX_REPEATS, max(MIN_REPEATS, math.ceil(min_seconds / per_region_s))))
+        reps = int(min(MAX_REPEATS, max(self.args.min_repeats,
+                                        math.ceil(min_seconds / per_region_s))))
         t0 = time.time()
         times = [self.one_region(steps, flush) for _ in range(reps)]
         return times, t0, time.time()
@@ -674,13 +680,15 @@ class DecodeBench:
         side = torch.cuda.Stream(self.dev)
 
         def step_body(s):
-            """Upload set 1 - s (the next step's inputs) beside the kernels of
-            set s, then read set s's output back."""
+            """The kernels of set s, and beside them the upload of set 1 - s
+            (the next step's inputs) and the read-back of set 1 - s's output
+            (the previous step's)."""
             cur = torch.cuda.current_stream(self.dev)   # the capture stream when capturing
             fork = torch.cuda.Event()
             fork.record(cur)
             side.wait_event(fork)
             with torch.cuda.stream(side):
+                out_host[1 - s].copy_(set_outs[1 - s], non_blocking=True)
                 dev_bufs[1 - s][:n_copy].copy_(host_bufs[1 - s][:n_copy], non_blocking=True)
             dset, out = sets[s], set_outs[s]
             for layer in range(w.layers):
@@ -689,7 +697,6 @@ class DecodeBench:
                 else:
                     self.append_on(dset, layer)
                     self.attend_on(dset, layer, out[layer])
-            out_host[s].copy_(out, non_blocking=True)
             cur.wait_stream(side)
 
         graphs = []
@@ -722,6 +729,9 @@ class DecodeBench:
                     plan_us.append((time.perf_counter() - t) * 1e6)
                 graphs[s]()
                 done[s].record(self.stream)
+            # the last step's output (the earlier ones were read back beside
+            # the following step's kernels)
+            out_host[(n - 1) % 2].copy_(set_outs[(n - 1) % 2], non_blocking=True)
 
         run_e2e(max(3, min(warmup, 20)))
         torch.cuda.synchronize(self.dev)
@@ -744,8 +754,9 @@ class DecodeBench:
         rec = {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": n_copy,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / steps, 5),
                "pipelining": "each step is one CUDA graph per input set: the upload of the next "
-                             "step's packed inputs runs beside this step's kernels, followed "
-                             "by the read-back of its output"}
+                             "step's packed inputs and the read-back of the previous step's "
+                             "output run beside this step's kernels; the last output is read "
+                             "back after the last step, inside the timed region"}
         if self.planned:
             rec["plan_built_per_step"] = True
             rec["plan_build_us_host_median"] = round(statistics.median(plan_us), 2) \
@@ -798,7 +809,7 @@ def measure_workload(name, args, dev, peak):
     db.warm_and_capture(args.warmup, args.graph)
     fits_l2 = w.kv_bytes() <= 96 * 2 ** 20
     flush, l2 = l2_flush_buffer(dev) if fits_l2 else (None, 0)
-    times, _, _ = db.timed(args.steps, flush, min_seconds=0.5)
+    times, _, _ = db.timed(args.steps, flush, min_seconds=min(0.5, args.repeat_seconds))
     db.check_err("timed runs")
     sp = spread(times, args.steps)
     ms = sp["ms_per_step_median"]
@@ -900,7 +911,8 @@ def measure_prefill(args, dev, peak):
         return e0.elapsed_time(e1)
 
     probe = region()
-    reps = int(min(MAX_REPEATS, max(MIN_REPEATS, math.ceil(0.5 / max(probe / 1e3, 1e-6)))))
+    reps = int(min(MAX_REPEATS, max(args.min_repeats, math.ceil(
+        min(0.5, args.repeat_seconds) / max(probe / 1e3, 1e-6)))))
     times = [region() for _ in range(reps)]
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} in the prefill write")
@@ -1028,7 +1040,7 @@ def run_ours(args, world, rank, local):
 
     # ---- end to end: per-step plan built on the host, inputs from pinned host
     # memory, output back to the host
-    e2e = db.e2e(args.steps, args.warmup)
+    e2e = db.e2e(args.steps, args.warmup) if args.e2e else None
 
     # ---- CPU baseline: the oracle on a bounded sample of the same workload, and
     # the same sample set against the GPU's outputs of the timed steps
@@ -1197,6 +1209,12 @@ def main(argv=None):
     ap.add_argument("--ref-seqs", type=int, default=1,
                     help="sequences per step of the --impl reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-repeats", type=int, default=MIN_REPEATS,
+                    help="fewest timed regions of K steps (the median is reported)")
+    ap.add_argument("--repeat-seconds", type=float, default=MIN_TIMED_SECONDS,
+                    help="shortest span of the repeated timed regions")
+    ap.add_argument("--e2e", action=argparse.BooleanOptionalAction, default=True,
+                    help="also measure the step end to end from pinned host memory")
     ap.add_argument("--per-workload", action=argparse.BooleanOptionalAction, default=True,
                     help="after the headline, measure the other workloads and the prefill "
                          "write the same way, each against the oracle (N = 1 only)")

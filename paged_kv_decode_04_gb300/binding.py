@@ -365,7 +365,7 @@ class Plan:
     planned calls take the plan object itself."""
 
     HEADER = ("magic", "batch", "max_blocks", "num_items", "num_merges", "num_slots",
-              "range_pages", "bytes_used", "num_shared", "shared_pages")
+              "range_pages", "bytes_used", "num_shared", "shared_pages", "num_segs")
 
     def __init__(self, seq_lens_host, max_blocks: int, *, num_sms: int = 0, device=None,
                  out=None, block_tables=None, min_shared_pages: int = 16):
@@ -456,6 +456,12 @@ class Plan:
         """[num_shared][36] int32: members, p_begin, n, 0, seq[16], slot[16]."""
         o = PLAN_HEADER_WORDS + 16 * self.num_items + 4 * self.num_merges
         return self.host[o:o + 36 * self.num_shared].reshape(self.num_shared, 36)
+
+    def segments(self) -> np.ndarray:
+        """[num_segs][8] int32: b, L, p_begin, n, slot (-1: writes the output), 0 x 3;
+        item i (kind 2) runs segments [items()[i, 1], items()[i, 1] + items()[i, 2])."""
+        o = PLAN_HEADER_WORDS + 16 * self.num_items + 4 * self.num_merges + 36 * self.num_shared
+        return self.host[o:o + 8 * self.num_segs].reshape(self.num_segs, 8)
 
     def to(self, device):
         """Copy the plan to `device`, asynchronously on the current stream (through

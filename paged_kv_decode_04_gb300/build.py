@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "pkv")
 LIB = os.path.join(PKG, "libpkv.so")
 SOURCES = ["kv_append.cu", "decode_attention.cu", "decode_pagebox.cu", "decode_shared.cu",
-           "pkv_api.cu", "scheduler.cpp", "planner.cpp"]
+           "decode_segments.cu", "pkv_api.cu", "scheduler.cpp", "planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -482,7 +482,7 @@ namespace {
 
 struct PlanHeader {
   int32_t magic, batch, max_blocks, num_items, num_merges, num_slots, range_pages, bytes_used;
-  int32_t num_shared, shared_pages, reserved0, reserved1;
+  int32_t num_shared, shared_pages, num_segs, reserved1;
 };
 static_assert(sizeof(PlanHeader) == 4 * pkv::kPlanHeaderWords, "plan header layout");
 
@@ -499,7 +499,28 @@ bool plan_body_valid(const PlanHeader& h) {
     return p >= 0 && n >= 0 && n <= cap && static_cast<int64_t>(p) + n <= h.max_blocks;
   };
   const int64_t lmax = static_cast<int64_t>(h.max_blocks) * kPageSize;
+  const int32_t* segs = w + static_cast<int64_t>(h.num_items) * pkv::kPlanItemWords +
+                        static_cast<int64_t>(h.num_merges) * pkv::kPlanMergeWords +
+                        static_cast<int64_t>(h.num_shared) * pkv::kPlanSharedWords;
   for (int i = 0; i < h.num_items; ++i, w += pkv::kPlanItemWords) {
+    if (h.num_segs > 0) {
+      // a segment plan: every item is a segment CTA, its segments inside the
+      // section, their pages summing to the item's, at most range_pages
+      if (w[0] != pkv::kPlanKindSegments || w[1] < 0 || w[2] < 1 || w[2] > pkv::kSegMax ||
+          static_cast<int64_t>(w[1]) + w[2] > h.num_segs || w[3] < 0 || w[3] > h.range_pages)
+        return false;
+      int64_t pages = 0;
+      for (int k = 0; k < w[2]; ++k) {
+        const int32_t* sg = segs + static_cast<int64_t>(w[1] + k) * pkv::kPlanSegWords;
+        const int64_t live = (static_cast<int64_t>(sg[1]) + kPageSize - 1) / kPageSize;
+        if (!seq_ok(sg[0]) || sg[1] < 0 || sg[1] > lmax || !range_ok(sg[2], sg[3], h.range_pages) ||
+            sg[2] + sg[3] > live || (sg[4] != -1 && (sg[4] < 0 || sg[4] >= h.num_slots)))
+          return false;
+        pages += sg[3];
+      }
+      if (pages != w[3]) return false;
+      continue;
+    }
     if (w[0] == pkv::kPlanKindRange) {
       if (!seq_ok(w[4]) || !range_ok(w[2], w[3], h.range_pages)) return false;
       if (w[1] != -1 && (w[1] < 0 || w[1] >= h.num_slots)) return false;
@@ -537,14 +558,15 @@ const PlanHeader* plan_header(const void* plan, int batch, int max_blocks) {
       h->max_blocks != max_blocks || h->num_items < 1 || h->num_items > 65535 ||
       h->num_merges < 0 || h->num_merges > batch || h->num_slots < 0 ||
       h->range_pages < 1 || h->range_pages > 1024 || h->num_shared < 0 ||
-      h->num_shared > 65535 ||
+      h->num_shared > 65535 || h->num_segs < 0 ||
       (h->num_shared > 0 && (h->shared_pages < 1 || h->shared_pages > 1024)))
     return nullptr;
   // bytes_used is exactly the header and the three sections the counts imply
   const int64_t words = pkv::kPlanHeaderWords +
                         static_cast<int64_t>(h->num_items) * pkv::kPlanItemWords +
                         static_cast<int64_t>(h->num_merges) * pkv::kPlanMergeWords +
-                        static_cast<int64_t>(h->num_shared) * pkv::kPlanSharedWords;
+                        static_cast<int64_t>(h->num_shared) * pkv::kPlanSharedWords +
+                        static_cast<int64_t>(h->num_segs) * pkv::kPlanSegWords;
   if (static_cast<int64_t>(h->bytes_used) != 4 * words) return nullptr;
   if (!plan_body_valid(*h)) return nullptr;
   return h;
@@ -585,6 +607,9 @@ cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pa
   args.plan_shared = reinterpret_cast<const int4*>(
       words + pkv::kPlanHeaderWords + static_cast<size_t>(h.num_items) * pkv::kPlanItemWords +
       static_cast<size_t>(h.num_merges) * pkv::kPlanMergeWords);
+  args.plan_segs = reinterpret_cast<const int4*>(
+      reinterpret_cast<const int32_t*>(args.plan_shared) +
+      static_cast<size_t>(h.num_shared) * pkv::kPlanSharedWords);
   args.dev_err = dev_err;
   args.num_pages = num_pages;
   args.max_blocks = max_blocks;
@@ -601,6 +626,13 @@ cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pa
     const cudaError_t err =
         pkv::launch_shared_prefix_attention(map, args, h.num_shared, h.shared_pages, stream);
     if (err != cudaSuccess) return err;
+  }
+  if (h.num_segs > 0) {
+    if (!pool_page_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
+    const cudaError_t err = pkv::launch_segments_attention(map, args, h.num_items,
+                                                           h.range_pages, stream, append);
+    if (err != cudaSuccess) return err;
+    return pkv::launch_split_merge(args, h.num_merges, stream);
   }
   if (use_pagebox(h.num_items, h.range_pages) && plan_has_only_ranges(h)) {
     if (!pool_page_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
@@ -624,6 +656,12 @@ PKV_API const char* pkv_attention_kernels(int batch, int max_blocks, int num_spl
   if (plan != nullptr) {
     const PlanHeader* h = plan_header(plan, batch, max_blocks);
     if (h == nullptr) return nullptr;
+    if (h->num_segs > 0) {
+      if (h->num_shared > 0)
+        return "paged_decode_shared_kernel+paged_decode_segments_kernel+merge_plan_kernel";
+      return h->num_merges > 0 ? "paged_decode_segments_kernel+merge_plan_kernel"
+                               : "paged_decode_segments_kernel";
+    }
     const bool pb = use_pagebox(h->num_items, h->range_pages) && plan_has_only_ranges(*h);
     if (h->num_shared > 0)  // a plan with shared groups always merges
       return pb ? "paged_decode_shared_kernel+paged_decode_pagebox_kernel+merge_plan_kernel"

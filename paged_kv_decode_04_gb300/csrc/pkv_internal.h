@@ -44,6 +44,19 @@ constexpr int kPlanWarps = 4;       // warps per attention CTA: one packed seque
 constexpr int kSharedMembers = 16;
 constexpr int kSharedCtasPerSm = 2;
 constexpr int kPlanSharedWords = 4 + 2 * kSharedMembers;
+// Segment plans (the plan's segment section, header word 10 = its count):
+// one CTA per item of kind kPlanKindSegments {2, first segment, segments,
+// pages, 0 ...} streams the pages of up to kSegMax segments {b, L, p_begin,
+// n, slot, 0, 0, 0} in order through one ring of whole-page boxes, all 8 kv
+// heads at once (paged_decode_segments_kernel); slot -1: the segment is the
+// whole sequence and writes its output, else a partial for the merge.  The
+// planner packs the layer's pages into one wave of kSegCtasPerSm CTAs per SM
+// of near-equal pages.
+constexpr int kPlanKindSegments = 2;
+constexpr int kPlanSegWords = 8;
+constexpr int kSegMax = 4;
+constexpr int kSegCtasPerSm = 2;
+constexpr int kSegMaxPages = 1024;  // pages of one segment CTA (its page list)
 
 // Host side of the work plans (planner.cpp): an upper bound on a plan's
 // bytes, and the plan itself from host lengths (PKV_* status).
@@ -127,6 +140,7 @@ struct AttnArgs {
   const int4* plan_items;   // work plan items (kPlanItemWords words each), or nullptr
   const int4* plan_merges;  // work plan merge entries (b, first slot, ranges, 0)
   const int4* plan_shared;  // work plan shared-prefix items (kPlanSharedWords words each)
+  const int4* plan_segs;    // work plan segments (kPlanSegWords words each)
   int32_t* dev_err;
   int64_t num_pages;
   int max_blocks;
@@ -170,6 +184,13 @@ cudaError_t launch_pagebox_attention(const CUtensorMap& page_map, const AttnArgs
                                      int num_items, int range_pages, cudaStream_t stream,
                                      const AppendArgs* append = nullptr);
 int pagebox_max_range_pages();
+
+// A segment plan's CTAs (decode_segments.cu): grid (num_items), each CTA
+// streaming its segments' pages (at most max_pages) through whole-page boxes
+// of page_map.  The caller launches the merge.
+cudaError_t launch_segments_attention(const CUtensorMap& page_map, const AttnArgs& args,
+                                      int num_items, int max_pages, cudaStream_t stream,
+                                      const AppendArgs* append = nullptr);
 
 // Launch the split merge of a plan (fixed: merge_splits_kernel when S > 1;
 // work plan: merge_plan_kernel over num_merges sequences).

@@ -24,6 +24,8 @@ namespace {
 constexpr int kMinRangePages = 8;     // shortest range worth a CTA of its own
 constexpr int kResidentPerSm = 4;     // attention CTAs resident per SM (shallow ring)
 constexpr int kMaxRangePages = 1024;  // the kernel's shared page list
+constexpr int kMinSegPages = 4;       // smallest bin size tried for a segment plan
+constexpr int kMinSegBinPages = 16;   // smallest bin size a segment plan is used with
 
 struct Range {
   int b, L, p_begin, n, slot;
@@ -49,11 +51,14 @@ void counting_sort(std::vector<T>& v, int nkeys, Key key) {
 size_t plan_bytes(int batch, int max_blocks) {
   if (batch < 1 || max_blocks < 1) return 0;
   const int rmin = max_blocks < kMinRangePages ? max_blocks : kMinRangePages;
-  const size_t items = static_cast<size_t>(batch) * ceil_div(max_blocks, rmin) + 1;
+  // range / packed items, or segment CTAs (at most one per segment)
+  const size_t pieces = static_cast<size_t>(batch) * (ceil_div(max_blocks, rmin) + 1);
+  const size_t items = pieces + 1;
   // shared-prefix items: at most one per (group of two or more, range)
   const size_t shared = static_cast<size_t>(batch / 2) * ceil_div(max_blocks, rmin);
   return 4 * (kPlanHeaderWords + items * kPlanItemWords +
-              static_cast<size_t>(batch) * kPlanMergeWords + shared * kPlanSharedWords);
+              static_cast<size_t>(batch) * kPlanMergeWords + shared * kPlanSharedWords +
+              pieces * kPlanSegWords);
 }
 
 // Sizes for work unit u (the pages one warp streams): ranges of R = 4 u
@@ -90,6 +95,253 @@ long long count_items(const std::vector<int>& pages, Sizes z) {
 struct SharedGroup {
   int first, members, k;
 };
+
+// Shared-prefix items at `item`: {members, p_begin, n, 0, seq[16], slot[16]},
+// range r of group gi taking slot slot_base[member] + r; returns the end.
+int32_t* write_shared_items(const std::vector<SharedGroup>& groups,
+                            const std::vector<int>& shared_ranges,
+                            const std::vector<int>& slot_base, int32_t* item) {
+  for (size_t gi = 0; gi < groups.size(); ++gi) {
+    const SharedGroup& g = groups[gi];
+    const int ns = shared_ranges[gi];
+    const int base = g.k / ns, extra = g.k % ns;
+    int begin = 0;
+    for (int r = 0; r < ns; ++r) {
+      const int n = base + (r < extra ? 1 : 0);
+      item[0] = g.members;
+      item[1] = begin;
+      item[2] = n;
+      for (int m = 0; m < kSharedMembers; ++m) {
+        const bool has = m < g.members;
+        item[4 + m] = has ? g.first + m : -1;
+        item[4 + kSharedMembers + m] = has ? slot_base[g.first + m] + r : -1;
+      }
+      begin += n;
+      item += kPlanSharedWords;
+    }
+  }
+  return item;
+}
+
+// A piece of a sequence's own pages for the segment kernel.
+struct Piece {
+  int b, p_begin, n;
+};
+
+// The pieces for bins of T pages: each sequence's own pages [start, start +
+// own) whole, or cut into ceil(own / T) near-equal chunks when longer than T
+// (an empty sequence is one piece of no pages, which writes its zero rows),
+// largest first (stable).
+std::vector<Piece> make_pieces(const std::vector<int>& own, const std::vector<int>& start,
+                               int T) {
+  std::vector<Piece> pieces;
+  pieces.reserve(own.size() + 16);
+  for (size_t b = 0; b < own.size(); ++b) {
+    const int p = own[b];
+    const int nr = p > T ? (p + T - 1) / T : 1;  // 32-bit divisions: this runs per step
+    const int base = p / nr, extra = p % nr;
+    int begin = start[b];
+    for (int r = 0; r < nr; ++r) {
+      const int n = base + (r < extra ? 1 : 0);
+      pieces.push_back({static_cast<int>(b), begin, n});
+      begin += n;
+    }
+  }
+  counting_sort(pieces, T + 1, [&](const Piece& x) { return T - x.n; });
+  return pieces;
+}
+
+// Best-fit packing of pieces (largest first) into bins of at most T pages and
+// kSegMax segments: a piece goes to the open bin with the least room that
+// takes it, else to a new bin.  Returns the number of bins; with `bin_of`,
+// also each piece's bin.
+long long pack_bins(const std::vector<Piece>& pieces, int T, std::vector<int>* bin_of) {
+  std::vector<std::vector<int>> by_room(static_cast<size_t>(T) + 1);
+  // bit r set: some open bin has exactly r pages of room
+  std::vector<uint64_t> nonempty((static_cast<size_t>(T) >> 6) + 1, 0);
+  auto mark = [&](int r, bool on) {
+    if (on) nonempty[r >> 6] |= 1ull << (r & 63);
+    else nonempty[r >> 6] &= ~(1ull << (r & 63));
+  };
+  auto first_room = [&](int n) {  // the least room >= n held by an open bin, or -1
+    for (int w = n >> 6; w < static_cast<int>(nonempty.size()); ++w) {
+      uint64_t bits = nonempty[w];
+      if (w == (n >> 6)) bits &= ~0ull << (n & 63);
+      if (bits) return (w << 6) + __builtin_ctzll(bits);
+    }
+    return -1;
+  };
+  std::vector<int> room, segs;
+  if (bin_of != nullptr) bin_of->assign(pieces.size(), -1);
+  for (size_t i = 0; i < pieces.size(); ++i) {
+    const int n = pieces[i].n;
+    int pick = -1;
+    const int r = first_room(n);
+    if (r >= 0 && r <= T) {
+      pick = by_room[r].back();
+      by_room[r].pop_back();
+      if (by_room[r].empty()) mark(r, false);
+    }
+    if (pick < 0) {
+      pick = static_cast<int>(room.size());
+      room.push_back(T);
+      segs.push_back(0);
+    }
+    room[pick] -= n;
+    segs[pick] += 1;
+    if (bin_of != nullptr) (*bin_of)[i] = pick;
+    if (segs[pick] < kSegMax) {
+      by_room[room[pick]].push_back(pick);
+      mark(room[pick], true);
+    }
+  }
+  return static_cast<long long>(room.size());
+}
+
+// The bin size of a segment plan: the smallest T from max(kMinSegPages,
+// ceil(P / C)) up (P: the pages to attend, C = kSegCtasPerSm CTAs per SM)
+// whose bins fit in one wave of C CTAs, else the largest (up to kSegMax x the
+// longest sequence, or kSegMaxPages).  A T whose pieces cannot fit -- more than C of
+// them longer than T / 2, or more than C * T pages -- is ruled out without
+// packing.
+int segment_bin_size(const std::vector<int>& own, const std::vector<int>& start, int num_sms,
+                     long long total) {
+  const long long C = static_cast<long long>(kSegCtasPerSm) * num_sms;
+  const int max_own = *std::max_element(own.begin(), own.end());
+  const int t0 = static_cast<int>(std::min<long long>(
+      kSegMaxPages, std::max<long long>(kMinSegPages, (total + C - 1) / C)));
+  // past kSegMax x the longest sequence a bin is bounded by its segment count
+  const int t1 = std::max(t0, std::min(kSegMax * std::max(max_own, 1), kSegMaxPages));
+  auto fits = [&](int T) {
+    long long big = 0;  // pieces longer than T / 2: no two share a bin
+    for (int p : own) {
+      const int nr = p > T ? (p + T - 1) / T : 1;
+      const int base = p / nr, extra = p % nr;
+      big += 2 * base > T ? nr : (2 * (base + 1) > T ? extra : 0);
+    }
+    if (big > C || (total + T - 1) / T > C) return false;
+    return pack_bins(make_pieces(own, start, T), T, nullptr) <= C;
+  };
+  // the smallest fitting T, searched first up to the longest sequence (where
+  // whole sequences become single pieces), then beyond it
+  auto smallest = [&](int lo, int hi) {  // the smallest T in [lo, hi] that fits, or -1
+    if (lo > hi || !fits(hi)) return -1;
+    while (lo < hi) {
+      const int mid = lo + (hi - lo) / 2;
+      if (fits(mid)) hi = mid;
+      else lo = mid + 1;
+    }
+    return lo;
+  };
+  const int whole = std::min(std::max(t0, max_own), t1);
+  int T = smallest(t0, whole);
+  if (T < 0) T = smallest(whole + 1, t1);
+  return T < 0 ? t1 : T;
+}
+
+// The segment plan for bins of T pages; bins run largest first.  A sequence
+// in more than one piece, or a member of a shared group, writes partials to
+// consecutive slots (its shared ranges first) and gets a merge entry; any
+// other sequence's segment writes its output.
+int build_segments(const int32_t* lens, int batch, int max_blocks, int T,
+                   const std::vector<int>& own, const std::vector<int>& start,
+                   const std::vector<int>& group_of, const std::vector<SharedGroup>& groups,
+                   const std::vector<int>& shared_ranges, int shared_max, int32_t* out,
+                   size_t out_bytes) {
+  const std::vector<Piece> pieces = make_pieces(own, start, T);
+  std::vector<int> bin_of;
+  const int nbins = static_cast<int>(pack_bins(pieces, T, &bin_of));
+  // each bin's pieces, in the order they were placed (largest first)
+  std::vector<int> by_bin(pieces.size());
+  for (size_t i = 0; i < pieces.size(); ++i) by_bin[i] = static_cast<int>(i);
+  counting_sort(by_bin, nbins, [&](int i) { return bin_of[i]; });
+  std::vector<int> bin_first(static_cast<size_t>(nbins) + 1, 0);
+  for (int i : by_bin) ++bin_first[bin_of[i] + 1];
+  for (int k = 0; k < nbins; ++k) bin_first[k + 1] += bin_first[k];
+
+  // partial slots: split sequences and group members, in sequence order
+  std::vector<int> npieces(batch, 0), slot_base(batch, -1), next_piece(batch, 0);
+  for (const Piece& pc : pieces) ++npieces[pc.b];
+  std::vector<int32_t> merges;
+  int slots = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int ns = group_of[b] >= 0 ? shared_ranges[group_of[b]] : 0;
+    if (npieces[b] > 1 || ns > 0) {
+      merges.insert(merges.end(), {b, slots, ns + npieces[b], 0});
+      slot_base[b] = slots;
+      slots += ns + npieces[b];
+    }
+  }
+  // a sequence's pieces take its slots in the order of their pages
+  std::vector<int> piece_slot(pieces.size(), -1);
+  {
+    std::vector<int> by_page(pieces.size());
+    for (size_t i = 0; i < pieces.size(); ++i) by_page[i] = static_cast<int>(i);
+    counting_sort(by_page, max_blocks + 1, [&](int i) { return pieces[i].p_begin; });
+    for (int i : by_page) {
+      const Piece& pc = pieces[i];
+      if (slot_base[pc.b] < 0) continue;
+      const int ns = group_of[pc.b] >= 0 ? shared_ranges[group_of[pc.b]] : 0;
+      piece_slot[i] = slot_base[pc.b] + ns + next_piece[pc.b]++;
+    }
+  }
+  // bins largest first (stable)
+  std::vector<int> bin_pages(nbins, 0), order(nbins);
+  int most = 0;
+  for (int k = 0; k < nbins; ++k) {
+    for (int j = bin_first[k]; j < bin_first[k + 1]; ++j) bin_pages[k] += pieces[by_bin[j]].n;
+    most = std::max(most, bin_pages[k]);
+    order[k] = k;
+  }
+  counting_sort(order, most + 1, [&](int k) { return most - bin_pages[k]; });
+
+  const size_t num_items = static_cast<size_t>(nbins);
+  const size_t num_merges = merges.size() / kPlanMergeWords;
+  size_t num_shared = 0;
+  for (int ns : shared_ranges) num_shared += static_cast<size_t>(ns);
+  if (num_items > 65535 || num_shared > 65535) return PKV_EUNSUPPORTED;  // grid limits
+  const size_t words = kPlanHeaderWords + num_items * kPlanItemWords + merges.size() +
+                       num_shared * kPlanSharedWords + pieces.size() * kPlanSegWords;
+  if (words * 4 > out_bytes) return PKV_EINVAL;
+  memset(out, 0, words * 4);
+  out[0] = static_cast<int32_t>(PKV_PLAN_MAGIC);
+  out[1] = batch;
+  out[2] = max_blocks;
+  out[3] = static_cast<int32_t>(num_items);
+  out[4] = static_cast<int32_t>(num_merges);
+  out[5] = slots;
+  out[6] = std::max(1, most);  // the largest CTA's page list
+  out[7] = static_cast<int32_t>(words * 4);
+  out[8] = static_cast<int32_t>(num_shared);
+  out[9] = shared_max;
+  out[10] = static_cast<int32_t>(pieces.size());
+  int32_t* item = out + kPlanHeaderWords;
+  int32_t* seg = out + kPlanHeaderWords + num_items * kPlanItemWords + merges.size() +
+                 num_shared * kPlanSharedWords;
+  int next_seg = 0;
+  for (int k : order) {
+    item[0] = kPlanKindSegments;
+    item[1] = next_seg;
+    item[2] = bin_first[k + 1] - bin_first[k];
+    item[3] = bin_pages[k];
+    for (int j = bin_first[k]; j < bin_first[k + 1]; ++j) {
+      const int i = by_bin[j];
+      const Piece& pc = pieces[i];
+      seg[0] = pc.b;
+      seg[1] = lens[pc.b];
+      seg[2] = pc.p_begin;
+      seg[3] = pc.n;
+      seg[4] = piece_slot[i];
+      seg += kPlanSegWords;
+      ++next_seg;
+    }
+    item += kPlanItemWords;
+  }
+  if (!merges.empty()) memcpy(item, merges.data(), merges.size() * 4);
+  item += merges.size();
+  write_shared_items(groups, shared_ranges, slot_base, item);
+  return PKV_OK;
+}
 
 // The work unit U: the smallest whose plan fits in one wave of resident
 // CTAs (kResidentPerSm per SM, 8 kv heads each item), starting from
@@ -128,6 +380,36 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
     total += own[b];
     if (group_of[b] < 0) solo.push_back(own[b]);
   }
+  // shared ranges per group: as many as keep the shared-prefix CTAs within
+  // one wave of kSharedCtasPerSm per SM, ranges of at least kMinRangePages pages
+  int ns_target = 1;
+  if (!groups.empty()) {
+    const long long per = static_cast<long long>(groups.size()) * kNumKvHeads;
+    ns_target = static_cast<int>(
+        std::max<long long>(1, (static_cast<long long>(kSharedCtasPerSm) * num_sms) / per));
+  }
+  std::vector<int> shared_ranges(groups.size());
+  int shared_max = 0;  // pages of the longest shared range
+  for (size_t gi = 0; gi < groups.size(); ++gi) {
+    const int k = groups[gi].k;
+    int ns = std::max(1, std::min(ns_target, ceil_div(k, kMinRangePages)));
+    ns = std::max(ns, ceil_div(k, kMaxRangePages));  // the kernel's page list
+    shared_ranges[gi] = ns;
+    shared_max = std::max(shared_max, ceil_div(k, ns));
+  }
+  // A layer whose segment plan has bins of at least kMinSegBinPages pages
+  // runs on the segment kernel (one wave of CTAs of near-equal pages); with
+  // smaller bins a segment CTA's life is mostly its prologue and the latency
+  // of its first pages, and the per-(item, kv head) kernel below, with more
+  // CTAs and deeper per-warp rings, is faster (a ragged 16-layer batch of
+  // 2067 pages per layer: 313.7 us with bins of 8 pages against 249.7 us).
+  if (total >= static_cast<long long>(kMinSegBinPages) * num_sms) {
+    const int T = segment_bin_size(own, start, num_sms, total);
+    if (T >= kMinSegBinPages)
+      return build_segments(lens, batch, max_blocks, T, own, start, group_of, groups,
+                            shared_ranges, shared_max, out, out_bytes);
+  }
+
   auto count = [&](Sizes z) {
     long long items = count_items(solo, z);
     for (int b = 0; b < batch; ++b)
@@ -147,23 +429,6 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
   const int range = z.range;
   const int pack_max = z.pack_max;
 
-  // shared ranges per group: as many as keep the shared-prefix CTAs within
-  // one wave of kSharedCtasPerSm per SM, ranges of at least kMinRangePages pages
-  int ns_target = 1;
-  if (!groups.empty()) {
-    const long long per = static_cast<long long>(groups.size()) * kNumKvHeads;
-    ns_target = static_cast<int>(
-        std::max<long long>(1, (static_cast<long long>(kSharedCtasPerSm) * num_sms) / per));
-  }
-  std::vector<int> shared_ranges(groups.size());
-  int shared_max = 0;  // pages of the longest shared range
-  for (size_t gi = 0; gi < groups.size(); ++gi) {
-    const int k = groups[gi].k;
-    int ns = std::max(1, std::min(ns_target, ceil_div(k, kMinRangePages)));
-    ns = std::max(ns, ceil_div(k, kMaxRangePages));  // the kernel's page list
-    shared_ranges[gi] = ns;
-    shared_max = std::max(shared_max, ceil_div(k, ns));
-  }
 
   std::vector<Range> ranges;
   std::vector<int> packed;
@@ -262,26 +527,7 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
   }
   if (!merges.empty()) memcpy(item, merges.data(), merges.size() * 4);
   item += merges.size();
-  // shared-prefix items: {members, p_begin, n, 0, seq[16], slot[16]}
-  for (size_t gi = 0; gi < groups.size(); ++gi) {
-    const SharedGroup& g = groups[gi];
-    const int ns = shared_ranges[gi];
-    const int base = g.k / ns, extra = g.k % ns;
-    int begin = 0;
-    for (int r = 0; r < ns; ++r) {
-      const int n = base + (r < extra ? 1 : 0);
-      item[0] = g.members;
-      item[1] = begin;
-      item[2] = n;
-      for (int m = 0; m < kSharedMembers; ++m) {
-        const bool has = m < g.members;
-        item[4 + m] = has ? g.first + m : -1;
-        item[4 + kSharedMembers + m] = has ? slot_base[g.first + m] + r : -1;
-      }
-      begin += n;
-      item += kPlanSharedWords;
-    }
-  }
+  write_shared_items(groups, shared_ranges, slot_base, item);
   return PKV_OK;
 }
 

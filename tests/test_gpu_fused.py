@@ -79,11 +79,11 @@ def test_fused_peak_full_size_every_output():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     # the benchmark's configuration: the same step under a host work plan (one
-    # range per sequence, the whole-page kernel), on a fresh copy of the inputs
+    # whole sequence per segment CTA), on a fresh copy of the inputs
     b = binding()
     d2 = synth.device_inputs(w, dev)
     plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, block_tables=w.block_tables[0])
-    assert b.attention_kernels(w.batch, w.max_blocks, 0, plan) == "paged_decode_pagebox_kernel"
+    assert b.attention_kernels(w.batch, w.max_blocks, 0, plan) == "paged_decode_segments_kernel"
     out2 = synth.bits(b.decode_step_planned(d2["q"][0], d2["k_new"][0], d2["v_new"][0], d2["pool"],
                                             d2["block_tables"][0], d2["seq_lens"], plan,
                                             rope_theta=w.rope_theta, scale=w.scale, dev_err=err))

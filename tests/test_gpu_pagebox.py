@@ -64,14 +64,15 @@ def test_fixed_plan_fused_step(splits):
 
 @pytest.mark.parametrize("num_sms", [152, 400])
 def test_planned_ranges(num_sms):
-    # long sequences only, so the plan holds ranges and no packed items; planned
-    # as for 400 SMs the 128-page sequences are cut in two (partials + merge)
+    # long sequences only: a segment plan (the whole-page segment kernel);
+    # planned as for 400 SMs the 128-page sequences are cut in pieces (partials
+    # + merge)
     dev = cuda_or_skip()
     w = workload(1100, 2048, 60)
     b = binding()
     plan = b.Plan(w.seq_lens, w.max_blocks, num_sms=num_sms, device=dev)
     assert not (plan.items()[:, 0] == 1).any() and plan.num_items >= 152
-    assert (plan.num_merges > 0) == (num_sms == 400)
+    assert num_sms == 152 or plan.num_merges > 0
     ref, host_pool = oracle_step(w)
     d = synth.device_inputs(w, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -79,7 +80,9 @@ def test_planned_ranges(num_sms):
                                 d["block_tables"][0], d["seq_lens"], plan, dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert_close(synth.bits(out), ref, f"whole-page kernel, plan for {num_sms} SMs")
+    assert b.attention_kernels(w.batch, w.max_blocks, 0, plan).startswith(
+        "paged_decode_segments_kernel")
+    assert_close(synth.bits(out), ref, f"segment kernel, plan for {num_sms} SMs")
     check_slots(w, d["pool"], host_pool)
 
 
@@ -144,8 +147,8 @@ def test_kernel_choice_is_reported():
     assert b.attention_kernels(sms - 1, 128, 1) == "paged_decode_kernel"
     assert b.attention_kernels(8, 128, 1) == "paged_decode_kernel"
     assert b.attention_kernels(1, 128, 0) == "paged_decode_kernel+merge_splits_kernel"
-    lens = np.full(big, 2048, np.int32)
-    assert b.attention_kernels(big, 128, 0, b.Plan(lens, 128)) == "paged_decode_pagebox_kernel"
+    lens = np.full(big, 2048, np.int32)    # planned: one whole-sequence segment per CTA
+    assert b.attention_kernels(big, 128, 0, b.Plan(lens, 128)) == "paged_decode_segments_kernel"
     mixed = np.concatenate([np.full(13, 2000), np.full(115, 60)]).astype(np.int32)
     assert b.attention_kernels(128, 128, 0, b.Plan(mixed, 128)) == \
         "paged_decode_kernel+merge_plan_kernel"

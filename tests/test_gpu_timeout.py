@@ -119,12 +119,35 @@ def test_planned_packed_kernel_times_out_then_recovers():
 def test_pagebox_kernel_times_out_then_recovers():
     dev = cuda_or_skip()
     b = binding()
-    # 160 sequences of 512 tokens (160 MiB of K/V): one range each, at least
-    # one CTA per SM, so the whole-page kernel runs (with the fused append)
+    # 160 sequences of 512 tokens (160 MiB of K/V), one range each (fixed
+    # plan): at least one CTA per SM, so the whole-page kernel runs, fused
     w = synth.make_workload("custom", 3, seq_lens=np.full(160, 512, np.int32), num_pages=8192)
     d = synth.device_inputs(w, dev)
+    assert b.attention_kernels(w.batch, w.max_blocks, 1) == "paged_decode_pagebox_kernel"
+
+    def step(err):
+        return b.decode_step(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"],
+                             d["block_tables"][0], d["seq_lens"], num_splits=1,
+                             rope_theta=w.rope_theta, scale=w.scale, dev_err=err)
+    bits, out = timed_out(step)
+    assert bits & b.DEVERR_TIMEOUT, f"no wait timed out (bits {bits})"
+    assert torch.isfinite(out.float()).all()
+    check_recovered(w, d, step, "whole-page kernel")
+
+
+def test_segment_kernel_times_out_then_recovers():
+    dev = cuda_or_skip()
+    b = binding()
+    # 600 sequences of 200-700 tokens (about 130 MiB of K/V): a segment plan,
+    # several whole sequences and pieces per CTA, fused
+    rng = np.random.default_rng(8)
+    w = synth.make_workload("custom", 8, seq_lens=rng.integers(200, 701, 600).astype(np.int32),
+                            num_pages=20000)
+    d = synth.device_inputs(w, dev)
     plan = b.Plan(w.seq_lens, w.max_blocks, device=dev)
-    assert b.attention_kernels(w.batch, w.max_blocks, 0, plan) == "paged_decode_pagebox_kernel"
+    assert plan.num_segs > 0 and plan.items()[:, 2].max() > 1
+    assert b.attention_kernels(w.batch, w.max_blocks, 0, plan).startswith(
+        "paged_decode_segments_kernel")
 
     def step(err):
         return b.decode_step_planned(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"],
@@ -133,7 +156,7 @@ def test_pagebox_kernel_times_out_then_recovers():
     bits, out = timed_out(step)
     assert bits & b.DEVERR_TIMEOUT, f"no wait timed out (bits {bits})"
     assert torch.isfinite(out.float()).all()
-    check_recovered(w, d, step, "whole-page kernel")
+    check_recovered(w, d, step, "segment kernel")
 
 
 def test_shared_prefix_kernel_times_out_then_recovers():

@@ -22,8 +22,22 @@ def coverage(plan, lens):
     """Per sequence: the list of (first page, count) pieces the plan attends."""
     pieces = {b: [] for b in range(len(lens))}
     slots = {}
+    segs = plan.segments() if plan.num_segs else None
     for it in plan.items():
         kind, slot, p0, n = (int(x) for x in it[:4])
+        if kind == 2:                                  # a segment CTA
+            first, nseg, pages = slot, p0, n
+            assert 1 <= nseg <= 4 and not it[4:].any()
+            mine = segs[first:first + nseg]
+            assert int(mine[:, 3].sum()) == pages
+            for b, L, q0, m, sl in (tuple(int(x) for x in sg[:5]) for sg in mine):
+                assert L == lens[b]
+                pieces[b].append((q0, m))
+                if sl >= 0:
+                    assert sl not in slots
+                    slots[sl] = (b, q0)
+            continue
+        assert segs is None
         seqs, ls = it[4:8], it[8:12]
         if kind == 0:
             assert len(set(seqs.tolist())) == 1 and len(set(ls.tolist())) == 1
@@ -79,7 +93,8 @@ def test_every_page_once_and_merges_consistent(lens):
     for it in plan.items():                        # words 12..15 are reserved zeros
         assert not it[12:].any()
     assert plan.num_shared == 0
-    assert plan.bytes_used == 4 * (12 + 16 * plan.num_items + 4 * plan.num_merges)
+    assert plan.bytes_used == 4 * (12 + 16 * plan.num_items + 4 * plan.num_merges
+                                   + 8 * plan.num_segs)
 
 
 def expected_sizes(lens, sms, max_blocks=128):
@@ -111,6 +126,8 @@ def test_sizes_follow_the_formula():
         lens = rng.integers(0, 2049, n)
         sms = int(rng.choice([1, 16, 132, 152]))
         plan = build(lens, sms=sms)
+        if plan.num_segs:                          # big layers: a segment plan (tested below)
+            continue
         R, pack = expected_sizes(lens, sms)
         assert plan.range_pages == R
         for it in plan.items():
@@ -131,8 +148,10 @@ def busiest_warp_pages(item):
 @pytest.mark.parametrize("seed", [5, 6, 7])
 def test_order_busiest_warp_first(seed):
     rng = np.random.default_rng(seed)
-    lens = np.concatenate([rng.integers(0, 200, 150), rng.integers(1000, 2049, 10)])
+    # about 1100 pages: below the segment plans' threshold at 152 SMs
+    lens = np.concatenate([rng.integers(0, 200, 100), rng.integers(1000, 2049, 5)])
     it = build(rng.permutation(lens)).items()
+    assert (it[:, 0] != 2).all()
     work = [busiest_warp_pages(x) for x in it]
     assert work == sorted(work, reverse=True)
     for a, b in zip(it[:-1], it[1:]):              # ranges before packed items on ties
@@ -140,12 +159,16 @@ def test_order_busiest_warp_first(seed):
             assert a[0] <= b[0]
 
 
-def test_uniform_batch_is_one_range_per_sequence():
+def test_uniform_batch_is_one_segment_per_sequence():
+    # 256 x 128 pages on 152 SMs: bins of 128 pages fit one wave of two CTAs
+    # per SM, so every sequence is one whole segment and nothing is merged
     plan = build([2048] * 256)
-    assert plan.num_items == 256 and plan.num_merges == 0 and plan.num_slots == 0
-    it = plan.items()
-    assert it[:, 4].tolist() == list(range(256))   # sequence order kept
-    assert set(it[:, 3].tolist()) == {128} and set(it[:, 1].tolist()) == {-1}
+    assert plan.num_segs == 256 and plan.num_items == 256
+    assert plan.num_merges == 0 and plan.num_slots == 0
+    sg = plan.segments()
+    assert sorted(sg[:, 0].tolist()) == list(range(256))
+    assert set(sg[:, 3].tolist()) == {128} and set(sg[:, 4].tolist()) == {-1}
+    assert set(plan.items()[:, 2].tolist()) == {1}
 
 
 def test_single_long_sequence_is_split_in_equal_ranges():
@@ -298,7 +321,7 @@ def test_shared_plan_covers_every_page_once(seed, groups, own):
     assert members <= set(merged)                  # every member is merged
     assert plan.num_slots == len(slots)
     assert plan.bytes_used == 4 * (12 + 16 * plan.num_items + 4 * plan.num_merges
-                                   + 36 * plan.num_shared)
+                                   + 36 * plan.num_shared + 8 * plan.num_segs)
     assert plan.shared_pages == max(int(n) for n in plan.shared()[:, 2])
 
 
@@ -423,3 +446,78 @@ def test_rebuild_in_place_gives_the_plan_of_the_new_lengths():
     p.rebuild(np.ascontiguousarray(lens2), np.ascontiguousarray(bt))
     q = B.Plan(lens2, 128, num_sms=SMS, block_tables=bt)
     assert np.array_equal(p.host, q.host) and p.num_shared == q.num_shared > 0
+
+
+# ---------------------------------------------------------- segment plans --
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_segment_plans_pack_one_wave_of_near_equal_ctas(seed):
+    # large ragged layers get segment plans: every page once, at most 4
+    # segments and range_pages pages per CTA, CTAs largest first, at most two
+    # CTAs per SM whenever the bins can be that small, split sequences merged
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(200, 2049, int(rng.integers(100, 300))).astype(np.int32)
+    lens[:5] = 0                                   # empty sequences get a segment too
+    plan = build(lens)
+    assert plan.num_segs > 0
+    pieces, slots = coverage(plan, [int(x) for x in lens])
+    for b, L in enumerate(lens.tolist()):
+        covered = sorted(p for p0, n in pieces[b] for p in range(p0, p0 + n))
+        assert covered == list(range(-(-L // 16)))
+    it = plan.items()
+    pages = it[:, 3]
+    assert pages.max() == plan.range_pages and list(pages) == sorted(pages, reverse=True)
+    assert (it[:, 2] <= 4).all()
+    P = int(sum(-(-int(L) // 16) for L in lens))
+    if plan.range_pages < 1024 and plan.range_pages < max(-(-int(L) // 16) for L in lens):
+        assert plan.num_items <= 2 * SMS
+    merged = {int(m[0]): int(m[2]) for m in plan.merges()}
+    for b in range(len(lens)):
+        if len(pieces[b]) > 1:
+            assert merged[b] == len(pieces[b])
+        else:
+            assert b not in merged
+    assert plan.num_slots == sum(merged.values())
+    assert P == int(pages.sum())
+
+
+def test_plan_kind_follows_the_bin_size():
+    # a segment plan only where its bins hold at least 16 pages: the mixed
+    # batch (2067 pages over 152 SMs) keeps the per-(item, kv head) plan;
+    # 256 x 128 pages is one whole sequence per segment CTA, nothing merged;
+    # 1024 x 16 pages packs about three sequences per CTA into one wave
+    from paged_kv_decode_04_gb300 import synth
+    w = synth.make_workload("mix", 0)
+    mix = B.Plan(w.seq_lens, w.max_blocks, num_sms=SMS)
+    assert mix.num_segs == 0 and set(mix.items()[:, 0].tolist()) == {0, 1}
+    peak = build([2048] * 256)
+    assert peak.num_segs == peak.num_items == 256 and peak.num_merges == 0
+    many = build([256] * 1024)
+    assert many.num_segs == 1024 and many.num_items <= 2 * SMS and many.num_merges == 0
+    assert many.range_pages >= 16 and many.items()[:, 2].max() <= 4
+
+
+def test_damaged_segment_plans_are_refused():
+    lens = np.random.default_rng(12).integers(200, 2049, 150).astype(np.int32)
+    plan = build(lens)
+    batch = len(lens)
+    good = plan.host.copy()
+    assert _kernels_for(good, batch) == "paged_decode_segments_kernel+merge_plan_kernel".encode()
+    sg0 = B.PLAN_HEADER_WORDS + 16 * plan.num_items + 4 * plan.num_merges
+    split = int(np.flatnonzero(plan.segments()[:, 4] >= 0)[0])
+    damage = {
+        "item kind": (12, 0),
+        "no segments": (14, 0),
+        "five segments": (14, 5),
+        "item pages": (15, int(good[15]) + 1),
+        "segments past the section": (13, plan.num_segs),
+        "segment sequence": (sg0, batch),
+        "segment length": (sg0 + 1, 2049),
+        "segment past its sequence": (sg0 + 2, 128),
+        "segment slot": (sg0 + 8 * split + 4, plan.num_slots),
+        "segment count in the header": (10, plan.num_segs + 1),
+    }
+    for what, (idx, value) in damage.items():
+        bad = good.copy()
+        bad[idx] = value
+        assert _kernels_for(bad, batch) is None, what
