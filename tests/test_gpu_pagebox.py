@@ -90,8 +90,10 @@ def test_fused_equals_unfused_and_plan_equals_fixed():
     dev = cuda_or_skip()
     w = workload(900, 2048, 70)
     b = binding()
+    # (planned: a segment plan, which may cut sequences in pieces; it equals
+    # the fixed plan within tolerance, and bit for bit when every segment is
+    # a whole sequence, which tests/test_gpu_segments.py checks)
     plan = b.Plan(w.seq_lens, w.max_blocks, device=dev)
-    assert plan.num_merges == 0 and not (plan.items()[:, 0] == 1).any()
     results = {}
     for mode in ("fused", "unfused", "planned"):
         d = synth.device_inputs(w, dev)
@@ -106,9 +108,14 @@ def test_fused_equals_unfused_and_plan_equals_fixed():
             out = b.decode_step_planned(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"], bt,
                                         lens, plan)
         results[mode] = (synth.bits(out), synth.bits(d["pool"]))
+    assert np.array_equal(results["unfused"][0], results["fused"][0])
     for mode in ("unfused", "planned"):
-        assert np.array_equal(results[mode][0], results["fused"][0]), mode
-        assert np.array_equal(results[mode][1], results["fused"][1]), mode
+        assert np.array_equal(results[mode][1], results["fused"][1]), mode   # the pool
+    if plan.num_merges == 0:
+        assert np.array_equal(results["planned"][0], results["fused"][0])
+    else:
+        ref, _ = oracle_step(w)
+        assert_close(results["planned"][0], ref, "segment plan")
 
 
 def test_bad_pages_and_lengths_reported():

@@ -119,14 +119,17 @@ def test_fused_step_equals_append_then_attention():
 
 
 def test_uniform_plan_matches_the_unplanned_call_bit_for_bit():
-    # 64 x 2048, planned as for a 16-SM part: one range per sequence, which is
-    # the fixed S = 1 split (a plan made for another SM count is still valid)
+    # 160 x 2048, planned as for a 16-SM part: a segment plan of whole
+    # sequences, four per CTA (a plan made for another SM count is still
+    # valid).  Each segment is attended exactly as the whole-page kernel
+    # attends one sequence, which the fixed S = 1 split runs for this batch.
     dev = cuda_or_skip()
-    w = synth.make_workload("edge", 21, seq_lens=np.full(64, 2048, np.int32), num_pages=8192)
+    w = synth.make_workload("edge", 21, seq_lens=np.full(160, 2048, np.int32), num_pages=20480)
     d = synth.device_inputs(w, dev)
     b = binding()
     plan = b.Plan(w.seq_lens, w.max_blocks, num_sms=16, device=dev)
-    assert plan.num_merges == 0 and set(plan.items()[:, 3].tolist()) == {128}
+    assert plan.num_merges == 0 and plan.num_segs == 160 and plan.items()[:, 2].max() == 4
+    assert b.attention_kernels(w.batch, w.max_blocks, 1) == "paged_decode_pagebox_kernel"
     bt = d["block_tables"][0]
     want = b.paged_decode_attention(d["q"][0], d["pool"], bt, d["seq_lens"], num_splits=1)
     got = b.paged_decode_attention_planned(d["q"][0], d["pool"], bt, d["seq_lens"], plan)

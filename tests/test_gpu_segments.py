@@ -9,10 +9,21 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_decode_04_gb300 import synth
-from _gpu_util import assert_close, binding, cuda_or_skip, oracle_step
+from _gpu_util import assert_close, binding, cuda_or_skip
 
 pytestmark = pytest.mark.gpu
+
+
+def oracle_step(w):
+    """The oracle's step (append of the live sequences, then attention) on a
+    compact host copy of layer 0; empty sequences append nothing."""
+    c = synth.compact(w, 0)
+    live = np.nonzero(c.seq_lens > 0)[0]
+    assert oracle.kv_append(c.k_new[live], c.v_new[live], c.pool, c.block_table[live],
+                            c.positions[live]) == 0
+    return oracle.decode_attention(c.q, c.pool, c.block_table, c.seq_lens), c
 
 
 def appended_ok(w, d, c):
@@ -41,7 +52,7 @@ def test_segment_plans_match_the_oracle(seed, num_sms):
     assert plan.num_segs > 0
     if num_sms > 152:
         assert plan.num_merges > 0 and plan.items()[:, 2].max() > 1
-    ref, c = oracle_step(w, 0)
+    ref, c = oracle_step(w)
     for fused in (True, False):
         d = synth.device_inputs(w, dev)
         err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -49,8 +60,9 @@ def test_segment_plans_match_the_oracle(seed, num_sms):
             out = b.decode_step_planned(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"],
                                         d["block_tables"][0], d["seq_lens"], plan, dev_err=err)
         else:
+            # (an empty sequence's position -1 is skipped and reported: no dev_err here)
             b.kv_append(d["k_new"][0], d["v_new"][0], d["pool"], d["block_tables"][0],
-                        d["positions"], dev_err=err)
+                        d["positions"])
             out = b.paged_decode_attention_planned(d["q"][0], d["pool"], d["block_tables"][0],
                                                    d["seq_lens"], plan, dev_err=err)
         got = synth.bits(out)
