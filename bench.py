@@ -49,16 +49,17 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_attention_peak_traff
 CSRC = os.path.join(ROOT, "paged_kv_decode_04_gb300", "csrc")
 # The source file of each decode kernel; every one of them also includes these headers.
 KERNEL_FILES = {
-    "paged_decode_kernel": "decode_attention.cu",
-    "merge_plan_kernel": "decode_attention.cu",
-    "merge_splits_kernel": "decode_attention.cu",
-    "paged_decode_pagebox_kernel": "decode_pagebox.cu",
-    "paged_decode_shared_kernel": "decode_shared.cu",
-    "paged_decode_segments_kernel": "decode_segments.cu",
+    "paged_decode_kernel": ("decode_attention.cu",),
+    "merge_plan_kernel": ("decode_attention.cu",),
+    "merge_splits_kernel": ("decode_attention.cu",),
+    "paged_decode_pagebox_kernel": ("decode_pagebox.cu",),
+    "paged_decode_shared_kernel": ("decode_shared.cu",),
+    "paged_decode_segments_kernel": ("decode_segments.cu",),
 }
 COMMON_SOURCES = ("decode_page.cuh", "pkv_device.cuh", "pkv_internal.h")
 KERNEL_SOURCES = [os.path.join(CSRC, f)
-                  for f in sorted(set(KERNEL_FILES.values())) + list(COMMON_SOURCES)]
+                  for f in sorted({f for fs in KERNEL_FILES.values() for f in fs})
+                  + list(COMMON_SOURCES)]
 # The traffic file holds a list of records {workload, kernel, kernel_sha, dram_bytes_per_launch};
 # kernel_sha covers the sources of the kernels the record names.
 # Every kernel of the library, for the per-kernel shares of a step.
@@ -144,7 +145,7 @@ def kernel_sources(kernel: str = None):
     if kernel is None:
         return KERNEL_SOURCES
     names = kernel.split(" (")[0].split("+")
-    files = sorted({KERNEL_FILES[n] for n in names if n in KERNEL_FILES})
+    files = sorted({f for n in names if n in KERNEL_FILES for f in KERNEL_FILES[n]})
     return [os.path.join(CSRC, f) for f in files + list(COMMON_SOURCES)]
 
 

@@ -24,17 +24,21 @@ def test_sources_follow_the_kernels_named():
     assert names(bench.kernel_sources(
         "paged_decode_shared_kernel+paged_decode_pagebox_kernel+merge_plan_kernel")) == \
         ["decode_attention.cu", "decode_pagebox.cu", "decode_shared.cu"] + headers
+    assert names(bench.kernel_sources(
+        "paged_decode_shared_kernel+paged_decode_segments_kernel+merge_plan_kernel")) == \
+        ["decode_attention.cu", "decode_segments.cu", "decode_shared.cu"] + headers
     assert set(names(bench.kernel_sources())) >= {"decode_attention.cu", "decode_pagebox.cu",
-                                                   "decode_shared.cu"}
+                                                   "decode_shared.cu", "decode_segments.cu"}
 
 
 def test_hash_ignores_comments_and_separates_kernels(tmp_path, monkeypatch):
     for f in ("decode_attention.cu", "decode_pagebox.cu", "decode_shared.cu",
-              "decode_page.cuh", "pkv_device.cuh", "pkv_internal.h"):
+              "decode_segments.cu", "decode_page.cuh", "pkv_device.cuh", "pkv_internal.h"):
         (tmp_path / f).write_text(f"// {f}\nint {f.split('.')[0]}_x = 1;\n")
     monkeypatch.setattr(bench, "CSRC", str(tmp_path))
     monkeypatch.setattr(bench, "KERNEL_SOURCES",
-                        [str(tmp_path / f) for f in sorted(set(bench.KERNEL_FILES.values()))])
+                        [str(tmp_path / f) for f in sorted({f for fs in bench.KERNEL_FILES.values()
+                                                            for f in fs})])
     pagebox = "paged_decode_pagebox_kernel (fused step)"
     shared = "paged_decode_shared_kernel+paged_decode_pagebox_kernel+merge_plan_kernel (fused step)"
     h_pb, h_sh = bench.kernel_sha(pagebox), bench.kernel_sha(shared)
