@@ -298,19 +298,30 @@ PKV_API int pkv_check_tables(const int32_t* block_table, int max_blocks,
  * whose plan fits in one wave of four CTAs per SM; when none does, the
  * ranges take the whole table width (a batch of long sequences then gets
  * one range each, as with num_splits = 1).
+ * Larger layers (P >= 16 x SMs) get a segment plan instead when its bins
+ * hold at least 16 pages: the pages are cut into pieces (a sequence of more
+ * than T pages into ceil(p / T) near-equal pieces) and packed best-fit,
+ * largest first, into bins of at most T pages and 4 segments, T the smallest
+ * bin size whose bins fit in one wave of two CTAs per SM; one CTA of all 8 kv
+ * heads streams each bin, each page one 32 KiB box.  A sequence in several
+ * pieces is combined by the merge kernel.
  * The plan is plain data: 12 header words
  *   {PKV_PLAN_MAGIC, batch, max_blocks, num_items, num_merges, num_slots,
- *    range_pages, bytes_used, num_shared, shared_pages, 0, 0},
- * then num_items items of 16 int32 words
- *   {kind (0 range, 1 packed), slot (-1: not split), p_begin, n,
- *    seq[4], len[4], 0, 0, 0, 0}
- * (a range item repeats its sequence in all four seq/len words; a packed
- * item holds one sequence per warp, -1 for none), then num_merges entries
- * {b, first slot, ranges, 0}, then num_shared shared-prefix items of 36
- * words {members, p_begin, n, 0, seq[16], slot[16]} (plans from
- * pkv_plan_build_shared only; shared_pages is the longest one's n).  The
- * results follow the same numerics as the calls above (same tolerance,
- * bit-identical on repeated runs of a plan).
+ *    range_pages, bytes_used, num_shared, shared_pages, num_segs, 0},
+ * then num_items items of 16 int32 words, all of kinds 0 and 1 or all of
+ * kind 2:
+ *   kind 0 (range), 1 (packed): {kind, slot (-1: not split), p_begin, n,
+ *     seq[4], len[4], 0, 0, 0, 0} -- a range item repeats its sequence in all
+ *     four seq/len words; a packed item holds one sequence per warp, -1 for
+ *     none;
+ *   kind 2 (segment CTA): {2, first segment, segments, pages, 0 x 12};
+ * then num_merges entries {b, first slot, pieces, 0}, then num_shared
+ * shared-prefix items of 36 words {members, p_begin, n, 0, seq[16],
+ * slot[16]} (plans from pkv_plan_build_shared only; shared_pages is the
+ * longest one's n), then num_segs segments of 8 words {b, L, p_begin, n,
+ * slot (-1: writes the output), 0, 0, 0}.  range_pages is the longest range
+ * or bin.  The results follow the same numerics as the calls above (same
+ * tolerance, bit-identical on repeated runs of a plan).
  */
 #define PKV_PLAN_MAGIC 0x32564b50 /* "PKV2" */
 

@@ -443,7 +443,9 @@ class Plan:
         return self
 
     def items(self) -> np.ndarray:
-        """[num_items][16] int32: kind, slot, p_begin, n, seq[4], len[4], 0 x 4."""
+        """[num_items][16] int32.  Kinds 0 (range) and 1 (packed): kind, slot,
+        p_begin, n, seq[4], len[4], 0 x 4.  Kind 2 (segment CTA): 2, first
+        segment, segments, pages, 0 x 12."""
         o = PLAN_HEADER_WORDS
         return self.host[o:o + 16 * self.num_items].reshape(self.num_items, 16)
 
@@ -459,7 +461,7 @@ class Plan:
 
     def segments(self) -> np.ndarray:
         """[num_segs][8] int32: b, L, p_begin, n, slot (-1: writes the output), 0 x 3;
-        item i (kind 2) runs segments [items()[i, 1], items()[i, 1] + items()[i, 2])."""
+        item i of kind 2 runs segments [items()[i, 1], items()[i, 1] + items()[i, 2])."""
         o = PLAN_HEADER_WORDS + 16 * self.num_items + 4 * self.num_merges + 36 * self.num_shared
         return self.host[o:o + 8 * self.num_segs].reshape(self.num_segs, 8)
 
