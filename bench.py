@@ -88,6 +88,9 @@ PREFILL_TEXT = "prefill write: 256 prompts x 2047 tokens, 8 kv heads x 64 bf16, 
 MIN_REPEATS = 10
 MIN_TIMED_SECONDS = 1.5
 MAX_REPEATS = 5000
+# Spin (clock cycles, about 50 us) that holds the stream after each L2 flush
+# while the host queues the next step.
+FLUSH_SPIN_CYCLES = 100000
 TOL_ABS, TOL_REL = 1e-3, 8e-3
 
 
@@ -497,7 +500,10 @@ class DecodeBench:
         """CUDA-event time (ms) of `steps` steps on the launching stream, with a
         barrier and a synchronize on both sides; with `flush` (a device buffer
         larger than L2), L2 is flushed before every step, outside the per-step
-        event pairs, and the region's time is the sum of the step events."""
+        event pairs, and the region's time is the sum of the step events.  After
+        each flush a short spin kernel holds the stream while the host queues
+        the step and its events, so a step's events time its kernels on the
+        device, not the host's launch of them."""
         torch = self.torch
         barrier(self.world)
         torch.cuda.synchronize(self.dev)
@@ -515,6 +521,7 @@ class DecodeBench:
                   for _ in range(steps)]
             for i in range(steps):
                 flush.fill_(i & 0xFF)
+                torch.cuda._sleep(FLUSH_SPIN_CYCLES)
                 ev[i][0].record(self.stream)
                 self.run_step()
                 ev[i][1].record(self.stream)
@@ -533,7 +540,7 @@ class DecodeBench:
         probe = self.one_region(steps, flush)
         per_region_s = max(probe, 1e-3) / 1e3
         if flush is not None:
-            per_region_s += steps * 1.2e-4         # the flushes between steps
+            per_region_s += steps * 1.7e-4         # the flushes and spins between steps
         reps = int(min(MAX_REPEATS, max(self.args.min_repeats,
                                         math.ceil(min_seconds / per_region_s))))
         t0 = time.time()
@@ -826,7 +833,9 @@ def measure_workload(name, args, dev, peak):
         "ms_per_step": ms, "timing": sp,
         "value": round(gbs, 2), "unit": "GB/s", "steps_per_s": round(1e3 / ms, 1),
         "l2": (f"flushed: {2 * l2 >> 20} MiB written between steps, outside the per-step "
-               f"CUDA-event pairs (K/V {w.kv_bytes() / 2 ** 20:.1f} MiB per step fits in L2)"
+               f"CUDA-event pairs (K/V {w.kv_bytes() / 2 ** 20:.1f} MiB per step fits in L2); "
+               f"each step queued behind a spin, so its events time the device, not the "
+               f"host's launch"
                if fits_l2 else f"inputs larger than L2: {w.kv_bytes() / 2 ** 30:.2f} GiB of "
                f"K/V streamed per step; no flush"),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
