@@ -319,8 +319,11 @@ PKV_API int pkv_check_tables(const int32_t* block_table, int max_blocks,
  * shared-prefix items of 36 words {members, p_begin, n, 0, seq[16],
  * slot[16]} (plans from pkv_plan_build_shared only; shared_pages is the
  * longest one's n), then num_segs segments of 8 words {b, L, p_begin, n,
- * slot (-1: writes the output), 0, 0, 0}.  range_pages is the longest range
- * or bin.  The results follow the same numerics as the calls above (same
+ * slot (-1: writes the output), fold, fold_slot, 0}: a segment with fold > 0
+ * writes the output of its sequence's pages [p_begin, p_begin + n) combined
+ * with the partials of slots [fold_slot, fold_slot + fold), which the
+ * shared-prefix items wrote (a group member whose own pages are one segment
+ * needs no merge entry).  range_pages is the longest range or bin.  The results follow the same numerics as the calls above (same
  * tolerance, bit-identical on repeated runs of a plan).
  */
 #define PKV_PLAN_MAGIC 0x32564b50 /* "PKV2" */

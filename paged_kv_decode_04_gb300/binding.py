@@ -460,7 +460,9 @@ class Plan:
         return self.host[o:o + 36 * self.num_shared].reshape(self.num_shared, 36)
 
     def segments(self) -> np.ndarray:
-        """[num_segs][8] int32: b, L, p_begin, n, slot (-1: writes the output), 0 x 3;
+        """[num_segs][8] int32: b, L, p_begin, n, slot (-1: writes the output), fold,
+        fold_slot, 0 (fold > 0: the output takes in the partials of slots
+        [fold_slot, fold_slot + fold) too);
         item i of kind 2 runs segments [items()[i, 1], items()[i, 1] + items()[i, 2])."""
         o = PLAN_HEADER_WORDS + 16 * self.num_items + 4 * self.num_merges + 36 * self.num_shared
         return self.host[o:o + 8 * self.num_segs].reshape(self.num_segs, 8)

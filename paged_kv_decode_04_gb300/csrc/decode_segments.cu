@@ -19,7 +19,10 @@
 // pages back to back through the same ring, so every CTA is busy for the
 // whole layer and all of them end together.  A segment that is a whole
 // sequence writes its output rows; a piece writes an unnormalised partial
-// that the merge kernel combines.
+// that the merge kernel combines.  Under a shared-prefix plan the
+// shared-prefix kernel runs first, and a member whose own pages are one
+// segment folds that kernel's partials for it into its rows and writes the
+// output itself, so such a sequence needs no merge.
 //
 // Per CTA, at the start: the segments' q rows (4 KiB each) arrive by bulk
 // copies; each warp computes the appended token's row of its head for every
@@ -144,6 +147,8 @@ __global__ void __launch_bounds__(kSgThreads, 2)
   auto seg_p0 = [&](int s) { return s_segs[2 * s].z; };
   auto seg_n = [&](int s) { return s_segs[2 * s].w; };
   auto seg_slot = [&](int s) { return s_segs[2 * s + 1].x; };
+  auto seg_fold = [&](int s) { return s_segs[2 * s + 1].y; };
+  auto seg_fold_slot = [&](int s) { return s_segs[2 * s + 1].z; };
 
   // page ids of the concatenated segments
   for (int i = tid; i < total; i += kSgThreads) {
@@ -272,15 +277,74 @@ __global__ void __launch_bounds__(kSgThreads, 2)
       }
     }
     __syncwarp();
-    const int b = seg_b(s), slot = seg_slot(s);
+    const int b = seg_b(s), slot = seg_slot(s), nf = seg_fold(s);
     const int d = 2 * lane;
+    float Mr[kGroup], Lr[kGroup];
+    float2 Or[kGroup];
 #pragma unroll
     for (int r = 0; r < kGroup; ++r) {
-      const float M = xch[r];
-      const float Ls = M == -INFINITY ? 0.f : xch[kGroup + r];
-      const float2 O = M == -INFINITY ? make_float2(0.f, 0.f)
-                                      : *reinterpret_cast<const float2*>(
-                                            xch + 2 * kGroup + r * kHeadDim + d);
+      Mr[r] = xch[r];
+      Lr[r] = Mr[r] == -INFINITY ? 0.f : xch[kGroup + r];
+      Or[r] = Mr[r] == -INFINITY ? make_float2(0.f, 0.f)
+                                 : *reinterpret_cast<const float2*>(
+                                       xch + 2 * kGroup + r * kHeadDim + d);
+    }
+    if (nf > 0) {
+      // fold in the partials of the sequence's shared ranges (slots
+      // fold_slot.., written by the shared-prefix kernel, which ended before
+      // this grid's wait returned), in slot order, then this segment's own
+      // rows, by an online combine; two slots' loads for all 4 rows are in
+      // flight at once
+      float Mx[kGroup], Lf[kGroup];
+      float2 Of[kGroup];
+#pragma unroll
+      for (int r = 0; r < kGroup; ++r) {
+        Mx[r] = -INFINITY;
+        Lf[r] = 0.f;
+        Of[r] = make_float2(0.f, 0.f);
+      }
+      auto combine = [&](int r, float m, float l, float2 o) {
+        if (!(l > 0.f)) return;
+        const float mn = fmaxf(Mx[r], m);
+        const float sc = Mx[r] == -INFINITY ? 0.f : fast_exp2(Mx[r] - mn);
+        const float w = fast_exp2(m - mn);
+        Lf[r] = fmaf(l, w, Lf[r] * sc);
+        Of[r].x = fmaf(w, o.x, Of[r].x * sc);
+        Of[r].y = fmaf(w, o.y, Of[r].y * sc);
+        Mx[r] = mn;
+      };
+      const int64_t p0 = static_cast<int64_t>(seg_fold_slot(s)) * kNumQHeads + g * kGroup;
+      for (int f = 0; f < nf; f += 2) {
+        float2 ml[2][kGroup], acc[2][kGroup];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int r = 0; r < kGroup; ++r) {
+            const int64_t part = p0 + static_cast<int64_t>(f + u) * kNumQHeads + r;
+            const bool has = f + u < nf;
+            ml[u][r] = has ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + part * 2))
+                           : make_float2(-INFINITY, 0.f);
+            acc[u][r] = has ? __ldcg(reinterpret_cast<const float2*>(
+                                  a.part_acc + part * kHeadDim + d))
+                            : make_float2(0.f, 0.f);
+          }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int r = 0; r < kGroup; ++r) combine(r, ml[u][r].x, ml[u][r].y, acc[u][r]);
+      }
+#pragma unroll
+      for (int r = 0; r < kGroup; ++r) {
+        combine(r, Mr[r], Lr[r], Or[r]);
+        Mr[r] = Mx[r];
+        Lr[r] = Lf[r];
+        Or[r] = Of[r];
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kGroup; ++r) {
+      const float M = Mr[r], Ls = Lr[r];
+      const float2 O = Or[r];
       if (slot < 0) {
         const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
         const uint32_t v = static_cast<uint32_t>(float_to_bf16_rne(O.x * inv)) |

@@ -516,6 +516,12 @@ bool plan_body_valid(const PlanHeader& h) {
         if (!seq_ok(sg[0]) || sg[1] < 0 || sg[1] > lmax || !range_ok(sg[2], sg[3], h.range_pages) ||
             sg[2] + sg[3] > live || (sg[4] != -1 && (sg[4] < 0 || sg[4] >= h.num_slots)))
           return false;
+        // partials folded into the output: slots [sg[6], sg[6] + sg[5])
+        if (sg[5] < 0 || sg[7] != 0 ||
+            (sg[5] == 0 ? sg[6] != 0
+                        : (sg[4] != -1 || sg[6] < 0 ||
+                           static_cast<int64_t>(sg[6]) + sg[5] > h.num_slots)))
+          return false;
         pages += sg[3];
       }
       if (pages != w[3]) return false;
@@ -658,7 +664,9 @@ PKV_API const char* pkv_attention_kernels(int batch, int max_blocks, int num_spl
     if (h == nullptr) return nullptr;
     if (h->num_segs > 0) {
       if (h->num_shared > 0)
-        return "paged_decode_shared_kernel+paged_decode_segments_kernel+merge_plan_kernel";
+        return h->num_merges > 0
+                   ? "paged_decode_shared_kernel+paged_decode_segments_kernel+merge_plan_kernel"
+                   : "paged_decode_shared_kernel+paged_decode_segments_kernel";
       return h->num_merges > 0 ? "paged_decode_segments_kernel+merge_plan_kernel"
                                : "paged_decode_segments_kernel";
     }

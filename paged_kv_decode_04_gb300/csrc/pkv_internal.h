@@ -47,11 +47,13 @@ constexpr int kPlanSharedWords = 4 + 2 * kSharedMembers;
 // Segment plans (the plan's segment section, header word 10 = its count):
 // one CTA per item of kind kPlanKindSegments {2, first segment, segments,
 // pages, 0 ...} streams the pages of up to kSegMax segments {b, L, p_begin,
-// n, slot, 0, 0, 0} in order through one ring of whole-page boxes, all 8 kv
-// heads at once (paged_decode_segments_kernel); slot -1: the segment is the
-// whole sequence and writes its output, else a partial for the merge.  The
-// planner packs the layer's pages into one wave of kSegCtasPerSm CTAs per SM
-// of near-equal pages.
+// n, slot, fold, fold_slot, 0} in order through one ring of whole-page boxes,
+// all 8 kv heads at once (paged_decode_segments_kernel); slot -1: the
+// segment writes its sequence's output, else a partial for the merge.  With
+// fold > 0 the output also takes in the partials of slots [fold_slot,
+// fold_slot + fold), which the shared-prefix kernel launched before it wrote.
+// The planner packs the layer's pages into one wave of kSegCtasPerSm CTAs
+// per SM of near-equal pages.
 constexpr int kPlanKindSegments = 2;
 constexpr int kPlanSegWords = 8;
 constexpr int kSegMax = 4;

@@ -240,9 +240,12 @@ int segment_bin_size(const std::vector<int>& own, const std::vector<int>& start,
 }
 
 // The segment plan for bins of T pages; bins run largest first.  A sequence
-// in more than one piece, or a member of a shared group, writes partials to
-// consecutive slots (its shared ranges first) and gets a merge entry; any
-// other sequence's segment writes its output.
+// in more than one piece writes partials to consecutive slots (a group
+// member's shared ranges first) and gets a merge entry.  A group member whose
+// own pages are one piece folds its shared ranges' partials into its own rows
+// and writes its output (the shared-prefix kernel has ended when the segment
+// kernel passes its grid wait): its slots hold only those partials, and it
+// gets no merge entry.  Any other sequence's segment writes its output.
 int build_segments(const int32_t* lens, int batch, int max_blocks, int T,
                    const std::vector<int>& own, const std::vector<int>& start,
                    const std::vector<int>& group_of, const std::vector<SharedGroup>& groups,
@@ -266,13 +269,16 @@ int build_segments(const int32_t* lens, int batch, int max_blocks, int T,
   int slots = 0;
   for (int b = 0; b < batch; ++b) {
     const int ns = group_of[b] >= 0 ? shared_ranges[group_of[b]] : 0;
-    if (npieces[b] > 1 || ns > 0) {
+    if (npieces[b] > 1) {
       merges.insert(merges.end(), {b, slots, ns + npieces[b], 0});
       slot_base[b] = slots;
       slots += ns + npieces[b];
+    } else if (ns > 0) {  // folded by its one own segment
+      slot_base[b] = slots;
+      slots += ns;
     }
   }
-  // a sequence's pieces take its slots in the order of their pages
+  // a split sequence's pieces take its slots in the order of their pages
   std::vector<int> piece_slot(pieces.size(), -1);
   {
     std::vector<int> by_page(pieces.size());
@@ -280,7 +286,7 @@ int build_segments(const int32_t* lens, int batch, int max_blocks, int T,
     counting_sort(by_page, max_blocks + 1, [&](int i) { return pieces[i].p_begin; });
     for (int i : by_page) {
       const Piece& pc = pieces[i];
-      if (slot_base[pc.b] < 0) continue;
+      if (npieces[pc.b] < 2) continue;
       const int ns = group_of[pc.b] >= 0 ? shared_ranges[group_of[pc.b]] : 0;
       piece_slot[i] = slot_base[pc.b] + ns + next_piece[pc.b]++;
     }
@@ -332,6 +338,10 @@ int build_segments(const int32_t* lens, int batch, int max_blocks, int T,
       seg[2] = pc.p_begin;
       seg[3] = pc.n;
       seg[4] = piece_slot[i];
+      if (npieces[pc.b] == 1 && group_of[pc.b] >= 0) {  // fold the shared partials
+        seg[5] = shared_ranges[group_of[pc.b]];
+        seg[6] = slot_base[pc.b];
+      }
       seg += kPlanSegWords;
       ++next_seg;
     }

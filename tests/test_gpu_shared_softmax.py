@@ -102,9 +102,11 @@ def bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("shared_plan", [True, False])
+@pytest.mark.parametrize("shared_plan,sms", [(True, 0), (False, 0), (True, 8)])
 @pytest.mark.parametrize("fused", [False, True])
-def test_shared_prefix_softmax_extremes(shared_plan, fused):
+def test_shared_prefix_softmax_extremes(shared_plan, sms, fused):
+    # sms 8: the plan made as for 8 SMs is a segment plan, in which every
+    # member's one own segment folds its shared partials into its output
     dev = cuda_or_skip()
     b = binding()
     q, pool, bt, lens, k_new, v_new = build(505)
@@ -120,13 +122,17 @@ def test_shared_prefix_softmax_extremes(shared_plan, fused):
     dq, dpool = dev_u16(q, dev), dev_u16(pool, dev)
     dbt, dl = torch.from_numpy(bt).to(dev), torch.from_numpy(lens).to(dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    plan = b.Plan(lens, bt.shape[1], device=dev, block_tables=bt if shared_plan else None)
+    plan = b.Plan(lens, bt.shape[1], device=dev, num_sms=sms,
+                  block_tables=bt if shared_plan else None)
     if shared_plan:
         assert plan.num_shared >= GROUPS
         assert b.attention_kernels(len(lens), bt.shape[1], 0, plan).startswith(
             "paged_decode_shared_kernel+")
     else:
         assert plan.num_shared == 0
+    if sms:
+        assert plan.num_segs > 0 and plan.num_merges == 0
+        assert (plan.segments()[:, 5] > 0).sum() == len(lens)
     if fused:
         out = b.decode_step_planned(dq, dev_u16(k_new, dev), dev_u16(v_new, dev), dpool, dbt, dl,
                                     plan, dev_err=err)
@@ -136,4 +142,4 @@ def test_shared_prefix_softmax_extremes(shared_plan, fused):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_close(got, ref, f"shared-prefix softmax extremes, shared_plan={shared_plan}, "
-                           f"fused={fused}")
+                           f"sms={sms}, fused={fused}")

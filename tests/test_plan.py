@@ -18,10 +18,14 @@ def build(lens, max_blocks=128, sms=SMS):
     return B.Plan(np.asarray(lens, np.int32), max_blocks, num_sms=sms)
 
 
-def coverage(plan, lens):
-    """Per sequence: the list of (first page, count) pieces the plan attends."""
+def coverage(plan, lens, folds=None):
+    """Per sequence: the list of (first page, count) pieces the plan attends.
+    folds (a dict): filled with b -> (first slot, count) of the partials a
+    segment folds into sequence b's output."""
     pieces = {b: [] for b in range(len(lens))}
     slots = {}
+    if folds is None:
+        folds = {}
     segs = plan.segments() if plan.num_segs else None
     for it in plan.items():
         kind, slot, p0, n = (int(x) for x in it[:4])
@@ -30,12 +34,17 @@ def coverage(plan, lens):
             assert 1 <= nseg <= 4 and not it[4:].any()
             mine = segs[first:first + nseg]
             assert int(mine[:, 3].sum()) == pages
-            for b, L, q0, m, sl in (tuple(int(x) for x in sg[:5]) for sg in mine):
-                assert L == lens[b]
+            for b, L, q0, m, sl, nf, fs, z in (tuple(int(x) for x in sg) for sg in mine):
+                assert L == lens[b] and z == 0
                 pieces[b].append((q0, m))
                 if sl >= 0:
-                    assert sl not in slots
+                    assert sl not in slots and nf == 0 and fs == 0
                     slots[sl] = (b, q0)
+                elif nf > 0:
+                    assert b not in folds
+                    folds[b] = (fs, nf)
+                else:
+                    assert fs == 0
             continue
         assert segs is None
         seqs, ls = it[4:8], it[8:12]
@@ -279,8 +288,8 @@ def shared_case(seed, groups, own, mb=128):
     return np.asarray(lens, np.int32), np.asarray(rows, np.int32)
 
 
-def shared_coverage(plan, lens, bt):
-    pieces, slots = coverage(plan, lens)
+def shared_coverage(plan, lens, bt, folds=None):
+    pieces, slots = coverage(plan, lens, folds)
     for it in plan.shared().tolist():
         members, p0, n = it[0], it[1], it[2]
         seqs, sl = it[4:4 + members], it[20:20 + members]
@@ -296,7 +305,9 @@ def shared_coverage(plan, lens, bt):
 
 
 @pytest.mark.parametrize("seed,groups,own", [
-    (0, [(16, 96)] * 4, (32, 32)),            # the prefix workload's shape
+    (0, [(16, 96)] * 4, (32, 32)),            # the prefix workload's groups, fewer of them
+    (0, [(16, 96)] * 16, (32, 32)),           # the prefix workload: a segment plan
+    (4, [(16, 40)] * 12 + [(2, 20)] * 8, (20, 80)),    # segments, some members split
     (1, [(3, 20), (1, 5), (8, 40), (2, 16)], (1, 60)),
     (2, [(5, 1000)], (1, 3)),                 # long prefixes: several shared ranges
 ])
@@ -305,7 +316,8 @@ def test_shared_plan_covers_every_page_once(seed, groups, own):
     lens, bt = shared_case(seed, groups, own, mb)
     plan = B.Plan(lens, mb, num_sms=SMS, block_tables=bt, min_shared_pages=16)
     assert plan.num_shared > 0
-    pieces, slots = shared_coverage(plan, lens, bt)
+    folds = {}
+    pieces, slots = shared_coverage(plan, lens, bt, folds)
     for b, L in enumerate(lens.tolist()):
         covered = []
         for p0, n in sorted(pieces[b]):
@@ -318,7 +330,19 @@ def test_shared_plan_covers_every_page_once(seed, groups, own):
         assert all(x[0] == b for x in merged[b])
         assert [x[1] for x in merged[b]] == sorted(x[1] for x in merged[b])
     members = {int(x) for it in plan.shared() for x in it[4:4 + it[0]]}
-    assert members <= set(merged)                  # every member is merged
+    # every member is merged, or (a segment plan, its own pages one segment)
+    # its segment folds exactly its shared ranges' partials, in page order
+    assert members <= set(merged) | set(folds) and not set(merged) & set(folds)
+    for b, (first, nf) in folds.items():
+        assert b in members
+        got = [slots[first + r] for r in range(nf)]
+        assert all(x[0] == b for x in got)
+        assert [x[1] for x in got] == sorted(x[1] for x in got)
+        assert len(pieces[b]) == nf + 1
+    if plan.num_segs:
+        assert folds or seed == 4
+    if groups == [(16, 96)] * 16:
+        assert plan.num_merges == 0 and len(folds) == 256
     assert plan.num_slots == len(slots)
     assert plan.bytes_used == 4 * (12 + 16 * plan.num_items + 4 * plan.num_merges
                                    + 36 * plan.num_shared + 8 * plan.num_segs)
@@ -521,3 +545,36 @@ def test_damaged_segment_plans_are_refused():
         bad = good.copy()
         bad[idx] = value
         assert _kernels_for(bad, batch) is None, what
+
+
+def test_damaged_fold_words_are_refused():
+    # a segment that folds partials into its output names slots inside the
+    # plan's partial area and writes the output itself (slot -1); reserved
+    # words stay zero
+    lens, bt = shared_case(0, [(16, 96)] * 16, (32, 32))
+    plan = B.Plan(lens, 128, num_sms=SMS, block_tables=bt, min_shared_pages=16)
+    batch = len(lens)
+    good = plan.host.copy()
+    assert _kernels_for(good, batch) == \
+        "paged_decode_shared_kernel+paged_decode_segments_kernel".encode()
+    sg0 = (B.PLAN_HEADER_WORDS + 16 * plan.num_items + 4 * plan.num_merges
+           + 36 * plan.num_shared)
+    segs = plan.segments()
+    f = int(np.flatnonzero((segs[:, 5] > 0) & (segs[:, 6] > 0))[0])
+    at = sg0 + 8 * f
+    damage = {
+        "fold past the slots": (at + 6, plan.num_slots - 1),
+        "negative fold slot": (at + 6, -1),
+        "negative fold count": (at + 5, -1),
+        "fold with a partial of its own": (at + 4, 0),
+        "reserved word": (at + 7, 1),
+    }
+    for what, (idx, value) in damage.items():
+        bad = good.copy()
+        bad[idx] = value
+        assert _kernels_for(bad, batch) is None, what
+    unfolded = good.copy()
+    unfolded[at + 5] = 0
+    assert _kernels_for(unfolded, batch) is None      # fold slot left without a fold
+    unfolded[at + 6] = 0
+    assert _kernels_for(unfolded, batch) is not None
