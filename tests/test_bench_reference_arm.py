@@ -9,6 +9,15 @@ import sys
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+def bench_metric():
+    """bench.py's METRIC, the metric both arms print."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_module", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.METRIC
+
+
 def run_bench(*args, timeout=600):
     return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
                           capture_output=True, text=True, timeout=timeout)
@@ -21,8 +30,7 @@ def test_reference_arm_prints_one_contract_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference"
-    with open(os.path.join(ROOT, "BASELINE.json")) as f:
-        assert d["metric"] == json.load(f)["metric"]
+    assert d["metric"] == bench_metric()          # the same metric line as the GPU arm
     assert d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
     assert d["value"] > 0 and d["data"] == "synthetic" and d["dtype"] == "f64"
