@@ -368,6 +368,10 @@ PKV_API size_t pkv_plan_workspace_bytes(const void* plan);
  * plan_host: the built plan (read on the host for the grid sizes);
  * plan_dev: a device copy of its first bytes_used bytes, 16-byte aligned,
  * which must stay unchanged until the call's kernels have run.  The kernels
+ * read plan_dev as soon as they start, which may be before the kernel queued
+ * just ahead of the call has finished (programmatic dependent launch): fill
+ * it with a copy (cudaMemcpyAsync, as the Python binding's Plan.to does) or
+ * earlier work, not with a kernel launched right before the call.  The kernels
  * take every length from the plan; seq_lens is only compared with it, and a
  * difference sets PKV_DEVERR_PLAN (the outputs then follow the plan's
  * lengths).  workspace: at least pkv_plan_workspace_bytes(plan_host).

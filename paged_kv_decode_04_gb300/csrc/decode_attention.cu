@@ -139,27 +139,27 @@ __device__ __forceinline__ int pick(int4 v, int i) {
 
 // Before griddepcontrol.wait: prefetch into L2 the head-g tiles that the
 // CTA's first ring fill will load, so that a CTA made resident while the
-// previous grid drains finds them there.  Every word read here may still be
-// written by that grid, so the values are only addresses for the prefetch:
-// reads bypass L1, every index is range-checked, nothing is recorded, and the
-// kernel reads everything again after the wait.  (A mixed 16..2048-token
+// previous grid drains finds them there.  The plan item (head, bs, ls) is
+// read before the wait: a plan is filled by a copy, never by a kernel, so it
+// is complete before this grid starts.  The lengths and block-table entries
+// read here may still be written by the previous grid, so they are only
+// addresses for the prefetch: reads bypass L1, every index is range-checked,
+// nothing is recorded, and the kernel reads them again after the wait.  (A mixed 16..2048-token
 // batch, 16 layers: 267.5 -> 252.4 us per step; prefetching twice the ring
 // fill: 257.0 us.)
 template <int kStages, bool kPlanned>
 __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map, const AttnArgs& a,
-                                                     int g, int tid) {
+                                                     int g, int tid, int4 head, int4 bs, int4 ls) {
   int b = -1, p = -1;  // this thread's tile: sequence b, logical page p
   if constexpr (kPlanned) {
-    const int4* it = a.plan_items + static_cast<int64_t>(blockIdx.y) * (kPlanItemWords / 4);
-    const int4 head = ld_cg(it);
     if (head.x == kPlanKindPacked) {
       const int w = tid >> 5, l = tid & 31;
       if (l < kStages) {
-        b = pick(ld_cg(it + 1), w);
-        if (l * kPageSize < pick(ld_cg(it + 2), w)) p = l;
+        b = pick(bs, w);
+        if (l * kPageSize < pick(ls, w)) p = l;
       }
     } else if (tid < kWarps * kStages && tid < head.w) {
-      b = ld_cg(it + 1).x;
+      b = bs.x;
       p = head.z + tid;
     }
   } else {
@@ -193,7 +193,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
   const int warp = tid >> 5;
   const int g = blockIdx.x % kNumKvHeads;
   if (tid == 0) tma_prefetch_desc(&pool_map);
-  prefetch_first_tiles<kStages, kPlanned>(&pool_map, a, g, tid);
+  // planned: the item {kind, slot, p_begin, n}, the warps' sequences and
+  // lengths (plan data: complete before this grid starts)
+  int4 p_head = make_int4(0, 0, 0, 0), p_bs = p_head, p_ls = p_head;
+  if constexpr (kPlanned) {
+    const int4* it = a.plan_items + static_cast<int64_t>(blockIdx.y) * (kPlanItemWords / 4);
+    p_head = it[0];
+    p_bs = it[1];
+    p_ls = it[2];
+  }
+  prefetch_first_tiles<kStages, kPlanned>(&pool_map, a, g, tid, p_head, p_bs, p_ls);
   wait_for_prior_grids();
   allow_dependent_grids();
 
@@ -210,10 +219,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
   int part_step = 0;       // slot distance between consecutive query rows
   const int Lmax = a.max_blocks * kPageSize;
   if constexpr (kPlanned) {
-    const int4* it = a.plan_items + static_cast<int64_t>(blockIdx.y) * (kPlanItemWords / 4);
-    const int4 head = it[0];  // (kind, slot, p_begin, n)
-    const int4 bs = it[1];    // sequence of each warp
-    const int4 ls = it[2];    // its length, as the plan was built for
+    const int4 head = p_head;  // (kind, slot, p_begin, n)
+    const int4 bs = p_bs;      // sequence of each warp
+    const int4 ls = p_ls;      // its length, as the plan was built for
     packed = head.x == kPlanKindPacked;
     p_begin = head.z;
     n = head.w;
@@ -455,8 +463,9 @@ __global__ void __launch_bounds__(32) merge_splits_kernel(const AttnArgs a) {
 // blockDim.x / 32 query rows per CTA.
 __global__ void __launch_bounds__(kMergeRowsMax * 32) merge_plan_kernel(const AttnArgs a) {
   allow_dependent_grids();  // the next grid may launch; it waits for this one itself
+  // (b, first slot, ranges, 0): plan data, complete before this grid starts
+  const int4 e = a.plan_merges[blockIdx.y];
   wait_for_prior_grids();
-  const int4 e = a.plan_merges[blockIdx.y];  // (b, first slot, ranges, 0)
   const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t row = static_cast<int64_t>(e.x) * kNumQHeads + j;
   merge_row(a, static_cast<int64_t>(e.y) * kNumQHeads + j, kNumQHeads, e.z,

@@ -73,18 +73,17 @@ __device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* m
 
 // Before griddepcontrol.wait: prefetch into L2 the CTA's first
 // kPbPrefetchPages pages (as prefetch_first_tiles does for the per-head
-// kernel: every word read here is only an address for the prefetch; reads
-// bypass L1, indices are range-checked, and everything is read again after
-// the wait).
+// kernel: the plan item, read before the wait, is plan data and complete;
+// the lengths and block-table entries read here are only addresses for the
+// prefetch: reads bypass L1, indices are range-checked, and they are read
+// again after the wait).
 template <bool kPlanned>
 __device__ __forceinline__ void prefetch_first_pages(const CUtensorMap* map, const AttnArgs& a,
-                                                     int tid) {
+                                                     int tid, int4 head, int item_b) {
   int b = -1, p = -1;
   if constexpr (kPlanned) {
-    const int4* it = a.plan_items + static_cast<int64_t>(blockIdx.x) * (kPlanItemWords / 4);
-    const int4 head = ld_cg(it);
     if (tid < kPbPrefetchPages && tid < head.w) {
-      b = ld_cg(it + 1).x;
+      b = item_b;
       p = head.z + tid;
     }
   } else if (tid < kPbPrefetchPages) {
@@ -118,7 +117,17 @@ __global__ void __launch_bounds__(kPbThreads, 2)
   const int lane = tid & 31;
   const int g = tid >> 5;  // this warp's kv head
   if (tid == 0) tma_prefetch_desc(&page_map);
-  prefetch_first_pages<kPlanned>(&page_map, a, tid);
+  // planned: the item {kind = range, slot, p_begin, n}, its sequence and
+  // length (plan data: complete before this grid starts)
+  int4 p_head = make_int4(0, 0, 0, 0);
+  int p_b = -1, p_L = 0;
+  if constexpr (kPlanned) {
+    const int4* it = a.plan_items + static_cast<int64_t>(blockIdx.x) * (kPlanItemWords / 4);
+    p_head = it[0];
+    p_b = it[1].x;
+    p_L = it[2].x;
+  }
+  prefetch_first_pages<kPlanned>(&page_map, a, tid, p_head, p_b);
   wait_for_prior_grids();
   allow_dependent_grids();
 
@@ -129,10 +138,9 @@ __global__ void __launch_bounds__(kPbThreads, 2)
   int dev_len = -2, plan_len = 0;  // work plan: device length read for the plan check
   const int Lmax = a.max_blocks * kPageSize;
   if constexpr (kPlanned) {
-    const int4* it = a.plan_items + static_cast<int64_t>(blockIdx.x) * (kPlanItemWords / 4);
-    const int4 head = it[0];  // (kind = range, slot, p_begin, n)
-    b = it[1].x;
-    L = it[2].x;
+    const int4 head = p_head;  // (kind = range, slot, p_begin, n)
+    b = p_b;
+    L = p_L;
     plan_len = L;
     // the lengths come from the plan; seq_lens is only checked against it
     // (the load is consumed at the end of the kernel, off the critical path)

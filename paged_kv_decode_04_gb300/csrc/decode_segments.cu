@@ -84,16 +84,15 @@ __device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* m
 }
 
 // Before griddepcontrol.wait: prefetch into L2 the first pages of the CTA's
-// first segment.  The words read here may still be being written by the
-// previous grid, so they only serve as prefetch addresses (L1-bypassing
-// loads, every index range-checked, nothing recorded); the kernel reads all
-// of it again after the wait.
+// first segment `seg` (plan data, read before the wait: a plan is filled by a
+// copy, never by a kernel, so it is complete before this grid starts).  The
+// block-table entries read here may still be being written by the previous
+// grid, so they only serve as prefetch addresses (L1-bypassing loads, every
+// index range-checked, nothing recorded); the kernel reads them again after
+// the wait.
 __device__ __forceinline__ void prefetch_first_pages(const CUtensorMap* map, const AttnArgs& a,
-                                                     int tid) {
+                                                     int tid, int4 seg) {
   if (tid >= kSgPrefetchPages) return;
-  const int4 head = ld_cg(a.plan_items + static_cast<int64_t>(blockIdx.x) * (kPlanItemWords / 4));
-  if (head.x != kPlanKindSegments || head.y < 0) return;
-  const int4 seg = ld_cg(a.plan_segs + static_cast<int64_t>(head.y) * (kPlanSegWords / 4));
   const int b = seg.x, p = seg.z + tid;
   if (tid < seg.w && b >= 0 && b < a.batch && p >= 0 && p < a.max_blocks) {
     const int pid = ld_cg(a.block_table + static_cast<int64_t>(b) * a.max_blocks + p);
@@ -122,11 +121,10 @@ __global__ void __launch_bounds__(kSgThreads, 2)
   const int lane = tid & 31;
   const int g = tid >> 5;  // this warp's kv head
   if (tid == 0) tma_prefetch_desc(&page_map);
-  prefetch_first_pages(&page_map, a, tid);
-  wait_for_prior_grids();
-  allow_dependent_grids();
 
-  // ---- this CTA's segments {b, L, p_begin, n, slot, 0, 0, 0}
+  // ---- this CTA's segments {b, L, p_begin, n, slot, fold, fold_slot, 0},
+  // and the barriers, before the grid wait (plan data: complete before this
+  // grid starts)
   const int4 head = a.plan_items[static_cast<int64_t>(blockIdx.x) * (kPlanItemWords / 4)];
   const int first = head.y, nseg = head.z, total = head.w;
   if (tid < 2 * nseg)
@@ -141,6 +139,9 @@ __global__ void __launch_bounds__(kSgThreads, 2)
     fence_barrier_init();
   }
   __syncthreads();
+  prefetch_first_pages(&page_map, a, tid, s_segs[0]);
+  wait_for_prior_grids();
+  allow_dependent_grids();
   const int Lmax = a.max_blocks * kPageSize;
   auto seg_b = [&](int s) { return s_segs[2 * s].x; };
   auto seg_L = [&](int s) { return min(max(s_segs[2 * s].y, 0), Lmax); };

@@ -129,20 +129,20 @@ __host__ __device__ constexpr size_t sh_smem_bytes(int pages) {
 }
 
 // Before the grid dependency wait: pull the first kPrefetchBatches batches'
-// K and V rows into L2.  The plan item and the leader's table entries read
-// here may still be being written by the previous grid, so they serve only
-// as prefetch addresses (L1-bypassing loads, every index range-checked,
-// nothing recorded); the kernel reads all of it again after the wait.
+// K and V rows of pages [p_begin, p_begin + n) of the leader's table into
+// L2.  The item (plan data) is complete before this grid starts; the
+// leader's table entries read here may still be being written by the
+// previous grid, so they serve only as prefetch addresses (L1-bypassing
+// loads, every index range-checked, nothing recorded), and the kernel reads
+// them again after the wait.
 __device__ __forceinline__ void prefetch_first_batches(const CUtensorMap* map, const AttnArgs& a,
-                                                       int g, int tid) {
+                                                       int g, int tid, int p_begin, int n,
+                                                       int leader) {
   constexpr int kPages = kPrefetchBatches * kTcBatch;
   if (tid >= 2 * kPages) return;
-  const int4* itp = a.plan_shared + static_cast<int64_t>(blockIdx.y) * (kPlanSharedWords / 4);
-  const int4 head = ld_cg(itp);      // members, p_begin, n, 0
-  const int leader = ld_cg(itp + 1).x;
   const int i = tid >> 1;            // page of the range; even tid: K rows, odd: V rows
-  if (i < head.z && leader >= 0 && leader < a.batch && head.y >= 0 && head.y + i < a.max_blocks) {
-    const int pid = ld_cg(a.block_table + static_cast<int64_t>(leader) * a.max_blocks + head.y + i);
+  if (i < n && leader >= 0 && leader < a.batch && p_begin >= 0 && p_begin + i < a.max_blocks) {
+    const int pid = ld_cg(a.block_table + static_cast<int64_t>(leader) * a.max_blocks + p_begin + i);
     if (pid >= 0 && pid < a.num_pages)
       tma_prefetch_l2_3d(map, g * kHeadDim, (tid & 1) ? kPageSize : 0, pid);
   }
@@ -186,16 +186,16 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   const int warp = tid >> 5;
   const int g = blockIdx.x;  // kv head
   if (tid == 0) tma_prefetch_desc(&half_map);
-  prefetch_first_batches(&half_map, a, g, tid);
-  wait_for_prior_grids();
-  allow_dependent_grids();
-
-  // ---- the item: {members, p_begin, n, 0, seq[16], slot[16]}
+  // ---- the item: {members, p_begin, n, 0, seq[16], slot[16]} (plan data,
+  // complete before this grid starts)
   const int32_t* it = reinterpret_cast<const int32_t*>(a.plan_shared) +
                       static_cast<int64_t>(blockIdx.y) * kPlanSharedWords;
   const int members = it[0], p_begin = it[1], n = it[2];
   const int leader = it[4];
   const int nb = (n + kTcBatch - 1) / kTcBatch;
+  prefetch_first_batches(&half_map, a, g, tid, p_begin, n, leader);
+  wait_for_prior_grids();
+  allow_dependent_grids();
 
   // page ids: the leader's table (every member's holds the same ones here)
   for (int i = tid; i < n; i += kTcThreads) {

@@ -1,7 +1,9 @@
 """Inputs rewritten on the stream right before each call.  The attention
-kernels read the plan, lengths and block tables before griddepcontrol.wait
-(only to prefetch pages into L2) and again after it; what they compute must
-come from the values the preceding kernel wrote.
+kernels read the lengths and block tables before griddepcontrol.wait (only
+to prefetch pages into L2) and again after it; what they compute must come
+from the values the preceding kernel wrote.  (A plan's device copy is filled
+by a copy, never by the kernel just before the call, so the kernels use it
+before the wait.)
 
 The pool holds two copies of every sequence's pages with different K/V;
 table variant A points at the first, variant B at the second.  A torch copy

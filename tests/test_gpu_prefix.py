@@ -202,3 +202,36 @@ def test_shared_plan_ragged_groups():
     assert int(err.item()) == 0
     assert_close(got, ref, "ragged shared groups")
     assert np.array_equal(synth.bits(dpool), ref_pool)    # appended slots, nothing else
+
+
+def test_folding_segment_plan_over_several_layers_in_one_call():
+    # the prefix workload with 3 layers under one shared plan of member
+    # segments that fold their shared partials (no merge): every layer's
+    # shared-prefix kernel rewrites the partial slots the previous layer's
+    # segments folded, so the multi-layer call must give the bits of one call
+    # per layer, and the oracle's outputs
+    dev = cuda_or_skip()
+    b = binding()
+    w = synth.make_workload("prefix", 6, layers=3)
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, block_tables=w.block_tables[0])
+    assert plan.num_segs > 0 and plan.num_merges == 0
+    assert (plan.segments()[:, 5] > 0).sum() == w.batch
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    d = synth.device_inputs(w, dev)
+    one = np.stack([synth.bits(b.decode_step_planned(
+        d["q"][layer], d["k_new"][layer], d["v_new"][layer], d["pool"],
+        d["block_tables"][layer], d["seq_lens"], plan, rope_theta=w.rope_theta, scale=w.scale,
+        dev_err=err)) for layer in range(w.layers)])
+    pool_one = synth.bits(d["pool"])
+    del d
+    d = synth.device_inputs(w, dev)
+    many = synth.bits(b.decode_steps_planned(
+        d["q"], d["k_new"], d["v_new"], d["pool"], d["block_tables"], d["seq_lens"], plan,
+        rope_theta=w.rope_theta, scale=w.scale, dev_err=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(many, one)
+    assert np.array_equal(synth.bits(d["pool"]), pool_one)
+    for layer in (1, 2):
+        ref, _ = oracle_step(w, layer)
+        assert_close(one[layer], ref, f"prefix layer {layer} under a folding segment plan")
