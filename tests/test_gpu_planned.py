@@ -287,3 +287,52 @@ def test_one_layer_multi_call_equals_the_single_layer_call():
                                         d["block_tables"][0], d["seq_lens"], plan)
         outs.append((synth.bits(out), synth.bits(d["pool"])))
     assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("shape", ["per_head", "segments"])
+def test_plans_swapped_by_copies_between_calls(shape):
+    # The planned kernels read their plan before the grid dependency wait: a
+    # plan's device copy is filled by a copy, which has finished before the
+    # next kernel on the stream can start.  Two plans for different lengths
+    # take turns in one device buffer, each copied in (with its lengths)
+    # right before its call on the same stream; every call must give the
+    # oracle's outputs for its own lengths.
+    dev = cuda_or_skip()
+    b = binding()
+    rng = np.random.default_rng(21 if shape == "per_head" else 22)
+    if shape == "per_head":
+        lens_a = mixed_lengths(rng, 115, 13)
+    else:
+        lens_a = rng.integers(200, 1400, 320).astype(np.int32)
+    lens_b = np.maximum(1, lens_a - rng.integers(0, 200, len(lens_a))).astype(np.int32)
+    w, pool = case(lens_a, seed=23)
+    plans = [b.Plan(lens, w.max_blocks) for lens in (lens_a, lens_b)]
+    if shape == "per_head":
+        assert all(p.num_segs == 0 and p.num_merges > 0 for p in plans)
+    else:
+        assert all(p.num_segs > 0 for p in plans)
+    refs = [oracle.decode_attention(w.q[0], pool, w.block_tables[0], lens)
+            for lens in (lens_a, lens_b)]
+    staged = [torch.from_numpy(p.host.copy()).pin_memory() for p in plans]
+    lens_pin = [torch.from_numpy(lens.copy()).pin_memory() for lens in (lens_a, lens_b)]
+    dbuf = torch.empty(max(p.bytes_used for p in plans) // 4, dtype=torch.int32, device=dev)
+    lens_dev = torch.empty(len(lens_a), dtype=torch.int32, device=dev)
+    ws = torch.empty(max(16, max(p.workspace_bytes for p in plans)), dtype=torch.uint8,
+                     device=dev)
+    q, pool_dev = dev_bf16(w.q[0], dev), dev_bf16(pool, dev)
+    bt = torch.from_numpy(w.block_tables[0]).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = []
+    for i in range(6):
+        k = i % 2
+        p = plans[k]
+        words = p.bytes_used // 4
+        dbuf[:words].copy_(staged[k], non_blocking=True)
+        lens_dev.copy_(lens_pin[k], non_blocking=True)
+        p.dev = dbuf[:words]
+        outs.append(b.paged_decode_attention_planned(q, pool_dev, bt, lens_dev, p, workspace=ws,
+                                                     dev_err=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for i, out in enumerate(outs):
+        assert_close(synth.bits(out), refs[i % 2], f"{shape} call {i}")
