@@ -135,11 +135,14 @@ def test_shared_plan_full_size_every_output():
     assert np.array_equal(got, want)
 
 
-def test_shared_plan_with_a_diverging_member_table_is_reported():
+@pytest.mark.parametrize("seq,page", [(5, 10), (15, 63), (17, 0), (30, 37)])
+def test_shared_plan_with_a_diverging_member_table_is_reported(seq, page):
     # A shared plan says that every member's table holds the leader's page ids
     # over the shared ranges.  A member whose table says otherwise (a plan
     # built from another layer's tables, or tables changed since) would attend
-    # the leader's pages; the kernel compares the tables and reports it.
+    # the leader's pages; the kernel compares the tables, batch by batch, and
+    # reports it -- for any member and any shared page (the first and last
+    # member of a group, the first and last shared page).
     dev = cuda_or_skip()
     b = binding()
     w = synth.make_workload("prefix", 6, batch=32, num_pages=4096, share_group=16,
@@ -152,7 +155,7 @@ def test_shared_plan_with_a_diverging_member_table_is_reported():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     bt = d["block_tables"][0]
-    bt[5, 10] = bt[20, 100]          # a valid page, but not the leader's shared one
+    bt[seq, page] = bt[20, 100]      # a valid page, but not the leader's shared one
     planned(w, d, plan, dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) & b.DEVERR_PLAN
