@@ -5,7 +5,8 @@ the same physical pages: group sizes 2..16, shared prefixes of 16..100 pages
 (so shared ranges end on any page of a 4-page batch), singletons between the
 groups, private tails of 1..27 pages whose last page is partly filled, and a
 random minimum shared extent.  The decode step runs fused and as append +
-attention under the plan built from the lengths and tables.  Every output is
+attention under the plan built from the lengths and tables, for this device
+and as for 8 SMs (mostly segment plans: folding members and merged ones).  Every output is
 checked against the FP64 oracle, every appended slot bit for bit, and fused
 against unfused bit for bit.
 """
@@ -51,8 +52,12 @@ def draw_case(seed):
     return lens, bt, pool, q, kn, vn, min_shared, expect_shared
 
 
+@pytest.mark.parametrize("sms", [0, 8])
 @pytest.mark.parametrize("seed", range(8))
-def test_random_shared_groups(seed):
+def test_random_shared_groups(seed, sms):
+    # sms 8: the plan made as for 8 SMs is mostly a segment plan, in which
+    # members whose own pages are one segment fold their shared partials and
+    # members cut into several pieces are merged
     dev = cuda_or_skip()
     b = binding()
     lens, bt, pool, q, kn, vn, min_shared, expect_shared = draw_case(seed)
@@ -64,7 +69,8 @@ def test_random_shared_groups(seed):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
             torch.bfloat16)
 
-    plan = b.Plan(lens, MAX_BLOCKS, device=dev, block_tables=bt, min_shared_pages=min_shared)
+    plan = b.Plan(lens, MAX_BLOCKS, device=dev, num_sms=sms, block_tables=bt,
+                  min_shared_pages=min_shared)
     assert (plan.num_shared > 0) == expect_shared
     if expect_shared:
         assert b.attention_kernels(len(lens), MAX_BLOCKS, 0, plan).startswith(
@@ -83,7 +89,7 @@ def test_random_shared_groups(seed):
         got = synth.bits(out)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
-        assert_close(got, ref, f"shared fuzz seed {seed}, fused={fused}")
+        assert_close(got, ref, f"shared fuzz seed {seed}, sms={sms}, fused={fused}")
         outs.append(got)
         pools.append(synth.bits(dpool))
     assert np.array_equal(outs[0], outs[1])
