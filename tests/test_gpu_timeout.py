@@ -183,6 +183,30 @@ def test_shared_prefix_kernel_times_out_then_recovers():
     check_recovered(w, d, step, "shared-prefix kernel")
 
 
+def test_folding_segment_plan_times_out_then_recovers():
+    dev = cuda_or_skip()
+    b = binding()
+    # 64 sequences in groups of 16 sharing 64 pages, 2048 tokens each, planned
+    # as for 8 SMs: the shared-prefix kernel, then segment CTAs that fold each
+    # member's shared partials into its output (no merge) -- both time out
+    w = synth.make_workload("prefix", 7, batch=64, num_pages=8192, share_group=16,
+                            share_blocks=64)
+    d = synth.device_inputs(w, dev)
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, num_sms=8,
+                  block_tables=w.block_tables[0])
+    assert plan.num_shared > 0 and plan.num_segs > 0 and plan.num_merges == 0
+    assert (plan.segments()[:, 5] > 0).all()
+
+    def step(err):
+        return b.decode_step_planned(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"],
+                                     d["block_tables"][0], d["seq_lens"], plan,
+                                     rope_theta=w.rope_theta, scale=w.scale, dev_err=err)
+    bits, out = timed_out(step)
+    assert bits & b.DEVERR_TIMEOUT, f"no wait timed out (bits {bits})"
+    assert torch.isfinite(out.float()).all()
+    check_recovered(w, d, step, "folding segment plan")
+
+
 def test_prefill_write_times_out_then_recovers():
     dev = cuda_or_skip()
     b = binding()
