@@ -35,15 +35,20 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 
 // Stable counting sort of v by key(x) in [0, nkeys), ascending; the keys here
 // are small page counts, so this is a few linear passes (a comparison sort of
-// a 256-sequence batch took most of the plan's host time).
+// a 256-sequence batch took most of the plan's host time).  Its buffers are
+// the calling thread's and keep their capacity from one plan to the next.
 template <typename T, typename Key>
 void counting_sort(std::vector<T>& v, int nkeys, Key key) {
-  std::vector<int> first(static_cast<size_t>(nkeys) + 1, 0);
+  static thread_local std::vector<int> first_buf;
+  static thread_local std::vector<T> out_buf;
+  std::vector<int>& first = first_buf;  // thread-local lookups once, not per element
+  std::vector<T>& out = out_buf;
+  first.assign(static_cast<size_t>(nkeys) + 1, 0);
   for (const T& x : v) ++first[static_cast<size_t>(key(x)) + 1];
   for (int k = 0; k < nkeys; ++k) first[k + 1] += first[k];
-  std::vector<T> out(v.size());
+  out.resize(v.size());
   for (const T& x : v) out[first[key(x)]++] = x;
-  v.swap(out);
+  std::copy(out.begin(), out.end(), v.begin());
 }
 
 }  // namespace
@@ -131,14 +136,17 @@ struct Piece {
 // The pieces for bins of T pages: each sequence's own pages [start, start +
 // own) whole, or cut into ceil(own / T) near-equal chunks when longer than T
 // (an empty sequence is one piece of no pages, which writes its zero rows),
-// largest first (stable).
-std::vector<Piece> make_pieces(const std::vector<int>& own, const std::vector<int>& start,
-                               int T) {
-  std::vector<Piece> pieces;
-  pieces.reserve(own.size() + 16);
+// largest first (stable), into `pieces`.
+void make_pieces(const std::vector<int>& own, const std::vector<int>& start, int T,
+                 std::vector<Piece>& pieces) {
+  pieces.clear();
   for (size_t b = 0; b < own.size(); ++b) {
     const int p = own[b];
-    const int nr = p > T ? (p + T - 1) / T : 1;  // 32-bit divisions: this runs per step
+    if (p <= T) {  // whole: no divisions (this runs several times per plan)
+      pieces.push_back({static_cast<int>(b), start[b], p});
+      continue;
+    }
+    const int nr = (p + T - 1) / T;
     const int base = p / nr, extra = p % nr;
     int begin = start[b];
     for (int r = 0; r < nr; ++r) {
@@ -148,7 +156,6 @@ std::vector<Piece> make_pieces(const std::vector<int>& own, const std::vector<in
     }
   }
   counting_sort(pieces, T + 1, [&](const Piece& x) { return T - x.n; });
-  return pieces;
 }
 
 // Best-fit packing of pieces (largest first) into bins of at most T pages and
@@ -156,13 +163,22 @@ std::vector<Piece> make_pieces(const std::vector<int>& own, const std::vector<in
 // takes it, else to a new bin.  Returns the number of bins; with `bin_of`,
 // also each piece's bin.
 long long pack_bins(const std::vector<Piece>& pieces, int T, std::vector<int>* bin_of) {
-  std::vector<std::vector<int>> by_room(static_cast<size_t>(T) + 1);
-  // bit r set: some open bin has exactly r pages of room
-  std::vector<uint64_t> nonempty((static_cast<size_t>(T) >> 6) + 1, 0);
-  auto mark = [&](int r, bool on) {
-    if (on) nonempty[r >> 6] |= 1ull << (r & 63);
-    else nonempty[r >> 6] &= ~(1ull << (r & 63));
-  };
+  // the open bins with r pages of room, a stack per r: head[r] the last bin
+  // put there, below[bin] the one under it (-1: none); all of it the calling
+  // thread's, reused from one packing to the next (the bin-size search packs
+  // several times per plan)
+  static thread_local std::vector<int> head_buf, below_buf, room_buf, segs_buf;
+  static thread_local std::vector<uint64_t> nonempty_buf;
+  std::vector<int>& head = head_buf;  // thread-local lookups once, not per piece
+  std::vector<int>& below = below_buf;
+  std::vector<int>& room = room_buf;
+  std::vector<int>& segs = segs_buf;
+  std::vector<uint64_t>& nonempty = nonempty_buf;  // bit r: head[r] >= 0
+  head.assign(static_cast<size_t>(T) + 1, -1);
+  nonempty.assign((static_cast<size_t>(T) >> 6) + 1, 0);
+  below.clear();
+  room.clear();
+  segs.clear();
   auto first_room = [&](int n) {  // the least room >= n held by an open bin, or -1
     for (int w = n >> 6; w < static_cast<int>(nonempty.size()); ++w) {
       uint64_t bits = nonempty[w];
@@ -171,56 +187,108 @@ long long pack_bins(const std::vector<Piece>& pieces, int T, std::vector<int>* b
     }
     return -1;
   };
-  std::vector<int> room, segs;
   if (bin_of != nullptr) bin_of->assign(pieces.size(), -1);
   for (size_t i = 0; i < pieces.size(); ++i) {
     const int n = pieces[i].n;
     int pick = -1;
     const int r = first_room(n);
     if (r >= 0 && r <= T) {
-      pick = by_room[r].back();
-      by_room[r].pop_back();
-      if (by_room[r].empty()) mark(r, false);
+      pick = head[r];
+      head[r] = below[pick];
+      if (head[r] < 0) nonempty[r >> 6] &= ~(1ull << (r & 63));
     }
     if (pick < 0) {
       pick = static_cast<int>(room.size());
       room.push_back(T);
       segs.push_back(0);
+      below.push_back(-1);
     }
     room[pick] -= n;
     segs[pick] += 1;
     if (bin_of != nullptr) (*bin_of)[i] = pick;
     if (segs[pick] < kSegMax) {
-      by_room[room[pick]].push_back(pick);
-      mark(room[pick], true);
+      const int rr = room[pick];
+      below[pick] = head[rr];
+      head[rr] = pick;
+      nonempty[rr >> 6] |= 1ull << (rr & 63);
     }
   }
   return static_cast<long long>(room.size());
 }
 
+// A packing of the pieces for bins of T pages (T = -1: none yet).
+struct Packing {
+  int T = -1;
+  long long bins = 0;
+  std::vector<Piece> pieces;
+  std::vector<int> bin_of;
+};
+
 // The bin size of a segment plan: the smallest T from max(kMinSegPages,
 // ceil(P / C)) up (P: the pages to attend, C = kSegCtasPerSm CTAs per SM)
 // whose bins fit in one wave of C CTAs, else the largest (up to kSegMax x the
-// longest sequence, or kSegMaxPages).  A T whose pieces cannot fit -- more than C of
-// them longer than T / 2, or more than C * T pages -- is ruled out without
-// packing.
+// longest sequence, or kSegMaxPages).  A T whose pieces cannot fit is ruled
+// out without packing, by lower bounds on the bins: more than C * T pages;
+// or, for k < kSegMax, more than k * C pieces longer than T / (k + 1) (at
+// most k of them share a bin); or more than kSegMax * C pieces.  One that
+// has at most C pieces fits without packing (best fit opens a bin only for
+// a piece that no open bin takes).
 int segment_bin_size(const std::vector<int>& own, const std::vector<int>& start, int num_sms,
-                     long long total) {
+                     long long total, Packing& best) {
   const long long C = static_cast<long long>(kSegCtasPerSm) * num_sms;
   const int max_own = *std::max_element(own.begin(), own.end());
   const int t0 = static_cast<int>(std::min<long long>(
       kSegMaxPages, std::max<long long>(kMinSegPages, (total + C - 1) / C)));
   // past kSegMax x the longest sequence a bin is bounded by its segment count
   const int t1 = std::max(t0, std::min(kSegMax * std::max(max_own, 1), kSegMaxPages));
+  // from T = max_own up every sequence is one piece, in the same order
+  static thread_local std::vector<Piece> whole_buf;
+  static thread_local Packing probe_buf;
+  std::vector<Piece>& whole_pieces = whole_buf;
+  Packing& probe = probe_buf;
+  bool have_whole = false;
+  best.T = -1;
+  // the sequences by page count: the bounds below take each count once
+  static thread_local std::vector<int> seqs_with_buf, counts_buf;
+  std::vector<int>& seqs_with = seqs_with_buf;
+  std::vector<int>& counts = counts_buf;
+  seqs_with.assign(static_cast<size_t>(max_own) + 1, 0);
+  counts.clear();
+  for (int p : own)
+    if (seqs_with[p]++ == 0) counts.push_back(p);
   auto fits = [&](int T) {
-    long long big = 0;  // pieces longer than T / 2: no two share a bin
-    for (int p : own) {
+    long long cnt[kSegMax + 1] = {};  // k < kSegMax: pieces with (k + 1) n > T; kSegMax: all
+    for (int p : counts) {
+      const long long m = seqs_with[p];
       const int nr = p > T ? (p + T - 1) / T : 1;
-      const int base = p / nr, extra = p % nr;
-      big += 2 * base > T ? nr : (2 * (base + 1) > T ? extra : 0);
+      const int base = nr == 1 ? p : p / nr, extra = nr == 1 ? 0 : p % nr;
+      for (int k = 1; k < kSegMax; ++k)
+        cnt[k] += m * ((k + 1) * base > T ? nr : ((k + 1) * (base + 1) > T ? extra : 0));
+      cnt[kSegMax] += m * nr;
     }
-    if (big > C || (total + T - 1) / T > C) return false;
-    return pack_bins(make_pieces(own, start, T), T, nullptr) <= C;
+    for (int k = 1; k <= kSegMax; ++k)
+      if (cnt[k] > k * C) return false;
+    if ((total + T - 1) / T > C) return false;
+    if (cnt[kSegMax] <= C) {  // a bin per piece fits: no need to pack
+      best.T = -1;            // (the plan packs its own T)
+      return true;
+    }
+    if (T >= max_own) {
+      if (!have_whole) {
+        make_pieces(own, start, T, whole_pieces);
+        have_whole = true;
+      }
+      probe.pieces = whole_pieces;
+    } else {
+      make_pieces(own, start, T, probe.pieces);
+    }
+    probe.T = T;
+    probe.bins = pack_bins(probe.pieces, T, &probe.bin_of);
+    if (probe.bins > C) return false;
+    // the fitting T only decreases as the search goes on: the last one kept
+    // is the answer's, which the plan then reuses
+    std::swap(best, probe);
+    return true;
   };
   // the smallest fitting T, searched first up to the longest sequence (where
   // whole sequences become single pieces), then beyond it
@@ -249,11 +317,16 @@ int segment_bin_size(const std::vector<int>& own, const std::vector<int>& start,
 int build_segments(const int32_t* lens, int batch, int max_blocks, int T,
                    const std::vector<int>& own, const std::vector<int>& start,
                    const std::vector<int>& group_of, const std::vector<SharedGroup>& groups,
-                   const std::vector<int>& shared_ranges, int shared_max, int32_t* out,
-                   size_t out_bytes) {
-  const std::vector<Piece> pieces = make_pieces(own, start, T);
-  std::vector<int> bin_of;
-  const int nbins = static_cast<int>(pack_bins(pieces, T, &bin_of));
+                   const std::vector<int>& shared_ranges, int shared_max, Packing& packing,
+                   int32_t* out, size_t out_bytes) {
+  if (packing.T != T) {  // not the bin-size search's packing
+    make_pieces(own, start, T, packing.pieces);
+    packing.T = T;
+    packing.bins = pack_bins(packing.pieces, T, &packing.bin_of);
+  }
+  const std::vector<Piece>& pieces = packing.pieces;
+  const std::vector<int>& bin_of = packing.bin_of;
+  const int nbins = static_cast<int>(packing.bins);
   // each bin's pieces, in the order they were placed (largest first)
   std::vector<int> by_bin(pieces.size());
   for (size_t i = 0; i < pieces.size(); ++i) by_bin[i] = static_cast<int>(i);
@@ -280,7 +353,7 @@ int build_segments(const int32_t* lens, int batch, int max_blocks, int T,
   }
   // a split sequence's pieces take its slots in the order of their pages
   std::vector<int> piece_slot(pieces.size(), -1);
-  {
+  if (pieces.size() > static_cast<size_t>(batch)) {  // some sequence is split
     std::vector<int> by_page(pieces.size());
     for (size_t i = 0; i < pieces.size(); ++i) by_page[i] = static_cast<int>(i);
     counting_sort(by_page, max_blocks + 1, [&](int i) { return pieces[i].p_begin; });
@@ -414,10 +487,12 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
   // CTAs and deeper per-warp rings, is faster (a ragged 16-layer batch of
   // 2067 pages per layer: 313.7 us with bins of 8 pages against 249.7 us).
   if (total >= static_cast<long long>(kMinSegBinPages) * num_sms) {
-    const int T = segment_bin_size(own, start, num_sms, total);
+    static thread_local Packing packing_buf;
+    Packing& packing = packing_buf;
+    const int T = segment_bin_size(own, start, num_sms, total, packing);
     if (T >= kMinSegBinPages)
       return build_segments(lens, batch, max_blocks, T, own, start, group_of, groups,
-                            shared_ranges, shared_max, out, out_bytes);
+                            shared_ranges, shared_max, packing, out, out_bytes);
   }
 
   auto count = [&](Sizes z) {
@@ -575,15 +650,24 @@ int build_plan_shared(const int32_t* lens, const int32_t* block_tables, int batc
     pages[b] = ceil_div(lens[b], kPageSize);
   }
   auto row = [&](int b) { return block_tables + static_cast<size_t>(b) * max_blocks; };
+  // the length of the common start of two rows, up to c entries (memcmp
+  // compares 16 entries at a time, then the last block is searched)
+  auto common = [](const int32_t* x, const int32_t* y, int c) {
+    constexpr int kBlock = 16;
+    int i = 0;
+    while (i + kBlock <= c && memcmp(x + i, y + i, kBlock * sizeof(int32_t)) == 0) i += kBlock;
+    while (i < c && x[i] == y[i]) ++i;
+    return i;
+  };
   std::vector<SharedGroup> groups;
   int b = 0;
   while (b < batch) {
-    int k = pages[b] - 1;  // the leader's last page stays its own
+    // the leader's last page stays its own, and only its valid ids are shared
+    int k = 0;
+    while (k < pages[b] - 1 && row(b)[k] >= 0) ++k;
     int e = b + 1;
     while (e < batch && e - b < kSharedMembers) {
-      int c = std::min(k, pages[e] - 1);
-      int agree = 0;
-      while (agree < c && row(b)[agree] == row(e)[agree] && row(b)[agree] >= 0) ++agree;
+      const int agree = common(row(b), row(e), std::min(k, pages[e] - 1));
       if (agree < min_shared_pages) break;
       k = agree;
       ++e;

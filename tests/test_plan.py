@@ -578,3 +578,39 @@ def test_damaged_fold_words_are_refused():
     assert _kernels_for(unfolded, batch) is None      # fold slot left without a fold
     unfolded[at + 6] = 0
     assert _kernels_for(unfolded, batch) is not None
+
+
+def test_concurrent_builds_match_sequential_ones():
+    """The planner keeps reusable buffers per calling thread: plans built
+    from many threads at once (ctypes drops the GIL for the call) are the
+    plans built one at a time."""
+    import threading
+    rng = np.random.default_rng(11)
+    cases = [(np.full(256, 2048, np.int32), None),                       # segment plan
+             (rng.integers(1, 2049, 1024).astype(np.int32), None),       # packed bins
+             (np.concatenate([rng.integers(16, 129, 115),
+                              rng.integers(1536, 2049, 13)]).astype(np.int32), None),
+             (np.full(64, 2048, np.int32), None),                        # split sequences
+             shared_case(3, [(16, 96)] * 16, (32, 32)),
+             shared_case(4, [(5, 20), (1, 0), (9, 40), (3, 17)], (1, 80))]
+
+    def plan_bytes(lens, bt):
+        p = B.Plan(lens, 128, num_sms=SMS, block_tables=bt)
+        return p.host.tobytes()
+
+    want = [plan_bytes(lens, bt) for lens, bt in cases]
+    bad = []
+
+    def worker(t):
+        order = np.random.default_rng(t).permutation(len(cases))
+        for _ in range(20):
+            for i in order:
+                if plan_bytes(*cases[i]) != want[i]:
+                    bad.append((t, int(i)))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(8)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not bad
