@@ -662,12 +662,17 @@ int build_plan_shared(const int32_t* lens, const int32_t* block_tables, int batc
   std::vector<SharedGroup> groups;
   int b = 0;
   while (b < batch) {
-    // the leader's last page stays its own, and only its valid ids are shared
-    int k = 0;
-    while (k < pages[b] - 1 && row(b)[k] >= 0) ++k;
+    int k = pages[b] - 1;  // the leader's last page stays its own
+    // only the leader's valid ids are shared: [0, valid) checked so far
+    // (stopped at the first negative id, if any)
+    int valid = 0;
+    auto valid_prefix = [&](int n) {
+      while (valid < n && row(b)[valid] >= 0) ++valid;
+      return std::min(valid, n);
+    };
     int e = b + 1;
     while (e < batch && e - b < kSharedMembers) {
-      const int agree = common(row(b), row(e), std::min(k, pages[e] - 1));
+      const int agree = valid_prefix(common(row(b), row(e), std::min(k, pages[e] - 1)));
       if (agree < min_shared_pages) break;
       k = agree;
       ++e;
