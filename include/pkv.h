@@ -307,7 +307,7 @@ PKV_API int pkv_check_tables(const int32_t* block_table, int max_blocks,
  * pieces is combined by the merge kernel.
  * The plan is plain data: 12 header words
  *   {PKV_PLAN_MAGIC, batch, max_blocks, num_items, num_merges, num_slots,
- *    range_pages, bytes_used, num_shared, shared_pages, num_segs, 0},
+ *    range_pages, bytes_used, num_shared, shared_pages, num_segs, layout},
  * then num_items items of 16 int32 words, all of kinds 0 and 1 or all of
  * kind 2:
  *   kind 0 (range), 1 (packed): {kind, slot (-1: not split), p_begin, n,
@@ -323,8 +323,15 @@ PKV_API int pkv_check_tables(const int32_t* block_table, int max_blocks,
  * writes the output of its sequence's pages [p_begin, p_begin + n) combined
  * with the partials of slots [fold_slot, fold_slot + fold), which the
  * shared-prefix items wrote (a group member whose own pages are one segment
- * needs no merge entry).  range_pages is the longest range or bin.  The results follow the same numerics as the calls above (same
- * tolerance, bit-identical on repeated runs of a plan).
+ * needs no merge entry).  range_pages is the longest range or bin.
+ * layout 0: the shared-prefix CTAs (if any) run first, two per SM, and the
+ * other kernels after them.  layout 1 (a shared-prefix plan of segment CTAs
+ * whose shared-prefix CTAs fit one per SM; pkv_plan_build_shared makes it
+ * whenever they do): the segment CTAs, sized for one per SM, run beside
+ * the shared-prefix CTAs, streaming their own pages from the start, and
+ * wait for the shared-prefix grid only to fold its partials.  Any other
+ * layout value is refused.  The results follow the same numerics as the
+ * calls above (same tolerance, bit-identical on repeated runs of a plan).
  */
 #define PKV_PLAN_MAGIC 0x32564b50 /* "PKV2" */
 

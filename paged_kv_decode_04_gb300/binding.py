@@ -365,7 +365,7 @@ class Plan:
     planned calls take the plan object itself."""
 
     HEADER = ("magic", "batch", "max_blocks", "num_items", "num_merges", "num_slots",
-              "range_pages", "bytes_used", "num_shared", "shared_pages", "num_segs")
+              "range_pages", "bytes_used", "num_shared", "shared_pages", "num_segs", "layout")
 
     def __init__(self, seq_lens_host, max_blocks: int, *, num_sms: int = 0, device=None,
                  out=None, block_tables=None, min_shared_pages: int = 16):

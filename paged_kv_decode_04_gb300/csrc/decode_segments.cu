@@ -49,29 +49,37 @@ namespace {
 constexpr int kSgWarps = kNumKvHeads;  // one warp per kv head
 constexpr int kSgThreads = kSgWarps * 32;
 constexpr int kSgStages = 2;           // page boxes in the ring (2 CTAs per SM)
+constexpr int kSgBesideStages = 4;     // the same beside a shared-prefix CTA (1 CTA per SM)
 constexpr int kSgBoxBytes = kNumKvHeads * kTileBytes;  // 32 KiB: one page
-constexpr int kSgPrefetchPages = 2 * kSgStages;        // into L2 before the grid wait
 constexpr int kQBytes = kNumQHeads * kHeadDim * 2;     // 4 KiB: q of one sequence
 constexpr int kXchFloats = 2 * kGroup + kGroup * kHeadDim;  // a warp's rows: m, l, o
 
-// Shared memory from a 1024-byte aligned base.
-constexpr int kOffRing = 0;
-constexpr int kOffQ = kOffRing + kSgStages * kSgBoxBytes;
-constexpr int kOffArow = kOffQ + kSegMax * kQBytes;
-constexpr int kOffXch = kOffArow + kSegMax * kSgWarps * 32 * 8;
-constexpr int kOffBars = kOffXch + kSgWarps * kXchFloats * 4;
-constexpr int kNumSgBars = kSgStages + 1;  // full[stages], q copies
-constexpr int kOffCounters = kOffBars + 8 * kNumSgBars;  // done[stages], last_issued[stages]
-constexpr int kOffSegs = (kOffCounters + 8 * kSgStages + 15) & ~15;
-constexpr int kOffPages = kOffSegs + kSegMax * kPlanSegWords * 4;
-
-static_assert(kOffBars % 8 == 0 && kOffSegs % 16 == 0, "shared-memory alignment");
-static_assert(2 * (1024 + kOffPages + 4 * 256 + 1024) <= 228 * 1024,
+// Shared memory from a 1024-byte aligned base, for a ring of kStages boxes.
+template <int kStages>
+struct SgLayout {
+  static constexpr int kPrefetchPages = 2 * kStages;  // into L2 before the grid wait
+  static constexpr int kOffRing = 0;
+  static constexpr int kOffQ = kOffRing + kStages * kSgBoxBytes;
+  static constexpr int kOffArow = kOffQ + kSegMax * kQBytes;
+  static constexpr int kOffXch = kOffArow + kSegMax * kSgWarps * 32 * 8;
+  static constexpr int kOffBars = kOffXch + kSgWarps * kXchFloats * 4;
+  static constexpr int kNumBars = kStages + 1;  // full[stages], q copies
+  static constexpr int kOffCounters = kOffBars + 8 * kNumBars;  // done[], last_issued[]
+  static constexpr int kOffSegs = (kOffCounters + 8 * kStages + 15) & ~15;
+  static constexpr int kOffPages = kOffSegs + kSegMax * kPlanSegWords * 4;
+  static_assert(kOffBars % 8 == 0 && kOffSegs % 16 == 0, "shared-memory alignment");
+  static constexpr size_t smem_bytes(int pages) {
+    return 1024 /* alignment slack */ + kOffPages + static_cast<size_t>(pages) * 4;
+  }
+};
+static_assert(2 * (1024 + SgLayout<kSgStages>::kOffPages + 4 * 256 + 1024) <= 228 * 1024,
               "two CTAs per SM for CTAs of up to 256 pages");
-
-__host__ __device__ constexpr size_t sg_smem_bytes(int pages) {
-  return 1024 /* alignment slack */ + kOffPages + static_cast<size_t>(pages) * 4;
-}
+// Beside one shared-prefix CTA, for CTAs of any size up to kSegMaxPages pages.
+static_assert(SgLayout<kSgBesideStages>::smem_bytes(kSegMaxPages) + 1024 + kSharedBesideSmemMax <=
+                  228 * 1024,
+              "a beside CTA fits next to a shared-prefix CTA");
+static_assert(2 * (SgLayout<kSgBesideStages>::smem_bytes(0) + 1024) > 228 * 1024,
+              "beside CTAs run one per SM");
 
 // 4-D tiled copy of one whole page (coordinates {0, 0, 0, page}).
 __device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -91,8 +99,8 @@ __device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* m
 // index range-checked, nothing recorded); the kernel reads them again after
 // the wait.
 __device__ __forceinline__ void prefetch_first_pages(const CUtensorMap* map, const AttnArgs& a,
-                                                     int tid, int4 seg) {
-  if (tid >= kSgPrefetchPages) return;
+                                                     int tid, int4 seg, int pages) {
+  if (tid >= pages) return;
   const int b = seg.x, p = seg.z + tid;
   if (tid < seg.w && b >= 0 && b < a.batch && p >= 0 && p < a.max_blocks) {
     const int pid = ld_cg(a.block_table + static_cast<int64_t>(b) * a.max_blocks + p);
@@ -100,22 +108,23 @@ __device__ __forceinline__ void prefetch_first_pages(const CUtensorMap* map, con
   }
 }
 
-template <bool kAppend>
+template <bool kAppend, int kStages, bool kBeside>
 __global__ void __launch_bounds__(kSgThreads, 2)
     paged_decode_segments_kernel(const __grid_constant__ CUtensorMap page_map, const AttnArgs a,
                                  const AppendArgs ap) {
+  using Ly = SgLayout<kStages>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_addr(smem);
-  const uint32_t ring0 = sb + kOffRing;
-  const uint32_t full0 = sb + kOffBars;                      // full[stage]
-  const uint32_t qbar = sb + kOffBars + 8 * kSgStages;       // the q copies
-  int32_t* done = reinterpret_cast<int32_t*>(smem + kOffCounters);  // warps done per stage
-  int32_t* last_issued = done + kSgStages;  // the last page each stage was given (-1: none)
-  int4* s_segs = reinterpret_cast<int4*>(smem + kOffSegs);
-  int32_t* s_pages = reinterpret_cast<int32_t*>(smem + kOffPages);
-  AppendRow* s_arow = reinterpret_cast<AppendRow*>(smem + kOffArow);  // [seg][warp][lane]
+  const uint32_t ring0 = sb + Ly::kOffRing;
+  const uint32_t full0 = sb + Ly::kOffBars;                      // full[stage]
+  const uint32_t qbar = sb + Ly::kOffBars + 8 * kStages;       // the q copies
+  int32_t* done = reinterpret_cast<int32_t*>(smem + Ly::kOffCounters);  // warps done per stage
+  int32_t* last_issued = done + kStages;  // the last page each stage was given (-1: none)
+  int4* s_segs = reinterpret_cast<int4*>(smem + Ly::kOffSegs);
+  int32_t* s_pages = reinterpret_cast<int32_t*>(smem + Ly::kOffPages);
+  AppendRow* s_arow = reinterpret_cast<AppendRow*>(smem + Ly::kOffArow);  // [seg][warp][lane]
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -130,7 +139,7 @@ __global__ void __launch_bounds__(kSgThreads, 2)
   if (tid < 2 * nseg)
     s_segs[tid] = a.plan_segs[static_cast<int64_t>(first) * (kPlanSegWords / 4) + tid];
   if (tid == 0) {
-    for (int s = 0; s < kSgStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       done[s] = 0;
       last_issued[s] = -1;
@@ -139,8 +148,19 @@ __global__ void __launch_bounds__(kSgThreads, 2)
     fence_barrier_init();
   }
   __syncthreads();
-  prefetch_first_pages(&page_map, a, tid, s_segs[0]);
-  wait_for_prior_grids();
+  prefetch_first_pages(&page_map, a, tid, s_segs[0], Ly::kPrefetchPages);
+  if constexpr (!kBeside) {
+    wait_for_prior_grids();
+  } else {
+    // Beside the shared-prefix grid launched just before: everything that
+    // grid waited for has completed (its CTAs let this grid launch only after
+    // their own wait), so the inputs read below -- q, k_new, v_new, the
+    // tables, the lengths and the members' own pages -- are final.  That grid
+    // writes only its partial slots and reads only shared pages, which are
+    // never a member's last page; so this CTA streams its pages, appends its
+    // token and writes outputs and its own partials without waiting, and
+    // waits for it only before folding its partials.
+  }
   allow_dependent_grids();
   const int Lmax = a.max_blocks * kPageSize;
   auto seg_b = [&](int s) { return s_segs[2 * s].x; };
@@ -169,7 +189,7 @@ __global__ void __launch_bounds__(kSgThreads, 2)
 
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int k) {  // one thread
-    const int st = k % kSgStages;
+    const int st = k % kStages;
     const int pid = s_pages[k];
     const uint32_t bar = full0 + 8 * st;
     last_issued[st] = k;
@@ -183,9 +203,9 @@ __global__ void __launch_bounds__(kSgThreads, 2)
   if (tid == 0) {
     mbar_arrive_expect_tx(qbar, nseg * kQBytes);
     for (int s = 0; s < nseg; ++s)
-      bulk_load(sb + kOffQ + s * kQBytes, a.q + static_cast<int64_t>(seg_b(s)) * (kQBytes / 2),
+      bulk_load(sb + Ly::kOffQ + s * kQBytes, a.q + static_cast<int64_t>(seg_b(s)) * (kQBytes / 2),
                 kQBytes, qbar, policy);
-    for (int k = 0; k < kSgStages && k < total; ++k) issue(k);
+    for (int k = 0; k < kStages && k < total; ++k) issue(k);
   }
 
   // ---- fused append: every warp computes its head's row of each segment
@@ -209,7 +229,7 @@ __global__ void __launch_bounds__(kSgThreads, 2)
 
   const LaneGeom G(lane);
   const float c = a.scale_log2;
-  float* xch = reinterpret_cast<float*>(smem + kOffXch) + g * kXchFloats;
+  float* xch = reinterpret_cast<float*>(smem + Ly::kOffXch) + g * kXchFloats;
   bool ok = __all_sync(kFullMask, mbar_wait_bounded(qbar, 0, a.wait_ns));
   if (!ok && lane == 0) record_error(a.dev_err, kErrTimeout);
 
@@ -221,11 +241,11 @@ __global__ void __launch_bounds__(kSgThreads, 2)
     S.reset();
     if (ok) {
       uint32_t qb[4][2];
-      load_q_frags(reinterpret_cast<const uint16_t*>(smem + kOffQ + s * kQBytes) +
+      load_q_frags(reinterpret_cast<const uint16_t*>(smem + Ly::kOffQ + s * kQBytes) +
                        g * kGroup * kHeadDim, G, qb);
       for (int i = 0; i < n; ++i, ++k) {
-        const int st = k % kSgStages;
-        const bool ready = mbar_wait_bounded(full0 + 8 * st, (k / kSgStages) & 1, a.wait_ns);
+        const int st = k % kStages;
+        const bool ready = mbar_wait_bounded(full0 + 8 * st, (k / kStages) & 1, a.wait_ns);
         if (!__all_sync(kFullMask, ready)) {
           // stop; this warp never releases stage st again, so the other
           // warps time out on it in turn, and the copies still in flight are
@@ -249,9 +269,9 @@ __global__ void __launch_bounds__(kSgThreads, 2)
           if (atomicAdd(done + st, 1) == kSgWarps - 1) {
             done[st] = 0;
             __threadfence_block();
-            if (k + kSgStages < total) {
+            if (k + kStages < total) {
               fence_proxy_async_smem();
-              issue(k + kSgStages);
+              issue(k + kStages);
             }
           }
         }
@@ -296,6 +316,7 @@ __global__ void __launch_bounds__(kSgThreads, 2)
       // this grid's wait returned), in slot order, then this segment's own
       // rows, by an online combine; two slots' loads for all 4 rows are in
       // flight at once
+      if constexpr (kBeside) wait_for_prior_grids();
       float Mx[kGroup], Lf[kGroup];
       float2 Of[kGroup];
 #pragma unroll
@@ -368,46 +389,70 @@ __global__ void __launch_bounds__(kSgThreads, 2)
   // likewise
   __syncthreads();
   if (tid == 0) {
-    for (int s = 0; s < kSgStages; ++s)
-      if (last_issued[s] >= 0) mbar_wait_bounded(full0 + 8 * s, (last_issued[s] / kSgStages) & 1);
+    for (int s = 0; s < kStages; ++s)
+      if (last_issued[s] >= 0) mbar_wait_bounded(full0 + 8 * s, (last_issued[s] / kStages) & 1);
     mbar_wait_bounded(qbar, 0);
   }
+  // Beside: no CTA ends before the shared-prefix grid has, even one that
+  // folds nothing, so that this grid's completion -- what the next launch
+  // (the merge, or the next layer) waits for -- covers that grid's partials
+  // and its use of the workspace too.
+  if constexpr (kBeside) wait_for_prior_grids();
 }
 
-template <bool kAppend>
+template <bool kAppend, int kStages, bool kBeside>
 cudaError_t configure_sg_once(int device) {
   static std::atomic<unsigned long long> configured{0};
   const unsigned long long bit = 1ull << (device & 63);
   if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  const cudaError_t err = cudaFuncSetAttribute(paged_decode_segments_kernel<kAppend>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(sg_smem_bytes(kSegMaxPages)));
-  if (err == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
-  return err;
+  cudaError_t err = cudaFuncSetAttribute(
+      paged_decode_segments_kernel<kAppend, kStages, kBeside>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(SgLayout<kStages>::smem_bytes(kSegMaxPages)));
+  if (err != cudaSuccess) return err;
+  if (kBeside) {
+    // one L1 / shared-memory split for both kernels of the beside layout
+    // (CTAs of two kernels share an SM only under the same split)
+    err = cudaFuncSetAttribute(paged_decode_segments_kernel<kAppend, kStages, kBeside>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+  }
+  configured.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
 }
 
-template <bool kAppend>
+template <bool kAppend, int kStages, bool kBeside>
 cudaError_t launch_sg(const CUtensorMap& page_map, const AttnArgs& args, const AppendArgs& ap,
                       int num_items, int max_pages, cudaStream_t stream) {
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
-  err = configure_sg_once<kAppend>(device);
+  err = configure_sg_once<kAppend, kStages, kBeside>(device);
   if (err != cudaSuccess) return err;
-  return launch_pdl(paged_decode_segments_kernel<kAppend>, dim3(num_items), dim3(kSgThreads),
-                    sg_smem_bytes(max_pages), stream, page_map, args, ap);
+  return launch_pdl(paged_decode_segments_kernel<kAppend, kStages, kBeside>, dim3(num_items),
+                    dim3(kSgThreads), SgLayout<kStages>::smem_bytes(max_pages), stream,
+                    page_map, args, ap);
 }
 
 }  // namespace
 
 cudaError_t launch_segments_attention(const CUtensorMap& page_map, const AttnArgs& args,
                                       int num_items, int max_pages, cudaStream_t stream,
-                                      const AppendArgs* append) {
+                                      const AppendArgs* append, bool beside) {
   if (num_items < 1 || max_pages < 1 || max_pages > kSegMaxPages) return cudaErrorInvalidValue;
   const AppendArgs none{};
+  if (beside)
+    return append != nullptr
+               ? launch_sg<true, kSgBesideStages, true>(page_map, args, *append, num_items,
+                                                        max_pages, stream)
+               : launch_sg<false, kSgBesideStages, true>(page_map, args, none, num_items,
+                                                         max_pages, stream);
   return append != nullptr
-             ? launch_sg<true>(page_map, args, *append, num_items, max_pages, stream)
-             : launch_sg<false>(page_map, args, none, num_items, max_pages, stream);
+             ? launch_sg<true, kSgStages, false>(page_map, args, *append, num_items, max_pages,
+                                                 stream)
+             : launch_sg<false, kSgStages, false>(page_map, args, none, num_items, max_pages,
+                                                  stream);
 }
 
 }  // namespace pkv

@@ -37,8 +37,8 @@
 // Roles (8 warps; one thread of each of warps 4..7 works):
 //   warp 6: K producer.  Per batch, head g's K rows of its 4 pages into one
 //     8 KiB region (64 rows: the N = 64 K-major B operand of S), in a ring of
-//     6 regions freed as soon as the batch's S has been computed.
-//   warp 7: V producer.  The V rows likewise into a ring of 6 regions (four
+//     5 regions freed as soon as the batch's S has been computed.
+//   warp 7: V producer.  The V rows likewise into a ring of 5 regions (four
 //     MN-major B operands of PV), freed once the batch's PV is done.  Both
 //     128B-swizzled by TMA, which is the operand layout the MMA reads.
 //   warp 5: issues S_b = Q K_b^T into X(b mod 2) once K_b has landed and
@@ -80,8 +80,8 @@ constexpr int kTcM = 2 * kTcRows;                 // MMA rows: two copies
 constexpr int kTcBatch = 4;                       // pages per S / P batch
 constexpr int kTcCols = kTcBatch * kPageSize;     // 64 score columns per S
 constexpr int kTcHalfCols = kTcCols / 2;          // a row's share of them
-constexpr int kKSlots = 6;                        // K regions in flight
-constexpr int kVSlots = 6;                        // V regions in flight
+constexpr int kSlotsSequential = 5;  // K (and V) regions in flight, two CTAs per SM
+constexpr int kSlotsBeside = 3;      // the same beside a segment CTA (one per SM)
 constexpr int kTcSoftmaxWarps = 4;
 constexpr int kPvWarp = 4;
 constexpr int kSWarp = 5;
@@ -98,35 +98,46 @@ constexpr int kMaxPagesPerItem = 1024;
 // Shared memory, from a 1024-byte aligned base.
 constexpr int kHalfTileBytes = kPageSize * kRowBytes;    // 2 KiB: one head's K (or V) rows
 constexpr int kRegionBytes = kTcBatch * kHalfTileBytes;  // 8 KiB: a batch's K (or V) rows
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kKSlots * kRegionBytes;
-constexpr int kOffBars = kOffV + kVSlots * kRegionBytes;
-// k_full[6], k_empty[6], v_full[6], v_empty[6], s_ready[2], x_free[2],
-// p_ready[2], pv_done, s_fin, pv_fin, q_ready
-constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 10;
 constexpr int kPrefetchBatches = 4;  // pulled into L2 before the grid dependency wait
-constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
-constexpr int kOffPages = kOffTmemSlot + 16;
+constexpr int kXchStride = kHeadDim + 4;  // floats per exchanged row: acc, then (m, l), 16-B aligned
+
+// Shared memory, from a 1024-byte aligned base, for rings of kSlots K and
+// kSlots V regions.
+template <int kSlots>
+struct ShLayout {
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kSlots * kRegionBytes;
+  static constexpr int kOffBars = kOffV + kSlots * kRegionBytes;
+  // k_full[kSlots], k_empty[kSlots], v_full[kSlots], v_empty[kSlots],
+  // s_ready[2], x_free[2], p_ready[2], pv_done, s_fin, pv_fin, q_ready
+  static constexpr int kNumBars = 4 * kSlots + 10;
+  static constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
+  static constexpr int kOffPages = kOffTmemSlot + 16;
+  static_assert(kTcRows * kXchStride * 4 <= kSlots * kRegionBytes, "end-of-CTA exchange fits");
+  static constexpr size_t smem_bytes(int pages) {
+    return 1024 /* alignment slack */ + kOffPages + static_cast<size_t>(pages) * 4;
+  }
+};
 
 static_assert(kTcM == 128 && 32 * kTcSoftmaxWarps == kTcM, "one softmax thread per TMEM lane");
 static_assert(kTmemQ + kHeadDim / 2 <= kTmemCols, "X0, X1, O and Q fit the allocation");
-constexpr int kXchStride = kHeadDim + 4;  // floats per exchanged row: acc, then (m, l), 16-B aligned
-static_assert(kTcRows * kXchStride * 4 <= kKSlots * kRegionBytes, "end-of-CTA exchange fits");
-// Shared memory alone keeps more than kTcCtasPerSm CTAs of this kernel off
-// one SM (228 KiB per SM, 1 KiB reserved per CTA), so their TMEM
-// allocations always fit the 512 columns and tcgen05.alloc never waits.
-static_assert((kTcCtasPerSm + 1) * (kOffPages + 1024 + 1024) > 228 * 1024,
+// In the sequential layout shared memory alone keeps more than
+// kTcCtasPerSm CTAs of this kernel off one SM (228 KiB per SM, 1 KiB
+// reserved per CTA), so their TMEM allocations always fit the 512 columns
+// and tcgen05.alloc never waits.  Beside a segment CTA the smaller rings
+// leave that to registers, which the launch checks (sh_occupancy_ok).
+static_assert((kTcCtasPerSm + 1) * (ShLayout<kSlotsSequential>::kOffPages + 1024 + 1024) >
+                  228 * 1024,
               "at most kTcCtasPerSm CTAs per SM");
 static_assert(kTcCtasPerSm * kTmemCols <= 512, "TMEM columns of the resident CTAs");
-static_assert(kTcCtasPerSm * (kOffPages + 1024 + 1024 + 4 * 64) <= 228 * 1024,
+static_assert(kTcCtasPerSm * (ShLayout<kSlotsSequential>::kOffPages + 1024 + 1024 + 4 * 64) <=
+                  228 * 1024,
               "kTcCtasPerSm CTAs per SM fit for ranges of up to 64 pages");
+static_assert(ShLayout<kSlotsBeside>::smem_bytes(kMaxPagesPerItem) + 1024 <= kSharedBesideSmemMax,
+              "a beside segment CTA fits next to any beside shared-prefix CTA");
 
 constexpr uint32_t kIdescS = tc_idesc_bf16(kTcM, kTcCols, false);   // K: K-major
 constexpr uint32_t kIdescPV = tc_idesc_bf16(kTcM, kHeadDim, true);  // V: MN-major
-
-__host__ __device__ constexpr size_t sh_smem_bytes(int pages) {
-  return 1024 /* alignment slack */ + kOffPages + static_cast<size_t>(pages) * 4;
-}
 
 // Before the grid dependency wait: pull the first kPrefetchBatches batches'
 // K and V rows of pages [p_begin, p_begin + n) of the leader's table into
@@ -153,8 +164,14 @@ __device__ __forceinline__ void softmax_warps_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kTcSoftmaxWarps) : "memory");
 }
 
+template <int kSlots>
 __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     paged_decode_shared_kernel(const __grid_constant__ CUtensorMap half_map, const AttnArgs a) {
+  using Ly = ShLayout<kSlots>;
+  constexpr int kKSlots = kSlots, kVSlots = kSlots;
+  constexpr int kOffK = Ly::kOffK, kOffV = Ly::kOffV, kOffBars = Ly::kOffBars;
+  constexpr int kNumBars = Ly::kNumBars, kOffTmemSlot = Ly::kOffTmemSlot;
+  constexpr int kOffPages = Ly::kOffPages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -194,6 +211,22 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   const int leader = it[4];
   const int nb = (n + kTcBatch - 1) / kTcBatch;
   prefetch_first_batches(&half_map, a, g, tid, p_begin, n, leader);
+  // The barriers and the TMEM allocation before the grid wait, so this CTA
+  // holds its columns before it lets a dependent grid launch: a dependent
+  // grid's CTAs on this SM (the next layer's, beside a segment grid that
+  // waits for this one) can then never take columns this CTA still needs.
+  if (tid == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      const uint32_t bar = bars + 8u * i;  // the softmax rows arrive on two
+      mbar_init(bar, (bar == p_ready(0) || bar == p_ready(1) || bar == q_ready) ? kTcM : 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kPvWarp) {
+    __syncwarp();
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
   wait_for_prior_grids();
   allow_dependent_grids();
 
@@ -225,18 +258,6 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       qw[c >> 2][4 * (c & 3) + 2] = v.z;
       qw[c >> 2][4 * (c & 3) + 3] = v.w;
     }
-  }
-  if (tid == 0) {
-    for (int i = 0; i < kNumBars; ++i) {
-      const uint32_t bar = bars + 8u * i;  // the softmax rows arrive on two
-      mbar_init(bar, (bar == p_ready(0) || bar == p_ready(1) || bar == q_ready) ? kTcM : 1);
-    }
-    fence_barrier_init();
-  }
-  if (warp == kPvWarp) {
-    __syncwarp();
-    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-    tmem_relinquish_alloc_permit();
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -568,30 +589,61 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   }
 }
 
+// Sets the kernel's shared-memory limit and checks that no more CTAs of it
+// fit on one SM than TMEM holds allocations for (kTcCtasPerSm x 256 of 512
+// columns), whatever else shares the SM: with that, tcgen05.alloc never
+// waits.  The sequential layout's rings guarantee it by shared memory; the
+// beside layout's smaller rings leave it to the registers (about 100 per
+// thread: two CTAs of 256 threads per SM).
+template <int kSlots>
 cudaError_t configure_sh_once(int device) {
   static std::atomic<unsigned long long> configured{0};
   const unsigned long long bit = 1ull << (device & 63);
   if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  const cudaError_t err =
-      cudaFuncSetAttribute(paged_decode_shared_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sh_smem_bytes(kMaxPagesPerItem)));
-  if (err == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
-  return err;
+  cudaError_t err = cudaFuncSetAttribute(
+      paged_decode_shared_kernel<kSlots>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(ShLayout<kSlots>::smem_bytes(kMaxPagesPerItem)));
+  if (err != cudaSuccess) return err;
+  if (kSlots == kSlotsBeside) {
+    // CTAs of two kernels share an SM only under one L1 / shared-memory
+    // split: ask for the largest shared part, which the segment CTAs that
+    // run beside these need (they ask for the same)
+    err = cudaFuncSetAttribute(paged_decode_shared_kernel<kSlots>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+  }
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, paged_decode_shared_kernel<kSlots>, kTcThreads, ShLayout<kSlots>::smem_bytes(1));
+  if (err != cudaSuccess) return err;
+  if (per_sm > static_cast<int>(512 / kTmemCols)) return cudaErrorInvalidConfiguration;
+  configured.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
+template <int kSlots>
+cudaError_t launch_sh(const CUtensorMap& pool_map, const AttnArgs& args, int num_shared,
+                      int range_pages, cudaStream_t stream) {
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
+  if (err != cudaSuccess) return err;
+  err = configure_sh_once<kSlots>(device);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(paged_decode_shared_kernel<kSlots>, dim3(kNumKvHeads, num_shared),
+                    dim3(kTcThreads), ShLayout<kSlots>::smem_bytes(range_pages), stream, pool_map,
+                    args);
 }
 
 }  // namespace
 
 cudaError_t launch_shared_prefix_attention(const CUtensorMap& pool_map, const AttnArgs& args,
-                                           int num_shared, int range_pages, cudaStream_t stream) {
+                                           int num_shared, int range_pages, cudaStream_t stream,
+                                           bool beside) {
   if (num_shared < 1 || range_pages < 1 || range_pages > kMaxPagesPerItem)
     return cudaErrorInvalidValue;
-  int device = 0;
-  cudaError_t err = cudaGetDevice(&device);
-  if (err != cudaSuccess) return err;
-  err = configure_sh_once(device);
-  if (err != cudaSuccess) return err;
-  return launch_pdl(paged_decode_shared_kernel, dim3(kNumKvHeads, num_shared), dim3(kTcThreads),
-                    sh_smem_bytes(range_pages), stream, pool_map, args);
+  return beside ? launch_sh<kSlotsBeside>(pool_map, args, num_shared, range_pages, stream)
+                : launch_sh<kSlotsSequential>(pool_map, args, num_shared, range_pages, stream);
 }
 
 }  // namespace pkv

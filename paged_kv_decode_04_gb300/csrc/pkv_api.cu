@@ -482,7 +482,7 @@ namespace {
 
 struct PlanHeader {
   int32_t magic, batch, max_blocks, num_items, num_merges, num_slots, range_pages, bytes_used;
-  int32_t num_shared, shared_pages, num_segs, reserved1;
+  int32_t num_shared, shared_pages, num_segs, layout;
 };
 static_assert(sizeof(PlanHeader) == 4 * pkv::kPlanHeaderWords, "plan header layout");
 
@@ -567,6 +567,10 @@ const PlanHeader* plan_header(const void* plan, int batch, int max_blocks) {
       h->num_shared > 65535 || h->num_segs < 0 ||
       (h->num_shared > 0 && (h->shared_pages < 1 || h->shared_pages > 1024)))
     return nullptr;
+  // the beside layout is for shared-prefix plans of segment CTAs only
+  if (h->layout != pkv::kPlanLayoutSequential &&
+      (h->layout != pkv::kPlanLayoutBeside || h->num_shared < 1 || h->num_segs < 1))
+    return nullptr;
   // bytes_used is exactly the header and the three sections the counts imply
   const int64_t words = pkv::kPlanHeaderWords +
                         static_cast<int64_t>(h->num_items) * pkv::kPlanItemWords +
@@ -630,13 +634,15 @@ cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pa
     // the merge that follows the attention kernel
     if (!pool_tensor_map(pool, num_pages, &map, kPageSize)) return cudaErrorInvalidValue;
     const cudaError_t err =
-        pkv::launch_shared_prefix_attention(map, args, h.num_shared, h.shared_pages, stream);
+        pkv::launch_shared_prefix_attention(map, args, h.num_shared, h.shared_pages, stream,
+                                            h.layout == pkv::kPlanLayoutBeside);
     if (err != cudaSuccess) return err;
   }
   if (h.num_segs > 0) {
     if (!pool_page_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
-    const cudaError_t err = pkv::launch_segments_attention(map, args, h.num_items,
-                                                           h.range_pages, stream, append);
+    const cudaError_t err =
+        pkv::launch_segments_attention(map, args, h.num_items, h.range_pages, stream, append,
+                                       h.layout == pkv::kPlanLayoutBeside);
     if (err != cudaSuccess) return err;
     return pkv::launch_split_merge(args, h.num_merges, stream);
   }

@@ -59,6 +59,18 @@ constexpr int kPlanSegWords = 8;
 constexpr int kSegMax = 4;
 constexpr int kSegCtasPerSm = 2;
 constexpr int kSegMaxPages = 1024;  // pages of one segment CTA (its page list)
+// Header word 11, the plan's layout.  kPlanLayoutBeside (a shared-prefix
+// plan with segment items only): the shared-prefix CTAs fit one per SM, and
+// the segment CTAs, one per SM too (deeper rings), run beside them: each
+// streams its own pages as soon as it starts and waits for the shared-prefix
+// grid only before it folds that grid's partials.
+constexpr int kPlanLayoutSequential = 0;
+constexpr int kPlanLayoutBeside = 1;
+constexpr int kSegBesideCtasPerSm = 1;
+constexpr int kSharedBesideCtasPerSm = 1;
+// Shared memory of one beside shared-prefix CTA with the SM's 1 KiB reserve
+// per CTA, at most (any page list): what a beside segment CTA leaves free.
+constexpr int kSharedBesideSmemMax = 55 * 1024;
 
 // Host side of the work plans (planner.cpp): an upper bound on a plan's
 // bytes, and the plan itself from host lengths (PKV_* status).
@@ -212,19 +224,23 @@ int pagebox_max_range_pages();
 
 // A segment plan's CTAs (decode_segments.cu): grid (num_items), each CTA
 // streaming its segments' pages (at most max_pages) through whole-page boxes
-// of page_map.  The caller launches the merge.
+// of page_map.  beside: the plan's layout is kPlanLayoutBeside (launched
+// right after the shared-prefix grid, whose CTAs it runs beside).  The
+// caller launches the merge.
 cudaError_t launch_segments_attention(const CUtensorMap& page_map, const AttnArgs& args,
                                       int num_items, int max_pages, cudaStream_t stream,
-                                      const AppendArgs* append = nullptr);
+                                      const AppendArgs* append = nullptr, bool beside = false);
 
 // Launch the split merge of a plan (fixed: merge_splits_kernel when S > 1;
 // work plan: merge_plan_kernel over num_merges sequences).
 cudaError_t launch_split_merge(const AttnArgs& args, int num_merges, cudaStream_t stream);
 
 // Shared-prefix items of a work plan: grid (Hkv, num_shared), each CTA
-// writing its members' partials (decode_shared.cu).
+// writing its members' partials (decode_shared.cu).  beside: the plan's
+// layout is kPlanLayoutBeside (smaller rings, to leave room for a segment CTA).
 cudaError_t launch_shared_prefix_attention(const CUtensorMap& pool_map, const AttnArgs& args,
-                                           int num_shared, int range_pages, cudaStream_t stream);
+                                           int num_shared, int range_pages, cudaStream_t stream,
+                                           bool beside = false);
 
 // Largest logical page range one attention CTA handles.
 int max_pages_per_split();

@@ -225,7 +225,7 @@ struct Packing {
 };
 
 // The bin size of a segment plan: the smallest T from max(kMinSegPages,
-// ceil(P / C)) up (P: the pages to attend, C = kSegCtasPerSm CTAs per SM)
+// ceil(P / C)) up (P: the pages to attend, C = ctas_per_sm CTAs per SM)
 // whose bins fit in one wave of C CTAs, else the largest (up to kSegMax x the
 // longest sequence, or kSegMaxPages).  A T whose pieces cannot fit is ruled
 // out without packing, by lower bounds on the bins: more than C * T pages;
@@ -234,8 +234,8 @@ struct Packing {
 // has at most C pieces fits without packing (best fit opens a bin only for
 // a piece that no open bin takes).
 int segment_bin_size(const std::vector<int>& own, const std::vector<int>& start, int num_sms,
-                     long long total, Packing& best) {
-  const long long C = static_cast<long long>(kSegCtasPerSm) * num_sms;
+                     int ctas_per_sm, long long total, Packing& best) {
+  const long long C = static_cast<long long>(ctas_per_sm) * num_sms;
   const int max_own = *std::max_element(own.begin(), own.end());
   const int t0 = static_cast<int>(std::min<long long>(
       kSegMaxPages, std::max<long long>(kMinSegPages, (total + C - 1) / C)));
@@ -317,8 +317,8 @@ int segment_bin_size(const std::vector<int>& own, const std::vector<int>& start,
 int build_segments(const int32_t* lens, int batch, int max_blocks, int T,
                    const std::vector<int>& own, const std::vector<int>& start,
                    const std::vector<int>& group_of, const std::vector<SharedGroup>& groups,
-                   const std::vector<int>& shared_ranges, int shared_max, Packing& packing,
-                   int32_t* out, size_t out_bytes) {
+                   const std::vector<int>& shared_ranges, int shared_max, int layout,
+                   Packing& packing, int32_t* out, size_t out_bytes) {
   if (packing.T != T) {  // not the bin-size search's packing
     make_pieces(own, start, T, packing.pieces);
     packing.T = T;
@@ -394,6 +394,7 @@ int build_segments(const int32_t* lens, int batch, int max_blocks, int T,
   out[8] = static_cast<int32_t>(num_shared);
   out[9] = shared_max;
   out[10] = static_cast<int32_t>(pieces.size());
+  out[11] = layout;
   int32_t* item = out + kPlanHeaderWords;
   int32_t* seg = out + kPlanHeaderWords + num_items * kPlanItemWords + merges.size() +
                  num_shared * kPlanSharedWords;
@@ -464,36 +465,57 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
     if (group_of[b] < 0) solo.push_back(own[b]);
   }
   // shared ranges per group: as many as keep the shared-prefix CTAs within
-  // one wave of kSharedCtasPerSm per SM, ranges of at least kMinRangePages pages
-  int ns_target = 1;
-  if (!groups.empty()) {
-    const long long per = static_cast<long long>(groups.size()) * kNumKvHeads;
-    ns_target = static_cast<int>(
-        std::max<long long>(1, (static_cast<long long>(kSharedCtasPerSm) * num_sms) / per));
-  }
+  // one wave of ctas_per_sm per SM, ranges of at least kMinRangePages pages
   std::vector<int> shared_ranges(groups.size());
   int shared_max = 0;  // pages of the longest shared range
-  for (size_t gi = 0; gi < groups.size(); ++gi) {
-    const int k = groups[gi].k;
-    int ns = std::max(1, std::min(ns_target, ceil_div(k, kMinRangePages)));
-    ns = std::max(ns, ceil_div(k, kMaxRangePages));  // the kernel's page list
-    shared_ranges[gi] = ns;
-    shared_max = std::max(shared_max, ceil_div(k, ns));
-  }
+  auto plan_shared_ranges = [&](int ctas_per_sm) {
+    int ns_target = 1;
+    if (!groups.empty()) {
+      const long long per = static_cast<long long>(groups.size()) * kNumKvHeads;
+      ns_target = static_cast<int>(
+          std::max<long long>(1, (static_cast<long long>(ctas_per_sm) * num_sms) / per));
+    }
+    shared_max = 0;
+    for (size_t gi = 0; gi < groups.size(); ++gi) {
+      const int k = groups[gi].k;
+      int ns = std::max(1, std::min(ns_target, ceil_div(k, kMinRangePages)));
+      ns = std::max(ns, ceil_div(k, kMaxRangePages));  // the kernel's page list
+      shared_ranges[gi] = ns;
+      shared_max = std::max(shared_max, ceil_div(k, ns));
+    }
+  };
   // A layer whose segment plan has bins of at least kMinSegBinPages pages
   // runs on the segment kernel (one wave of CTAs of near-equal pages); with
   // smaller bins a segment CTA's life is mostly its prologue and the latency
   // of its first pages, and the per-(item, kv head) kernel below, with more
   // CTAs and deeper per-warp rings, is faster (a ragged 16-layer batch of
   // 2067 pages per layer: 313.7 us with bins of 8 pages against 249.7 us).
+  // With shared groups whose shared-prefix CTAs fit one per SM, the segment
+  // CTAs are sized to run beside them, one per SM (kPlanLayoutBeside).
   if (total >= static_cast<long long>(kMinSegBinPages) * num_sms) {
     static thread_local Packing packing_buf;
     Packing& packing = packing_buf;
-    const int T = segment_bin_size(own, start, num_sms, total, packing);
-    if (T >= kMinSegBinPages)
+    const bool beside = !groups.empty() &&
+        static_cast<long long>(groups.size()) * kNumKvHeads <=
+            static_cast<long long>(kSharedBesideCtasPerSm) * num_sms;
+    if (beside) {
+      const int T = segment_bin_size(own, start, num_sms, kSegBesideCtasPerSm, total, packing);
+      if (T >= kMinSegBinPages) {
+        plan_shared_ranges(kSharedBesideCtasPerSm);
+        return build_segments(lens, batch, max_blocks, T, own, start, group_of, groups,
+                              shared_ranges, shared_max, kPlanLayoutBeside, packing, out,
+                              out_bytes);
+      }
+    }
+    const int T = segment_bin_size(own, start, num_sms, kSegCtasPerSm, total, packing);
+    if (T >= kMinSegBinPages) {
+      plan_shared_ranges(kSharedCtasPerSm);
       return build_segments(lens, batch, max_blocks, T, own, start, group_of, groups,
-                            shared_ranges, shared_max, packing, out, out_bytes);
+                            shared_ranges, shared_max, kPlanLayoutSequential, packing, out,
+                            out_bytes);
+    }
   }
+  plan_shared_ranges(kSharedCtasPerSm);
 
   auto count = [&](Sizes z) {
     long long items = count_items(solo, z);

@@ -183,19 +183,23 @@ def test_shared_prefix_kernel_times_out_then_recovers():
     check_recovered(w, d, step, "shared-prefix kernel")
 
 
-def test_folding_segment_plan_times_out_then_recovers():
+@pytest.mark.parametrize("sms, layout", [(8, 0), (32, 1)])
+def test_folding_segment_plan_times_out_then_recovers(sms, layout):
     dev = cuda_or_skip()
     b = binding()
-    # 64 sequences in groups of 16 sharing 64 pages, 2048 tokens each, planned
-    # as for 8 SMs: the shared-prefix kernel, then segment CTAs that fold each
-    # member's shared partials into its output (no merge) -- both time out
+    # 64 sequences in groups of 16 sharing 64 pages, 2048 tokens each: the
+    # shared-prefix kernel and segment CTAs that fold each member's shared
+    # partials into its output (no merge) -- both time out.  Planned as for
+    # 8 SMs the shared-prefix CTAs run first (layout 0); as for 32 SMs the
+    # segment CTAs run beside them and stream before their grid wait (layout 1)
     w = synth.make_workload("prefix", 7, batch=64, num_pages=8192, share_group=16,
                             share_blocks=64)
     d = synth.device_inputs(w, dev)
-    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, num_sms=8,
+    plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, num_sms=sms,
                   block_tables=w.block_tables[0])
     assert plan.num_shared > 0 and plan.num_segs > 0 and plan.num_merges == 0
     assert (plan.segments()[:, 5] > 0).all()
+    assert plan.layout == layout
 
     def step(err):
         return b.decode_step_planned(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"],

@@ -370,26 +370,47 @@ def test_without_tables_or_sharing_the_plan_is_the_plain_one():
     assert np.array_equal(a.host, b.host)
 
 
-@pytest.mark.parametrize("sms", [1, 132, 152])
-def test_shared_ranges_fill_one_wave_of_two_ctas_per_sm(sms):
-    # the prefix workload: 16 groups of 16 sequences sharing 96 pages.  Each
-    # group's prefix is cut into as many near-equal ranges as keep the
-    # shared-prefix CTAs (one per item and kv head, two resident per SM)
-    # within one wave: 2 ranges of 48 pages at 132 or 152 SMs, 1 of 96 at 1
+@pytest.mark.parametrize("sms", [1, 100, 132, 152])
+def test_shared_ranges_fill_one_wave(sms):
+    # the prefix workload: 16 groups of 16 sequences sharing 96 pages, 128
+    # (group, kv head) pairs.  With at least 128 SMs the shared-prefix CTAs
+    # fit one per SM and the plan runs its segment CTAs beside them, one per
+    # SM too (layout 1); otherwise the shared-prefix CTAs run first, two per
+    # SM (layout 0).  Each group's prefix is cut into as many near-equal
+    # ranges as keep its CTAs within that one wave: one range of 96 pages here.
     from paged_kv_decode_04_gb300 import synth
     w = synth.make_workload("prefix", 0)
     plan = B.Plan(w.seq_lens, w.max_blocks, num_sms=sms, block_tables=w.block_tables[0])
     sh = plan.shared()
-    ranges = 1 if sms == 1 else 2
-    assert plan.num_shared == 16 * ranges
+    beside = sms >= 128
+    assert plan.layout == (1 if beside else 0)
+    assert plan.num_shared == 16
     assert all(int(it[0]) == 16 for it in sh)
-    assert sorted({int(it[2]) for it in sh}) == [96 // ranges]
-    if sms > 1:
-        assert plan.num_shared * 8 <= 2 * sms
+    assert sorted({int(it[2]) for it in sh}) == [96]
+    assert plan.num_segs > 0
+    if beside:
+        assert plan.num_shared * 8 <= sms and plan.num_items <= sms
+    elif sms > 1:
+        assert plan.num_shared * 8 <= 2 * sms or plan.num_shared == 16
     for g in range(16):   # each group's ranges tile its 96 shared pages
         mine = sorted((int(it[1]), int(it[2])) for it in sh if int(it[4]) == 16 * g)
         assert mine[0][0] == 0 and all(a + n == b for (a, n), (b, _) in zip(mine, mine[1:]))
         assert mine[-1][0] + mine[-1][1] == 96
+
+
+@pytest.mark.parametrize("groups, sms, layout, ranges", [
+    (8, 152, 1, 2),      # 64 pairs: beside, two ranges of 48 per group (128 CTAs)
+    (8, 64, 1, 1),       # 64 pairs on 64 SMs: beside, one range each
+    (32, 152, 0, 1),     # 256 pairs > 152 SMs: shared-prefix CTAs first
+])
+def test_beside_layout_when_the_shared_ctas_fit_one_per_sm(groups, sms, layout, ranges):
+    lens, bt = shared_case(5, [(16, 96)] * groups, (32, 32))
+    plan = B.Plan(lens, 128, num_sms=sms, block_tables=bt, min_shared_pages=16)
+    assert plan.num_segs > 0 and plan.num_shared == groups * ranges
+    assert plan.layout == layout
+    if layout == 1:
+        assert plan.num_shared * 8 <= sms and plan.num_items <= sms
+    pieces, slots = shared_coverage(plan, lens, bt)
 
 
 def _kernels_for(plan_words, batch, mb=128):
@@ -563,7 +584,7 @@ def test_damaged_fold_words_are_refused():
     f = int(np.flatnonzero((segs[:, 5] > 0) & (segs[:, 6] > 0))[0])
     at = sg0 + 8 * f
     damage = {
-        "fold past the slots": (at + 6, plan.num_slots - 1),
+        "fold past the slots": (at + 6, plan.num_slots - int(segs[f, 5]) + 1),
         "negative fold slot": (at + 6, -1),
         "negative fold count": (at + 5, -1),
         "fold with a partial of its own": (at + 4, 0),
@@ -614,3 +635,30 @@ def test_concurrent_builds_match_sequential_ones():
     for th in threads:
         th.join()
     assert not bad
+
+
+def test_layout_word_is_checked():
+    # header word 11: 0 (shared-prefix CTAs first) or 1 (segment CTAs beside
+    # them), and 1 only for a shared-prefix plan of segment CTAs
+    lens, bt = shared_case(0, [(16, 96)] * 16, (32, 32))
+    beside = B.Plan(lens, 128, num_sms=SMS, block_tables=bt, min_shared_pages=16)
+    assert beside.layout == 1
+    good = beside.host.copy()
+    assert _kernels_for(good, len(lens)) is not None
+    seq = good.copy()
+    seq[11] = 0                      # the same plan run in sequence is still a plan
+    assert _kernels_for(seq, len(lens)) is not None
+    for bad_layout in (2, -1):
+        bad = good.copy()
+        bad[11] = bad_layout
+        assert _kernels_for(bad, len(lens)) is None
+    plain = B.Plan(np.full(256, 2048, np.int32), 128, num_sms=SMS)      # segments, no groups
+    small_lens, small_bt = shared_case(1, [(3, 20), (1, 5), (8, 40), (2, 16)], (1, 60))
+    small = B.Plan(small_lens, 128, num_sms=SMS, block_tables=small_bt, min_shared_pages=16)
+    assert plain.num_segs > 0 and plain.num_shared == 0
+    assert small.num_shared > 0 and small.num_segs == 0                 # per-head items
+    for plan, batch in ((plain, 256), (small, len(small_lens))):
+        assert plan.layout == 0
+        bad = plan.host.copy()
+        bad[11] = 1
+        assert _kernels_for(bad, batch) is None
