@@ -238,3 +238,66 @@ def test_folding_segment_plan_over_several_layers_in_one_call():
     for layer in (1, 2):
         ref, _ = oracle_step(w, layer)
         assert_close(one[layer], ref, f"prefix layer {layer} under a folding segment plan")
+
+
+@pytest.mark.parametrize("sms, layout", [(24, 0), (48, 1)])
+def test_layers_of_folding_and_merged_members_in_both_layouts(sms, layout):
+    # 48 sequences in 4 groups (16 members sharing 48 pages, 8 sharing 30),
+    # own tails of 8..70 pages: planned as for 24 SMs the shared-prefix CTAs
+    # run first (layout 0); as for 48 SMs the segment CTAs run beside them
+    # (layout 1).  Either way some members fold their shared partial in their
+    # one segment and others, cut into pieces, go through the merge kernel.
+    # Three layers in one call (each layer's kernels reuse the partial slots
+    # the previous layer's merge and folds read) must give the bits of one
+    # call per layer, and the oracle's outputs.
+    import oracle
+    from _gpu_util import bf16_normal
+    dev = cuda_or_skip()
+    b = binding()
+    rng = np.random.default_rng(1)
+    lens, rows, nxt = [], [], 0
+    for size, k in [(16, 48)] * 2 + [(8, 30)] * 2:
+        common = list(range(nxt, nxt + k))
+        nxt += k
+        for _ in range(size):
+            o = int(rng.integers(8, 71))
+            rows.append(common + list(range(nxt, nxt + o)))
+            nxt += o
+            lens.append(16 * (k + o) - int(rng.integers(0, 16)))
+    lens = np.asarray(lens, np.int32)
+    B, L, P = len(lens), 3, nxt + 16
+    bt = np.full((L, B, 128), -1, np.int32)
+    for layer in range(L):                 # each layer: the same sharing, its own pages
+        perm = rng.permutation(P).astype(np.int32) + layer * P
+        for i, r in enumerate(rows):
+            bt[layer, i, :len(r)] = perm[r]
+    pool = bf16_normal(rng, (L * P, 2, 16, 8, 64))
+    q = bf16_normal(rng, (L, B, 32, 64))
+    kn = bf16_normal(rng, (L, B, 8, 64))
+    vn = bf16_normal(rng, (L, B, 8, 64))
+    plan = b.Plan(lens, 128, device=dev, num_sms=sms, block_tables=bt[0])
+    assert plan.layout == layout and plan.num_segs > 0 and plan.num_merges > 0
+    assert (plan.segments()[:, 5] > 0).any()
+
+    def u16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+            torch.bfloat16)
+    dbt, dl = torch.from_numpy(bt).to(dev), torch.from_numpy(lens).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pool_one = u16(pool)
+    one = np.stack([synth.bits(b.decode_step_planned(
+        u16(q[layer]), u16(kn[layer]), u16(vn[layer]), pool_one, dbt[layer], dl, plan,
+        dev_err=err)) for layer in range(L)])
+    pool_many = u16(pool)
+    many = synth.bits(b.decode_steps_planned(u16(q), u16(kn), u16(vn), pool_many, dbt, dl, plan,
+                                             dev_err=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(many, one)
+    ref_pool = pool.copy()
+    for layer in range(L):
+        assert oracle.kv_append(kn[layer], vn[layer], ref_pool, bt[layer], lens - 1) == 0
+        ref = oracle.decode_attention(q[layer], ref_pool, bt[layer], lens)
+        assert_close(one[layer], ref, f"layer {layer}, layout {layout}")
+    assert np.array_equal(synth.bits(pool_one), ref_pool)
+    assert np.array_equal(synth.bits(pool_many), ref_pool)
