@@ -20,9 +20,13 @@
 // whole layer and all of them end together.  A segment that is a whole
 // sequence writes its output rows; a piece writes an unnormalised partial
 // that the merge kernel combines.  Under a shared-prefix plan the
-// shared-prefix kernel runs first, and a member whose own pages are one
-// segment folds that kernel's partials for it into its rows and writes the
-// output itself, so such a sequence needs no merge.
+// shared-prefix kernel is launched first, and a member whose own pages are
+// one segment folds that kernel's partials for it into its rows and writes
+// the output itself, so such a sequence needs no merge.  In the plan's
+// beside layout the CTAs (one per SM, a deeper ring) run next to the
+// shared-prefix CTAs, whose kernel is bound by its own MMA and softmax
+// chain rather than by DRAM: they stream from the start and wait for that
+// kernel only to fold its partials.
 //
 // Per CTA, at the start: the segments' q rows (4 KiB each) arrive by bulk
 // copies; each warp computes the appended token's row of its head for every

@@ -53,7 +53,10 @@
 //     row in TMEM.  At the end each query row's (max, sum, acc) partial,
 //     unnormalised, goes to the slot the plan gives its member; the members'
 //     own pages are attended by the ordinary planned kernels into the
-//     following slots, and the merge kernel combines them.
+//     following slots, and the merge kernel (or the member's own segment)
+//     combines them.  In the plan's beside layout the CTAs take smaller K
+//     and V rings (kSlotsBeside), one per SM, and the segment kernel's CTAs
+//     run next to them.
 // A shared page is never a member's last page, so every shared page is full
 // and none takes the step's append.  Every wait is bounded: a wait on
 // another role's progress by the call's limit (2 s unless the caller set
