@@ -344,7 +344,11 @@ PKV_API size_t pkv_plan_bytes(int batch, int max_blocks);
  * plan: host memory, 16-byte aligned, at least pkv_plan_bytes() bytes.
  * Returns PKV_OK, PKV_EINVAL (a length outside [0, max_blocks * page_size],
  * bad sizes or buffer), PKV_EALIGN, PKV_EUNSUPPORTED (more than 65535 work
- * items) or PKV_ECUDA (no device to size it for).  Pure host code.
+ * items) or PKV_ECUDA (no device to size it for).  Pure host code; thread-safe.
+ * The planner keeps its working buffers per calling thread and reuses them
+ * from one call to the next (a few MB for the largest batches), so a
+ * serving loop that plans every step allocates nothing once warm; they are
+ * freed when the thread exits.
  */
 PKV_API int pkv_plan_build(const int32_t* seq_lens_host, int batch, int max_blocks,
                            int num_sms, void* plan, size_t plan_bytes);
