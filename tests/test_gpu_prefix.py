@@ -301,3 +301,55 @@ def test_layers_of_folding_and_merged_members_in_both_layouts(sms, layout):
         assert_close(one[layer], ref, f"layer {layer}, layout {layout}")
     assert np.array_equal(synth.bits(pool_one), ref_pool)
     assert np.array_equal(synth.bits(pool_many), ref_pool)
+
+
+@pytest.mark.parametrize("sms", [24, 48, 152])
+def test_long_shared_prefixes_beside(sms):
+    # 1024-entry tables: groups of 8, 8 and 6 sequences sharing 400, 250 and
+    # 600 pages, own tails of 100..300 pages (up to 14,208 tokens).  Planned as
+    # for 24, 48 and 152 SMs these are beside-layout plans with shared ranges
+    # of 600, 300 and 100 pages and segment CTAs of up to 258 pages; some
+    # members fold, others are merged.  Fused step against the oracle.
+    import oracle
+    from _gpu_util import bf16_normal
+    dev = cuda_or_skip()
+    b = binding()
+    mb = 1024
+    rng = np.random.default_rng(3)
+    lens, rows, nxt = [], [], 0
+    for size, k in [(8, 400), (8, 250), (6, 600)]:
+        common = list(range(nxt, nxt + k))
+        nxt += k
+        for _ in range(size):
+            o = int(rng.integers(100, 301))
+            rows.append(common + list(range(nxt, nxt + o)))
+            nxt += o
+            lens.append(16 * (k + o) - int(rng.integers(0, 16)))
+    lens = np.asarray(lens, np.int32)
+    B = len(lens)
+    bt = np.full((B, mb), -1, np.int32)
+    perm = np.random.default_rng(4).permutation(nxt + 16).astype(np.int32)
+    for i, r in enumerate(rows):
+        bt[i, :len(r)] = perm[r]
+    pool = bf16_normal(rng, (nxt + 16, 2, 16, 8, 64))
+    q = bf16_normal(rng, (B, 32, 64))
+    kn = bf16_normal(rng, (B, 8, 64))
+    vn = bf16_normal(rng, (B, 8, 64))
+    ref_pool = pool.copy()
+    assert oracle.kv_append(kn, vn, ref_pool, bt, lens - 1) == 0
+    ref = oracle.decode_attention(q, ref_pool, bt, lens)
+    plan = b.Plan(lens, mb, device=dev, num_sms=sms, block_tables=bt)
+    assert plan.layout == 1 and plan.num_shared > 0 and plan.num_merges > 0
+
+    def u16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+            torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    dpool = u16(pool)
+    out = b.decode_step_planned(u16(q), u16(kn), u16(vn), dpool, torch.from_numpy(bt).to(dev),
+                                torch.from_numpy(lens).to(dev), plan, dev_err=err)
+    got = synth.bits(out)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(got, ref, f"long shared prefixes, sms={sms}")
+    assert np.array_equal(synth.bits(dpool), ref_pool)
