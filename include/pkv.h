@@ -327,7 +327,8 @@ PKV_API int pkv_check_tables(const int32_t* block_table, int max_blocks,
  * layout 0: the shared-prefix CTAs (if any) run first, two per SM, and the
  * other kernels after them.  layout 1 (a shared-prefix plan of segment CTAs
  * whose shared-prefix CTAs fit one per SM; pkv_plan_build_shared makes it
- * whenever they do): the segment CTAs, sized for one per SM, run beside
+ * whenever they do and bins of one CTA per SM reach 16 pages, whatever P):
+ * the segment CTAs, sized for one per SM, run beside
  * the shared-prefix CTAs, streaming their own pages from the start, and
  * wait for the shared-prefix grid only to fold its partials.  Any other
  * layout value is refused.  The results follow the same numerics as the

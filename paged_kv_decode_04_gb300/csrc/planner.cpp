@@ -491,13 +491,17 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
   // CTAs and deeper per-warp rings, is faster (a ragged 16-layer batch of
   // 2067 pages per layer: 313.7 us with bins of 8 pages against 249.7 us).
   // With shared groups whose shared-prefix CTAs fit one per SM, the segment
-  // CTAs are sized to run beside them, one per SM (kPlanLayoutBeside).
-  if (total >= static_cast<long long>(kMinSegBinPages) * num_sms) {
+  // CTAs are sized to run beside them, one per SM (kPlanLayoutBeside), for
+  // any layer size whose bins reach kMinSegBinPages: those CTAs overlap the
+  // shared-prefix kernel, so small bins cost little there (64 sequences of
+  // 2048 tokens in 16-way groups sharing 1536: 26.6 -> 22.8 us against the
+  // per-(item, kv head) plan).
+  const bool beside = !groups.empty() &&
+      static_cast<long long>(groups.size()) * kNumKvHeads <=
+          static_cast<long long>(kSharedBesideCtasPerSm) * num_sms;
+  if (beside || total >= static_cast<long long>(kMinSegBinPages) * num_sms) {
     static thread_local Packing packing_buf;
     Packing& packing = packing_buf;
-    const bool beside = !groups.empty() &&
-        static_cast<long long>(groups.size()) * kNumKvHeads <=
-            static_cast<long long>(kSharedBesideCtasPerSm) * num_sms;
     if (beside) {
       const int T = segment_bin_size(own, start, num_sms, kSegBesideCtasPerSm, total, packing);
       if (T >= kMinSegBinPages) {
@@ -507,7 +511,9 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
                               out_bytes);
       }
     }
-    const int T = segment_bin_size(own, start, num_sms, kSegCtasPerSm, total, packing);
+    const int T = total >= static_cast<long long>(kMinSegBinPages) * num_sms
+                      ? segment_bin_size(own, start, num_sms, kSegCtasPerSm, total, packing)
+                      : 0;
     if (T >= kMinSegBinPages) {
       plan_shared_ranges(kSharedCtasPerSm);
       return build_segments(lens, batch, max_blocks, T, own, start, group_of, groups,

@@ -159,19 +159,22 @@ def test_segment_kernel_times_out_then_recovers():
     check_recovered(w, d, step, "segment kernel")
 
 
-def test_shared_prefix_kernel_times_out_then_recovers():
+@pytest.mark.parametrize("share, kernels", [
+    (64, "paged_decode_shared_kernel+paged_decode_segments_kernel+merge_plan_kernel"),
+    (120, "paged_decode_shared_kernel+paged_decode_kernel+merge_plan_kernel")])
+def test_shared_prefix_kernel_times_out_then_recovers(share, kernels):
     dev = cuda_or_skip()
     b = binding()
-    # two groups of 16 sequences sharing 64 pages, 2048 tokens each: the
-    # tcgen05 shared-prefix kernel (copies, MMAs and TMEM in flight when its
-    # waits give up), the per-sequence kernel and the merge
+    # two groups of 16 sequences sharing 64 (or 120) pages, 2048 tokens each:
+    # the tcgen05 shared-prefix kernel (copies, MMAs and TMEM in flight when
+    # its waits give up), then segment CTAs beside it (own tails of 64 pages)
+    # or the per-(item, kv head) kernel after it (tails of 8), and the merge
     w = synth.make_workload("prefix", 4, batch=32, num_pages=4096, share_group=16,
-                            share_blocks=64)
+                            share_blocks=share)
     d = synth.device_inputs(w, dev)
     plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, block_tables=w.block_tables[0])
     assert plan.num_shared > 0
-    assert b.attention_kernels(w.batch, w.max_blocks, 0, plan).startswith(
-        "paged_decode_shared_kernel+")
+    assert b.attention_kernels(w.batch, w.max_blocks, 0, plan) == kernels
 
     def step(err):
         return b.decode_step_planned(d["q"][0], d["k_new"][0], d["v_new"][0], d["pool"],

@@ -339,8 +339,8 @@ def test_shared_plan_covers_every_page_once(seed, groups, own):
         assert all(x[0] == b for x in got)
         assert [x[1] for x in got] == sorted(x[1] for x in got)
         assert len(pieces[b]) == nf + 1
-    if plan.num_segs:
-        assert folds or seed == 4
+    if plan.num_segs:   # members fold, or (cut into pieces) are merged
+        assert len(folds) + len(members & set(merged)) == len(members)
     if groups == [(16, 96)] * 16:
         assert plan.num_merges == 0 and len(folds) == 256
     assert plan.num_slots == len(slots)
