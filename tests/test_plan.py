@@ -402,12 +402,16 @@ def test_shared_ranges_fill_one_wave(sms):
     (8, 152, 1, 2),      # 64 pairs: beside, two ranges of 48 per group (128 CTAs)
     (8, 64, 1, 1),       # 64 pairs on 64 SMs: beside, one range each
     (32, 152, 0, 1),     # 256 pairs > 152 SMs: shared-prefix CTAs first
+    (4, 152, 1, 4),      # 2048 own pages, under the 16-pages-per-SM gate of other segment
+                         # plans: beside all the same (bins of 16, members cut in two)
 ])
 def test_beside_layout_when_the_shared_ctas_fit_one_per_sm(groups, sms, layout, ranges):
     lens, bt = shared_case(5, [(16, 96)] * groups, (32, 32))
     plan = B.Plan(lens, 128, num_sms=sms, block_tables=bt, min_shared_pages=16)
     assert plan.num_segs > 0 and plan.num_shared == groups * ranges
     assert plan.layout == layout
+    if groups == 4:
+        assert plan.range_pages == 16 and plan.num_merges == 64
     if layout == 1:
         assert plan.num_shared * 8 <= sms and plan.num_items <= sms
     pieces, slots = shared_coverage(plan, lens, bt)
@@ -662,3 +666,14 @@ def test_layout_word_is_checked():
         bad = plan.host.copy()
         bad[11] = 1
         assert _kernels_for(bad, batch) is None
+
+
+@pytest.mark.parametrize("groups", [1, 2])
+def test_small_shared_batches_stay_on_the_per_head_plan(groups):
+    # 16 or 32 sequences (512 or 1024 own pages): bins of one CTA per SM would
+    # hold fewer than 16 pages, so no segment plan; the shared-prefix CTAs run
+    # first and the per-(item, kv head) kernel and the merge after them
+    lens, bt = shared_case(5, [(16, 96)] * groups, (32, 32))
+    plan = B.Plan(lens, 128, num_sms=SMS, block_tables=bt, min_shared_pages=16)
+    assert plan.num_segs == 0 and plan.layout == 0 and plan.num_merges == 16 * groups
+    shared_coverage(plan, lens, bt)
