@@ -227,14 +227,14 @@ struct Packing {
 // The bin size of a segment plan: the smallest T from max(kMinSegPages,
 // ceil(P / C)) up (P: the pages to attend, C = ctas_per_sm CTAs per SM)
 // whose bins fit in one wave of C CTAs, else the largest (up to kSegMax x the
-// longest sequence, or kSegMaxPages).  A T whose pieces cannot fit is ruled
+// longest sequence, or kSegMaxPages; *fitted says which).  A T whose pieces cannot fit is ruled
 // out without packing, by lower bounds on the bins: more than C * T pages;
 // or, for k < kSegMax, more than k * C pieces longer than T / (k + 1) (at
 // most k of them share a bin); or more than kSegMax * C pieces.  One that
 // has at most C pieces fits without packing (best fit opens a bin only for
 // a piece that no open bin takes).
 int segment_bin_size(const std::vector<int>& own, const std::vector<int>& start, int num_sms,
-                     int ctas_per_sm, long long total, Packing& best) {
+                     int ctas_per_sm, long long total, Packing& best, bool* fitted = nullptr) {
   const long long C = static_cast<long long>(ctas_per_sm) * num_sms;
   const int max_own = *std::max_element(own.begin(), own.end());
   const int t0 = static_cast<int>(std::min<long long>(
@@ -304,6 +304,7 @@ int segment_bin_size(const std::vector<int>& own, const std::vector<int>& start,
   const int whole = std::min(std::max(t0, max_own), t1);
   int T = smallest(t0, whole);
   if (T < 0) T = smallest(whole + 1, t1);
+  if (fitted != nullptr) *fitted = T >= 0;
   return T < 0 ? t1 : T;
 }
 
@@ -503,8 +504,10 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
     static thread_local Packing packing_buf;
     Packing& packing = packing_buf;
     if (beside) {
-      const int T = segment_bin_size(own, start, num_sms, kSegBesideCtasPerSm, total, packing);
-      if (T >= kMinSegBinPages) {
+      bool fitted = false;
+      const int T =
+          segment_bin_size(own, start, num_sms, kSegBesideCtasPerSm, total, packing, &fitted);
+      if (fitted && T >= kMinSegBinPages) {  // one segment CTA per SM, at most
         plan_shared_ranges(kSharedBesideCtasPerSm);
         return build_segments(lens, batch, max_blocks, T, own, start, group_of, groups,
                               shared_ranges, shared_max, kPlanLayoutBeside, packing, out,

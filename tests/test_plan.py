@@ -677,3 +677,38 @@ def test_small_shared_batches_stay_on_the_per_head_plan(groups):
     plan = B.Plan(lens, 128, num_sms=SMS, block_tables=bt, min_shared_pages=16)
     assert plan.num_segs == 0 and plan.layout == 0 and plan.num_merges == 16 * groups
     shared_coverage(plan, lens, bt)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_shared_plans_keep_their_layout_rules(seed):
+    # random groups (2..16 members, 16..100 shared pages), singletons, own
+    # tails of 1..80 pages, planned for a random SM count: every page is
+    # attended once; a beside plan (layout 1) has at most one shared-prefix
+    # CTA and one segment CTA per SM; segment bins hold at least 16 pages;
+    # members either fold or are merged; the library accepts the plan
+    rng = np.random.default_rng(500 + seed)
+    sms = int(rng.choice([8, 16, 32, 64, 100, 132, 152]))
+    groups = []
+    for _ in range(int(rng.integers(1, 9))):
+        if rng.random() < 0.3:
+            groups.append((1, 0))
+        groups.append((int(rng.integers(2, 17)), int(rng.integers(16, 101))))
+    kmax = max(k for _, k in groups)
+    own = (1, int(min(rng.choice([8, 30, 80]), 127 - kmax)))   # within the 128-entry table
+    lens, bt = shared_case(int(rng.integers(0, 1 << 30)), groups, own)
+    plan = B.Plan(lens, 128, num_sms=sms, block_tables=bt, min_shared_pages=16)
+    folds = {}
+    pieces, slots = shared_coverage(plan, lens, bt, folds)
+    for b, L in enumerate(lens.tolist()):
+        covered = sorted(p for p0, n in pieces[b] for p in range(p0, p0 + n))
+        assert covered == list(range(-(-L // 16))), b
+    members = {int(x) for it in plan.shared() for x in it[4:4 + it[0]]}
+    merged = {int(m[0]) for m in plan.merges()}
+    assert members <= merged | set(folds) and not merged & set(folds)
+    if plan.layout == 1:
+        assert plan.num_segs > 0 and plan.num_shared > 0
+        assert plan.num_shared * 8 <= sms and plan.num_items <= sms
+        assert plan.range_pages >= 16
+    elif plan.num_segs:   # one wave of two per SM when some bin size fits it
+        assert plan.range_pages >= 16
+    assert _kernels_for(plan.host.copy(), len(lens)) is not None
