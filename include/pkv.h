@@ -325,13 +325,14 @@ PKV_API int pkv_check_tables(const int32_t* block_table, int max_blocks,
  * shared-prefix items wrote (a group member whose own pages are one segment
  * needs no merge entry).  range_pages is the longest range or bin.
  * layout 0: the shared-prefix CTAs (if any) run first, two per SM, and the
- * other kernels after them.  layout 1 (a shared-prefix plan of segment CTAs
- * whose shared-prefix CTAs fit one per SM; pkv_plan_build_shared makes it
- * whenever they do and bins of one CTA per SM reach 16 pages, whatever P):
- * the segment CTAs, sized for one per SM, run beside
- * the shared-prefix CTAs, streaming their own pages from the start, and
- * wait for the shared-prefix grid only to fold its partials.  Any other
- * layout value is refused.  The results follow the same numerics as the
+ * other kernels after them.  layout 1 (a shared-prefix plan whose
+ * shared-prefix CTAs fit one per SM; pkv_plan_build_shared makes it whenever
+ * they do): the other attention CTAs run beside the shared-prefix CTAs,
+ * streaming their own pages from the start, and wait for the shared-prefix
+ * grid only to fold its partials and before they end -- segment CTAs sized
+ * for one per SM when bins of one CTA per SM reach 16 pages (whatever P),
+ * else per-(item, kv head) CTAs sized for two per SM next to each
+ * shared-prefix CTA.  Any other layout value is refused.  The results follow the same numerics as the
  * calls above (same tolerance, bit-identical on repeated runs of a plan).
  */
 #define PKV_PLAN_MAGIC 0x32564b50 /* "PKV2" */

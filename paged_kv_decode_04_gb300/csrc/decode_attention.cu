@@ -182,10 +182,11 @@ __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map, con
   }
 }
 
-template <bool kAppend, int kStages, bool kPlanned>
+template <bool kAppend, int kStages, bool kPlanned, bool kBeside = false>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
     paged_decode_kernel(const __grid_constant__ CUtensorMap pool_map,
                         const AttnArgs a, const AppendArgs ap) {
+  static_assert(kPlanned || !kBeside, "only planned grids run beside the shared-prefix grid");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -207,7 +208,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
     p_ls = it[2];
   }
   prefetch_first_tiles<kStages, kPlanned>(&pool_map, a, g, tid, p_head, p_bs, p_ls);
-  wait_for_prior_grids();
+  // Beside (a shared-prefix plan's layout 1): the grid before this one is the
+  // shared-prefix grid, whose CTAs let this grid launch only after their own
+  // wait, so this CTA's inputs are final; that grid reads only shared pages
+  // (never a sequence's last page) and writes only its partial slots.  So
+  // this CTA starts at once and waits for that grid only before it exits.
+  if constexpr (!kBeside) wait_for_prior_grids();
   allow_dependent_grids();
 
   // ---- this CTA's work.  Range: the 4 warps share the logical pages
@@ -443,6 +449,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kStages))
     }
     write_row(wb, r, M, Ls, O, part_row0 < 0 ? -1 : part_row0 + static_cast<int64_t>(r) * part_step);
   }
+  // Beside: no CTA ends before the shared-prefix grid has, so that this
+  // grid's completion (what the merge waits for) covers that grid's partials
+  if constexpr (kBeside) wait_for_prior_grids();
 }
 
 // Combine the split partials of one (b, j): grid (Hq, B), one warp.
@@ -518,24 +527,32 @@ int max_pages_per_split() { return kMaxPagesPerSplit; }
 
 namespace {
 
-// The dynamic shared-memory opt-in is per device and per kernel.
-template <bool kAppend, int kStages, bool kPlanned>
+// The dynamic shared-memory opt-in is per device and per kernel; beside
+// instances also ask for the largest shared-memory carveout, the one the
+// shared-prefix CTAs they run next to ask for (CTAs of two kernels share an
+// SM only under one L1 / shared-memory split).
+template <bool kAppend, int kStages, bool kPlanned, bool kBeside>
 cudaError_t configure_once(int device) {
   static std::atomic<unsigned long long> configured{0};
   const unsigned long long bit = 1ull << (device & 63);
   if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  const cudaError_t err = cudaFuncSetAttribute(
-      paged_decode_kernel<kAppend, kStages, kPlanned>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(
+      paged_decode_kernel<kAppend, kStages, kPlanned, kBeside>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize,
       static_cast<int>(smem_bytes(kStages, kMaxPagesPerSplit)));
+  if (err == cudaSuccess && kBeside)
+    err = cudaFuncSetAttribute(paged_decode_kernel<kAppend, kStages, kPlanned, kBeside>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
   if (err == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
 
-template <bool kAppend, int kStages, bool kPlanned>
+template <bool kAppend, int kStages, bool kPlanned, bool kBeside>
 cudaError_t launch_variant(const CUtensorMap& pool_map, const AttnArgs& args,
                            const AppendArgs& append, dim3 grid, int page_list, int device,
                            cudaStream_t stream) {
-  const cudaError_t err = configure_once<kAppend, kStages, kPlanned>(device);
+  const cudaError_t err = configure_once<kAppend, kStages, kPlanned, kBeside>(device);
   if (err != cudaSuccess) return err;
   if constexpr (kPlanned) {
     // Planned grids (kv head, item) run in clusters of kHeadPair CTAs: kv
@@ -545,30 +562,31 @@ cudaError_t launch_variant(const CUtensorMap& pool_map, const AttnArgs& args,
     // layers 250.2 -> 243.5 us, a 2048-token sequence of 16 layers 92.8 ->
     // 90.6 us; clusters of 4 and 8 (harder to place in one wave) 267 and
     // 277 us on the mixed batch.
-    return launch_pdl_cluster(paged_decode_kernel<kAppend, kStages, kPlanned>, grid,
+    return launch_pdl_cluster(paged_decode_kernel<kAppend, kStages, kPlanned, kBeside>, grid,
                               dim3(kThreads), smem_bytes(kStages, page_list), stream, kHeadPair,
                               pool_map, args, append);
   }
-  return launch_pdl(paged_decode_kernel<kAppend, kStages, kPlanned>, grid, dim3(kThreads),
-                    smem_bytes(kStages, page_list), stream, pool_map, args, append);
+  return launch_pdl(paged_decode_kernel<kAppend, kStages, kPlanned, kBeside>, grid,
+                    dim3(kThreads), smem_bytes(kStages, page_list), stream, pool_map, args,
+                    append);
 }
 
 // Ring depth by the pages a warp gets: deep when the ring holds them all.
-template <bool kPlanned>
+template <bool kPlanned, bool kBeside = false>
 cudaError_t launch_attention_kernel(const CUtensorMap& pool_map, const AttnArgs& args,
                                     const AppendArgs* append, dim3 grid, int range_pages,
                                     int page_list, int device, cudaStream_t stream) {
   const bool deep = range_pages <= kWarps * kDeepStages;
   const AppendArgs none{};
   if (append != nullptr)
-    return deep ? launch_variant<true, kDeepStages, kPlanned>(pool_map, args, *append, grid,
-                                                              page_list, device, stream)
-                : launch_variant<true, kShallowStages, kPlanned>(pool_map, args, *append, grid,
-                                                                 page_list, device, stream);
-  return deep ? launch_variant<false, kDeepStages, kPlanned>(pool_map, args, none, grid,
-                                                             page_list, device, stream)
-              : launch_variant<false, kShallowStages, kPlanned>(pool_map, args, none, grid,
-                                                                page_list, device, stream);
+    return deep ? launch_variant<true, kDeepStages, kPlanned, kBeside>(
+                      pool_map, args, *append, grid, page_list, device, stream)
+                : launch_variant<true, kShallowStages, kPlanned, kBeside>(
+                      pool_map, args, *append, grid, page_list, device, stream);
+  return deep ? launch_variant<false, kDeepStages, kPlanned, kBeside>(
+                    pool_map, args, none, grid, page_list, device, stream)
+              : launch_variant<false, kShallowStages, kPlanned, kBeside>(
+                    pool_map, args, none, grid, page_list, device, stream);
 }
 
 }  // namespace
@@ -606,13 +624,17 @@ cudaError_t launch_split_merge(const AttnArgs& args, int num_merges, cudaStream_
 cudaError_t launch_planned_decode_attention(const CUtensorMap& pool_map,
                                             const AttnArgs& args, int num_items,
                                             int num_merges, int range_pages,
-                                            cudaStream_t stream, const AppendArgs* append) {
+                                            cudaStream_t stream, const AppendArgs* append,
+                                            bool beside) {
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
   const int page_list = range_pages > kWarps * kPackPages ? range_pages : kWarps * kPackPages;
-  err = launch_attention_kernel<true>(pool_map, args, append, dim3(kNumKvHeads, num_items),
-                                      range_pages, page_list, device, stream);
+  const dim3 grid(kNumKvHeads, num_items);
+  err = beside ? launch_attention_kernel<true, true>(pool_map, args, append, grid, range_pages,
+                                                     page_list, device, stream)
+               : launch_attention_kernel<true>(pool_map, args, append, grid, range_pages,
+                                               page_list, device, stream);
   if (err != cudaSuccess) return err;
   if (num_merges > 0) err = launch_merge_plan(args, num_merges, stream);
   return err;

@@ -567,9 +567,9 @@ const PlanHeader* plan_header(const void* plan, int batch, int max_blocks) {
       h->num_shared > 65535 || h->num_segs < 0 ||
       (h->num_shared > 0 && (h->shared_pages < 1 || h->shared_pages > 1024)))
     return nullptr;
-  // the beside layout is for shared-prefix plans of segment CTAs only
+  // the beside layout is for shared-prefix plans only
   if (h->layout != pkv::kPlanLayoutSequential &&
-      (h->layout != pkv::kPlanLayoutBeside || h->num_shared < 1 || h->num_segs < 1))
+      (h->layout != pkv::kPlanLayoutBeside || h->num_shared < 1))
     return nullptr;
   // bytes_used is exactly the header and the three sections the counts imply
   const int64_t words = pkv::kPlanHeaderWords +
@@ -646,7 +646,8 @@ cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pa
     if (err != cudaSuccess) return err;
     return pkv::launch_split_merge(args, h.num_merges, stream);
   }
-  if (use_pagebox(h.num_items, h.range_pages) && plan_has_only_ranges(h)) {
+  const bool beside = h.layout == pkv::kPlanLayoutBeside;
+  if (!beside && use_pagebox(h.num_items, h.range_pages) && plan_has_only_ranges(h)) {
     if (!pool_page_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
     const cudaError_t err = pkv::launch_pagebox_attention(map, args, h.num_items, h.range_pages,
                                                           stream, append);
@@ -655,7 +656,7 @@ cudaError_t launch_planned(const PlanHeader& h, const void* pool, int64_t num_pa
   }
   if (!pool_tensor_map(pool, num_pages, &map)) return cudaErrorInvalidValue;
   return pkv::launch_planned_decode_attention(map, args, h.num_items, h.num_merges,
-                                              h.range_pages, stream, append);
+                                              h.range_pages, stream, append, beside);
 }
 
 }  // namespace
@@ -676,7 +677,8 @@ PKV_API const char* pkv_attention_kernels(int batch, int max_blocks, int num_spl
       return h->num_merges > 0 ? "paged_decode_segments_kernel+merge_plan_kernel"
                                : "paged_decode_segments_kernel";
     }
-    const bool pb = use_pagebox(h->num_items, h->range_pages) && plan_has_only_ranges(*h);
+    const bool pb = h->layout != pkv::kPlanLayoutBeside &&
+                    use_pagebox(h->num_items, h->range_pages) && plan_has_only_ranges(*h);
     if (h->num_shared > 0)  // a plan with shared groups always merges
       return pb ? "paged_decode_shared_kernel+paged_decode_pagebox_kernel+merge_plan_kernel"
                 : "paged_decode_shared_kernel+paged_decode_kernel+merge_plan_kernel";

@@ -207,11 +207,14 @@ cudaError_t launch_paged_decode_attention(const CUtensorMap& pool_map,
 
 // The same under a work plan: grid (Hkv, num_items), then the merge of the
 // num_merges split sequences.  range_pages sizes the shared page list.
+// beside: the plan's layout is kPlanLayoutBeside (launched right after the
+// shared-prefix grid, whose CTAs it runs next to).
 cudaError_t launch_planned_decode_attention(const CUtensorMap& pool_map,
                                             const AttnArgs& args, int num_items,
                                             int num_merges, int range_pages,
                                             cudaStream_t stream,
-                                            const AppendArgs* append = nullptr);
+                                            const AppendArgs* append = nullptr,
+                                            bool beside = false);
 
 // The same attention (fixed plan: args.plan_items == nullptr, grid (S, B);
 // work plan: range items only, grid (num_items)) with one CTA per (sequence,

@@ -26,6 +26,7 @@ constexpr int kResidentPerSm = 4;     // attention CTAs resident per SM (shallow
 constexpr int kMaxRangePages = 1024;  // the kernel's shared page list
 constexpr int kMinSegPages = 4;       // smallest bin size tried for a segment plan
 constexpr int kMinSegBinPages = 16;   // smallest bin size a segment plan is used with
+constexpr int kPerHeadBesideCtasPerSm = 2;  // per-head CTAs next to a shared-prefix CTA (registers)
 
 struct Range {
   int b, L, p_begin, n, slot;
@@ -524,7 +525,20 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
                             out_bytes);
     }
   }
-  plan_shared_ranges(kSharedCtasPerSm);
+  // Below the segment plans, the per-(item, kv head) CTAs run beside the
+  // shared-prefix CTAs too when those fit one per SM: an SM holding a
+  // shared-prefix CTA has registers for kPerHeadBesideCtasPerSm of them.
+  long long wave = static_cast<long long>(kResidentPerSm) * num_sms;  // CTAs
+  int layout = kPlanLayoutSequential;
+  if (beside) {
+    plan_shared_ranges(kSharedBesideCtasPerSm);
+    long long shared_ctas = 0;
+    for (int ns : shared_ranges) shared_ctas += static_cast<long long>(ns) * kNumKvHeads;
+    wave -= (kResidentPerSm - kPerHeadBesideCtasPerSm) * std::min<long long>(shared_ctas, num_sms);
+    layout = kPlanLayoutBeside;
+  } else {
+    plan_shared_ranges(kSharedCtasPerSm);
+  }
 
   auto count = [&](Sizes z) {
     long long items = count_items(solo, z);
@@ -532,7 +546,6 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
       if (group_of[b] >= 0) items += (own[b] + z.range - 1) / z.range;
     return items;
   };
-  const long long wave = static_cast<long long>(kResidentPerSm) * num_sms;  // CTAs
   const long long u0 = std::max<long long>(1, (total + 2LL * num_sms - 1) / (2LL * num_sms));
   const long long umax = std::max<long long>(u0, (max_blocks + kPlanWarps - 1) / kPlanWarps);
   long long lo = u0, hi = umax;  // smallest u in [u0, umax] that fits, else umax
@@ -617,6 +630,7 @@ int build_core(const int32_t* lens, int batch, int max_blocks, int num_sms,
   out[7] = static_cast<int32_t>(words * 4);
   out[8] = static_cast<int32_t>(num_shared);
   out[9] = shared_max;
+  out[11] = layout;
   int32_t* item = out + kPlanHeaderWords;
   for (const Item& o : order) {
     if (o.kind == kPlanKindRange) {

@@ -657,25 +657,34 @@ def test_layout_word_is_checked():
         bad[11] = bad_layout
         assert _kernels_for(bad, len(lens)) is None
     plain = B.Plan(np.full(256, 2048, np.int32), 128, num_sms=SMS)      # segments, no groups
+    assert plain.num_segs > 0 and plain.num_shared == 0 and plain.layout == 0
+    bad = plain.host.copy()
+    bad[11] = 1                      # nothing to run beside
+    assert _kernels_for(bad, 256) is None
+    # per-head items beside the shared-prefix CTAs: either layout is a valid plan
     small_lens, small_bt = shared_case(1, [(3, 20), (1, 5), (8, 40), (2, 16)], (1, 60))
     small = B.Plan(small_lens, 128, num_sms=SMS, block_tables=small_bt, min_shared_pages=16)
-    assert plain.num_segs > 0 and plain.num_shared == 0
-    assert small.num_shared > 0 and small.num_segs == 0                 # per-head items
-    for plan, batch in ((plain, 256), (small, len(small_lens))):
-        assert plan.layout == 0
-        bad = plan.host.copy()
-        bad[11] = 1
-        assert _kernels_for(bad, batch) is None
+    assert small.num_shared > 0 and small.num_segs == 0 and small.layout == 1
+    seq = small.host.copy()
+    seq[11] = 0
+    assert _kernels_for(seq, len(small_lens)) == \
+        b"paged_decode_shared_kernel+paged_decode_kernel+merge_plan_kernel"
+    bad = small.host.copy()
+    bad[11] = 2
+    assert _kernels_for(bad, len(small_lens)) is None
 
 
 @pytest.mark.parametrize("groups", [1, 2])
-def test_small_shared_batches_stay_on_the_per_head_plan(groups):
+def test_small_shared_batches_run_per_head_items_beside(groups):
     # 16 or 32 sequences (512 or 1024 own pages): bins of one CTA per SM would
-    # hold fewer than 16 pages, so no segment plan; the shared-prefix CTAs run
-    # first and the per-(item, kv head) kernel and the merge after them
+    # hold fewer than 16 pages, so no segment plan; the per-(item, kv head)
+    # CTAs (two per SM next to a shared-prefix CTA) run beside the
+    # shared-prefix CTAs (layout 1), and the merge after them
     lens, bt = shared_case(5, [(16, 96)] * groups, (32, 32))
     plan = B.Plan(lens, 128, num_sms=SMS, block_tables=bt, min_shared_pages=16)
-    assert plan.num_segs == 0 and plan.layout == 0 and plan.num_merges == 16 * groups
+    assert plan.num_segs == 0 and plan.layout == 1 and plan.num_merges == 16 * groups
+    assert plan.num_shared * 8 <= SMS
+    assert plan.num_items * 8 <= 4 * SMS - 2 * plan.num_shared * 8
     shared_coverage(plan, lens, bt)
 
 
@@ -684,7 +693,8 @@ def test_random_shared_plans_keep_their_layout_rules(seed):
     # random groups (2..16 members, 16..100 shared pages), singletons, own
     # tails of 1..80 pages, planned for a random SM count: every page is
     # attended once; a beside plan (layout 1) has at most one shared-prefix
-    # CTA and one segment CTA per SM; segment bins hold at least 16 pages;
+    # CTA per SM, and one segment CTA per SM if it has segments; segment bins
+    # hold at least 16 pages;
     # members either fold or are merged; the library accepts the plan
     rng = np.random.default_rng(500 + seed)
     sms = int(rng.choice([8, 16, 32, 64, 100, 132, 152]))
@@ -706,9 +716,9 @@ def test_random_shared_plans_keep_their_layout_rules(seed):
     merged = {int(m[0]) for m in plan.merges()}
     assert members <= merged | set(folds) and not merged & set(folds)
     if plan.layout == 1:
-        assert plan.num_segs > 0 and plan.num_shared > 0
-        assert plan.num_shared * 8 <= sms and plan.num_items <= sms
-        assert plan.range_pages >= 16
+        assert plan.num_shared > 0 and plan.num_shared * 8 <= sms
+        if plan.num_segs:
+            assert plan.num_items <= sms and plan.range_pages >= 16
     elif plan.num_segs:   # one wave of two per SM when some bin size fits it
         assert plan.range_pages >= 16
     assert _kernels_for(plan.host.copy(), len(lens)) is not None
