@@ -20,16 +20,20 @@ from _gpu_util import binding, cuda_or_skip
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name,steps,layers", [("prefix", 4000, None), ("prefix", 1000, 4),
-                                               ("mix", 600, None), ("peak", 1200, None),
-                                               ("small", 4000, None)])
-def test_many_steps_raise_no_device_error(name, steps, layers):
+@pytest.mark.parametrize("name,steps,layers,batch", [
+    ("prefix", 4000, None, None), ("prefix", 1000, 4, None), ("prefix", 2000, 4, 32),
+    ("mix", 600, None, None), ("peak", 1200, None, None), ("small", 4000, None, None)])
+def test_many_steps_raise_no_device_error(name, steps, layers, batch):
     # prefix with 4 layers: each layer's shared-prefix grid is launched while
-    # the previous layer's segment CTAs still run beside its own (the plan's
-    # beside layout), 4000 times in a row
+    # the previous layer's segment CTAs (256 sequences) or per-(item, kv head)
+    # CTAs (32 sequences) still run beside its own (the plan's beside
+    # layout), thousands of times in a row
     dev = cuda_or_skip()
     b = binding()
-    w = synth.make_workload(name, 0, **({"layers": layers} if layers else {}))
+    kw = {"layers": layers} if layers else {}
+    if batch:
+        kw.update(batch=batch, num_pages=12000)
+    w = synth.make_workload(name, 0, **kw)
     d = synth.device_inputs(w, dev)
     plan = b.Plan(w.seq_lens, w.max_blocks, device=dev, block_tables=w.block_tables[0])
     ws = torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device=dev)
