@@ -36,6 +36,9 @@
 //  * Before griddepcontrol.wait a CTA only prefetches its first ring fill
 //    into L2 (prefetch_first_tiles), so that a CTA made resident while the
 //    previous grid drains already pulls its pages.
+//  * kBeside (planned, a shared-prefix plan's beside layout): the grid runs
+//    next to the shared-prefix grid launched just before it and waits for
+//    it only at its end; its CTAs share each SM with a shared-prefix CTA.
 //  * Batches that fill the SMs go to decode_pagebox.cu instead (one CTA per
 //    sequence range for all heads, whole-page boxes).
 #include <cuda.h>

@@ -60,10 +60,12 @@ constexpr int kSegMax = 4;
 constexpr int kSegCtasPerSm = 2;
 constexpr int kSegMaxPages = 1024;  // pages of one segment CTA (its page list)
 // Header word 11, the plan's layout.  kPlanLayoutBeside (a shared-prefix
-// plan with segment items only): the shared-prefix CTAs fit one per SM, and
-// the segment CTAs, one per SM too (deeper rings), run beside them: each
-// streams its own pages as soon as it starts and waits for the shared-prefix
-// grid only before it folds that grid's partials.
+// plan whose shared-prefix CTAs fit one per SM): the other attention CTAs
+// run beside them -- segment CTAs, one per SM (deeper rings), or
+// per-(item, kv head) CTAs, two per SM next to each shared-prefix CTA --
+// each streaming its own pages as soon as it starts and waiting for the
+// shared-prefix grid only before it folds that grid's partials and before
+// it ends.
 constexpr int kPlanLayoutSequential = 0;
 constexpr int kPlanLayoutBeside = 1;
 constexpr int kSegBesideCtasPerSm = 1;
